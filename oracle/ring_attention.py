@@ -1,0 +1,489 @@
+"""Plain fp64 restatement of context-parallel causal ring attention.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): no product code may
+import this module.
+
+Sources (page title, then section):
+* [MaxText] "Announcing Long-Context Training on TPUs with MaxText Context
+  Parallelism": "Context Parallelism in MaxText" (P2P ring attention: KV
+  chunks move one hop per step, each chip attends its queries to the chunk it
+  holds and merges partial results as it goes) and "Built on a fast attention
+  kernel" (block-sparse flash attention that skips fully masked blocks and
+  handles packed sequences; called once per ring step, forward and
+  backward).
+* [CP-Inference] "Context Parallelism for Scalable Million-Token Inference":
+  "Attention Compute Patterns in Multi-Turn Chat" (full prefill is the lower
+  triangle; partial prefill lets new tokens see the cached prefix and their
+  own triangle), "Load Balancing in CP" (2R chunks, two per rank, worked
+  example with 4 tokens and 2 ranks), "Ring Attention Algorithms" (Pass KV:
+  Q stays, KV circulates, partial outputs merged at the end; Pass Q: KV
+  stays, Q circulates, partial outputs permuted back to order, returned to
+  their owners by an all-to-all, then merged), and "Context Parallelism (CP)
+  vs. Tensor Parallelism (TP)" (grouped-query heads: few KV heads shared by
+  many Q heads).
+
+Readings where the pages are silent (each is listed in the design doc):
+* Rank r holds chunks r and 2R-1-r, in that order ("Load Balancing in CP"
+  says rank 0 may take the first and last chunk).
+* Ring direction: at step t rank r holds the KV (Pass KV) or the Q (Pass Q)
+  that rank (r - t) mod R started with.
+* The merge is the log-sum-exp combination of partial softmax results
+  (the pages name the "merge attention operation" but print no formula):
+  LSE = M + ln sum_i exp(LSE_i - M), O = sum_i exp(LSE_i - LSE) O_i.
+* LSE is natural-log, with the softmax scale applied to the scores.
+* A row that sees no key in a step has O = 0 and LSE = -inf there.
+* GQA: query head h uses KV head h // G (contiguous groups).
+* Packed sequences: a key is visible iff it lies in the same document as the
+  query and at a position not after it. Documents are given by cu_seqlens
+  in natural token positions.
+* Partial prefill: cache and new tokens are each split 2R ways the same way;
+  rank r's KV is [its cache chunks, its new chunks]; new token i sits at
+  global position P + i (P = cached length).
+* Backward: the standard softmax gradient with the global (merged) LSE, so
+  each ring step's share uses P = exp(S - LSE_global).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "rank_chunks",
+    "shard_positions",
+    "plan_positions",
+    "ring_schedule",
+    "doc_index",
+    "visible_mask",
+    "block_mask",
+    "count_visible",
+    "partial_attention",
+    "attention",
+    "lse_merge",
+    "ring_forward",
+    "attention_backward",
+    "ring_backward",
+    "sampled_forward",
+    "sampled_dq",
+    "sampled_dkdv",
+    "TILE",
+]
+
+TILE = 128
+EMPTY, PARTIAL, FULL = 0, 1, 2
+
+
+# ---------------------------------------------------------------------------
+# Chunk plan  ([CP-Inference] "Load Balancing in CP")
+# ---------------------------------------------------------------------------
+def rank_chunks(R: int, layout: str = "zigzag"):
+    """Chunk indices held by each rank, in the rank's local order.
+
+    zigzag: the sequence is cut into 2R chunks and rank r takes chunks r and
+    2R-1-r. contiguous: R chunks, rank r takes chunk r (no balancing).
+    """
+    if layout == "zigzag":
+        return [[r, 2 * R - 1 - r] for r in range(R)]
+    if layout == "contiguous":
+        return [[r] for r in range(R)]
+    raise ValueError(layout)
+
+
+def shard_positions(n_tokens: int, R: int, layout: str = "zigzag",
+                    offset: int = 0):
+    """Global positions held by each rank, in local order, for a run of
+    ``n_tokens`` tokens starting at global position ``offset``."""
+    chunks = rank_chunks(R, layout)
+    n_chunks = 2 * R if layout == "zigzag" else R
+    assert n_tokens % n_chunks == 0
+    c = n_tokens // n_chunks
+    out = []
+    for r in range(R):
+        pos = [np.arange(ch * c, (ch + 1) * c, dtype=np.int64) + offset
+               for ch in chunks[r]]
+        out.append(np.concatenate(pos))
+    return out
+
+
+def plan_positions(seq_len: int, R: int, layout: str = "zigzag",
+                   kv_prefix_len: int = 0):
+    """Per-rank global positions of the query tokens and of the KV tokens.
+
+    Full prefill: Q and KV are the same tokens. Partial prefill (a cached
+    prefix of length P): the cache and the new tokens are each sharded the
+    same way; rank r's KV is its cache shard followed by its new-token shard,
+    and the new tokens (the queries) sit at positions P, P+1, ...
+    """
+    P = int(kv_prefix_len)
+    q_pos = shard_positions(seq_len, R, layout, offset=P)
+    if P == 0:
+        kv_pos = [p.copy() for p in q_pos]
+    else:
+        cache = shard_positions(P, R, layout, offset=0)
+        kv_pos = [np.concatenate([cache[r], q_pos[r]]) for r in range(R)]
+    return q_pos, kv_pos
+
+
+def ring_schedule(R: int, variant: str = "pass_kv"):
+    """sched[t][r] = (q_owner, kv_owner) of the pair rank r computes at step t.
+
+    Pass KV: rank r keeps its Q and holds the KV that started on rank
+    (r - t) mod R. Pass Q: rank r keeps its KV and holds the Q that started
+    on rank (r - t) mod R.
+    """
+    sched = []
+    for t in range(R):
+        row = []
+        for r in range(R):
+            other = (r - t) % R
+            if variant == "pass_kv":
+                row.append((r, other))
+            elif variant == "pass_q":
+                row.append((other, r))
+            else:
+                raise ValueError(variant)
+        sched.append(row)
+    return sched
+
+
+# ---------------------------------------------------------------------------
+# Mask  ([CP-Inference] "Attention Compute Patterns in Multi-Turn Chat";
+#        [MaxText] "Built on a fast attention kernel": packed sequences)
+# ---------------------------------------------------------------------------
+def doc_index(pos: np.ndarray, cu_seqlens) -> np.ndarray:
+    """Document id of each global position (all zero without documents)."""
+    pos = np.asarray(pos, dtype=np.int64)
+    if cu_seqlens is None:
+        return np.zeros(pos.shape, dtype=np.int64)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    return np.searchsorted(cu, pos, side="right") - 1
+
+
+def visible_mask(qpos, kpos, cu_seqlens=None) -> np.ndarray:
+    """vis[i, j]: key at kpos[j] is visible from the query at qpos[i]."""
+    qpos = np.asarray(qpos, dtype=np.int64)
+    kpos = np.asarray(kpos, dtype=np.int64)
+    causal = kpos[None, :] <= qpos[:, None]
+    same_doc = doc_index(kpos, cu_seqlens)[None, :] == \
+        doc_index(qpos, cu_seqlens)[:, None]
+    return causal & same_doc
+
+
+def block_mask(q_pos, kv_pos, cu_seqlens=None, tile: int = TILE):
+    """Tile class per (q_owner, kv_owner, q_tile, kv_tile), by brute force.
+
+    EMPTY (0) if no (query, key) pair of the tile is visible, FULL (2) if all
+    are, PARTIAL (1) otherwise. Computed from the elementwise mask with
+    ``any``/``all`` over each tile.
+    """
+    R = len(q_pos)
+    nq = len(q_pos[0])
+    nk = len(kv_pos[0])
+    assert nq % tile == 0 and nk % tile == 0
+    out = np.zeros((R, R, nq // tile, nk // tile), dtype=np.uint8)
+    for a in range(R):
+        for b in range(R):
+            vis = visible_mask(q_pos[a], kv_pos[b], cu_seqlens)
+            v4 = vis.reshape(nq // tile, tile, nk // tile, tile)
+            anyv = v4.any(axis=(1, 3))
+            allv = v4.all(axis=(1, 3))
+            out[a, b] = np.where(allv, FULL, np.where(anyv, PARTIAL, EMPTY))
+    return out
+
+
+def count_visible(qpos, kpos, cu_seqlens=None) -> int:
+    """Number of visible (query, key) pairs (per query head)."""
+    return int(visible_mask(qpos, kpos, cu_seqlens).sum())
+
+
+# ---------------------------------------------------------------------------
+# Attention and merge
+# ---------------------------------------------------------------------------
+def _as_f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _key_index(keep):
+    """Indices of kept keys; a slice when they are one contiguous run."""
+    kidx = np.nonzero(keep)[0]
+    if kidx.size and kidx[-1] - kidx[0] + 1 == kidx.size:
+        return slice(int(kidx[0]), int(kidx[-1]) + 1), kidx
+    return kidx, kidx
+
+
+def _per_head(x):
+    """[m, H, d] -> list of H contiguous [m, d] fp64 arrays."""
+    return [np.ascontiguousarray(x[:, h, :], dtype=np.float64)
+            for h in range(x.shape[1])]
+
+
+def partial_attention(q, k, v, qpos, kpos, cu_seqlens=None, scale=None,
+                      row_block: int = 512):
+    """Softmax attention of queries ``q`` over keys ``k``/values ``v``.
+
+    q: [n, Hq, d], k and v: [m, Hkv, d]. Returns O [n, Hq, d] and LSE [Hq, n]
+    (natural log of the sum of exp(scale * q.k) over the visible keys), in
+    fp64. Each row's softmax is taken over that row's complete visible set in
+    two passes (max, then exp and sum). Rows with no visible key get O = 0
+    and LSE = -inf. Rows are processed in blocks only to bound memory; keys
+    outside every row's [document start, position] range of a block are
+    skipped because they are invisible to all of its rows.
+    """
+    q = _as_f64(q)
+    n, Hq, d = q.shape
+    m, Hkv, _ = k.shape
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kh_ = _per_head(k)
+    vh_ = _per_head(v)
+    qpos = np.asarray(qpos, dtype=np.int64)
+    kpos = np.asarray(kpos, dtype=np.int64)
+    qdoc = doc_index(qpos, cu_seqlens)
+    kdoc = doc_index(kpos, cu_seqlens)
+    O = np.zeros((n, Hq, d))
+    LSE = np.full((Hq, n), -np.inf)
+    for r0 in range(0, n, row_block):
+        r1 = min(n, r0 + row_block)
+        qp = qpos[r0:r1]
+        qd = qdoc[r0:r1]
+        keep = (kpos <= qp.max()) & (kdoc >= qd.min()) & (kdoc <= qd.max())
+        ksel, kidx = _key_index(keep)
+        if kidx.size == 0:
+            continue
+        vis = (kpos[kidx][None, :] <= qp[:, None]) & \
+              (kdoc[kidx][None, :] == qd[:, None])
+        has = vis.any(axis=1)
+        for h in range(Hq):
+            kh = h // G
+            s = scale * (q[r0:r1, h, :] @ kh_[kh][ksel].T)
+            s = np.where(vis, s, -np.inf)
+            mx = s.max(axis=1)
+            mx_safe = np.where(has, mx, 0.0)
+            p = np.exp(s - mx_safe[:, None])
+            l = p.sum(axis=1)
+            l_safe = np.where(has, l, 1.0)
+            o = (p @ vh_[kh][ksel]) / l_safe[:, None]
+            O[r0:r1, h, :] = np.where(has[:, None], o, 0.0)
+            LSE[h, r0:r1] = np.where(has, mx_safe + np.log(l_safe), -np.inf)
+    return O, LSE
+
+
+def attention(q, k, v, qpos, kpos, cu_seqlens=None, scale=None):
+    """Monolithic (no context parallelism) causal attention over all keys."""
+    return partial_attention(q, k, v, qpos, kpos, cu_seqlens, scale)
+
+
+def lse_merge(parts):
+    """Merge partial results [(O_i [n,H,d], LSE_i [H,n]), ...] of disjoint
+    key sets into the softmax result over their union."""
+    lses = np.stack([_as_f64(p[1]) for p in parts])          # [k, H, n]
+    outs = np.stack([_as_f64(p[0]) for p in parts])          # [k, n, H, d]
+    M = lses.max(axis=0)                                     # [H, n]
+    finite = np.isfinite(M)
+    M_safe = np.where(finite, M, 0.0)
+    w = np.exp(lses - M_safe[None])                          # 0 for -inf
+    S = w.sum(axis=0)
+    LSE = np.where(finite, M_safe + np.log(np.where(finite, S, 1.0)), -np.inf)
+    LSE_safe = np.where(finite, LSE, 0.0)
+    coef = np.where(finite[None], np.exp(lses - LSE_safe[None]), 0.0)  # [k,H,n]
+    O = np.einsum("khn,knhd->nhd", coef, outs)
+    return O, LSE
+
+
+def _split(x, R):
+    n = x.shape[0] // R
+    return [x[r * n:(r + 1) * n] for r in range(R)]
+
+
+def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
+                 variant: str = "pass_kv"):
+    """Explicit ring over R virtual ranks; inputs in rank-major order.
+
+    q: [R*n_q, Hq, d] (rank r's queries are rows r*n_q ...), k/v:
+    [R*n_kv, Hkv, d]. Pass KV merges each step's partial result into a
+    running result in step order. Pass Q stores the partial result of
+    (q_owner, kv_owner) at the kv_owner's slot (the permutation back to
+    order), hands each q_owner its R partials (the all-to-all), and merges
+    them in kv_owner order. Returns O [R*n_q, Hq, d], LSE [Hq, R*n_q].
+    """
+    R = len(q_pos)
+    Q = _split(_as_f64(q), R)
+    K = _split(_as_f64(k), R)
+    V = _split(_as_f64(v), R)
+    sched = ring_schedule(R, variant)
+    if variant == "pass_kv":
+        acc = [None] * R
+        for t in range(R):
+            for r in range(R):
+                qo, ko = sched[t][r]
+                part = partial_attention(Q[qo], K[ko], V[ko], q_pos[qo],
+                                         kv_pos[ko], cu_seqlens, scale)
+                acc[qo] = part if acc[qo] is None else lse_merge([acc[qo], part])
+        outs = acc
+    else:
+        slots = [[None] * R for _ in range(R)]   # slots[q_owner][kv_owner]
+        for t in range(R):
+            for r in range(R):
+                qo, ko = sched[t][r]
+                slots[qo][ko] = partial_attention(Q[qo], K[ko], V[ko],
+                                                  q_pos[qo], kv_pos[ko],
+                                                  cu_seqlens, scale)
+        outs = [lse_merge(slots[qo]) for qo in range(R)]
+    O = np.concatenate([o for o, _ in outs], axis=0)
+    LSE = np.concatenate([l for _, l in outs], axis=1)
+    return O, LSE
+
+
+# ---------------------------------------------------------------------------
+# Backward  (softmax gradient with recomputed probabilities)
+# ---------------------------------------------------------------------------
+def _pair_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens, scale,
+                   dq, dk, dv, row_block: int = 512, want_dkdv: bool = True):
+    """Add one (query set, key set) share of the gradients into dq/dk/dv.
+
+    P = exp(scale q.k - LSE) on visible pairs (LSE = the merged, global one),
+    dV += P^T dO, dP = dO V^T, D = rowsum(dO * O), dS = P (dP - D),
+    dQ += scale dS K, dK += scale dS^T Q; dK and dV sum over the query heads
+    of each KV head's group.
+    """
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    kh_ = _per_head(k)
+    vh_ = _per_head(v)
+    qpos = np.asarray(qpos, dtype=np.int64)
+    kpos = np.asarray(kpos, dtype=np.int64)
+    qdoc = doc_index(qpos, cu_seqlens)
+    kdoc = doc_index(kpos, cu_seqlens)
+    D = np.einsum("nhd,nhd->hn", dout, o)
+    for r0 in range(0, n, row_block):
+        r1 = min(n, r0 + row_block)
+        qp = qpos[r0:r1]
+        qd = qdoc[r0:r1]
+        keep = (kpos <= qp.max()) & (kdoc >= qd.min()) & (kdoc <= qd.max())
+        ksel, kidx = _key_index(keep)
+        if kidx.size == 0:
+            continue
+        vis = (kpos[kidx][None, :] <= qp[:, None]) & \
+              (kdoc[kidx][None, :] == qd[:, None])
+        for h in range(Hq):
+            kh = h // G
+            kk = kh_[kh][ksel]
+            s = scale * (q[r0:r1, h, :] @ kk.T)
+            lse_h = lse[h, r0:r1]
+            lse_safe = np.where(np.isfinite(lse_h), lse_h, 0.0)
+            p = np.where(vis, np.exp(s - lse_safe[:, None]), 0.0)
+            dp = dout[r0:r1, h, :] @ vh_[kh][ksel].T
+            ds = p * (dp - D[h, r0:r1][:, None])
+            dq[r0:r1, h, :] += scale * (ds @ kk)
+            if want_dkdv:
+                dv[ksel, kh, :] += p.T @ dout[r0:r1, h, :]
+                dk[ksel, kh, :] += scale * (ds.T @ q[r0:r1, h, :])
+
+
+def attention_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens=None,
+                       scale=None):
+    """Gradients of monolithic attention. o/lse are the forward results."""
+    q, k, v, dout, o, lse = map(_as_f64, (q, k, v, dout, o, lse))
+    d = q.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    _pair_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens, scale,
+                   dq, dk, dv)
+    return dq, dk, dv
+
+
+def ring_backward(q, k, v, dout, o, lse, q_pos, kv_pos, cu_seqlens=None,
+                  scale=None, variant: str = "pass_kv"):
+    """Explicit ring backward: each step adds the share of the pair it holds.
+
+    Rank-major inputs as in ``ring_forward``; o and lse are the merged
+    forward results. dQ of a pair lands at its q_owner, dK/dV at its
+    kv_owner (in a real ring they travel back with the chunk).
+    """
+    q, k, v, dout, o, lse = map(_as_f64, (q, k, v, dout, o, lse))
+    R = len(q_pos)
+    d = q.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    nq = q.shape[0] // R
+    nk = k.shape[0] // R
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for t, row in enumerate(ring_schedule(R, variant)):
+        for qo, ko in row:
+            qs = slice(qo * nq, (qo + 1) * nq)
+            ks = slice(ko * nk, (ko + 1) * nk)
+            dq_p = np.zeros((nq,) + q.shape[1:])
+            dk_p = np.zeros((nk,) + k.shape[1:])
+            dv_p = np.zeros((nk,) + v.shape[1:])
+            _pair_backward(q[qs], k[ks], v[ks], dout[qs], o[qs], lse[:, qs],
+                           q_pos[qo], kv_pos[ko], cu_seqlens, scale,
+                           dq_p, dk_p, dv_p)
+            dq[qs] += dq_p
+            dk[ks] += dk_p
+            dv[ks] += dv_p
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Sampled rows for workloads too large for the full oracle
+# ---------------------------------------------------------------------------
+def sampled_forward(q, k, v, rows, qpos, kpos, cu_seqlens=None, scale=None,
+                    row_block: int = 32):
+    """O [len(rows), Hq, d] and LSE [Hq, len(rows)] at the given query rows,
+    each an exact full-prefix softmax over all of that row's visible keys."""
+    rows = np.asarray(rows, dtype=np.int64)
+    return partial_attention(_as_f64(np.asarray(q)[rows]), k, v,
+                             np.asarray(qpos)[rows], kpos, cu_seqlens, scale,
+                             row_block=row_block)
+
+
+def sampled_dq(q, k, v, dout, rows, qpos, kpos, cu_seqlens=None, scale=None,
+               row_block: int = 32):
+    """dQ at the given rows, using the oracle's own O and LSE of those rows."""
+    d = q.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.asarray(rows, dtype=np.int64)
+    o, lse = sampled_forward(q, k, v, rows, qpos, kpos, cu_seqlens, scale,
+                             row_block)
+    q_rows = _as_f64(np.asarray(q)[rows])
+    dout_rows = _as_f64(np.asarray(dout)[rows])
+    dq = np.zeros_like(q_rows)
+    _pair_backward(q_rows, k, v, dout_rows, o, lse,
+                   np.asarray(qpos)[rows], kpos, cu_seqlens, scale,
+                   dq, None, None, row_block=row_block, want_dkdv=False)
+    return dq
+
+
+def sampled_dkdv(q, k, v, dout, key_rows, qpos, kpos, cu_seqlens=None,
+                 scale=None):
+    """dK and dV at the given key rows.
+
+    Only the queries that can see one of those keys contribute; for each of
+    them the full-prefix O and LSE are computed first. Returns
+    (dk [len(key_rows), Hkv, d], dv [...]).
+    """
+    q = np.asarray(q)
+    d = q.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    qpos = np.asarray(qpos, dtype=np.int64)
+    kpos = np.asarray(kpos, dtype=np.int64)
+    key_rows = np.asarray(key_rows, dtype=np.int64)
+    kp = kpos[key_rows]
+    vis = visible_mask(qpos, kp, cu_seqlens)
+    qrows = np.nonzero(vis.any(axis=1))[0]
+    o, lse = sampled_forward(q, k, v, qrows, qpos, kpos, cu_seqlens, scale)
+    kk = _as_f64(np.asarray(k)[key_rows])
+    vv = _as_f64(np.asarray(v)[key_rows])
+    dq = np.zeros((len(qrows),) + q.shape[1:])
+    dk = np.zeros_like(kk)
+    dv = np.zeros_like(vv)
+    _pair_backward(_as_f64(q[qrows]), kk, vv, _as_f64(np.asarray(dout)[qrows]),
+                   o, lse, qpos[qrows], kp, cu_seqlens, scale, dq, dk, dv)
+    return dk, dv

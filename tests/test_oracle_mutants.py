@@ -1,0 +1,76 @@
+"""Planted mistakes in the oracle (on the CPU) must be caught by its pins.
+
+Each case rewrites one line of an oracle function (a flipped comparison, a
+dropped term, a wrong index), installs the rewritten function in the oracle
+module for the duration of the test, and checks that at least one of the
+pins in ``test_oracle_pins.py`` then fails.
+"""
+import inspect
+import textwrap
+
+import pytest
+
+import oracle
+import oracle.ring_attention as ra
+import test_oracle_pins as pins
+
+
+def _mutant(func, old, new):
+    src = textwrap.dedent(inspect.getsource(func))
+    assert src.count(old) >= 1, (func.__name__, old)
+    src = src.replace(old, new)
+    ns = {}
+    exec(compile(src, f"<mutant {func.__name__}>", "exec"), ra.__dict__, ns)
+    return ns[func.__name__]
+
+
+CASES = [
+    # (function, original text, planted text, pins that should catch it)
+    ("partial_attention", "kh = h // G", "kh = h % Hkv",
+     [pins.test_cp1_equals_library_causal_sdpa]),
+    ("partial_attention", "(kpos[kidx][None, :] <= qp[:, None])",
+     "(kpos[kidx][None, :] < qp[:, None])",
+     [lambda: pins.test_forward_matches_brute_force(None)]),
+    ("partial_attention", "mx_safe + np.log(l_safe)", "np.log(l_safe)",
+     [lambda: pins.test_forward_matches_brute_force(None)]),
+    ("partial_attention", "np.exp(s - mx_safe[:, None])", "np.exp(s)",
+     [lambda: pins.test_forward_matches_brute_force(None)]),
+    ("visible_mask", "kpos[None, :] <= qpos[:, None]",
+     "kpos[None, :] < qpos[:, None]",
+     [pins.test_worked_example_load_balance]),
+    ("doc_index", 'side="right"', 'side="left"',
+     [lambda: pins.test_forward_matches_brute_force([0, 5, 6, 13, 20])]),
+    ("rank_chunks", "[r, 2 * R - 1 - r]", "[r, R + r]",
+     [pins.test_worked_example_load_balance]),
+    ("ring_schedule", "row.append((r, other))", "row.append((r, r))",
+     [lambda: pins.test_ring_equals_monolithic("pass_kv", "zigzag", False)]),
+    ("lse_merge", "np.exp(lses - LSE_safe[None])", "np.exp(lses - M_safe[None])",
+     [lambda: pins.test_ring_equals_monolithic("pass_q", "zigzag", False)]),
+    ("plan_positions", "np.concatenate([cache[r], q_pos[r]])",
+     "np.concatenate([q_pos[r], cache[r]])",
+     [pins.test_partial_prefill_plan]),
+    ("_pair_backward", "ds = p * (dp - D[h, r0:r1][:, None])", "ds = p * dp",
+     [lambda: pins.test_backward_finite_differences(None)]),
+    ("_pair_backward", "dq[r0:r1, h, :] += scale * (ds @ kk)",
+     "dq[r0:r1, h, :] += (ds @ kk)",
+     [pins.test_backward_equals_library_autograd]),
+    ("_pair_backward", "dv[ksel, kh, :] += p.T @ dout[r0:r1, h, :]",
+     "dv[ksel, kh, :] += p.T @ dout[r0:r1, kh, :]",
+     [pins.test_backward_equals_library_autograd]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}:{c[2]}" for c in CASES])
+def test_planted_mistake_is_caught(case, monkeypatch):
+    name, old, new, checks = case
+    fn = _mutant(getattr(ra, name), old, new)
+    monkeypatch.setattr(ra, name, fn)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, fn)
+    caught = 0
+    for check in checks:
+        try:
+            check()
+        except (AssertionError, ValueError, IndexError):
+            caught += 1
+    assert caught > 0, f"planted mistake in {name} was not caught"
