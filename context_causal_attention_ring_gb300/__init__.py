@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) context-parallel causal ring-attention step.
+
+Python binding of libcp_attn.so; see ``include/cp_attn.h`` for the C ABI.
+The library is built in-tree by ``build.build()`` and loaded on first use;
+there is no CPU fallback.
+"""
+from ._abi import (  # noqa: F401
+    ACCUMULATE, CpAttnError, LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG, OP_BACKWARD,
+    OP_FORWARD, PASS_KV, PASS_Q, Plan, TENSOR_KV, TENSOR_Q, TO_NATURAL,
+    TO_RANK_MAJOR, WRITE_PARTIAL, exported_symbols, launch_count, lib_path,
+    load, merge_lse, status_string,
+)

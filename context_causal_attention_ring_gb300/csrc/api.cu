@@ -1,0 +1,525 @@
+// C ABI of the ring-attention step library: argument checks, plan upload,
+// tensor-map encoding and the emulated ring driver (an ordered loop of step
+// launches on the caller's stream).
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.h"
+
+namespace cpa {
+
+namespace {
+thread_local std::string g_err;
+std::atomic<int64_t> g_launches{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// [rows, heads, d] bf16 viewed as a 3-D tensor (d, heads, rows); boxes of
+// 64 x 1 x 128 elements land in shared memory as 128 rows of 128 bytes with
+// the 128-byte swizzle.
+cp_attn_status tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(CP_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(heads) * d * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(CP_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed with code " + std::to_string(r));
+  return CP_ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cp_attn_status check_device_plan(const cp_attn_plan_s* p) {
+  if (!p) return fail(CP_ATTN_ERR_INVALID_ARG, "null plan");
+  if (!p->on_device)
+    return fail(CP_ATTN_ERR_CUDA, "plan has no device tables (no CUDA device when it was built)");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "plan was built on CUDA device " +
+                                             std::to_string(p->device) +
+                                             " but another device is current");
+  return CP_ATTN_OK;
+}
+
+template <typename T>
+cp_attn_status upload(T** dst, const T* src, size_t n) {
+  if (n == 0) n = 1;
+  if (cudaMalloc(reinterpret_cast<void**>(dst), n * sizeof(T)) != cudaSuccess) {
+    cudaGetLastError();
+    *dst = nullptr;
+    return fail(CP_ATTN_ERR_OOM, "plan: cudaMalloc of device tables failed");
+  }
+  if (src && cudaMemcpy(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(CP_ATTN_ERR_CUDA, "plan: copy of device tables failed");
+  return CP_ATTN_OK;
+}
+
+}  // namespace
+
+cp_attn_status fail(cp_attn_status s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+void clear_error() { g_err.clear(); }
+void count_launch(int n) { g_launches += n; }
+
+cp_attn_status upload_plan(cp_attn_plan_s* p) {
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+    cudaGetLastError();
+    p->on_device = false;
+    return CP_ATTN_OK;
+  }
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    cudaGetLastError();
+    p->on_device = false;
+    return CP_ATTN_OK;
+  }
+  std::vector<int32_t> row_q(p->q_pos.size()), row_kv(p->kv_pos.size());
+  for (size_t i = 0; i < row_q.size(); ++i) row_q[i] = static_cast<int32_t>(p->q_pos[i] - p->P);
+  for (size_t i = 0; i < row_kv.size(); ++i) row_kv[i] = static_cast<int32_t>(p->kv_pos[i]);
+  const int32_t zeros[kStatusWords] = {0, 0, 0, 0};
+  cp_attn_status st;
+  if ((st = upload(&p->d_q_tile_pos, p->q_tile_pos.data(), p->q_tile_pos.size())) != CP_ATTN_OK ||
+      (st = upload(&p->d_kv_tile_pos, p->kv_tile_pos.data(), p->kv_tile_pos.size())) != CP_ATTN_OK ||
+      (st = upload(&p->d_cu, p->cu.data(), p->cu.size())) != CP_ATTN_OK ||
+      (st = upload(&p->d_fwd, p->fwd_items.data(), p->fwd_items.size())) != CP_ATTN_OK ||
+      (st = upload(&p->d_bwd, p->bwd_items.data(), p->bwd_items.size())) != CP_ATTN_OK ||
+      (st = upload(&p->d_status, zeros, kStatusWords)) != CP_ATTN_OK ||
+      (st = upload(&p->d_row_q, row_q.data(), row_q.size())) != CP_ATTN_OK ||
+      (st = upload(&p->d_row_kv, row_kv.data(), row_kv.size())) != CP_ATTN_OK) {
+    free_plan_device(p);
+    return st;
+  }
+  p->on_device = true;
+  return CP_ATTN_OK;
+}
+
+void free_plan_device(cp_attn_plan_s* p) {
+  void* ptrs[] = {p->d_q_tile_pos, p->d_kv_tile_pos, p->d_cu,    p->d_fwd,
+                  p->d_bwd,        p->d_status,      p->d_row_q, p->d_row_kv};
+  for (void* q : ptrs)
+    if (q) cudaFree(q);
+  p->d_q_tile_pos = p->d_kv_tile_pos = p->d_cu = p->d_status = p->d_row_q = p->d_row_kv = nullptr;
+  p->d_fwd = p->d_bwd = nullptr;
+  p->on_device = false;
+}
+
+}  // namespace cpa
+
+using namespace cpa;
+
+extern "C" {
+
+const char* cp_attn_last_error(void) { return g_err.c_str(); }
+
+const char* cp_attn_status_string(cp_attn_status s) {
+  switch (s) {
+    case CP_ATTN_OK: return "ok";
+    case CP_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case CP_ATTN_ERR_SHAPE: return "bad shape";
+    case CP_ATTN_ERR_UNSUPPORTED: return "unsupported";
+    case CP_ATTN_ERR_CUDA: return "CUDA error";
+    case CP_ATTN_ERR_OOM: return "out of device memory";
+    case CP_ATTN_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+int64_t cp_attn_launch_count(void) { return g_launches.load(); }
+
+cp_attn_status cp_attn_plan_ex(cp_attn_plan_t* out, const cp_attn_plan_desc* desc) {
+  clear_error();
+  if (!out) return fail(CP_ATTN_ERR_INVALID_ARG, "plan: null output handle");
+  *out = nullptr;
+  auto* p = new (std::nothrow) cp_attn_plan_s();
+  if (!p) return fail(CP_ATTN_ERR_OOM, "plan: host allocation failed");
+  cp_attn_status st = build_plan(p, desc);
+  if (st == CP_ATTN_OK) st = upload_plan(p);
+  if (st != CP_ATTN_OK) {
+    delete p;
+    return st;
+  }
+  *out = p;
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_plan(cp_attn_plan_t* out, int64_t seq_len, int cp, int n_q_heads,
+                            int n_kv_heads, int head_dim, cp_attn_layout layout,
+                            cp_attn_variant variant, const int32_t* cu_seqlens, int n_docs) {
+  cp_attn_plan_desc d;
+  std::memset(&d, 0, sizeof(d));
+  d.seq_len = seq_len;
+  d.kv_prefix_len = 0;
+  d.cp = cp;
+  d.n_q_heads = n_q_heads;
+  d.n_kv_heads = n_kv_heads;
+  d.head_dim = head_dim;
+  d.layout = layout;
+  d.variant = variant;
+  d.cu_seqlens = cu_seqlens;
+  d.n_docs = n_docs;
+  d.softmax_scale = 0.f;
+  return cp_attn_plan_ex(out, &d);
+}
+
+void cp_attn_plan_destroy(cp_attn_plan_t plan) {
+  if (!plan) return;
+  free_plan_device(plan);
+  delete plan;
+}
+
+cp_attn_status cp_attn_plan_info(cp_attn_plan_t p, int64_t* info, int n) {
+  clear_error();
+  if (!p || !info || n < 0 || n > 12) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_info: bad arguments");
+  const int64_t v[12] = {p->T_q, p->T_kv, p->n_q, p->n_kv, p->R, p->Hq, p->Hkv, p->d,
+                         p->n_qt, p->n_kt, static_cast<int64_t>(p->cu.size()) - 1,
+                         p->on_device ? 1 : 0};
+  for (int i = 0; i < n; ++i) info[i] = v[i];
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_plan_positions(cp_attn_plan_t p, cp_attn_tensor_kind kind, int rank,
+                                      int32_t* out) {
+  clear_error();
+  if (!p || !out || rank < 0 || rank >= p->R)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "plan_positions: bad arguments");
+  if (kind == CP_ATTN_TENSOR_Q) {
+    for (int64_t i = 0; i < p->n_q; ++i) out[i] = static_cast<int32_t>(p->q_pos[rank * p->n_q + i]);
+  } else if (kind == CP_ATTN_TENSOR_KV) {
+    for (int64_t i = 0; i < p->n_kv; ++i) out[i] = static_cast<int32_t>(p->kv_pos[rank * p->n_kv + i]);
+  } else {
+    return fail(CP_ATTN_ERR_INVALID_ARG, "plan_positions: bad tensor kind");
+  }
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_plan_schedule(cp_attn_plan_t p, int32_t* out) {
+  clear_error();
+  if (!p || !out) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_schedule: bad arguments");
+  std::memcpy(out, p->sched.data(), p->sched.size() * sizeof(int32_t));
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_plan_block_mask(cp_attn_plan_t p, uint8_t* out) {
+  clear_error();
+  if (!p || !out) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_block_mask: bad arguments");
+  size_t idx = 0;
+  for (int a = 0; a < p->R; ++a)
+    for (int b = 0; b < p->R; ++b)
+      for (int i = 0; i < p->n_qt; ++i)
+        for (int j = 0; j < p->n_kt; ++j) out[idx++] = static_cast<uint8_t>(tile_class(p, a, i, b, j));
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_plan_visible_pairs(cp_attn_plan_t p, int step, int64_t* out) {
+  clear_error();
+  if (!p || !out || step < -1 || step >= p->R)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "plan_visible_pairs: bad arguments");
+  if (step >= 0) {
+    *out = p->step_pairs[step];
+  } else {
+    int64_t s = 0;
+    for (int64_t v : p->step_pairs) s += v;
+    *out = s;
+  }
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_workspace_size(cp_attn_plan_t p, cp_attn_op op, size_t* bytes) {
+  clear_error();
+  if (!p || !bytes) return fail(CP_ATTN_ERR_INVALID_ARG, "workspace_size: bad arguments");
+  const size_t o = static_cast<size_t>(p->T_q) * p->Hq * p->d * sizeof(float);
+  const size_t l = static_cast<size_t>(p->T_q) * p->Hq * sizeof(float);
+  auto round = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  if (op == CP_ATTN_OP_FORWARD) {
+    *bytes = p->variant == CP_ATTN_PASS_KV ? round(o) : round(o * p->R) + round(l * p->R);
+  } else if (op == CP_ATTN_OP_BACKWARD) {
+    *bytes = round(l);
+  } else {
+    return fail(CP_ATTN_ERR_INVALID_ARG, "workspace_size: bad op");
+  }
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const void* k,
+                                const void* v, float* o_part, float* lse_part,
+                                cp_attn_merge_mode mode, void* o_final, void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  if (step < 0 || step >= p->R) return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd: step out of range");
+  if (mode != CP_ATTN_WRITE_PARTIAL && mode != CP_ATTN_ACCUMULATE)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd: bad merge mode");
+  if (!q || !k || !v || !o_part || !lse_part)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd: null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) ||
+      (o_final && !aligned16(o_final)))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd: tensors must be 16-byte aligned");
+  CUtensorMap tq, tk, tv;
+  if ((st = tmap_bf16(&tq, q, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
+  if ((st = tmap_bf16(&tk, k, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+  if ((st = tmap_bf16(&tv, v, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+  FwdParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.items = p->d_fwd + p->fwd_off[step];
+  fp.q_tile_pos = p->d_q_tile_pos;
+  fp.kv_tile_pos = p->d_kv_tile_pos;
+  fp.cu = p->d_cu;
+  fp.n_cu = static_cast<int>(p->cu.size());
+  fp.n_qt = p->n_qt;
+  fp.n_kt = p->n_kt;
+  fp.n_q = p->n_q;
+  fp.n_kv = p->n_kv;
+  fp.T_q = p->T_q;
+  fp.Hq = p->Hq;
+  fp.G = p->Hq / p->Hkv;
+  fp.scale_log2 = p->scale * 1.44269504088896340736f;
+  fp.mode = mode;
+  fp.first = (mode == CP_ATTN_ACCUMULATE && step == 0) ? 1 : 0;
+  fp.o_part = o_part;
+  fp.lse_part = lse_part;
+  fp.o_final = mode == CP_ATTN_ACCUMULATE ? static_cast<__nv_bfloat16*>(o_final) : nullptr;
+  fp.status = p->d_status;
+  fp.wait_limit_ns = kWaitLimitNs;
+  // Items without visible tiles still run when every row must be written:
+  // partial outputs, accumulator initialisation, or the final bf16 output.
+  const bool all_items = (mode == CP_ATTN_WRITE_PARTIAL) || fp.first || fp.o_final != nullptr;
+  const int n_items = all_items ? (p->fwd_off[step + 1] - p->fwd_off[step]) : p->fwd_nonempty[step];
+  if (n_items == 0) return CP_ATTN_OK;
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_items) * p->Hq));
+  return launch_step_fwd(p->d, grid, step_fwd_smem_bytes(p->d), static_cast<cudaStream_t>(stream),
+                         tq, tk, tv, fp);
+}
+
+cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* q, const void* k,
+                                const void* v, const void* dout, const float* lse,
+                                const float* delta, float* dq_acc, float* dk_acc, float* dv_acc,
+                                void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  if (step < 0 || step >= p->R) return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: step out of range");
+  if (!q || !k || !v || !dout || !lse || !delta || !dq_acc || !dk_acc || !dv_acc)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq_acc) ||
+      !aligned16(dk_acc) || !aligned16(dv_acc))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: tensors must be 16-byte aligned");
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = tmap_bf16(&tq, q, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
+  if ((st = tmap_bf16(&tk, k, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+  if ((st = tmap_bf16(&tv, v, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+  if ((st = tmap_bf16(&tdo, dout, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
+  BwdParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.items = p->d_bwd + p->bwd_off[step];
+  bp.q_tile_pos = p->d_q_tile_pos;
+  bp.kv_tile_pos = p->d_kv_tile_pos;
+  bp.cu = p->d_cu;
+  bp.n_cu = static_cast<int>(p->cu.size());
+  bp.n_qt = p->n_qt;
+  bp.n_kt = p->n_kt;
+  bp.n_q = p->n_q;
+  bp.n_kv = p->n_kv;
+  bp.T_q = p->T_q;
+  bp.T_kv = p->T_kv;
+  bp.Hq = p->Hq;
+  bp.Hkv = p->Hkv;
+  bp.G = p->Hq / p->Hkv;
+  bp.scale = p->scale;
+  bp.scale_log2 = p->scale * 1.44269504088896340736f;
+  bp.lse = lse;
+  bp.delta = delta;
+  bp.dq = dq_acc;
+  bp.dk = dk_acc;
+  bp.dv = dv_acc;
+  bp.status = p->d_status;
+  bp.wait_limit_ns = kWaitLimitNs;
+  const int n_items = p->bwd_off[step + 1] - p->bwd_off[step];
+  if (n_items == 0) return CP_ATTN_OK;
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_items) * p->Hkv));
+  return launch_step_bwd(p->d, grid, step_bwd_smem_bytes(p->d), static_cast<cudaStream_t>(stream),
+                         tq, tk, tv, tdo, bp);
+}
+
+cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* o, const void* dout,
+                                      float* delta, float* dq_acc, float* dk_acc, float* dv_acc,
+                                      void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  if (!o || !dout || !delta) return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: null pointer");
+  if (!aligned16(o) || !aligned16(dout) || (dq_acc && !aligned16(dq_acc)) ||
+      (dk_acc && !aligned16(dk_acc)) || (dv_acc && !aligned16(dv_acc)))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = launch_bwd_preprocess(p->T_q, p->Hq, p->d, static_cast<const __nv_bfloat16*>(o),
+                                  static_cast<const __nv_bfloat16*>(dout), delta, s)) != CP_ATTN_OK)
+    return st;
+  if (dq_acc && (st = launch_zero_f32(dq_acc, p->T_q * p->Hq * p->d, s)) != CP_ATTN_OK) return st;
+  if (dk_acc && (st = launch_zero_f32(dk_acc, p->T_kv * p->Hkv * p->d, s)) != CP_ATTN_OK) return st;
+  if (dv_acc && (st = launch_zero_f32(dv_acc, p->T_kv * p->Hkv * p->d, s)) != CP_ATTN_OK) return st;
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_merge_lse(int n_parts, int64_t rows, int heads, int head_dim,
+                                 const float* o_parts, int64_t part_stride,
+                                 const float* lse_parts, int64_t lse_part_stride, void* o_out,
+                                 float* o_out_f32, float* lse_out, void* stream) {
+  clear_error();
+  if (n_parts < 1 || rows < 0 || heads < 1 || head_dim < 4 || head_dim % 4 || head_dim > 256)
+    return fail(CP_ATTN_ERR_SHAPE, "merge_lse: bad sizes");
+  if (!o_parts || !lse_parts || !lse_out)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "merge_lse: null pointer");
+  if (!aligned16(o_parts) || (part_stride % 4) || (o_out && (reinterpret_cast<uintptr_t>(o_out) & 7)) ||
+      (o_out_f32 && !aligned16(o_out_f32)))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "merge_lse: misaligned pointer or stride");
+  return launch_merge_lse(n_parts, rows, heads, head_dim, o_parts, part_stride, lse_parts,
+                          lse_part_stride, static_cast<__nv_bfloat16*>(o_out), o_out_f32, lse_out,
+                          static_cast<cudaStream_t>(stream));
+}
+
+cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, const void* v,
+                               void* o, float* lse, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  size_t need = 0;
+  cp_attn_workspace_size(p, CP_ATTN_OP_FORWARD, &need);
+  if (!workspace || workspace_bytes < need)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "forward: workspace smaller than cp_attn_workspace_size");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "forward: workspace must be 256-byte aligned");
+  if (!o || !lse) return fail(CP_ATTN_ERR_INVALID_ARG, "forward: null output");
+  float* ws = static_cast<float*>(workspace);
+  if (p->variant == CP_ATTN_PASS_KV) {
+    // Q stays, KV moves; merge "as it goes" into the fp32 accumulator
+    for (int t = 0; t < p->R; ++t) {
+      st = cp_attn_step_fwd(p, t, q, k, v, ws, lse, CP_ATTN_ACCUMULATE, t == p->R - 1 ? o : nullptr,
+                            stream);
+      if (st != CP_ATTN_OK) return st;
+    }
+    return CP_ATTN_OK;
+  }
+  // Pass Q: KV stays, Q moves. Each step writes its partials to the slot of
+  // the kv owner (the permutation back to order); the n-way merge per q owner
+  // stands for the all-to-all plus merge.
+  const int64_t o_slot = p->T_q * p->Hq * p->d;
+  const int64_t l_slot = p->T_q * p->Hq;
+  const size_t o_bytes = (static_cast<size_t>(o_slot) * p->R * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  for (int t = 0; t < p->R; ++t) {
+    st = cp_attn_step_fwd(p, t, q, k, v, ws, ws_lse, CP_ATTN_WRITE_PARTIAL, nullptr, stream);
+    if (st != CP_ATTN_OK) return st;
+  }
+  return cp_attn_merge_lse(p->R, p->T_q, p->Hq, p->d, ws, o_slot, ws_lse, l_slot, o, nullptr, lse,
+                           stream);
+}
+
+cp_attn_status cp_attn_backward(cp_attn_plan_t p, const void* q, const void* k, const void* v,
+                                const void* o, const float* lse, const void* dout, float* dq,
+                                float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  size_t need = 0;
+  cp_attn_workspace_size(p, CP_ATTN_OP_BACKWARD, &need);
+  if (!workspace || workspace_bytes < need)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "backward: workspace smaller than cp_attn_workspace_size");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "backward: workspace must be 256-byte aligned");
+  float* delta = static_cast<float*>(workspace);
+  if ((st = cp_attn_bwd_preprocess(p, o, dout, delta, dq, dk, dv, stream)) != CP_ATTN_OK) return st;
+  for (int t = 0; t < p->R; ++t) {
+    st = cp_attn_step_bwd(p, t, q, k, v, dout, lse, delta, dq, dk, dv, stream);
+    if (st != CP_ATTN_OK) return st;
+  }
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_layout_apply(cp_attn_plan_t p, cp_attn_tensor_kind kind,
+                                    cp_attn_direction direction, const void* in, void* out,
+                                    int64_t row_bytes, void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  if (!in || !out || in == out) return fail(CP_ATTN_ERR_INVALID_ARG, "layout_apply: bad pointers");
+  if (row_bytes <= 0 || row_bytes % 16) return fail(CP_ATTN_ERR_SHAPE, "layout_apply: row_bytes must be a positive multiple of 16");
+  if (!aligned16(in) || !aligned16(out)) return fail(CP_ATTN_ERR_INVALID_ARG, "layout_apply: pointers must be 16-byte aligned");
+  if (direction != CP_ATTN_TO_RANK_MAJOR && direction != CP_ATTN_TO_NATURAL)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "layout_apply: bad direction");
+  const int32_t* map;
+  int64_t rows;
+  if (kind == CP_ATTN_TENSOR_Q) {
+    map = p->d_row_q;
+    rows = p->T_q;
+  } else if (kind == CP_ATTN_TENSOR_KV) {
+    map = p->d_row_kv;
+    rows = p->T_kv;
+  } else {
+    return fail(CP_ATTN_ERR_INVALID_ARG, "layout_apply: bad tensor kind");
+  }
+  return launch_permute_rows(map, rows, row_bytes, direction == CP_ATTN_TO_NATURAL ? 1 : 0, in, out,
+                             static_cast<cudaStream_t>(stream));
+}
+
+cp_attn_status cp_attn_selftest_wait_timeout(cp_attn_plan_t p, uint64_t limit_ns, void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  if (limit_ns == 0 || limit_ns > 2000000000ull)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "selftest_wait_timeout: limit must be in (0, 2 s]");
+  return launch_selftest_wait(p->d_status, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+cp_attn_status cp_attn_sync_status(cp_attn_plan_t p, void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("sync: ") + cudaGetErrorString(err));
+  int32_t host[kStatusWords] = {0, 0, 0, 0};
+  err = cudaMemcpy(host, p->d_status, sizeof(host), cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("status read: ") + cudaGetErrorString(err));
+  if (host[0] != 0) {
+    const int32_t zeros[kStatusWords] = {0, 0, 0, 0};
+    cudaMemcpy(p->d_status, zeros, sizeof(zeros), cudaMemcpyHostToDevice);
+    return fail(static_cast<cp_attn_status>(host[0]),
+                "device status " + std::to_string(host[0]) + " in block " + std::to_string(host[1]) +
+                    " at 0x" + [&] { char b[16]; std::snprintf(b, sizeof(b), "%x", host[2]); return std::string(b); }());
+  }
+  return CP_ATTN_OK;
+}
+
+}  // extern "C"

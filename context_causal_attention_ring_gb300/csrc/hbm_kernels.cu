@@ -1,0 +1,229 @@
+// HBM-bound kernels of the ring-attention step:
+//   K4 merge_lse     -- n-way log-sum-exp merge of partial attention results
+//                       ("merge attention operation", "Ring Attention
+//                       Algorithms" in "Context Parallelism for Scalable
+//                       Million-Token Inference")
+//   K5 permute_rows  -- natural <-> rank-major token order ("Load Balancing
+//                       in CP": two chunks per rank)
+//   K3 bwd_preprocess-- delta = rowsum(dO * O) for the softmax backward
+//   zero_f32         -- clears fp32 gradient accumulators
+// All use 16-byte vector accesses with consecutive threads on consecutive
+// addresses.
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace cpa {
+namespace {
+
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// One warp per (row, head). Lane l handles float4 chunks l, l+32, ...
+template <int CHUNKS>  // float4 chunks per lane (d/4/32 rounded up)
+__global__ void __launch_bounds__(256) merge_lse_kernel(
+    int n_parts, int64_t rows, int heads, int d, const float* __restrict__ o_parts,
+    int64_t part_stride, const float* __restrict__ lse_parts, int64_t lse_part_stride,
+    __nv_bfloat16* __restrict__ o_out, float* __restrict__ o_out_f32,
+    float* __restrict__ lse_out) {
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= rows * heads) return;
+  const int64_t row = wid / heads;
+  const int h = static_cast<int>(wid % heads);
+  const int64_t lse_idx = static_cast<int64_t>(h) * rows + row;
+  // M = max_i LSE_i (base 2)
+  float M = -INFINITY;
+  for (int i = lane; i < n_parts; i += 32)
+    M = fmaxf(M, __ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const int n4 = d >> 2;
+  float4 acc[CHUNKS];
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = -INFINITY;
+  if (M != -INFINITY) {
+    float S = 0.f;
+    for (int i = lane; i < n_parts; i += 32)
+      S += ptx::ex2(__ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    L = M + ptx::lg2(S);
+    const int64_t o_off = (row * heads + h) * static_cast<int64_t>(d);
+    for (int i = 0; i < n_parts; ++i) {
+      const float w = ptx::ex2(__ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e - L);
+      if (w == 0.f) continue;  // empty part (LSE = -inf) or negligible
+      const float4* src = reinterpret_cast<const float4*>(o_parts + i * part_stride + o_off);
+#pragma unroll
+      for (int c = 0; c < CHUNKS; ++c) {
+        const int j = lane + 32 * c;
+        if (j < n4) {
+          const float4 v = __ldg(src + j);
+          acc[c].x = fmaf(w, v.x, acc[c].x);
+          acc[c].y = fmaf(w, v.y, acc[c].y);
+          acc[c].z = fmaf(w, v.z, acc[c].z);
+          acc[c].w = fmaf(w, v.w, acc[c].w);
+        }
+      }
+    }
+  }
+  const int64_t o_off = (row * heads + h) * static_cast<int64_t>(d);
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    const int j = lane + 32 * c;
+    if (j < n4) {
+      if (o_out_f32) reinterpret_cast<float4*>(o_out_f32 + o_off)[j] = acc[c];
+      if (o_out) {
+        uint2 pk;
+        pk.x = ptx::pack_bf16(acc[c].x, acc[c].y);
+        pk.y = ptx::pack_bf16(acc[c].z, acc[c].w);
+        reinterpret_cast<uint2*>(o_out + o_off)[j] = pk;
+      }
+    }
+  }
+  if (lane == 0) lse_out[lse_idx] = (M == -INFINITY) ? -INFINITY : L * kLn2;
+}
+
+// out[dst] = in[src] for 16-byte vectors; row_map[i] = natural row of
+// rank-major row i. to_natural: out[row_map[i]] = in[i]; else
+// out[i] = in[row_map[i]].
+__global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __restrict__ row_map,
+                                                           int64_t rows, int64_t vec_per_row,
+                                                           int to_natural,
+                                                           const uint4* __restrict__ in,
+                                                           uint4* __restrict__ out) {
+  const int64_t total = rows * vec_per_row;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = idx / vec_per_row;
+    const int64_t v = idx - i * vec_per_row;
+    const int64_t nat = __ldg(row_map + i);
+    if (to_natural) out[nat * vec_per_row + v] = __ldg(in + i * vec_per_row + v);
+    else out[i * vec_per_row + v] = __ldg(in + nat * vec_per_row + v);
+  }
+}
+
+// delta[h][t] = sum_x dO[t,h,x] * O[t,h,x], one warp per (t, h); lanes read
+// 8-byte (4 x bf16) pieces.
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(int64_t rows, int heads, int d,
+                                                             const __nv_bfloat16* __restrict__ o,
+                                                             const __nv_bfloat16* __restrict__ dout,
+                                                             float* __restrict__ delta) {
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= rows * heads) return;
+  const int64_t t = wid / heads;
+  const int h = static_cast<int>(wid % heads);
+  const int64_t off = wid * d;  // (t*heads + h)*d
+  float acc = 0.f;
+  for (int x = lane * 4; x < d; x += 128) {
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(o + off + x));
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(dout + off + x));
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 fa = __bfloat1622float2(a2[k]);
+      const float2 fb = __bfloat1622float2(b2[k]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) delta[static_cast<int64_t>(h) * rows + t] = acc;
+}
+
+__global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ p, int64_t n4,
+                                                       float* __restrict__ tail, int n_tail) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (blockIdx.x == 0 && threadIdx.x < n_tail) tail[threadIdx.x] = 0.f;
+}
+
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait
+// gives up after limit_ns and records the timeout like every kernel wait.
+__global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 &&
+      !ptx::mbar_wait(ptx::smem_u32(&bar), 0, &abort_flag, limit_ns))
+    ptx::record_timeout(status, &abort_flag, 0xdead);
+}
+
+int grid_for(int64_t work, int per_block, int cap) {
+  const int64_t g = (work + per_block - 1) / per_block;
+  return static_cast<int>(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+cp_attn_status check_launch(const char* what) {
+  const cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(err));
+  count_launch();
+  return CP_ATTN_OK;
+}
+
+}  // namespace
+
+cp_attn_status launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return check_launch("selftest_wait");
+}
+
+cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
+                                const float* o_parts, int64_t part_stride,
+                                const float* lse_parts, int64_t lse_part_stride,
+                                __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
+                                cudaStream_t s) {
+  const int64_t warps = rows * heads;
+  if (warps == 0) return CP_ATTN_OK;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (d <= 128)
+    merge_lse_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
+        o_out_f32, lse_out);
+  else
+    merge_lse_kernel<2><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
+        o_out_f32, lse_out);
+  return check_launch("merge_lse");
+}
+
+cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t row_bytes,
+                                   int to_natural, const void* in, void* out, cudaStream_t s) {
+  const int64_t vpr = row_bytes / 16;
+  if (rows * vpr == 0) return CP_ATTN_OK;
+  permute_rows_kernel<<<grid_for(rows * vpr, 256, 152 * 16), 256, 0, s>>>(
+      row_map, rows, vpr, to_natural, static_cast<const uint4*>(in), static_cast<uint4*>(out));
+  return check_launch("permute_rows");
+}
+
+cp_attn_status launch_bwd_preprocess(int64_t rows, int heads, int d, const __nv_bfloat16* o,
+                                     const __nv_bfloat16* dout, float* delta, cudaStream_t s) {
+  const int64_t warps = rows * heads;
+  if (warps == 0) return CP_ATTN_OK;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  bwd_preprocess_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(rows, heads, d, o, dout,
+                                                                      delta);
+  return check_launch("bwd_preprocess");
+}
+
+cp_attn_status launch_zero_f32(float* p, int64_t n, cudaStream_t s) {
+  if (n == 0) return CP_ATTN_OK;
+  const int64_t n4 = n / 4;
+  const int n_tail = static_cast<int>(n - n4 * 4);
+  zero_f32_kernel<<<grid_for(n4 > 0 ? n4 : 1, 256, 152 * 16), 256, 0, s>>>(
+      reinterpret_cast<float4*>(p), n4, p + n4 * 4, n_tail);
+  return check_launch("zero_f32");
+}
+
+}  // namespace cpa

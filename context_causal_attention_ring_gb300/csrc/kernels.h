@@ -1,0 +1,81 @@
+// Kernel parameter blocks and host-side launchers of the ring-attention step.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace cpa {
+
+// Default limit of every pipeline wait inside a kernel (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+struct FwdParams {
+  const WorkItem* items;
+  const int32_t* q_tile_pos;  // [R][n_qt] first global position of each q tile
+  const int32_t* kv_tile_pos; // [R][n_kt]
+  const int32_t* cu;          // document offsets
+  int n_cu;                   // n_docs + 1
+  int n_qt, n_kt;
+  int64_t n_q, n_kv, T_q;
+  int Hq, G;
+  float scale_log2;           // softmax scale * log2(e)
+  int mode;                   // cp_attn_merge_mode
+  int first;                  // ACCUMULATE: initialise the accumulators
+  float* o_part;
+  float* lse_part;
+  __nv_bfloat16* o_final;     // optional
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+struct BwdParams {
+  const WorkItem* items;
+  const int32_t* q_tile_pos;
+  const int32_t* kv_tile_pos;
+  const int32_t* cu;
+  int n_cu;
+  int n_qt, n_kt;
+  int64_t n_q, n_kv, T_q, T_kv;
+  int Hq, Hkv, G;
+  float scale;                // softmax scale
+  float scale_log2;
+  const float* lse;           // [Hq, T_q] natural log
+  const float* delta;         // [Hq, T_q]
+  float* dq;                  // [T_q, Hq, d]
+  float* dk;                  // [T_kv, Hkv, d]
+  float* dv;
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const FwdParams& p);
+size_t step_fwd_smem_bytes(int d);
+
+cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const CUtensorMap& tdo,
+                               const BwdParams& p);
+size_t step_bwd_smem_bytes(int d);
+
+cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
+                                const float* o_parts, int64_t part_stride,
+                                const float* lse_parts, int64_t lse_part_stride,
+                                __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
+                                cudaStream_t s);
+
+cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t row_bytes,
+                                   int to_natural, const void* in, void* out, cudaStream_t s);
+
+cp_attn_status launch_bwd_preprocess(int64_t rows, int heads, int d, const __nv_bfloat16* o,
+                                     const __nv_bfloat16* dout, float* delta, cudaStream_t s);
+
+cp_attn_status launch_zero_f32(float* p, int64_t n, cudaStream_t s);
+
+cp_attn_status launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace cpa

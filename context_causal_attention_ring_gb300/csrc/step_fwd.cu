@@ -1,0 +1,418 @@
+// K1: forward ring step on sm_103a (TMA + tcgen05 + TMEM).
+//
+// One CTA computes one (work item, query head): a 128-row query tile of rank
+// q_owner against the run [lo, hi) of non-empty 128-key tiles of rank
+// kv_owner ("Built on a fast attention kernel": fully masked blocks are
+// skipped; "Ring Attention Algorithms": partial attention of the local
+// queries against the visiting KV chunk, merged with the other steps'
+// partial results).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax + epilogue; thread r owns query row r (TMEM lane r)
+//   warp 4     TMA producer (Q once, K/V tiles through a 2-stage ring)
+//   warp 5     TMEM owner and single-thread tcgen05.mma issuer
+//
+// TMEM columns: S double buffer at [0,128) and [128,256), O at [256,256+d).
+// The MMA warp issues S(j+1) = Q K_{j+1}^T while the softmax warps turn S(j)
+// into P(j); P goes to shared memory in the canonical 128-byte-swizzled
+// K-major layout and O += P V_j runs as an SS MMA with V as an MN-major B.
+//
+// Online softmax in base 2 (scores scaled by scale*log2 e). The running max
+// is only raised (and O rescaled in TMEM) when a tile's max exceeds it by
+// more than 8, so exponentials stay below 2^8 -- the result is the same
+// softmax; only the reference point of the exponentials moves.
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace cpa {
+namespace {
+
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+// Barrier slots in shared memory.
+enum : int {
+  BAR_Q = 0,
+  BAR_K = 1,                       // [kStages]
+  BAR_V = BAR_K + kStages,         // [kStages]
+  BAR_EMPTY = BAR_V + kStages,     // [kStages]
+  BAR_S = BAR_EMPTY + kStages,     // [2]
+  BAR_P = BAR_S + 2,
+  BAR_O = BAR_P + 1,
+  BAR_DRAIN = BAR_O + 1,
+  BAR_COUNT = BAR_DRAIN + 1
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTileBytes = 128 * D * 2;  // one Q/K/V tile, bf16
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kP = kV + kStages * kTileBytes;
+  static constexpr int kBar = kP + 128 * 128 * 2;
+  static constexpr int kMisc = kBar + BAR_COUNT * 8;
+  static constexpr int kBytes = kMisc + 16;
+  // 1 KB of slack to align the base; at least 116 KB so that a single CTA
+  // (the only one that can hold the 512 TMEM columns) fits per SM.
+  static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
+};
+
+// Offset of element (row r, column c) of a 128-row bf16 tile stored as
+// 64-column blocks of 128 rows x 128 bytes with the 128-byte swizzle (the
+// layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B, and the layout the
+// tcgen05 descriptor reads with swizzle mode 128 B).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int chunk16) {
+  // chunk16: index of the 16-byte chunk along the row (8 bf16 each)
+  const int block = chunk16 >> 3;
+  const int c = (chunk16 & 7) ^ (r & 7);
+  return static_cast<uint32_t>(block * 16384 + r * 128 + (c << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    step_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_u32 + pad;
+
+  const uint32_t sQ = sbase + L::kQ;
+  const uint32_t sK = sbase + L::kK;
+  const uint32_t sV = sbase + L::kV;
+  const uint32_t sP = sbase + L::kP;
+  const uint32_t bar0 = sbase + L::kBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x / p.Hq;
+  const int h = blockIdx.x % p.Hq;
+  const WorkItem w = p.items[item];
+  const int kh = h / p.G;
+  const int n_tiles = w.hi - w.lo;
+  const int64_t q_row0 = static_cast<int64_t>(w.q_owner) * p.n_q + static_cast<int64_t>(w.tile) * 128;
+  const int32_t qpos0 = __ldg(p.q_tile_pos + static_cast<int64_t>(w.q_owner) * p.n_qt + w.tile);
+  const int64_t kv_row_base = static_cast<int64_t>(w.kv_owner) * p.n_kv;
+  const int32_t* kv_tile_pos = p.kv_tile_pos + static_cast<int64_t>(w.kv_owner) * p.n_kt;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < BAR_COUNT; ++i) ptx::mbar_init(bar(i), i == BAR_P ? 128u : 1u);
+    *s_abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO = tmem + 256;
+
+  if (n_tiles > 0 && warp == 4 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::mbar_arrive_expect_tx(bar(BAR_Q), L::kTileBytes);
+    for (int b = 0; b < D / 64; ++b)
+      ptx::tma_load_3d(sQ + b * 16384, &tm_q, bar(BAR_Q), b * 64, h, static_cast<int>(q_row0));
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages) {
+        if (!ptx::mbar_wait(bar(BAR_EMPTY + s), ((j / kStages) - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, 0x100 + j);
+          break;
+        }
+      }
+      const int row = static_cast<int>(kv_row_base + static_cast<int64_t>(w.lo + j) * 128);
+      ptx::mbar_arrive_expect_tx(bar(BAR_K + s), L::kTileBytes);
+      for (int b = 0; b < D / 64; ++b)
+        ptx::tma_load_3d(sK + s * L::kTileBytes + b * 16384, &tm_k, bar(BAR_K + s), b * 64, kh, row);
+      ptx::mbar_arrive_expect_tx(bar(BAR_V + s), L::kTileBytes);
+      for (int b = 0; b < D / 64; ++b)
+        ptx::tma_load_3d(sV + s * L::kTileBytes + b * 16384, &tm_v, bar(BAR_V + s), b * 64, kh, row);
+      issued = j + 1;
+    }
+    // Drain: every issued copy must land before the CTA may exit.
+    {
+      const volatile int never = 0;
+      ptx::mbar_wait(bar(BAR_Q), 0, &never, p.wait_limit_ns);
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+        ptx::mbar_wait(bar(BAR_K + j % kStages), (j / kStages) & 1, &never, p.wait_limit_ns);
+        ptx::mbar_wait(bar(BAR_V + j % kStages), (j / kStages) & 1, &never, p.wait_limit_ns);
+      }
+    }
+  } else if (n_tiles > 0 && warp == 5 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
+    bool ok = ptx::mbar_wait(bar(BAR_Q), 0, s_abort, p.wait_limit_ns);
+    if (!ok) ptx::record_timeout(p.status, s_abort, 0x200);
+    auto issue_pv = [&](int i) -> bool {
+      if (!ptx::mbar_wait(bar(BAR_P), i & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x300 + i);
+        return false;
+      }
+      const int s = i % kStages;
+      if (!ptx::mbar_wait(bar(BAR_V + s), (i / kStages) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x400 + i);
+        return false;
+      }
+      ptx::tc_fence_after();
+      const uint32_t v_tile = sV + s * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        // A = P [128 q x 128 keys], K-major, swizzled, 64-key blocks of 16 KB
+        const uint64_t a = ptx::sdesc_sw128(sP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        // B = V [keys x d], d contiguous (MN-major): 8-key groups at 1024 B,
+        // 64-column blocks at 16 KB
+        const uint64_t b = ptx::sdesc_sw128(v_tile + kk * 2048, 16384, 1024);
+        ptx::mma_bf16_ss(tO, a, b, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(BAR_O));
+      ptx::mma_commit(bar(BAR_EMPTY + s));
+      return true;
+    };
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int s = j % kStages;
+      if (!ptx::mbar_wait(bar(BAR_K + s), (j / kStages) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x500 + j);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t k_tile = sK + s * L::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint64_t a = ptx::sdesc_sw128(sQ + off, 16, 1024);
+        const uint64_t b = ptx::sdesc_sw128(k_tile + off, 16, 1024);
+        ptx::mma_bf16_ss(tS[j & 1], a, b, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(BAR_S + (j & 1)));
+      if (j >= 1 && !issue_pv(j - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok) issue_pv(n_tiles - 1);
+    // Drain: wait for every MMA this thread issued.
+    ptx::mma_commit(bar(BAR_DRAIN));
+    const volatile int never = 0;
+    ptx::mbar_wait(bar(BAR_DRAIN), 0, &never, p.wait_limit_ns);
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int r = threadIdx.x;  // query row within the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int32_t my_pos = qpos0 + r;
+    const int32_t my_ds = ptx::doc_start(p.cu, p.n_cu, my_pos);
+    const int32_t ds_last = ptx::doc_start(p.cu, p.n_cu, qpos0 + 127);
+    float m_used = -INFINITY;  // reference point of the exponentials (base 2)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int32_t kpos0 = __ldg(kv_tile_pos + w.lo + j);
+      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ds_last);
+      if (!ptx::mbar_wait(bar(BAR_S + (j & 1)), (j >> 1) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x600 + j);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ptx::tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        ptx::tmem_ld32(tS[j & 1] + lane_base + c * 32, *reinterpret_cast<float(*)[32]>(s + c * 32));
+      if (!full) {
+        const int lo = my_ds - kpos0;
+        const int hi = my_pos - kpos0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < lo || c > hi) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * p.scale_log2;
+      float alpha = 1.f;
+      if (m_tile > m_used + kRescaleThreshold) {
+        alpha = ptx::ex2(m_used - m_tile);  // 0 when m_used = -inf
+        l *= alpha;
+        m_used = m_tile;
+      }
+      const float base = (m_used == -INFINITY) ? 0.f : m_used;
+      float rowsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        s[c] = ptx::ex2(fmaf(s[c], p.scale_log2, -base));
+        rowsum += s[c];
+      }
+      l += rowsum;
+      if (j > 0) {
+        // P buffer and O are still in use by PV(j-1)
+        if (!ptx::mbar_wait(bar(BAR_O), (j - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, 0x700 + j);
+          ok = false;
+        }
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            ptx::tmem_ld32(tO + lane_base + c * 32, o);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] *= alpha;
+            ptx::tmem_st32(tO + lane_base + c * 32, o);
+          }
+        }
+      }
+      // P (bf16) -> shared memory, swizzled K-major
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const float* x = s + ch * 8;
+        ptx::st_shared_v4(sP + sw128_offset(r, ch), ptx::pack_bf16(x[0], x[1]),
+                          ptx::pack_bf16(x[2], x[3]), ptx::pack_bf16(x[4], x[5]),
+                          ptx::pack_bf16(x[6], x[7]));
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(BAR_P));
+    }
+    if (ok && n_tiles > 0) {
+      if (!ptx::mbar_wait(bar(BAR_O), (n_tiles - 1) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x800);
+        ok = false;
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      ptx::tc_fence_after();
+      // ---------------------------------------------------------- epilogue
+      const int64_t g = q_row0 + r;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float lse_t = l > 0.f ? (m_used + ptx::lg2(l)) * kLn2 : -INFINITY;
+      const int64_t row_off = (g * p.Hq + h) * D;
+      const int64_t lse_off = static_cast<int64_t>(h) * p.T_q + g;
+      float w_old = 0.f, w_new = 1.f, lse_out = lse_t;
+      const bool merge = (p.mode == CP_ATTN_ACCUMULATE) && !p.first;
+      float* o_dst = p.o_part;
+      float* lse_dst = p.lse_part;
+      if (p.mode == CP_ATTN_WRITE_PARTIAL) {
+        o_dst += static_cast<int64_t>(w.kv_owner) * p.T_q * p.Hq * D;
+        lse_dst += static_cast<int64_t>(w.kv_owner) * p.Hq * p.T_q;
+      }
+      if (merge) {
+        const float a = lse_dst[lse_off] * kLog2e;
+        const float b = lse_t * kLog2e;
+        const float M = fmaxf(a, b);
+        if (M == -INFINITY) {
+          w_old = 0.f;
+          w_new = 0.f;
+          lse_out = -INFINITY;
+        } else {
+          const float ea = ptx::ex2(a - M), eb = ptx::ex2(b - M);
+          const float sum = ea + eb;
+          w_old = ea / sum;
+          w_new = eb / sum;
+          lse_out = (M + ptx::lg2(sum)) * kLn2;
+        }
+      }
+      lse_dst[lse_off] = lse_out;
+      float4* od = reinterpret_cast<float4*>(o_dst + row_off);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (n_tiles > 0) {
+          ptx::tmem_ld32(tO + lane_base + c * 32, o);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        }
+#pragma unroll
+        for (int x4 = 0; x4 < 8; ++x4) {
+          float4 v;
+          v.x = o[x4 * 4 + 0] * inv_l;
+          v.y = o[x4 * 4 + 1] * inv_l;
+          v.z = o[x4 * 4 + 2] * inv_l;
+          v.w = o[x4 * 4 + 3] * inv_l;
+          if (merge) {
+            const float4 u = od[c * 8 + x4];
+            v.x = u.x * w_old + v.x * w_new;
+            v.y = u.y * w_old + v.y * w_new;
+            v.z = u.z * w_old + v.z * w_new;
+            v.w = u.w * w_old + v.w * w_new;
+          }
+          od[c * 8 + x4] = v;
+          if (p.o_final) {
+            uint2 pk;
+            pk.x = ptx::pack_bf16(v.x, v.y);
+            pk.y = ptx::pack_bf16(v.z, v.w);
+            *reinterpret_cast<uint2*>(p.o_final + row_off + c * 32 + x4 * 4) = pk;
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t step_fwd_smem_bytes(int d) {
+  return d == 128 ? FwdSmem<128>::kAlloc : FwdSmem<64>::kAlloc;
+}
+
+cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const FwdParams& p) {
+  static bool attr_done[2] = {false, false};
+  cudaError_t err;
+  if (d == 128) {
+    if (!attr_done[1]) {
+      err = cudaFuncSetAttribute(step_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+      if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd attr: ") + cudaGetErrorString(err));
+      attr_done[1] = true;
+    }
+    step_fwd_kernel<128><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+  } else {
+    if (!attr_done[0]) {
+      err = cudaFuncSetAttribute(step_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+      if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd attr: ") + cudaGetErrorString(err));
+      attr_done[0] = true;
+    }
+    step_fwd_kernel<64><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+  }
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd launch: ") + cudaGetErrorString(err));
+  count_launch();
+  return CP_ATTN_OK;
+}
+
+}  // namespace cpa

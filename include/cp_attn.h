@@ -1,0 +1,264 @@
+/*
+ * cp_attn.h -- C ABI of the GB300 (sm_103a) context-parallel causal
+ * ring-attention step.
+ *
+ * What it computes. One ring-attention step is block-causal flash attention
+ * of a query chunk against one visiting KV chunk, followed by the
+ * log-sum-exp merge of partial outputs ("Context Parallelism for Scalable
+ * Million-Token Inference", section "Ring Attention Algorithms"; "Announcing
+ * Long-Context Training on TPUs with MaxText Context Parallelism", sections
+ * "Context Parallelism in MaxText" (P2P) and "Built on a fast attention
+ * kernel"). The ring of R context-parallel ranks is emulated on one GPU:
+ * rank r owns rows [r*n, (r+1)*n) of each tensor ("rank-major" order), and
+ * a ring step is one launch that computes every pair (q_owner, kv_owner)
+ * active at that step.
+ *
+ * Conventions (all entry points):
+ *  - Tensors are caller-owned DEVICE memory unless stated otherwise. The
+ *    library never allocates on a compute call; plans allocate their own
+ *    small device tables at creation time.
+ *  - Q, K, V, O, dO are bf16, row-major [tokens, heads, head_dim] with
+ *    head_dim contiguous, in rank-major token order (see
+ *    cp_attn_layout_apply). Base addresses must be 16-byte aligned.
+ *  - LSE and delta are fp32 [heads, tokens] (natural log, softmax scale
+ *    applied). Gradients and fp32 partial outputs are fp32
+ *    [tokens, heads, head_dim].
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Compute calls are asynchronous on that stream; argument errors
+ *    are detected on the host before anything is enqueued.
+ *  - Every call returns a cp_attn_status; on failure cp_attn_last_error()
+ *    returns a thread-local message. Device-side failures (a pipeline wait
+ *    that exceeded its time limit) are recorded in the plan's device status
+ *    word and reported by cp_attn_sync_status().
+ *  - Supported: head_dim 64 or 128; n_q_heads a multiple of n_kv_heads;
+ *    every chunk a multiple of 128 tokens.
+ */
+#ifndef CP_ATTN_H
+#define CP_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cp_attn_status {
+  CP_ATTN_OK = 0,
+  CP_ATTN_ERR_INVALID_ARG = 1, /* null pointer, misaligned pointer, bad enum */
+  CP_ATTN_ERR_SHAPE = 2,       /* sizes that violate the plan's rules */
+  CP_ATTN_ERR_UNSUPPORTED = 3, /* valid but not implemented (e.g. head_dim 96) */
+  CP_ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  CP_ATTN_ERR_OOM = 5,         /* plan table allocation failed */
+  CP_ATTN_ERR_TIMEOUT = 6      /* a kernel pipeline wait ran out of time */
+} cp_attn_status;
+
+/* Chunk layout ("Load Balancing in CP"): ZIGZAG cuts the sequence into 2R
+ * chunks and gives rank r chunks r and 2R-1-r (in that order); CONTIGUOUS
+ * gives rank r the r-th of R equal chunks (no compute balancing). */
+typedef enum cp_attn_layout {
+  CP_ATTN_LAYOUT_CONTIGUOUS = 0,
+  CP_ATTN_LAYOUT_ZIGZAG = 1
+} cp_attn_layout;
+
+/* Ring ordering ("Ring Attention Algorithms"): PASS_KV keeps Q on its rank
+ * and moves KV (at step t rank r holds the KV of rank (r-t) mod R);
+ * PASS_Q keeps KV and moves Q (at step t rank r holds the Q of rank
+ * (r-t) mod R), then returns partial outputs to their owners and merges. */
+typedef enum cp_attn_variant {
+  CP_ATTN_PASS_KV = 0,
+  CP_ATTN_PASS_Q = 1
+} cp_attn_variant;
+
+/* Epilogue of cp_attn_step_fwd.
+ * WRITE_PARTIAL: the partial (O_t, LSE_t) of pair (q_owner, kv_owner) is
+ *   written to slot kv_owner: o_part + kv_owner*T_q*Hq*d and
+ *   lse_part + kv_owner*Hq*T_q, at the q_owner's rows. Rows that see no key
+ *   in this step get O = 0, LSE = -inf. (Storing by kv_owner is the
+ *   permutation back to order that Pass Q needs before its merge.)
+ * ACCUMULATE: the running merge "as it goes" of the P2P ring. o_part is an
+ *   fp32 accumulator [T_q, Hq, d] and lse_part an fp32 [Hq, T_q]
+ *   accumulator; step 0 initialises them, later steps merge into them. */
+typedef enum cp_attn_merge_mode {
+  CP_ATTN_WRITE_PARTIAL = 0,
+  CP_ATTN_ACCUMULATE = 1
+} cp_attn_merge_mode;
+
+typedef enum cp_attn_op {
+  CP_ATTN_OP_FORWARD = 0,
+  CP_ATTN_OP_BACKWARD = 1
+} cp_attn_op;
+
+typedef enum cp_attn_tensor_kind {
+  CP_ATTN_TENSOR_Q = 0,  /* query-side tensors: Q, O, dO, dQ (T_q rows) */
+  CP_ATTN_TENSOR_KV = 1  /* key-side tensors: K, V, dK, dV (T_kv rows) */
+} cp_attn_tensor_kind;
+
+typedef enum cp_attn_direction {
+  CP_ATTN_TO_RANK_MAJOR = 0, /* natural token order -> rank-major order */
+  CP_ATTN_TO_NATURAL = 1     /* rank-major order -> natural token order */
+} cp_attn_direction;
+
+typedef struct cp_attn_plan_s* cp_attn_plan_t;
+
+/* Full description of a plan. Zero-initialise and set the fields. */
+typedef struct cp_attn_plan_desc {
+  int64_t seq_len;        /* new (query) tokens N, > 0 */
+  int64_t kv_prefix_len;  /* cached tokens P before them (partial prefill;
+                             "Attention Compute Patterns in Multi-Turn
+                             Chat"); 0 for full prefill */
+  int cp;                 /* ring size R >= 1 */
+  int n_q_heads;          /* Hq */
+  int n_kv_heads;         /* Hkv; Hq % Hkv == 0; query head h uses KV head
+                             h / (Hq/Hkv) */
+  int head_dim;           /* d: 64 or 128 */
+  cp_attn_layout layout;
+  cp_attn_variant variant;
+  const int32_t* cu_seqlens; /* HOST pointer, n_docs+1 entries, or NULL for
+                                one document. Offsets of packed documents in
+                                natural positions 0..P+N: cu[0] = 0, strictly
+                                increasing, cu[n_docs] = P + N. A key is
+                                visible iff it is in the query's document
+                                and not after it. Copied by the plan. */
+  int n_docs;
+  float softmax_scale;    /* 0 selects 1/sqrt(head_dim) */
+} cp_attn_plan_desc;
+
+/* Build a plan: per-rank positions (zigzag or contiguous), the per-step
+ * (q_owner, kv_owner) schedule, the 128x128 block classes and the per-step
+ * work lists, uploaded to the current CUDA device if there is one (a plan
+ * made without a device serves the host-side queries only).
+ * Chunk rule: zigzag needs N and P to be multiples of 256*R; contiguous
+ * needs multiples of 128*R. Returns ERR_SHAPE otherwise. On success *out
+ * owns host and device tables until cp_attn_plan_destroy. */
+cp_attn_status cp_attn_plan(cp_attn_plan_t* out, int64_t seq_len, int cp,
+                            int n_q_heads, int n_kv_heads, int head_dim,
+                            cp_attn_layout layout, cp_attn_variant variant,
+                            const int32_t* cu_seqlens, int n_docs);
+cp_attn_status cp_attn_plan_ex(cp_attn_plan_t* out, const cp_attn_plan_desc* desc);
+void cp_attn_plan_destroy(cp_attn_plan_t plan);
+
+/* Sizes of a plan, written to info[0..n-1] (n <= 12):
+ * 0 T_q (= R*n_q), 1 T_kv (= R*n_kv), 2 n_q (query rows per rank),
+ * 3 n_kv (KV rows per rank), 4 R, 5 Hq, 6 Hkv, 7 d, 8 q tiles per rank,
+ * 9 kv tiles per rank, 10 n_docs, 11 has device tables (0/1). */
+cp_attn_status cp_attn_plan_info(cp_attn_plan_t plan, int64_t* info, int n);
+
+/* Host queries (bit-exact plan artefacts; no device needed).
+ * positions: global positions of rank `rank`'s query (kind Q, n_q values) or
+ *   KV (kind KV, n_kv values) tokens, in local order, into a host int32 array.
+ * schedule: out[(t*R + r)*2 + {0,1}] = (q_owner, kv_owner) of rank r at
+ *   step t, for the plan's variant.
+ * block_mask: out[((a*R + b)*nqt + i)*nkt + j] = class of q tile i of rank a
+ *   against kv tile j of rank b: 0 EMPTY, 1 PARTIAL, 2 FULL.
+ * visible_pairs: number of visible (query, key) pairs per query head at
+ *   step `step` (or over the whole ring when step == -1). */
+cp_attn_status cp_attn_plan_positions(cp_attn_plan_t plan, cp_attn_tensor_kind kind,
+                                      int rank, int32_t* out);
+cp_attn_status cp_attn_plan_schedule(cp_attn_plan_t plan, int32_t* out);
+cp_attn_status cp_attn_plan_block_mask(cp_attn_plan_t plan, uint8_t* out);
+cp_attn_status cp_attn_plan_visible_pairs(cp_attn_plan_t plan, int step, int64_t* out);
+
+/* Device workspace, in bytes, for cp_attn_forward (op FORWARD: the fp32
+ * running output for Pass KV, or R fp32 partial slots for Pass Q) or
+ * cp_attn_backward (op BACKWARD: the fp32 delta rows). */
+cp_attn_status cp_attn_workspace_size(cp_attn_plan_t plan, cp_attn_op op, size_t* bytes);
+
+/* One forward ring step (kernel K1). For every pair (q_owner, kv_owner) of
+ * step `step` and every query head: S = scale*Q K^T on the visible 128x128
+ * tiles only (fully masked tiles are skipped, partial ones masked), online
+ * softmax, O = P V, then the epilogue of `mode` (see cp_attn_merge_mode).
+ * q: [T_q, Hq, d] bf16; k, v: [T_kv, Hkv, d] bf16.
+ * o_final: optional bf16 [T_q, Hq, d]; when non-NULL in ACCUMULATE mode the
+ *   merged result is also written there in bf16 (use on the last step).
+ * ERR_INVALID_ARG for null/misaligned pointers or a step outside [0, R). */
+cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
+                                const void* q, const void* k, const void* v,
+                                float* o_part, float* lse_part,
+                                cp_attn_merge_mode mode, void* o_final,
+                                void* stream);
+
+/* Backward preprocess (kernel K3): delta[h][t] = sum_d dO[t,h,:]*O[t,h,:]
+ * in fp32, and zeroes the fp32 gradient accumulators dq [T_q,Hq,d],
+ * dk and dv [T_kv,Hkv,d] (any of the three may be NULL to skip). */
+cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t plan, const void* o,
+                                      const void* dout, float* delta,
+                                      float* dq_acc, float* dk_acc, float* dv_acc,
+                                      void* stream);
+
+/* One backward ring step (kernel K2), with the merged (global) lse and
+ * delta: P = exp(scale*Q K^T - LSE) on visible pairs, dV += P^T dO,
+ * dP = dO V^T, dS = P*(dP - delta), dQ += scale*dS K, dK += scale*dS^T Q.
+ * dK and dV are summed over the query heads of each KV head. All three
+ * accumulators are fp32 and are added to (zero them first with
+ * cp_attn_bwd_preprocess). */
+cp_attn_status cp_attn_step_bwd(cp_attn_plan_t plan, int step,
+                                const void* q, const void* k, const void* v,
+                                const void* dout, const float* lse,
+                                const float* delta, float* dq_acc,
+                                float* dk_acc, float* dv_acc, void* stream);
+
+/* LSE merge of n_parts partial results (kernel K4): for each (row, head),
+ * LSE = M + ln sum_i exp(LSE_i - M) with M = max_i LSE_i, and
+ * O = sum_i exp(LSE_i - LSE) * O_i. Parts with LSE_i = -inf weigh 0; a row
+ * whose parts are all -inf gets O = 0, LSE = -inf.
+ * o_parts: fp32, part i at o_parts + i*part_stride, each [rows, heads, d].
+ * lse_parts: fp32, part i at lse_parts + i*lse_part_stride, each
+ *   [heads, rows] (row stride 1, head stride `rows`).
+ * o_out (bf16) and o_out_f32 may each be NULL; lse_out [heads, rows] is
+ * required. head_dim must be a multiple of 4 and at most 256. */
+cp_attn_status cp_attn_merge_lse(int n_parts, int64_t rows, int heads, int head_dim,
+                                 const float* o_parts, int64_t part_stride,
+                                 const float* lse_parts, int64_t lse_part_stride,
+                                 void* o_out, float* o_out_f32, float* lse_out,
+                                 void* stream);
+
+/* Whole forward pass over the emulated ring: R step launches in step
+ * order, then (Pass Q) the n-way merge over kv_owner slots. o: bf16
+ * [T_q,Hq,d]; lse: fp32 [Hq,T_q]. workspace: device buffer of at least
+ * cp_attn_workspace_size(plan, FORWARD) bytes, 256-byte aligned. */
+cp_attn_status cp_attn_forward(cp_attn_plan_t plan, const void* q, const void* k,
+                               const void* v, void* o, float* lse,
+                               void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Whole backward pass: preprocess, then R backward steps in the plan's
+ * ring order. dq: fp32 [T_q,Hq,d]; dk, dv: fp32 [T_kv,Hkv,d] (overwritten).
+ * workspace: at least cp_attn_workspace_size(plan, BACKWARD) bytes. */
+cp_attn_status cp_attn_backward(cp_attn_plan_t plan, const void* q, const void* k,
+                                const void* v, const void* o, const float* lse,
+                                const void* dout, float* dq, float* dk, float* dv,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Reorder a [tokens, row_bytes] tensor between natural token order and the
+ * plan's rank-major order (kernel K5), for the query-side (T_q rows) or the
+ * key-side (T_kv rows) token set. row_bytes = heads*head_dim*element size,
+ * a multiple of 16. `in` and `out` must not overlap. */
+cp_attn_status cp_attn_layout_apply(cp_attn_plan_t plan, cp_attn_tensor_kind kind,
+                                    cp_attn_direction direction, const void* in,
+                                    void* out, int64_t row_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the plan's device status word.
+ * Returns CP_ATTN_OK or the first device-side error (ERR_TIMEOUT). */
+cp_attn_status cp_attn_sync_status(cp_attn_plan_t plan, void* stream);
+
+/* Failure-path self test: launches one CTA whose pipeline wait has nothing
+ * to wait for. After limit_ns nanoseconds (at most 2 s) the wait gives up,
+ * exactly as a stalled wait in K1/K2 would, and records
+ * CP_ATTN_ERR_TIMEOUT in the plan's status word (read and cleared by
+ * cp_attn_sync_status). No fault, trap or hang is involved. */
+cp_attn_status cp_attn_selftest_wait_timeout(cp_attn_plan_t plan, uint64_t limit_ns,
+                                             void* stream);
+
+/* Number of kernel launches the library made in this process so far. */
+int64_t cp_attn_launch_count(void);
+
+const char* cp_attn_last_error(void);
+const char* cp_attn_status_string(cp_attn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CP_ATTN_H */

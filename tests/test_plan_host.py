@@ -1,0 +1,142 @@
+"""Host planner of the C library vs the oracle: bit-exact positions, ring
+schedule, block classes and visible-pair counts; argument validation; the
+exported C ABI. Runs without a GPU (plans built without a device serve the
+host queries)."""
+import re
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import WORKLOADS, cu_seqlens_from_lengths, doc_lengths
+
+cpa = pytest.importorskip("context_causal_attention_ring_gb300")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _plan(N, R, Hq=2, Hkv=1, d=64, layout="zigzag", variant="pass_kv", cu=None, P=0):
+    return cpa.Plan(N, R, Hq, Hkv, d, layout=layout, variant=variant,
+                    cu_seqlens=cu, kv_prefix_len=P)
+
+
+def _check_plan(p, N, R, layout, variant, cu, P, full_mask=True, n_samples=0):
+    q_pos, kv_pos = oracle.plan_positions(N, R, layout, kv_prefix_len=P)
+    for r in range(R):
+        assert np.array_equal(p.positions(cpa.TENSOR_Q, r), q_pos[r])
+        assert np.array_equal(p.positions(cpa.TENSOR_KV, r), kv_pos[r])
+    sched = np.array(oracle.ring_schedule(R, variant), dtype=np.int32)
+    assert np.array_equal(p.schedule(), sched)
+    bm = p.block_mask()
+    if full_mask:
+        assert np.array_equal(bm, oracle.block_mask(q_pos, kv_pos, cu))
+    if n_samples:
+        rng = np.random.default_rng(1)
+        T = oracle.TILE
+        for _ in range(n_samples):
+            a, b = rng.integers(R, size=2)
+            i = rng.integers(p.n_qt)
+            j = rng.integers(p.n_kt)
+            sub = oracle.block_mask([q_pos[a][i * T:(i + 1) * T]],
+                                    [kv_pos[b][j * T:(j + 1) * T]], cu)[0, 0, 0, 0]
+            assert bm[a, b, i, j] == sub, (a, b, i, j)
+    return q_pos, kv_pos, sched
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("variant", ["pass_kv", "pass_q"])
+def test_tiny_ring_plan_bit_exact(layout, variant):
+    w = WORKLOADS["tiny_ring"]
+    p = _plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim, layout, variant)
+    q_pos, kv_pos, sched = _check_plan(p, w.seq_len, w.cp, layout, variant, None, 0)
+    allk = np.concatenate(kv_pos)
+    assert p.visible_pairs() == sum(oracle.count_visible(x, allk) for x in q_pos)
+    for t in range(w.cp):
+        exp = sum(oracle.count_visible(q_pos[qo], kv_pos[ko]) for qo, ko in sched[t])
+        assert p.visible_pairs(t) == exp
+
+
+def test_documents_and_ragged_boundaries_bit_exact():
+    N, R = 4096, 4
+    cu = np.array([0, 1, 130, 1000, 1023, 1024, 2500, 4096], dtype=np.int32)
+    p = _plan(N, R, cu=cu)
+    q_pos, kv_pos, sched = _check_plan(p, N, R, "zigzag", "pass_kv", cu, 0)
+    for t in range(R):
+        exp = sum(oracle.count_visible(q_pos[qo], kv_pos[ko], cu) for qo, ko in sched[t])
+        assert p.visible_pairs(t) == exp
+
+
+@pytest.mark.parametrize("variant", ["pass_kv", "pass_q"])
+def test_partial_prefill_plan_bit_exact(variant):
+    N, P, R = 1024, 3072, 2
+    p = _plan(N, R, variant=variant, P=P)
+    q_pos, kv_pos, sched = _check_plan(p, N, R, "zigzag", variant, None, P)
+    for t in range(R):
+        exp = sum(oracle.count_visible(q_pos[qo], kv_pos[ko]) for qo, ko in sched[t])
+        assert p.visible_pairs(t) == exp
+
+
+def test_llama3_8b_layer_plan_bit_exact():
+    w = WORKLOADS["llama3_8b_layer"]
+    p = _plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    _check_plan(p, w.seq_len, w.cp, "zigzag", "pass_kv", None, 0)
+    assert p.visible_pairs() == w.seq_len * (w.seq_len + 1) // 2
+
+
+def test_partial_prefill_405b_plan_bit_exact():
+    w = WORKLOADS["prefill_405b_partial"]
+    p = _plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim,
+              variant="pass_q", P=w.kv_prefix_len)
+    _check_plan(p, w.seq_len, w.cp, "zigzag", "pass_q", None, w.kv_prefix_len)
+    # every new token sees the whole prefix plus its own causal triangle
+    n, P = w.seq_len, w.kv_prefix_len
+    assert p.visible_pairs() == n * P + n * (n + 1) // 2
+
+
+def test_packed_docs_plan_sampled_tiles():
+    w = WORKLOADS["packed_docs"]
+    cu = cu_seqlens_from_lengths(doc_lengths(w.seq_len))
+    p = _plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim, cu=cu)
+    q_pos, kv_pos, _ = _check_plan(p, w.seq_len, w.cp, "zigzag", "pass_kv", cu, 0,
+                                   full_mask=False, n_samples=400)
+    lens = np.diff(cu.astype(np.int64))
+    assert p.visible_pairs() == int((lens * (lens + 1) // 2).sum())
+
+
+def test_million_token_plan_sampled_tiles():
+    w = WORKLOADS["million_token_group"]
+    p = _plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    _check_plan(p, w.seq_len, w.cp, "zigzag", "pass_kv", None, 0, full_mask=False,
+                n_samples=300)
+    N = w.seq_len
+    assert p.visible_pairs() == N * (N + 1) // 2
+    # zigzag balance: every step has the same number of non-empty tiles per rank
+    bm = p.block_mask()
+    m = p.n_qt // 2
+    counts = (bm > 0).sum(axis=(2, 3))
+    for t in range(1, w.cp, 7):
+        for r in range(w.cp):
+            assert counts[r, (r - t) % w.cp] == 2 * m * m
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=1000, R=4), 2),                      # not a multiple of 2*R*128
+    (dict(N=1024, R=4, Hq=3, Hkv=2), 2),         # Hq % Hkv != 0
+    (dict(N=1024, R=4, d=96), 3),                # head_dim unsupported
+    (dict(N=1024, R=4, cu=[0, 10, 1000]), 2),    # does not end at N
+    (dict(N=1024, R=4, cu=[0, 10, 10, 1024]), 2),  # not strictly increasing
+    (dict(N=1024, R=0), 2),
+])
+def test_plan_rejects_bad_arguments(kw, status):
+    with pytest.raises(cpa.CpAttnError) as e:
+        _plan(**kw)
+    assert e.value.status == status
+
+
+def test_header_declarations_are_exported():
+    hdr = open(os.path.join(ROOT, "include", "cp_attn.h")).read()
+    declared = sorted(set(re.findall(r"\b(cp_attn_[a-z_]+)\s*\(", hdr)))
+    lib = cpa.load()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(cpa.exported_symbols())
