@@ -1,0 +1,386 @@
+"""Benchmark of the context-parallel causal ring-attention step on GB300.
+
+One bench step = one pass of the whole hot path over the workload: the
+emulated ring forward (R step launches with the running LSE merge, the last
+one writing bf16 O) and the ring backward (delta preprocess and R backward
+step launches), on inputs already resident in HBM. The metric is attention
+TFLOPS counting unmasked FLOPs only: forward 4*d*Hq per visible (query, key)
+pair, backward 2.5x that.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (the ring is
+emulated inside one GPU; nothing is exchanged between ranks), timing is
+max-over-ranks and the value is the whole-job FLOP rate ("scaling": "weak").
+``--impl reference`` times the CPU fp64 oracle on a bounded sample of the
+same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, bf16_bits_to_f64, make_inputs  # noqa: E402
+
+METRIC = "causal attn TFLOPS fwd/bwd (unmasked FLOPs) and % of GB300 dense BF16 peak"
+UNIT = "TFLOPS"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx = max(mx, float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, budget_heads: int, inp=None):
+    """Time the fp64 oracle's forward and backward of one off-diagonal ring
+    pair (step 1, rank 1) over `budget_heads` query heads. Returns
+    (TFLOPS, seconds, description)."""
+    import oracle
+    if inp is None:
+        inp = make_inputs(w)
+    q_pos, kv_pos = oracle.plan_positions(w.seq_len, w.cp, w.layout, w.kv_prefix_len)
+    qo, ko = 1 % w.cp, 0
+    H = min(budget_heads, w.n_q_heads)
+    G = w.group
+    Hk = max(1, H // G)
+    qrows = q_pos[qo] - w.kv_prefix_len
+    q = bf16_bits_to_f64(inp.q[qrows][:, :H])
+    k = bf16_bits_to_f64(inp.k[kv_pos[ko]][:, :Hk])
+    v = bf16_bits_to_f64(inp.v[kv_pos[ko]][:, :Hk])
+    do = bf16_bits_to_f64(inp.dout[qrows][:, :H])
+    pairs = oracle.count_visible(q_pos[qo], kv_pos[ko])
+    flops = 4.0 * w.head_dim * H * pairs * (1 + 2.5)
+    t0 = time.perf_counter()
+    O, L = oracle.partial_attention(q, k, v, q_pos[qo], kv_pos[ko])
+    # backward share of the pair with the pair's own softmax (same work)
+    oracle.attention_backward(q, k, v, do, O, L, q_pos[qo], kv_pos[ko])
+    dt = time.perf_counter() - t0
+    desc = (f"oracle fp64 forward+backward of ring pair (q_owner={qo}, kv_owner={ko}) "
+            f"of {w.name}: {len(qrows)} queries x {len(kv_pos[ko])} keys, "
+            f"{H} of {w.n_q_heads} query heads, {pairs} visible pairs per head")
+    return flops / dt / 1e12, dt, desc
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    heads = int(os.environ.get("CP_BENCH_CPU_HEADS", "4"))
+    inp = make_inputs(w)
+    cpu_oracle_sample(w, 1, inp)  # warm-up (page-in, BLAS threads)
+    vals, times = [], []
+    desc = ""
+    for _ in range(args.steps):
+        v, dt, desc = cpu_oracle_sample(w, heads, inp)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.median(times) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "seq_len": w.seq_len, "cp": w.cp,
+                   "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                   "head_dim": w.head_dim, "layout": w.layout, "variant": "pass_kv",
+                   "sample": "one ring pair, subset of heads"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    import context_causal_attention_ring_gb300 as cpa
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    plan = cpa.Plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                    layout=w.layout, variant="pass_kv", kv_prefix_len=w.kv_prefix_len)
+    inp = make_inputs(w)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    qn, kn, vn, don = (dev_bf16(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    q, k, v, do = (torch.empty_like(x) for x in (qn, kn, vn, don))
+    plan.layout_apply(cpa.TENSOR_Q, cpa.TO_RANK_MAJOR, qn, q)
+    plan.layout_apply(cpa.TENSOR_KV, cpa.TO_RANK_MAJOR, kn, k)
+    plan.layout_apply(cpa.TENSOR_KV, cpa.TO_RANK_MAJOR, vn, v)
+    plan.layout_apply(cpa.TENSOR_Q, cpa.TO_RANK_MAJOR, don, do)
+    R, Hq, Hkv, d = plan.R, plan.Hq, plan.Hkv, plan.d
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, plan.T_q), dtype=torch.float32, device=dev)
+    o_acc = torch.empty((plan.T_q, Hq, d), dtype=torch.float32, device=dev)
+    delta = torch.empty((Hq, plan.T_q), dtype=torch.float32, device=dev)
+    half_ops = torch.empty(plan.half_ops_size(), dtype=torch.uint8, device=dev)
+    dq = torch.empty((plan.T_q, Hq, d), dtype=torch.float32, device=dev)
+    dk = torch.empty((plan.T_kv, Hkv, d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+
+    pairs = [plan.visible_pairs(t) for t in range(R)]
+    fwd_flops = 4.0 * d * Hq * sum(pairs)
+    bwd_flops = 2.5 * fwd_flops
+
+    def step(ev=None):
+        # forward: R ring steps, running merge, last step writes bf16 O
+        if ev is not None:
+            ev[0].record(stream)
+        for t in range(R):
+            plan.step_fwd(t, q, k, v, o_acc, lse, cpa.ACCUMULATE,
+                          o if t == R - 1 else None, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        plan.bwd_preprocess(q, k, v, o, do, delta, half_ops, dq, dk, dv, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        for t in range(R):
+            plan.step_bwd(t, half_ops, lse, delta, dq, dk, dv, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    plan.sync_status(stream)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+              for _ in range(args.steps)]
+    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
+        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/cp_clocks.csv")
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = cpa.launch_count()
+    for i in range(args.steps):
+        step(events[i])
+    torch.cuda.synchronize()
+    n_launches = cpa.launch_count() - n_launch0
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    plan.sync_status(stream)
+
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in events]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in events]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in events]
+    step_ms = [e[0].elapsed_time(e[3]) for e in events]
+    total_ms = events[0][0].elapsed_time(events[-1][3])
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * (fwd_flops + bwd_flops) / (ms_per_step * 1e-3) / 1e12
+    fwd_tflops = fwd_flops / (statistics.median(fwd_ms) * 1e-3) / 1e12
+    bwd_tflops = bwd_flops / (statistics.median(bwd_ms) * 1e-3) / 1e12
+
+    peaks, peak_kind = _peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # dominant kernel: the one with more device time per step
+    if sum(bwd_ms) >= sum(fwd_ms):
+        dom, dom_flops, dom_ms = "step_bwd", bwd_flops, sum(bwd_ms) / args.steps
+    else:
+        dom, dom_flops, dom_ms = "step_fwd", fwd_flops, sum(fwd_ms) / args.steps
+    achieved = (dom_flops / R) / (dom_ms / R * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_kind": f"bf16_tflops_sustained ({peak_kind}): timed inside a long loop",
+                "flops_per_launch": dom_flops / R}
+
+    # end to end through the public whole-op calls with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, plan, inp, dev, stream, fwd_flops + bwd_flops, ws)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        heads = int(os.environ.get("CP_BENCH_CPU_HEADS", str(w.n_q_heads)))
+        val, dt, desc = cpu_oracle_sample(w, heads, inp)
+        cpu = {"value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": desc, "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "seq_len": w.seq_len, "cp": w.cp,
+                       "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d,
+                       "layout": w.layout, "variant": "pass_kv", "parallelism": f"replicas{ws}",
+                       "l2": "inputs larger than L2 (Q 256 MiB, dO 256 MiB)",
+                       "flops_per_step": fwd_flops + bwd_flops},
+            "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+            "fwd_ms": statistics.median(fwd_ms), "bwd_ms": statistics.median(bwd_ms),
+            "preprocess_ms": statistics.median(pre_ms),
+            "pct_of_peak_burst": 100.0 * value / ws / peaks["bf16_tflops"],
+            "gpu_launches": n_launches,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, plan, inp, dev, stream, flops, ws):
+    import torch
+    import context_causal_attention_ring_gb300 as cpa
+
+    def pinned(bits):
+        t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    hq, hk, hv, hdo = (pinned(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    d_nat = [torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (hq, hk, hv, hdo)]
+    d_rm = [torch.empty_like(x) for x in d_nat]
+    o = torch.empty_like(d_rm[0])
+    o_nat = torch.empty_like(o)
+    lse = torch.empty((plan.Hq, plan.T_q), dtype=torch.float32, device=dev)
+    dq = torch.empty((plan.T_q, plan.Hq, plan.d), dtype=torch.float32, device=dev)
+    dk = torch.empty((plan.T_kv, plan.Hkv, plan.d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    g_nat = [torch.empty_like(x) for x in (dq, dk, dv)]
+    ws_f = torch.empty(plan.workspace_size(cpa.OP_FORWARD), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(plan.workspace_size(cpa.OP_BACKWARD), dtype=torch.uint8, device=dev)
+    h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o_nat, lse, *g_nat)]
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+    def step():
+        for h, dd in zip((hq, hk, hv, hdo), d_nat):
+            dd.copy_(h, non_blocking=True)
+        kinds = (cpa.TENSOR_Q, cpa.TENSOR_KV, cpa.TENSOR_KV, cpa.TENSOR_Q)
+        for kind, a, b in zip(kinds, d_nat, d_rm):
+            plan.layout_apply(kind, cpa.TO_RANK_MAJOR, a, b, stream=stream)
+        plan.forward(d_rm[0], d_rm[1], d_rm[2], o, lse, ws_f, stream=stream)
+        plan.backward(d_rm[0], d_rm[1], d_rm[2], o, lse, d_rm[3], dq, dk, dv, ws_b,
+                      stream=stream)
+        plan.layout_apply(cpa.TENSOR_Q, cpa.TO_NATURAL, o, o_nat, stream=stream)
+        plan.layout_apply(cpa.TENSOR_Q, cpa.TO_NATURAL, dq, g_nat[0], stream=stream)
+        plan.layout_apply(cpa.TENSOR_KV, cpa.TO_NATURAL, dk, g_nat[1], stream=stream)
+        plan.layout_apply(cpa.TENSOR_KV, cpa.TO_NATURAL, dv, g_nat[2], stream=stream)
+        for h, dd in zip(h_out, (o_nat, lse, *g_nat)):
+            h.copy_(dd, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    plan.sync_status(stream)
+    ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": ws * flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pinned host -> device, layout to rank-major, cp_attn_forward, "
+                    "cp_attn_backward, layout to natural, device -> pinned host"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b_layer", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

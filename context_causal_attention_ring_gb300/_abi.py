@@ -17,7 +17,8 @@ import numpy as np
 from . import build as _build
 
 # enums (match include/cp_attn.h)
-OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT = range(7)
+(OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT,
+ ERR_RANGE) = range(8)
 LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG = 0, 1
 PASS_KV, PASS_Q = 0, 1
 WRITE_PARTIAL, ACCUMULATE = 0, 1
@@ -66,8 +67,9 @@ _SIG = {
     "cp_attn_plan_visible_pairs": (_I, [_P, _I, ctypes.POINTER(_I64)]),
     "cp_attn_workspace_size": (_I, [_P, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "cp_attn_step_fwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _I, _P, _P]),
-    "cp_attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _P, _P, _P, _P]),
-    "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "cp_attn_half_ops_size": (_I, [_P, ctypes.POINTER(ctypes.c_size_t)]),
+    "cp_attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_merge_lse": (_I, [_I, _I64, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "cp_attn_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -115,6 +117,9 @@ def _ptr(x) -> Optional[int]:
     if isinstance(x, int):
         return x
     if hasattr(x, "data_ptr"):
+        if hasattr(x, "is_contiguous") and not x.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous (the C ABI takes "
+                             "dense row-major buffers)")
         return x.data_ptr()
     raise TypeError(f"cannot pass {type(x)} as a device pointer")
 
@@ -222,14 +227,21 @@ class Plan:
                                        _ptr(o_part), _ptr(lse_part), mode, _ptr(o_final),
                                        _stream(stream)))
 
-    def bwd_preprocess(self, o, dout, delta, dq=None, dk=None, dv=None, stream=None):
-        _check(load().cp_attn_bwd_preprocess(self.handle, _ptr(o), _ptr(dout), _ptr(delta),
+    def half_ops_size(self) -> int:
+        out = ctypes.c_size_t()
+        _check(load().cp_attn_half_ops_size(self.handle, ctypes.byref(out)))
+        return int(out.value)
+
+    def bwd_preprocess(self, q, k, v, o, dout, delta, half_ops, dq=None, dk=None, dv=None,
+                       stream=None):
+        _check(load().cp_attn_bwd_preprocess(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                             _ptr(dout), _ptr(delta), _ptr(half_ops),
                                              _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
-    def step_bwd(self, step, q, k, v, dout, lse, delta, dq, dk, dv, stream=None):
-        _check(load().cp_attn_step_bwd(self.handle, step, _ptr(q), _ptr(k), _ptr(v),
-                                       _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dq),
-                                       _ptr(dk), _ptr(dv), _stream(stream)))
+    def step_bwd(self, step, half_ops, lse, delta, dq, dk, dv, stream=None):
+        _check(load().cp_attn_step_bwd(self.handle, step, _ptr(half_ops), _ptr(lse),
+                                       _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv),
+                                       _stream(stream)))
 
     def forward(self, q, k, v, o, lse, workspace, workspace_bytes=None, stream=None):
         if workspace_bytes is None:

@@ -38,7 +38,8 @@ EncodeTiledFn encode_fn() {
 // [rows, heads, d] bf16 viewed as a 3-D tensor (d, heads, rows); boxes of
 // 64 x 1 x 128 elements land in shared memory as 128 rows of 128 bytes with
 // the 128-byte swizzle.
-cp_attn_status tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int d) {
+cp_attn_status tmap_3d(CUtensorMap* m, const void* base, int64_t rows, int heads, int d,
+                       CUtensorMapDataType dtype) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(CP_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
@@ -47,13 +48,35 @@ cp_attn_status tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int hea
                                  static_cast<cuuint64_t>(heads) * d * 2};
   const cuuint32_t box[3] = {64, 1, 128};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  const CUresult r = enc(m, dtype, 3, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(CP_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed with code " + std::to_string(r));
   return CP_ATTN_OK;
+}
+
+cp_attn_status tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int d) {
+  return tmap_3d(m, base, rows, heads, d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Offsets of the fp16 copies of q, k, v, dout inside the half-operand buffer.
+struct HalfOps {
+  size_t q, k, v, dout, total;
+};
+HalfOps half_ops_layout(const cp_attn_plan_s* p) {
+  HalfOps h;
+  const size_t qb = round256(static_cast<size_t>(p->T_q) * p->Hq * p->d * 2);
+  const size_t kb = round256(static_cast<size_t>(p->T_kv) * p->Hkv * p->d * 2);
+  h.q = 0;
+  h.k = qb;
+  h.v = qb + kb;
+  h.dout = qb + 2 * kb;
+  h.total = 2 * qb + 2 * kb;
+  return h;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -151,6 +174,7 @@ const char* cp_attn_status_string(cp_attn_status s) {
     case CP_ATTN_ERR_CUDA: return "CUDA error";
     case CP_ATTN_ERR_OOM: return "out of device memory";
     case CP_ATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    case CP_ATTN_ERR_RANGE: return "input value out of the supported range";
   }
   return "unknown status";
 }
@@ -260,14 +284,21 @@ cp_attn_status cp_attn_workspace_size(cp_attn_plan_t p, cp_attn_op op, size_t* b
   if (!p || !bytes) return fail(CP_ATTN_ERR_INVALID_ARG, "workspace_size: bad arguments");
   const size_t o = static_cast<size_t>(p->T_q) * p->Hq * p->d * sizeof(float);
   const size_t l = static_cast<size_t>(p->T_q) * p->Hq * sizeof(float);
-  auto round = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  auto round = round256;
   if (op == CP_ATTN_OP_FORWARD) {
     *bytes = p->variant == CP_ATTN_PASS_KV ? round(o) : round(o * p->R) + round(l * p->R);
   } else if (op == CP_ATTN_OP_BACKWARD) {
-    *bytes = round(l);
+    *bytes = round(l) + half_ops_layout(p).total;
   } else {
     return fail(CP_ATTN_ERR_INVALID_ARG, "workspace_size: bad op");
   }
+  return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_half_ops_size(cp_attn_plan_t p, size_t* bytes) {
+  clear_error();
+  if (!p || !bytes) return fail(CP_ATTN_ERR_INVALID_ARG, "half_ops_size: bad arguments");
+  *bytes = half_ops_layout(p).total;
   return CP_ATTN_OK;
 }
 
@@ -321,24 +352,27 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const
                          tq, tk, tv, fp);
 }
 
-cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* q, const void* k,
-                                const void* v, const void* dout, const float* lse,
-                                const float* delta, float* dq_acc, float* dk_acc, float* dv_acc,
-                                void* stream) {
+cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops,
+                                const float* lse, const float* delta, float* dq_acc,
+                                float* dk_acc, float* dv_acc, void* stream) {
   clear_error();
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
   if (step < 0 || step >= p->R) return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: step out of range");
-  if (!q || !k || !v || !dout || !lse || !delta || !dq_acc || !dk_acc || !dv_acc)
+  if (!half_ops || !lse || !delta || !dq_acc || !dk_acc || !dv_acc)
     return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: null tensor pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq_acc) ||
+  if ((reinterpret_cast<uintptr_t>(half_ops) & 255u) || !aligned16(dq_acc) ||
       !aligned16(dk_acc) || !aligned16(dv_acc))
-    return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: tensors must be 16-byte aligned");
+    return fail(CP_ATTN_ERR_INVALID_ARG,
+                "step_bwd: half_ops must be 256-byte and accumulators 16-byte aligned");
+  const HalfOps ho = half_ops_layout(p);
+  const char* hb = static_cast<const char*>(half_ops);
   CUtensorMap tq, tk, tv, tdo;
-  if ((st = tmap_bf16(&tq, q, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
-  if ((st = tmap_bf16(&tk, k, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
-  if ((st = tmap_bf16(&tv, v, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
-  if ((st = tmap_bf16(&tdo, dout, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
+  const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if ((st = tmap_3d(&tq, hb + ho.q, p->T_q, p->Hq, p->d, f16)) != CP_ATTN_OK) return st;
+  if ((st = tmap_3d(&tk, hb + ho.k, p->T_kv, p->Hkv, p->d, f16)) != CP_ATTN_OK) return st;
+  if ((st = tmap_3d(&tv, hb + ho.v, p->T_kv, p->Hkv, p->d, f16)) != CP_ATTN_OK) return st;
+  if ((st = tmap_3d(&tdo, hb + ho.dout, p->T_q, p->Hq, p->d, f16)) != CP_ATTN_OK) return st;
   BwdParams bp;
   std::memset(&bp, 0, sizeof(bp));
   bp.items = p->d_bwd + p->bwd_off[step];
@@ -371,23 +405,33 @@ cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* q, const
                          tq, tk, tv, tdo, bp);
 }
 
-cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* o, const void* dout,
-                                      float* delta, float* dq_acc, float* dk_acc, float* dv_acc,
-                                      void* stream) {
+cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* q, const void* k,
+                                      const void* v, const void* o, const void* dout,
+                                      float* delta, void* half_ops, float* dq_acc,
+                                      float* dk_acc, float* dv_acc, void* stream) {
   clear_error();
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
-  if (!o || !dout || !delta) return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: null pointer");
-  if (!aligned16(o) || !aligned16(dout) || (dq_acc && !aligned16(dq_acc)) ||
+  if (!q || !k || !v || !o || !dout || !delta || !half_ops)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      (reinterpret_cast<uintptr_t>(half_ops) & 255u) || (dq_acc && !aligned16(dq_acc)) ||
       (dk_acc && !aligned16(dk_acc)) || (dv_acc && !aligned16(dv_acc)))
-    return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: tensors must be 16-byte aligned");
+    return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: misaligned pointer");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = launch_bwd_preprocess(p->T_q, p->Hq, p->d, static_cast<const __nv_bfloat16*>(o),
                                   static_cast<const __nv_bfloat16*>(dout), delta, s)) != CP_ATTN_OK)
     return st;
-  if (dq_acc && (st = launch_zero_f32(dq_acc, p->T_q * p->Hq * p->d, s)) != CP_ATTN_OK) return st;
-  if (dk_acc && (st = launch_zero_f32(dk_acc, p->T_kv * p->Hkv * p->d, s)) != CP_ATTN_OK) return st;
-  if (dv_acc && (st = launch_zero_f32(dv_acc, p->T_kv * p->Hkv * p->d, s)) != CP_ATTN_OK) return st;
+  const HalfOps ho = half_ops_layout(p);
+  char* hb = static_cast<char*>(half_ops);
+  const int64_t nq = p->T_q * p->Hq * p->d, nk = p->T_kv * p->Hkv * p->d;
+  if ((st = launch_bf16_to_f16(q, hb + ho.q, nq, p->d_status, s)) != CP_ATTN_OK) return st;
+  if ((st = launch_bf16_to_f16(k, hb + ho.k, nk, p->d_status, s)) != CP_ATTN_OK) return st;
+  if ((st = launch_bf16_to_f16(v, hb + ho.v, nk, p->d_status, s)) != CP_ATTN_OK) return st;
+  if ((st = launch_bf16_to_f16(dout, hb + ho.dout, nq, p->d_status, s)) != CP_ATTN_OK) return st;
+  if (dq_acc && (st = launch_zero_f32(dq_acc, nq, s)) != CP_ATTN_OK) return st;
+  if (dk_acc && (st = launch_zero_f32(dk_acc, nk, s)) != CP_ATTN_OK) return st;
+  if (dv_acc && (st = launch_zero_f32(dv_acc, nk, s)) != CP_ATTN_OK) return st;
   return CP_ATTN_OK;
 }
 
@@ -460,9 +504,13 @@ cp_attn_status cp_attn_backward(cp_attn_plan_t p, const void* q, const void* k, 
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(CP_ATTN_ERR_INVALID_ARG, "backward: workspace must be 256-byte aligned");
   float* delta = static_cast<float*>(workspace);
-  if ((st = cp_attn_bwd_preprocess(p, o, dout, delta, dq, dk, dv, stream)) != CP_ATTN_OK) return st;
+  void* half_ops = static_cast<char*>(workspace) +
+                   round256(static_cast<size_t>(p->T_q) * p->Hq * sizeof(float));
+  if ((st = cp_attn_bwd_preprocess(p, q, k, v, o, dout, delta, half_ops, dq, dk, dv, stream)) !=
+      CP_ATTN_OK)
+    return st;
   for (int t = 0; t < p->R; ++t) {
-    st = cp_attn_step_bwd(p, t, q, k, v, dout, lse, delta, dq, dk, dv, stream);
+    st = cp_attn_step_bwd(p, t, half_ops, lse, delta, dq, dk, dv, stream);
     if (st != CP_ATTN_OK) return st;
   }
   return CP_ATTN_OK;

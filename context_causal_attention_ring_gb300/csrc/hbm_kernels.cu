@@ -7,6 +7,7 @@
 //                       in CP": two chunks per rank)
 //   K3 bwd_preprocess-- delta = rowsum(dO * O) for the softmax backward
 //   zero_f32         -- clears fp32 gradient accumulators
+//   bf16_to_f16      -- exact fp16 copies of the backward's bf16 operands
 // All use 16-byte vector accesses with consecutive threads on consecutive
 // addresses.
 #include <cmath>
@@ -144,6 +145,30 @@ __global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ p, i
   if (blockIdx.x == 0 && threadIdx.x < n_tail) tail[threadIdx.x] = 0.f;
 }
 
+// 8 values per thread. bf16 values in [2^-14, 65504] convert exactly; a
+// finite value above 65504 records CP_ATTN_ERR_RANGE in the status word.
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ in,
+                                                          uint4* __restrict__ out, int64_t n8,
+                                                          int32_t* status) {
+  bool bad = false;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 a = __ldg(in + i);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    uint4 r;
+    uint32_t* rr = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(b2[k]);
+      bad |= (fabsf(f.x) > 65504.f && fabsf(f.x) <= 3.4e38f) ||
+             (fabsf(f.y) > 65504.f && fabsf(f.y) <= 3.4e38f);
+      rr[k] = ptx::pack_f16(f.x, f.y);
+    }
+    out[i] = r;
+  }
+  if (bad) atomicCAS(status, 0, static_cast<int>(CP_ATTN_ERR_RANGE));
+}
+
 // One CTA waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up after limit_ns and records the timeout like every kernel wait.
 __global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
@@ -173,6 +198,15 @@ cp_attn_status check_launch(const char* what) {
 }
 
 }  // namespace
+
+cp_attn_status launch_bf16_to_f16(const void* in, void* out, int64_t n, int32_t* status,
+                                  cudaStream_t s) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return CP_ATTN_OK;
+  bf16_to_f16_kernel<<<grid_for(n8, 256, 152 * 16), 256, 0, s>>>(
+      static_cast<const uint4*>(in), static_cast<uint4*>(out), n8, status);
+  return check_launch("bf16_to_f16");
+}
 
 cp_attn_status launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s) {
   selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);

@@ -78,4 +78,8 @@ cp_attn_status launch_zero_f32(float* p, int64_t n, cudaStream_t s);
 
 cp_attn_status launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);
 
+// n = element count, a multiple of 8
+cp_attn_status launch_bf16_to_f16(const void* in, void* out, int64_t n, int32_t* status,
+                                  cudaStream_t s);
+
 }  // namespace cpa

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "../../include/cp_attn.h"
 
@@ -132,16 +133,24 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
+// Instruction descriptor for kind::f16 with fp32 D. `ab_format` is the
+// common type of A and B: 0 = fp16, 1 = bf16 (A and B always share it).
 // a_mn / b_mn select MN-major (1) or K-major (0) operands.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int a_mn, int b_mn,
+                                                    uint32_t ab_format) {
   return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
+         | (ab_format << 7)                         // A format
+         | (ab_format << 10)                        // B format
          | (static_cast<uint32_t>(a_mn) << 15)      // A major
          | (static_cast<uint32_t>(b_mn) << 16)      // B major
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return idesc_f16kind(M, N, a_mn, b_mn, 1u);
+}
+__host__ __device__ constexpr uint32_t idesc_fp16(int M, int N, int a_mn, int b_mn) {
+  return idesc_f16kind(M, N, a_mn, b_mn, 0u);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -206,6 +215,11 @@ __device__ __forceinline__ float lg2(float x) {
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 

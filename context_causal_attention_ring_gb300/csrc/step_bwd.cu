@@ -1,14 +1,408 @@
-// K2: backward ring step (placeholder until the tcgen05 kernel lands).
+// K2: backward ring step on sm_103a (TMA + tcgen05 + TMEM).
+//
+// One CTA owns one 128-key tile of rank kv_owner and one KV head, and loops
+// over the G query heads of that KV head times the run [lo, hi) of visible
+// query tiles of rank q_owner. With the merged (global) LSE and
+// delta = rowsum(dO * O) of each query row, every iteration computes
+//   S^T  = K Q^T                     (keys x queries, TMEM)
+//   dP^T = V dO^T                    (TMEM)
+//   P^T  = exp(scale S^T - LSE)      masked, -> fp16 in shared memory
+//   dS^T = P^T (dP^T - delta)        -> fp16 in shared memory
+//   dV  += P^T dO,  dK += dS^T Q     (TMEM accumulators for the whole CTA)
+//   dQ   = dS K                      (TMEM, then fp32 atomics into dq)
+// so dK and dV are summed over the GQA group inside the CTA and written once
+// per step. The backward pass is called once per ring step like the forward
+// ("Built on a fast attention kernel": P2P runs the kernel per ring step in
+// the forward and backward pass).
+//
+// Warp roles (192 threads): warps 0-3 compute (thread j owns key row j for
+// P/dS and query row j for the dQ read-out), warp 4 TMA producer, warp 5
+// TMEM owner and tcgen05.mma issuer.
+// TMEM columns: S^T [0,128), dP^T and then dQ [128,256), dV [256,256+d),
+// dK [256+d,256+2d).
+// All operands are fp16 (exact copies of the bf16 inputs, and P / dS rounded
+// to fp16): the probabilities keep 11 significant bits instead of 8, which
+// keeps the fp32 gradients within 1e-2 of the exact ones.
+#include <cmath>
+
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace cpa {
+namespace {
 
-size_t step_bwd_smem_bytes(int) { return 0; }
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.44269504088896340736f;
 
-cp_attn_status launch_step_bwd(int, dim3, size_t, cudaStream_t, const CUtensorMap&,
-                               const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                               const BwdParams&) {
-  return fail(CP_ATTN_ERR_UNSUPPORTED, "step_bwd: backward kernel not built yet");
+enum : int {
+  BAR_KV = 0,
+  BAR_QF = 1,  // [2] Q and dO of a stage landed
+  BAR_QE = 3,  // [2] stage free again
+  BAR_S = 5,
+  BAR_DP = 6,
+  BAR_P = 7,       // 128 arrivals: P^T and dS^T written
+  BAR_DQ = 8,      // all MMAs of the iteration done
+  BAR_DQFREE = 9,  // 128 arrivals: dQ read out of TMEM
+  BAR_DRAIN = 10,
+  BAR_ROW = 11,    // 128 arrivals: this iteration's LSE/delta row staged
+  BAR_COUNT = 12
+};
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kStages = D == 128 ? 1 : 2;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;                 // [kStages]
+  static constexpr int kDO = kQ + kStages * kTileBytes;      // [kStages]
+  static constexpr int kPt = kDO + kStages * kTileBytes;     // P^T  [128 keys x 128 q] bf16
+  static constexpr int kDSt = kPt + 128 * 128 * 2;           // dS^T [128 keys x 128 q] bf16
+  static constexpr int kRow = kDSt + 128 * 128 * 2;          // lse2/delta [2][2][128] f32
+  static constexpr int kBar = kRow + 2 * 2 * 128 * 4;
+  static constexpr int kMisc = kBar + BAR_COUNT * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
+};
+
+__device__ __forceinline__ uint32_t sw128_offset(int r, int chunk16) {
+  const int block = chunk16 >> 3;
+  const int c = (chunk16 & 7) ^ (r & 7);
+  return static_cast<uint32_t>(block * 16384 + r * 128 + (c << 4));
+}
+
+// End (exclusive) of the document that contains `pos`: the smallest
+// cu[i] > pos.
+__device__ __forceinline__ int32_t doc_end(const int32_t* __restrict__ cu, int n_cu,
+                                           int32_t pos) {
+  int lo = 0, hi = n_cu - 1;  // cu[lo] <= pos < cu[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) <= pos) lo = mid;
+    else hi = mid;
+  }
+  return __ldg(cu + hi);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    step_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using L = BwdSmem<D>;
+  constexpr int NS = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_u32 + pad;
+  const uint32_t sK = sbase + L::kK;
+  const uint32_t sV = sbase + L::kV;
+  const uint32_t sQ = sbase + L::kQ;
+  const uint32_t sDO = sbase + L::kDO;
+  const uint32_t sPt = sbase + L::kPt;
+  const uint32_t sDSt = sbase + L::kDSt;
+  float* s_row = reinterpret_cast<float*>(smem + L::kRow);  // [buf][0=lse2,1=delta][128]
+  const uint32_t bar0 = sbase + L::kBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x / p.Hkv;
+  const int kh = blockIdx.x % p.Hkv;
+  const WorkItem w = p.items[item];
+  const int n_qtiles = w.hi - w.lo;
+  const int n_iter = n_qtiles * p.G;
+  const int64_t kv_row0 = static_cast<int64_t>(w.kv_owner) * p.n_kv + static_cast<int64_t>(w.tile) * 128;
+  const int32_t kpos0 = __ldg(p.kv_tile_pos + static_cast<int64_t>(w.kv_owner) * p.n_kt + w.tile);
+  const int32_t* q_tile_pos = p.q_tile_pos + static_cast<int64_t>(w.q_owner) * p.n_qt;
+  const int64_t q_row_base = static_cast<int64_t>(w.q_owner) * p.n_q;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < BAR_COUNT; ++i)
+      ptx::mbar_init(bar(i), (i == BAR_P || i == BAR_DQFREE || i == BAR_ROW) ? 128u : 1u);
+    *s_abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tS = tmem;
+  const uint32_t tDP = tmem + 128;  // dP^T, then dQ
+  const uint32_t tDV = tmem + 256;
+  const uint32_t tDK = tmem + 256 + D;
+
+  if (n_iter > 0 && warp == 4 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::prefetch_tmap(&tm_do);
+    ptx::mbar_arrive_expect_tx(bar(BAR_KV), 2 * L::kTileBytes);
+    for (int b = 0; b < D / 64; ++b) {
+      ptx::tma_load_3d(sK + b * 16384, &tm_k, bar(BAR_KV), b * 64, kh, static_cast<int>(kv_row0));
+      ptx::tma_load_3d(sV + b * 16384, &tm_v, bar(BAR_KV), b * 64, kh, static_cast<int>(kv_row0));
+    }
+    int issued = 0;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % NS;
+      if (it >= NS) {
+        if (!ptx::mbar_wait(bar(BAR_QE + s), ((it / NS) - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, 0x1100 + it);
+          break;
+        }
+      }
+      const int h = kh * p.G + it / n_qtiles;
+      const int row = static_cast<int>(q_row_base + static_cast<int64_t>(w.lo + it % n_qtiles) * 128);
+      ptx::mbar_arrive_expect_tx(bar(BAR_QF + s), 2 * L::kTileBytes);
+      for (int b = 0; b < D / 64; ++b) {
+        ptx::tma_load_3d(sQ + s * L::kTileBytes + b * 16384, &tm_q, bar(BAR_QF + s), b * 64, h, row);
+        ptx::tma_load_3d(sDO + s * L::kTileBytes + b * 16384, &tm_do, bar(BAR_QF + s), b * 64, h, row);
+      }
+      issued = it + 1;
+    }
+    const volatile int never = 0;
+    ptx::mbar_wait(bar(BAR_KV), 0, &never, p.wait_limit_ns);
+    for (int it = issued > NS ? issued - NS : 0; it < issued; ++it)
+      ptx::mbar_wait(bar(BAR_QF + it % NS), (it / NS) & 1, &never, p.wait_limit_ns);
+  } else if (n_iter > 0 && warp == 5 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = ptx::idesc_fp16(128, 128, 0, 0);  // K-major A and B
+    constexpr uint32_t idesc_kb = ptx::idesc_fp16(128, D, 0, 1);   // A K-major, B MN-major
+    constexpr uint32_t idesc_q = ptx::idesc_fp16(128, D, 1, 1);    // A and B MN-major
+    bool ok = ptx::mbar_wait(bar(BAR_KV), 0, s_abort, p.wait_limit_ns);
+    if (!ok) ptx::record_timeout(p.status, s_abort, 0x1200);
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int s = it % NS;
+      const uint32_t q_tile = sQ + s * L::kTileBytes;
+      const uint32_t do_tile = sDO + s * L::kTileBytes;
+      if (!ptx::mbar_wait(bar(BAR_QF + s), (it / NS) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x1300 + it);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      // S^T = K Q^T: M = keys, N = queries, K = d; both operands K-major
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::mma_bf16_ss(tS, ptx::sdesc_sw128(sK + off, 16, 1024),
+                         ptx::sdesc_sw128(q_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(BAR_S));
+      if (it > 0) {
+        if (!ptx::mbar_wait(bar(BAR_DQFREE), (it - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, 0x1400 + it);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+      }
+      // dP^T = V dO^T
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::mma_bf16_ss(tDP, ptx::sdesc_sw128(sV + off, 16, 1024),
+                         ptx::sdesc_sw128(do_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(BAR_DP));
+      if (!ptx::mbar_wait(bar(BAR_P), it & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x1500 + it);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      // dV += P^T dO and dK += dS^T Q: M = keys, N = d, K = queries.
+      // A (P^T / dS^T) K-major; B (dO / Q, [queries][d]) MN-major.
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t boff = kk * 2048;
+        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+        ptx::mma_bf16_ss(tDV, ptx::sdesc_sw128(sPt + aoff, 16, 1024),
+                         ptx::sdesc_sw128(do_tile + boff, 16384, 1024), idesc_kb, acc);
+        ptx::mma_bf16_ss(tDK, ptx::sdesc_sw128(sDSt + aoff, 16, 1024),
+                         ptx::sdesc_sw128(q_tile + boff, 16384, 1024), idesc_kb, acc);
+      }
+      ptx::mma_commit(bar(BAR_QE + s));
+      // dQ = dS K: M = queries, N = d, K = keys. A = dS read from dS^T
+      // ([keys][queries]) as MN-major; B = K ([keys][d]) MN-major.
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        ptx::mma_bf16_ss(tDP, ptx::sdesc_sw128(sDSt + kk * 2048, 16384, 1024),
+                         ptx::sdesc_sw128(sK + kk * 2048, 16384, 1024), idesc_q,
+                         kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(BAR_DQ));
+    }
+    ptx::mma_commit(bar(BAR_DRAIN));
+    const volatile int never = 0;
+    ptx::mbar_wait(bar(BAR_DRAIN), 0, &never, p.wait_limit_ns);
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ compute
+    const int j = threadIdx.x;  // key row (P/dS) and query row (dQ read-out)
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int32_t kpos = kpos0 + j;
+    const int32_t dend = doc_end(p.cu, p.n_cu, kpos);
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int h = kh * p.G + it / n_qtiles;
+      const int qt = w.lo + it % n_qtiles;
+      const int64_t q_row0 = q_row_base + static_cast<int64_t>(qt) * 128;
+      const int32_t qpos0 = __ldg(q_tile_pos + qt);
+      float* lse2 = s_row + (it & 1) * 256;
+      float* dlt = lse2 + 128;
+      lse2[j] = __ldg(p.lse + static_cast<int64_t>(h) * p.T_q + q_row0 + j) * kLog2e;
+      dlt[j] = __ldg(p.delta + static_cast<int64_t>(h) * p.T_q + q_row0 + j);
+      // all compute threads staged their entry (bounded wait, no bar.sync,
+      // so an aborting warp can never strand the others)
+      ptx::mbar_arrive(bar(BAR_ROW));
+      if (!ptx::mbar_wait(bar(BAR_ROW), it & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x1800 + it);
+        ok = false;
+      }
+      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ptx::doc_start(p.cu, p.n_cu, qpos0 + 127));
+      const int lo_i = kpos - qpos0;        // first visible query column
+      const int hi_i = dend - 1 - qpos0;    // last visible query column
+      if (!ptx::mbar_wait(bar(BAR_S), it & 1, s_abort, p.wait_limit_ns) ||
+          !ptx::mbar_wait(bar(BAR_DP), it & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x1600 + it);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float sv[32], dp[32];
+        ptx::tmem_ld32(tS + lane_base + c * 32, sv);
+        ptx::tmem_ld32(tDP + lane_base + c * 32, dp);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int i = c * 32 + x;
+          const bool vis = full || (i >= lo_i && i <= hi_i);
+          const float pv = vis ? ptx::ex2(fmaf(sv[x], p.scale_log2, -lse2[i])) : 0.f;
+          sv[x] = pv;
+          dp[x] = pv * (dp[x] - dlt[i]);
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int chunk = c * 4 + ch;
+          const float* a = sv + ch * 8;
+          const float* b = dp + ch * 8;
+          ptx::st_shared_v4(sPt + sw128_offset(j, chunk), ptx::pack_f16(a[0], a[1]),
+                            ptx::pack_f16(a[2], a[3]), ptx::pack_f16(a[4], a[5]),
+                            ptx::pack_f16(a[6], a[7]));
+          ptx::st_shared_v4(sDSt + sw128_offset(j, chunk), ptx::pack_f16(b[0], b[1]),
+                            ptx::pack_f16(b[2], b[3]), ptx::pack_f16(b[4], b[5]),
+                            ptx::pack_f16(b[6], b[7]));
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(BAR_P));
+      if (!ptx::mbar_wait(bar(BAR_DQ), it & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x1700 + it);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ptx::tc_fence_after();
+      // dQ row j of this query tile: scale * (dS K)[j, :], added in fp32
+      float* dq_row = p.dq + ((q_row0 + j) * p.Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float v[32];
+        ptx::tmem_ld32(tDP + lane_base + c * 32, v);
+#pragma unroll
+        for (int x4 = 0; x4 < 8; ++x4) {
+          float4 a = make_float4(v[x4 * 4] * p.scale, v[x4 * 4 + 1] * p.scale,
+                                 v[x4 * 4 + 2] * p.scale, v[x4 * 4 + 3] * p.scale);
+          atomicAdd(reinterpret_cast<float4*>(dq_row + c * 32 + x4 * 4), a);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(BAR_DQFREE));
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && n_iter > 0) {
+      // all MMAs finished (the last BAR_DQ covers them): dK and dV rows
+      float* dk_row = p.dk + ((kv_row0 + j) * p.Hkv + kh) * D;
+      float* dv_row = p.dv + ((kv_row0 + j) * p.Hkv + kh) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float a[32], b[32];
+        ptx::tmem_ld32(tDK + lane_base + c * 32, a);
+        ptx::tmem_ld32(tDV + lane_base + c * 32, b);
+        float4* dk4 = reinterpret_cast<float4*>(dk_row + c * 32);
+        float4* dv4 = reinterpret_cast<float4*>(dv_row + c * 32);
+#pragma unroll
+        for (int x4 = 0; x4 < 8; ++x4) {
+          float4 u = dk4[x4];
+          u.x += a[x4 * 4] * p.scale;
+          u.y += a[x4 * 4 + 1] * p.scale;
+          u.z += a[x4 * 4 + 2] * p.scale;
+          u.w += a[x4 * 4 + 3] * p.scale;
+          dk4[x4] = u;
+          float4 t = dv4[x4];
+          t.x += b[x4 * 4];
+          t.y += b[x4 * 4 + 1];
+          t.z += b[x4 * 4 + 2];
+          t.w += b[x4 * 4 + 3];
+          dv4[x4] = t;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t step_bwd_smem_bytes(int d) {
+  return d == 128 ? BwdSmem<128>::kAlloc : BwdSmem<64>::kAlloc;
+}
+
+cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const CUtensorMap& tdo,
+                               const BwdParams& p) {
+  static bool attr_done[2] = {false, false};
+  cudaError_t err;
+  if (d == 128) {
+    if (!attr_done[1]) {
+      err = cudaFuncSetAttribute(step_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+      if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_bwd attr: ") + cudaGetErrorString(err));
+      attr_done[1] = true;
+    }
+    step_bwd_kernel<128><<<grid, kThreads, smem, s>>>(tq, tk, tv, tdo, p);
+  } else {
+    if (!attr_done[0]) {
+      err = cudaFuncSetAttribute(step_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+      if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_bwd attr: ") + cudaGetErrorString(err));
+      attr_done[0] = true;
+    }
+    step_bwd_kernel<64><<<grid, kThreads, smem, s>>>(tq, tk, tv, tdo, p);
+  }
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_bwd launch: ") + cudaGetErrorString(err));
+  count_launch();
+  return CP_ATTN_OK;
 }
 
 }  // namespace cpa

@@ -50,7 +50,8 @@ typedef enum cp_attn_status {
   CP_ATTN_ERR_UNSUPPORTED = 3, /* valid but not implemented (e.g. head_dim 96) */
   CP_ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
   CP_ATTN_ERR_OOM = 5,         /* plan table allocation failed */
-  CP_ATTN_ERR_TIMEOUT = 6      /* a kernel pipeline wait ran out of time */
+  CP_ATTN_ERR_TIMEOUT = 6,     /* a kernel pipeline wait ran out of time */
+  CP_ATTN_ERR_RANGE = 7        /* an input value outside the supported range */
 } cp_attn_status;
 
 /* Chunk layout ("Load Balancing in CP"): ZIGZAG cuts the sequence into 2R
@@ -161,7 +162,8 @@ cp_attn_status cp_attn_plan_visible_pairs(cp_attn_plan_t plan, int step, int64_t
 
 /* Device workspace, in bytes, for cp_attn_forward (op FORWARD: the fp32
  * running output for Pass KV, or R fp32 partial slots for Pass Q) or
- * cp_attn_backward (op BACKWARD: the fp32 delta rows). */
+ * cp_attn_backward (op BACKWARD: the fp32 delta rows, then the fp16 operand
+ * copies of cp_attn_half_ops_size). */
 cp_attn_status cp_attn_workspace_size(cp_attn_plan_t plan, cp_attn_op op, size_t* bytes);
 
 /* One forward ring step (kernel K1). For every pair (q_owner, kv_owner) of
@@ -178,24 +180,33 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
                                 cp_attn_merge_mode mode, void* o_final,
                                 void* stream);
 
+/* Bytes of the fp16 operand copies used by the backward step: exact IEEE
+ * fp16 copies of q, k, v and dout, in that order, each starting on a
+ * 256-byte boundary. The backward MMAs run on fp16 operands so that the
+ * probabilities P and dS they multiply keep 11 significant bits (bf16 keeps
+ * 8); every bf16 value of magnitude in [2^-14, 65504] converts exactly. */
+cp_attn_status cp_attn_half_ops_size(cp_attn_plan_t plan, size_t* bytes);
+
 /* Backward preprocess (kernel K3): delta[h][t] = sum_d dO[t,h,:]*O[t,h,:]
- * in fp32, and zeroes the fp32 gradient accumulators dq [T_q,Hq,d],
- * dk and dv [T_kv,Hkv,d] (any of the three may be NULL to skip). */
-cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t plan, const void* o,
-                                      const void* dout, float* delta,
-                                      float* dq_acc, float* dk_acc, float* dv_acc,
-                                      void* stream);
+ * in fp32; fp16 copies of q, k, v, dout into `half_ops` (a device buffer of
+ * cp_attn_half_ops_size bytes, 256-byte aligned); zeroes the fp32 gradient
+ * accumulators dq [T_q,Hq,d], dk and dv [T_kv,Hkv,d] (any of the three may
+ * be NULL to skip). A finite input of magnitude above 65504 (not
+ * representable in fp16) sets CP_ATTN_ERR_RANGE in the plan's status word. */
+cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t plan, const void* q, const void* k,
+                                      const void* v, const void* o, const void* dout,
+                                      float* delta, void* half_ops, float* dq_acc,
+                                      float* dk_acc, float* dv_acc, void* stream);
 
 /* One backward ring step (kernel K2), with the merged (global) lse and
  * delta: P = exp(scale*Q K^T - LSE) on visible pairs, dV += P^T dO,
- * dP = dO V^T, dS = P*(dP - delta), dQ += scale*dS K, dK += scale*dS^T Q.
- * dK and dV are summed over the query heads of each KV head. All three
- * accumulators are fp32 and are added to (zero them first with
- * cp_attn_bwd_preprocess). */
-cp_attn_status cp_attn_step_bwd(cp_attn_plan_t plan, int step,
-                                const void* q, const void* k, const void* v,
-                                const void* dout, const float* lse,
-                                const float* delta, float* dq_acc,
+ * dP = dO V^T, dS = P*(dP - delta), dQ += scale*dS K, dK += scale*dS^T Q
+ * ("Built on a fast attention kernel": the ring calls the kernel once per
+ * step in the backward pass too). dK and dV are summed over the query heads
+ * of each KV head. half_ops: the buffer filled by cp_attn_bwd_preprocess.
+ * All three accumulators are fp32 and are added to. */
+cp_attn_status cp_attn_step_bwd(cp_attn_plan_t plan, int step, const void* half_ops,
+                                const float* lse, const float* delta, float* dq_acc,
                                 float* dk_acc, float* dv_acc, void* stream);
 
 /* LSE merge of n_parts partial results (kernel K4): for each (row, head),

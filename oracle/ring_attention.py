@@ -396,12 +396,13 @@ def attention_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens=None,
 
 
 def ring_backward(q, k, v, dout, o, lse, q_pos, kv_pos, cu_seqlens=None,
-                  scale=None, variant: str = "pass_kv"):
+                  scale=None, variant: str = "pass_kv", steps=None):
     """Explicit ring backward: each step adds the share of the pair it holds.
 
     Rank-major inputs as in ``ring_forward``; o and lse are the merged
     forward results. dQ of a pair lands at its q_owner, dK/dV at its
-    kv_owner (in a real ring they travel back with the chunk).
+    kv_owner (in a real ring they travel back with the chunk). ``steps``
+    restricts the sum to those ring steps (default: all of them).
     """
     q, k, v, dout, o, lse = map(_as_f64, (q, k, v, dout, o, lse))
     R = len(q_pos)
@@ -414,6 +415,8 @@ def ring_backward(q, k, v, dout, o, lse, q_pos, kv_pos, cu_seqlens=None,
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     for t, row in enumerate(ring_schedule(R, variant)):
+        if steps is not None and t not in steps:
+            continue
         for qo, ko in row:
             qs = slice(qo * nq, (qo + 1) * nq)
             ks = slice(ko * nk, (ko + 1) * nk)

@@ -1,0 +1,175 @@
+"""GPU parity of the backward path (K3 preprocess, K2 backward step) against
+the fp64 oracle, through the C ABI.
+
+Gradients are produced in fp32 and compared at max-abs 1e-2 (the target's
+output tolerance); delta at 5e-2 (it is a dot product of 128 products with the
+bf16-rounded O). The device backward consumes
+the device forward's bf16 O and fp32 LSE, as a training step would; the
+oracle uses its own fp64 forward.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from workloads import WORKLOADS, Workload, bf16_bits_to_f64, make_inputs, sample_rows
+from gpu_utils import DeviceRun, assert_close, cuda_ok, f32_to_f64
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA GPU")]
+
+if cuda_ok():
+    import torch
+    import context_causal_attention_ring_gb300 as cpa
+
+GRAD_TOL = 1e-2
+
+
+def _plan(w, variant="pass_kv", layout="zigzag", cu=None):
+    return cpa.Plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim, layout=layout,
+                    variant=variant, cu_seqlens=cu, kv_prefix_len=w.kv_prefix_len)
+
+
+def _grads(run):
+    p = run.plan
+    o, lse, _ = run.forward()
+    dq = torch.full((p.T_q, p.Hq, p.d), float("nan"), device="cuda")
+    dk = torch.full((p.T_kv, p.Hkv, p.d), float("nan"), device="cuda")
+    dv = torch.full_like(dk, float("nan"))
+    ws = torch.empty(p.workspace_size(cpa.OP_BACKWARD), dtype=torch.uint8, device="cuda")
+    p.backward(run.q, run.k, run.v, o, lse, run.dout, dq, dk, dv, ws)
+    p.sync_status()
+    return o, lse, dq, dk, dv, ws
+
+
+def _oracle_grads(inp, plan, cu):
+    q, k, v, do = (bf16_bits_to_f64(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    P = plan.kv_prefix_len
+    N = q.shape[0]
+    qp, kp = P + np.arange(N), np.arange(P + N)
+    O, L = oracle.attention(q, k, v, qp, kp, cu)
+    return O, L, oracle.attention_backward(q, k, v, do, O, L, qp, kp, cu)
+
+
+def _check(run, cu, what):
+    _, _, dq, dk, dv, ws = _grads(run)
+    O, L, (dq_r, dk_r, dv_r) = _oracle_grads(run.inp, run.plan, cu)
+    assert_close(run.to_natural_rows(f32_to_f64(dq)), dq_r, GRAD_TOL, what + " dQ")
+    assert_close(run.to_natural_rows(f32_to_f64(dk), "kv"), dk_r, GRAD_TOL, what + " dK")
+    assert_close(run.to_natural_rows(f32_to_f64(dv), "kv"), dv_r, GRAD_TOL, what + " dV")
+    # delta (workspace) against the oracle's rowsum(dO * O)
+    do = bf16_bits_to_f64(run.inp.dout)
+    delta = f32_to_f64(ws[: run.plan.Hq * run.plan.T_q * 4].view(torch.float32)
+                       .view(run.plan.Hq, run.plan.T_q))
+    D_ref = np.einsum("nhd,nhd->hn", do, O)
+    assert_close(run.to_natural_rows(delta, axis=1), D_ref, 5e-2, what + " delta")
+
+
+def test_tiny_ring_backward():
+    w = Workload("tiny_bwd", 1024, 2, 1, 64, 4, backward=True)
+    run = DeviceRun(_plan(w), make_inputs(w))
+    _check(run, None, "tiny")
+
+
+@pytest.mark.parametrize("variant", ["pass_kv", "pass_q"])
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("docs", [False, True])
+def test_backward_variants(variant, layout, docs):
+    w = Workload("bv", 4096, 4, 2, 128, 4, backward=True)
+    cu = np.array([0, 1, 130, 1000, 1023, 1024, 2500, 4096], dtype=np.int32) if docs else None
+    run = DeviceRun(_plan(w, variant, layout, cu), make_inputs(w))
+    _check(run, cu, f"{variant}/{layout}/docs={docs}")
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(64, 8, 1), (128, 8, 2)])
+def test_backward_gqa_groups(d, Hq, Hkv):
+    w = Workload("gqa", 2048, Hq, Hkv, d, 2, backward=True)
+    run = DeviceRun(_plan(w), make_inputs(w))
+    _check(run, None, f"gqa d={d} G={Hq // Hkv}")
+
+
+def test_partial_prefill_backward():
+    w = Workload("ppb", 1024, 8, 2, 128, 2, kv_prefix_len=3072, backward=True)
+    run = DeviceRun(_plan(w, "pass_q"), make_inputs(w))
+    _check(run, None, "partial prefill")
+
+
+def test_single_step_shares():
+    """One backward step adds exactly the oracle's share of that step's pairs
+    (computed with the oracle's O and LSE, uploaded to the device)."""
+    w = Workload("share", 2048, 4, 2, 128, 4, backward=True)
+    inp = make_inputs(w)
+    plan = _plan(w)
+    run = DeviceRun(plan, inp)
+    q, k, v, do = (bf16_bits_to_f64(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    pos = np.arange(w.seq_len)
+    O, L = oracle.attention(q, k, v, pos, pos)
+    qn, kn = run.q_nat, run.kv_nat
+    q_pos = [plan.positions(cpa.TENSOR_Q, r) for r in range(plan.R)]
+    kv_pos = [plan.positions(cpa.TENSOR_KV, r) for r in range(plan.R)]
+    o_dev = torch.from_numpy(O[qn].astype(np.float32)).cuda().to(torch.bfloat16)
+    O_b = o_dev.float().cpu().numpy().astype(np.float64)  # the O the device sees
+    lse_dev = torch.from_numpy(np.ascontiguousarray(L[:, qn], dtype=np.float32)).cuda()
+    delta = torch.empty((plan.Hq, plan.T_q), dtype=torch.float32, device="cuda")
+    half_ops = torch.empty(plan.half_ops_size(), dtype=torch.uint8, device="cuda")
+    for t in (0, 2):
+        dq = torch.empty((plan.T_q, plan.Hq, plan.d), device="cuda")
+        dk = torch.empty((plan.T_kv, plan.Hkv, plan.d), device="cuda")
+        dv = torch.empty_like(dk)
+        plan.bwd_preprocess(run.q, run.k, run.v, o_dev, run.dout, delta, half_ops, dq, dk, dv)
+        plan.step_bwd(t, half_ops, lse_dev, delta, dq, dk, dv)
+        plan.sync_status()
+        r_dq, r_dk, r_dv = oracle.ring_backward(q[qn], k[kn], v[kn], do[qn], O_b, L[:, qn],
+                                                q_pos, kv_pos, steps=[t])
+        msgs = []
+        for name, got, ref in (("dQ", dq, r_dq), ("dK", dk, r_dk), ("dV", dv, r_dv)):
+            g = f32_to_f64(got)
+            err = np.abs(g - ref)
+            if not err.max() <= GRAD_TOL:
+                idx = np.unravel_index(np.nanargmax(err), err.shape)
+                msgs.append(f"{name}: max err {err.max():.3e} at {idx} got {g[idx]:.4f} "
+                            f"want {ref[idx]:.4f}; rows bad {np.unique(np.nonzero(err > GRAD_TOL)[0])[:12]}")
+        assert not msgs, f"step {t}: " + " | ".join(msgs)
+
+
+def test_llama3_8b_layer_backward_sampled():
+    """Full-size backward (bench launch configuration): dQ at sampled rows,
+    dK/dV at the last 128 key positions, and sum_k dK_k = 0 per KV head."""
+    w = WORKLOADS["llama3_8b_layer"]
+    inp = make_inputs(w)
+    plan = _plan(w)
+    run = DeviceRun(plan, inp)
+    _, _, dq, dk, dv, _ = _grads(run)
+    DQ = run.to_natural_rows(f32_to_f64(dq))
+    DK = run.to_natural_rows(f32_to_f64(dk), "kv")
+    DV = run.to_natural_rows(f32_to_f64(dv), "kv")
+    q, k, v, do = (bf16_bits_to_f64(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    pos = np.arange(w.seq_len)
+    rows = sample_rows(w.seq_len, 48)
+    assert_close(DQ[rows], oracle.sampled_dq(q, k, v, do, rows, pos, pos), GRAD_TOL,
+                 "sampled dQ")
+    krows = np.arange(w.seq_len - 128, w.seq_len)
+    dk_r, dv_r = oracle.sampled_dkdv(q, k, v, do, krows, pos, pos)
+    assert_close(DK[krows], dk_r, GRAD_TOL, "last-key dK")
+    assert_close(DV[krows], dv_r, GRAD_TOL, "last-key dV")
+    # dS rows sum to zero: sum over keys of dK vanishes (fp64 sum of fp32)
+    assert np.abs(DK.sum(axis=0)).max() < 0.5
+    assert np.isfinite(DQ).all() and np.isfinite(DK).all() and np.isfinite(DV).all()
+
+
+def test_fp16_range_violation_is_reported():
+    """A finite input above the fp16 range cannot be copied exactly for the
+    fp16 backward MMAs: preprocess flags CP_ATTN_ERR_RANGE."""
+    w = Workload("range", 1024, 2, 1, 64, 4, backward=True)
+    plan = _plan(w)
+    run = DeviceRun(plan, make_inputs(w))
+    k_big = run.k.clone()
+    k_big[5, 0, 3] = 1.0e5
+    o = torch.zeros_like(run.q)
+    delta = torch.empty((plan.Hq, plan.T_q), dtype=torch.float32, device="cuda")
+    half_ops = torch.empty(plan.half_ops_size(), dtype=torch.uint8, device="cuda")
+    plan.bwd_preprocess(run.q, k_big, run.v, o, run.dout, delta, half_ops)
+    with pytest.raises(cpa.CpAttnError) as e:
+        plan.sync_status()
+    assert e.value.status == 7
+    plan.bwd_preprocess(run.q, run.k, run.v, o, run.dout, delta, half_ops)
+    plan.sync_status()

@@ -449,3 +449,17 @@ def test_ring_backward_equals_monolithic(variant, prefix):
     np.testing.assert_allclose(rdq, dq[qperm], atol=1e-12)
     np.testing.assert_allclose(rdk, dk[kperm], atol=1e-12)
     np.testing.assert_allclose(rdv, dv[kperm], atol=1e-12)
+
+
+def test_ring_backward_steps_sum_to_whole():
+    R, n, Hq, Hkv, d = 4, 64, 2, 1, 4
+    q, k, v = rand((n, Hq, d), 50), rand((n, Hkv, d), 51), rand((n, Hkv, d), 52)
+    do = rand((n, Hq, d), 53)
+    q_pos, kv_pos = oracle.plan_positions(n, R, "zigzag")
+    perm = np.concatenate(q_pos)
+    O, L = oracle.attention(q, k, v, np.arange(n), np.arange(n))
+    args = (q[perm], k[perm], v[perm], do[perm], O[perm], L[:, perm], q_pos, kv_pos)
+    whole = oracle.ring_backward(*args)
+    parts = [oracle.ring_backward(*args, steps=[t]) for t in range(R)]
+    for i in range(3):
+        np.testing.assert_allclose(sum(p[i] for p in parts), whole[i], atol=1e-13)
