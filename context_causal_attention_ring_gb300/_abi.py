@@ -72,6 +72,8 @@ _SIG = {
     "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_merge_lse": (_I, [_I, _I64, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "cp_attn_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "cp_attn_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P]),
+    "cp_attn_forward_noalloc_capacity": (ctypes.c_size_t, []),
     "cp_attn_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                               ctypes.c_size_t, _P]),
     "cp_attn_layout_apply": (_I, [_P, _I, _I, _P, _P, _I64, _P]),

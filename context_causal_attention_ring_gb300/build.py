@@ -19,7 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libcp_attn.so")
 STAMP = os.path.join(BUILD, "stamp.txt")
 
-SOURCES = ["api.cu", "plan.cpp", "step_fwd.cu", "step_bwd.cu", "hbm_kernels.cu"]
+SOURCES = ["api.cu", "plan.cpp", "step_fwd.cu", "step_bwd.cu", "hbm_kernels.cu",
+           "noalloc.cu"]
 HEADERS = ["internal.h", "kernels.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

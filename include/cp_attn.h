@@ -233,6 +233,28 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t plan, const void* q, const void* k
                                void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Forward pass that allocates nothing (no counterpart on the pages; a
+ * convenience of this library). For callers that cannot call cudaMalloc --
+ * a plugin inside a host program that owns the whole device-memory pool and
+ * gives plugins no allocator, or a serving path that must never enter the
+ * allocator -- and so cannot pass the forward workspace. Same result as
+ * cp_attn_forward; the workspace comes from a fixed device array inside the
+ * library of cp_attn_forward_noalloc_capacity() bytes (32 MiB), which every
+ * GPU that loads the library keeps until the process exits.
+ *  - Plans whose forward workspace (cp_attn_workspace_size, FORWARD) exceeds
+ *    the capacity are rejected with CP_ATTN_ERR_SHAPE before any launch.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress); make that first call before
+ *    any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents
+ *    (nothing in it needs to start at zero). Calls that overlap on the GPU
+ *    (on different streams, or from different threads) race on it: order
+ *    them on one stream.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine. */
+cp_attn_status cp_attn_forward_noalloc(cp_attn_plan_t plan, const void* q, const void* k,
+                                       const void* v, void* o, float* lse, void* stream);
+size_t cp_attn_forward_noalloc_capacity(void);
+
 /* Whole backward pass: preprocess, then R backward steps in the plan's
  * ring order. dq: fp32 [T_q,Hq,d]; dk, dv: fp32 [T_kv,Hkv,d] (overwritten).
  * workspace: at least cp_attn_workspace_size(plan, BACKWARD) bytes. */
