@@ -374,8 +374,18 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_layer", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--q-heads", type=int, default=0,
+                    help="profiling aid: override the workload's query heads")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="profiling aid: override the workload's KV heads")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
+    if args.q_heads or args.kv_heads:
+        import dataclasses
+        w = dataclasses.replace(w, n_q_heads=args.q_heads or w.n_q_heads,
+                                n_kv_heads=args.kv_heads or w.n_kv_heads,
+                                name=w.name + f"_h{args.q_heads or w.n_q_heads}"
+                                     f"kv{args.kv_heads or w.n_kv_heads}")
     if args.impl == "reference":
         run_reference(args, w)
     else:
