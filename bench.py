@@ -211,7 +211,8 @@ def run_ours(args, w):
                           o if t == R - 1 else None, stream)
         if ev is not None:
             ev[1].record(stream)
-        plan.bwd_preprocess(q, k, v, o, do, delta, half_ops, dq, dk, dv, stream)
+        plan.bwd_preprocess(q, k, v, o, do, delta, half_ops, dq, dk, dv, o_f32=o_acc,
+                            stream=stream)
         if ev is not None:
             ev[2].record(stream)
         for t in range(R):
@@ -334,7 +335,7 @@ def run_e2e(args, plan, inp, dev, stream, flops, ws):
             plan.layout_apply(kind, cpa.TO_RANK_MAJOR, a, b, stream=stream)
         plan.forward(d_rm[0], d_rm[1], d_rm[2], o, lse, ws_f, stream=stream)
         plan.backward(d_rm[0], d_rm[1], d_rm[2], o, lse, d_rm[3], dq, dk, dv, ws_b,
-                      stream=stream)
+                      o_f32=ws_f, stream=stream)
         plan.layout_apply(cpa.TENSOR_Q, cpa.TO_NATURAL, o, o_nat, stream=stream)
         plan.layout_apply(cpa.TENSOR_Q, cpa.TO_NATURAL, dq, g_nat[0], stream=stream)
         plan.layout_apply(cpa.TENSOR_KV, cpa.TO_NATURAL, dk, g_nat[1], stream=stream)

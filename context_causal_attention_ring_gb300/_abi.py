@@ -68,13 +68,13 @@ _SIG = {
     "cp_attn_workspace_size": (_I, [_P, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "cp_attn_step_fwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _I, _P, _P]),
     "cp_attn_half_ops_size": (_I, [_P, ctypes.POINTER(ctypes.c_size_t)]),
-    "cp_attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "cp_attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_merge_lse": (_I, [_I, _I64, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "cp_attn_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_forward_noalloc_capacity": (ctypes.c_size_t, []),
-    "cp_attn_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+    "cp_attn_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                               ctypes.c_size_t, _P]),
     "cp_attn_layout_apply": (_I, [_P, _I, _I, _P, _P, _I64, _P]),
     "cp_attn_sync_status": (_I, [_P, _P]),
@@ -235,10 +235,11 @@ class Plan:
         return int(out.value)
 
     def bwd_preprocess(self, q, k, v, o, dout, delta, half_ops, dq=None, dk=None, dv=None,
-                       stream=None):
+                       o_f32=None, stream=None):
         _check(load().cp_attn_bwd_preprocess(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
-                                             _ptr(dout), _ptr(delta), _ptr(half_ops),
-                                             _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
+                                             _ptr(o_f32), _ptr(dout), _ptr(delta),
+                                             _ptr(half_ops), _ptr(dq), _ptr(dk), _ptr(dv),
+                                             _stream(stream)))
 
     def step_bwd(self, step, half_ops, lse, delta, dq, dk, dv, stream=None):
         _check(load().cp_attn_step_bwd(self.handle, step, _ptr(half_ops), _ptr(lse),
@@ -253,12 +254,12 @@ class Plan:
                                       _stream(stream)))
 
     def backward(self, q, k, v, o, lse, dout, dq, dk, dv, workspace,
-                 workspace_bytes=None, stream=None):
+                 workspace_bytes=None, o_f32=None, stream=None):
         if workspace_bytes is None:
             workspace_bytes = workspace.numel() * workspace.element_size()
         _check(load().cp_attn_backward(self.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
-                                       _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                                       _ptr(workspace), int(workspace_bytes),
+                                       _ptr(o_f32), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                       _ptr(dv), _ptr(workspace), int(workspace_bytes),
                                        _stream(stream)))
 
     def layout_apply(self, kind, direction, x_in, x_out, row_bytes=None, stream=None):

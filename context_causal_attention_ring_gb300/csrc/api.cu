@@ -406,21 +406,24 @@ cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops
 }
 
 cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* q, const void* k,
-                                      const void* v, const void* o, const void* dout,
-                                      float* delta, void* half_ops, float* dq_acc,
-                                      float* dk_acc, float* dv_acc, void* stream) {
+                                      const void* v, const void* o, const float* o_f32,
+                                      const void* dout, float* delta, void* half_ops,
+                                      float* dq_acc, float* dk_acc, float* dv_acc,
+                                      void* stream) {
   clear_error();
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
-  if (!q || !k || !v || !o || !dout || !delta || !half_ops)
+  if (!q || !k || !v || (!o && !o_f32) || !dout || !delta || !half_ops)
     return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: null pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (o && !aligned16(o)) ||
+      (o_f32 && !aligned16(o_f32)) || !aligned16(dout) ||
       (reinterpret_cast<uintptr_t>(half_ops) & 255u) || (dq_acc && !aligned16(dq_acc)) ||
       (dk_acc && !aligned16(dk_acc)) || (dv_acc && !aligned16(dv_acc)))
     return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: misaligned pointer");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = launch_bwd_preprocess(p->T_q, p->Hq, p->d, static_cast<const __nv_bfloat16*>(o),
-                                  static_cast<const __nv_bfloat16*>(dout), delta, s)) != CP_ATTN_OK)
+                                  o_f32, static_cast<const __nv_bfloat16*>(dout), delta, s)) !=
+      CP_ATTN_OK)
     return st;
   const HalfOps ho = half_ops_layout(p);
   char* hb = static_cast<char*>(half_ops);
@@ -486,14 +489,16 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, c
     st = cp_attn_step_fwd(p, t, q, k, v, ws, ws_lse, CP_ATTN_WRITE_PARTIAL, nullptr, stream);
     if (st != CP_ATTN_OK) return st;
   }
-  return cp_attn_merge_lse(p->R, p->T_q, p->Hq, p->d, ws, o_slot, ws_lse, l_slot, o, nullptr, lse,
+  // The merge also leaves the fp32 result in slot 0 (each (row, head) is read
+  // completely by one warp before that warp writes it).
+  return cp_attn_merge_lse(p->R, p->T_q, p->Hq, p->d, ws, o_slot, ws_lse, l_slot, o, ws, lse,
                            stream);
 }
 
 cp_attn_status cp_attn_backward(cp_attn_plan_t p, const void* q, const void* k, const void* v,
-                                const void* o, const float* lse, const void* dout, float* dq,
-                                float* dk, float* dv, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+                                const void* o, const float* o_f32, const float* lse,
+                                const void* dout, float* dq, float* dk, float* dv,
+                                void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
@@ -506,7 +511,8 @@ cp_attn_status cp_attn_backward(cp_attn_plan_t p, const void* q, const void* k, 
   float* delta = static_cast<float*>(workspace);
   void* half_ops = static_cast<char*>(workspace) +
                    round256(static_cast<size_t>(p->T_q) * p->Hq * sizeof(float));
-  if ((st = cp_attn_bwd_preprocess(p, q, k, v, o, dout, delta, half_ops, dq, dk, dv, stream)) !=
+  if ((st = cp_attn_bwd_preprocess(p, q, k, v, o, o_f32, dout, delta, half_ops, dq, dk, dv,
+                                   stream)) !=
       CP_ATTN_OK)
     return st;
   for (int t = 0; t < p->R; ++t) {

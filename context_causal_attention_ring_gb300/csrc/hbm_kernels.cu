@@ -107,9 +107,10 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
 }
 
 // delta[h][t] = sum_x dO[t,h,x] * O[t,h,x], one warp per (t, h); lanes read
-// 8-byte (4 x bf16) pieces.
+// 4 elements at a time. O is bf16 or fp32.
+template <typename OT>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(int64_t rows, int heads, int d,
-                                                             const __nv_bfloat16* __restrict__ o,
+                                                             const OT* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              float* __restrict__ delta) {
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -120,17 +121,23 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(int64_t rows, int h
   const int64_t off = wid * d;  // (t*heads + h)*d
   float acc = 0.f;
   for (int x = lane * 4; x < d; x += 128) {
-    const uint2 a = __ldg(reinterpret_cast<const uint2*>(o + off + x));
-    const uint2 b = __ldg(reinterpret_cast<const uint2*>(dout + off + x));
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float2 fa = __bfloat1622float2(a2[k]);
-      const float2 fb = __bfloat1622float2(b2[k]);
-      acc = fmaf(fa.x, fb.x, acc);
-      acc = fmaf(fa.y, fb.y, acc);
+    float fo[4];
+    if constexpr (sizeof(OT) == 4) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(o + off + x));
+      fo[0] = a.x; fo[1] = a.y; fo[2] = a.z; fo[3] = a.w;
+    } else {
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(o + off + x));
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const float2 f0 = __bfloat1622float2(a2[0]), f1 = __bfloat1622float2(a2[1]);
+      fo[0] = f0.x; fo[1] = f0.y; fo[2] = f1.x; fo[3] = f1.y;
     }
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(dout + off + x));
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const float2 g0 = __bfloat1622float2(b2[0]), g1 = __bfloat1622float2(b2[1]);
+    acc = fmaf(fo[0], g0.x, acc);
+    acc = fmaf(fo[1], g0.y, acc);
+    acc = fmaf(fo[2], g1.x, acc);
+    acc = fmaf(fo[3], g1.y, acc);
   }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
@@ -242,12 +249,17 @@ cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t
 }
 
 cp_attn_status launch_bwd_preprocess(int64_t rows, int heads, int d, const __nv_bfloat16* o,
-                                     const __nv_bfloat16* dout, float* delta, cudaStream_t s) {
+                                     const float* o_f32, const __nv_bfloat16* dout,
+                                     float* delta, cudaStream_t s) {
   const int64_t warps = rows * heads;
   if (warps == 0) return CP_ATTN_OK;
   const int64_t blocks = (warps * 32 + 255) / 256;
-  bwd_preprocess_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(rows, heads, d, o, dout,
-                                                                      delta);
+  if (o_f32)
+    bwd_preprocess_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, s>>>(rows, heads, d,
+                                                                               o_f32, dout, delta);
+  else
+    bwd_preprocess_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        rows, heads, d, o, dout, delta);
   return check_launch("bwd_preprocess");
 }
 

@@ -71,8 +71,10 @@ cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
 cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t row_bytes,
                                    int to_natural, const void* in, void* out, cudaStream_t s);
 
+// O from o_f32 when it is not null, else from the bf16 o.
 cp_attn_status launch_bwd_preprocess(int64_t rows, int heads, int d, const __nv_bfloat16* o,
-                                     const __nv_bfloat16* dout, float* delta, cudaStream_t s);
+                                     const float* o_f32, const __nv_bfloat16* dout,
+                                     float* delta, cudaStream_t s);
 
 cp_attn_status launch_zero_f32(float* p, int64_t n, cudaStream_t s);
 

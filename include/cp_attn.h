@@ -188,15 +188,20 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
 cp_attn_status cp_attn_half_ops_size(cp_attn_plan_t plan, size_t* bytes);
 
 /* Backward preprocess (kernel K3): delta[h][t] = sum_d dO[t,h,:]*O[t,h,:]
- * in fp32; fp16 copies of q, k, v, dout into `half_ops` (a device buffer of
- * cp_attn_half_ops_size bytes, 256-byte aligned); zeroes the fp32 gradient
- * accumulators dq [T_q,Hq,d], dk and dv [T_kv,Hkv,d] (any of the three may
- * be NULL to skip). A finite input of magnitude above 65504 (not
- * representable in fp16) sets CP_ATTN_ERR_RANGE in the plan's status word. */
+ * in fp32, taking O from o_f32 (fp32 [T_q,Hq,d], e.g. the fp32 output that
+ * cp_attn_forward leaves at the start of its workspace) when it is not NULL,
+ * else from the bf16 o; fp16 copies of q, k, v, dout into `half_ops` (a
+ * device buffer of cp_attn_half_ops_size bytes, 256-byte aligned); zeroes the
+ * fp32 gradient accumulators dq [T_q,Hq,d], dk and dv [T_kv,Hkv,d] (any of
+ * the three may be NULL to skip). A finite input of magnitude above 65504
+ * (not representable in fp16) sets CP_ATTN_ERR_RANGE in the plan's status
+ * word. Using the fp32 O keeps the bf16 rounding of O out of delta (it
+ * otherwise moves dQ and dK by up to ~6e-3 on N(0,1) inputs). */
 cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t plan, const void* q, const void* k,
-                                      const void* v, const void* o, const void* dout,
-                                      float* delta, void* half_ops, float* dq_acc,
-                                      float* dk_acc, float* dv_acc, void* stream);
+                                      const void* v, const void* o, const float* o_f32,
+                                      const void* dout, float* delta, void* half_ops,
+                                      float* dq_acc, float* dk_acc, float* dv_acc,
+                                      void* stream);
 
 /* One backward ring step (kernel K2), with the merged (global) lse and
  * delta: P = exp(scale*Q K^T - LSE) on visible pairs, dV += P^T dO,
@@ -227,7 +232,9 @@ cp_attn_status cp_attn_merge_lse(int n_parts, int64_t rows, int heads, int head_
 /* Whole forward pass over the emulated ring: R step launches in step
  * order, then (Pass Q) the n-way merge over kv_owner slots. o: bf16
  * [T_q,Hq,d]; lse: fp32 [Hq,T_q]. workspace: device buffer of at least
- * cp_attn_workspace_size(plan, FORWARD) bytes, 256-byte aligned. */
+ * cp_attn_workspace_size(plan, FORWARD) bytes, 256-byte aligned. On return
+ * the workspace starts with O in fp32 [T_q,Hq,d] (the unrounded result),
+ * which cp_attn_backward can take as o_f32. */
 cp_attn_status cp_attn_forward(cp_attn_plan_t plan, const void* q, const void* k,
                                const void* v, void* o, float* lse,
                                void* workspace, size_t workspace_bytes,
@@ -256,12 +263,14 @@ cp_attn_status cp_attn_forward_noalloc(cp_attn_plan_t plan, const void* q, const
 size_t cp_attn_forward_noalloc_capacity(void);
 
 /* Whole backward pass: preprocess, then R backward steps in the plan's
- * ring order. dq: fp32 [T_q,Hq,d]; dk, dv: fp32 [T_kv,Hkv,d] (overwritten).
- * workspace: at least cp_attn_workspace_size(plan, BACKWARD) bytes. */
+ * ring order. o: bf16 [T_q,Hq,d]; o_f32: optional fp32 O used for delta
+ * (see cp_attn_bwd_preprocess); dq: fp32 [T_q,Hq,d]; dk, dv: fp32
+ * [T_kv,Hkv,d] (overwritten). workspace: at least
+ * cp_attn_workspace_size(plan, BACKWARD) bytes, 256-byte aligned. */
 cp_attn_status cp_attn_backward(cp_attn_plan_t plan, const void* q, const void* k,
-                                const void* v, const void* o, const float* lse,
-                                const void* dout, float* dq, float* dk, float* dv,
-                                void* workspace, size_t workspace_bytes,
+                                const void* v, const void* o, const float* o_f32,
+                                const float* lse, const void* dout, float* dq, float* dk,
+                                float* dv, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
 /* Reorder a [tokens, row_bytes] tensor between natural token order and the

@@ -89,6 +89,22 @@ class DeviceRun:
         p.sync_status()
         return o, lse, ws
 
+    def take_index(self, nat_rows, kind="q") -> np.ndarray:
+        """Rank-major row index of each natural row."""
+        nat = self.q_nat if kind == "q" else self.kv_nat
+        inv = np.empty_like(nat)
+        inv[nat] = np.arange(len(nat))
+        return inv[np.asarray(nat_rows)].astype(np.int64)
+
+    def take(self, t, nat_rows, kind="q", axis=0) -> np.ndarray:
+        """Rows (natural indices) of a rank-major device tensor, gathered on
+        the device and returned as fp64 host data."""
+        idx = torch.from_numpy(self.take_index(nat_rows, kind)).to(t.device)
+        g = torch.index_select(t, axis, idx)
+        if g.dtype == torch.bfloat16:
+            return bf16_to_f64(g.contiguous())
+        return g.double().cpu().numpy()
+
     def to_natural_rows(self, x_rm: np.ndarray, kind="q", axis=0):
         """Reorder a host array from rank-major rows to natural rows."""
         nat = self.q_nat if kind == "q" else self.kv_nat
