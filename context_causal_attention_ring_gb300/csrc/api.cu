@@ -39,14 +39,14 @@ EncodeTiledFn encode_fn() {
 // 64 x 1 x 128 elements land in shared memory as 128 rows of 128 bytes with
 // the 128-byte swizzle.
 cp_attn_status tmap_3d(CUtensorMap* m, const void* base, int64_t rows, int heads, int d,
-                       CUtensorMapDataType dtype) {
+                       CUtensorMapDataType dtype, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(CP_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(heads) * d * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(m, dtype, 3, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -369,10 +369,11 @@ cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops
   const char* hb = static_cast<const char*>(half_ops);
   CUtensorMap tq, tk, tv, tdo;
   const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if ((st = tmap_3d(&tq, hb + ho.q, p->T_q, p->Hq, p->d, f16)) != CP_ATTN_OK) return st;
+  const int qbox = step_bwd_q_box_rows(p->d);
+  if ((st = tmap_3d(&tq, hb + ho.q, p->T_q, p->Hq, p->d, f16, qbox)) != CP_ATTN_OK) return st;
   if ((st = tmap_3d(&tk, hb + ho.k, p->T_kv, p->Hkv, p->d, f16)) != CP_ATTN_OK) return st;
   if ((st = tmap_3d(&tv, hb + ho.v, p->T_kv, p->Hkv, p->d, f16)) != CP_ATTN_OK) return st;
-  if ((st = tmap_3d(&tdo, hb + ho.dout, p->T_q, p->Hq, p->d, f16)) != CP_ATTN_OK) return st;
+  if ((st = tmap_3d(&tdo, hb + ho.dout, p->T_q, p->Hq, p->d, f16, qbox)) != CP_ATTN_OK) return st;
   BwdParams bp;
   std::memset(&bp, 0, sizeof(bp));
   bp.items = p->d_bwd + p->bwd_off[step];

@@ -61,6 +61,8 @@ cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tv, const CUtensorMap& tdo,
                                const BwdParams& p);
 size_t step_bwd_smem_bytes(int d);
+// Rows of the Q / dO tensor-map box the backward kernel for head_dim d uses.
+int step_bwd_q_box_rows(int d);
 
 cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
                                 const float* o_parts, int64_t part_stride,

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_bf16_ss(tS, ptx::sdesc_sw128(sK + off, 16, 1024),
+        ptx::mma_ss(tS, ptx::sdesc_sw128(sK + off, 16, 1024),
                          ptx::sdesc_sw128(q_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
       }
       ptx::mma_commit(bar(BAR_S));
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_bf16_ss(tDP, ptx::sdesc_sw128(sV + off, 16, 1024),
+        ptx::mma_ss(tDP, ptx::sdesc_sw128(sV + off, 16, 1024),
                          ptx::sdesc_sw128(do_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
       }
       ptx::mma_commit(bar(BAR_DP));
@@ -227,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
         const uint32_t boff = kk * 2048;
         const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-        ptx::mma_bf16_ss(tDV, ptx::sdesc_sw128(sPt + aoff, 16, 1024),
+        ptx::mma_ss(tDV, ptx::sdesc_sw128(sPt + aoff, 16, 1024),
                          ptx::sdesc_sw128(do_tile + boff, 16384, 1024), idesc_kb, acc);
-        ptx::mma_bf16_ss(tDK, ptx::sdesc_sw128(sDSt + aoff, 16, 1024),
+        ptx::mma_ss(tDK, ptx::sdesc_sw128(sDSt + aoff, 16, 1024),
                          ptx::sdesc_sw128(q_tile + boff, 16384, 1024), idesc_kb, acc);
       }
       ptx::mma_commit(bar(BAR_QE + s));
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ([keys][queries]) as MN-major; B = K ([keys][d]) MN-major.
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        ptx::mma_bf16_ss(tDP, ptx::sdesc_sw128(sDSt + kk * 2048, 16384, 1024),
+        ptx::mma_ss(tDP, ptx::sdesc_sw128(sDSt + kk * 2048, 16384, 1024),
                          ptx::sdesc_sw128(sK + kk * 2048, 16384, 1024), idesc_q,
                          kk > 0 ? 1u : 0u);
       }
@@ -370,11 +370,364 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ===========================================================================
+// d = 128: pipelined variant with 64-row query sub-tiles.
+//
+// Per iteration (one 64-row query sub-tile of one head of the group):
+//   S^T  = K Q^T    (M = 128 keys, N = 64)   TMEM buffer b = it & 1
+//   dP^T = V dO^T   (M = 128 keys, N = 64)   TMEM buffer b
+//   P^T, dS^T (fp16) -> shared-memory buffer b   by compute warpgroup b
+//   dV += P^T dO,  dK += dS^T Q              (M = 128 keys, N = 128, K = 64)
+//   dQ^T = K^T dS^T (M = 128 = d, N = 64)   TMEM, in buffer b's S^T columns
+// Two compute warpgroups take alternate iterations, so one warpgroup's
+// exponentials and its dQ read-out overlap the other's MMAs, and both TMEM
+// buffers and both shared-memory buffers alternate with them. dQ comes out
+// transposed (TMEM lane = column of d), so each warp's fp32 reduction into
+// dq covers 32 consecutive floats of one query row: one 128-byte line per
+// instruction.
+// Warps: 0-3 compute warpgroup 0, 4-7 compute warpgroup 1, 8 TMA producer,
+// 9 TMEM owner + MMA issuer (320 threads).
+// TMEM columns: buffer b: S^T/dQ^T [128b, 128b+64), dP^T [128b+64, 128b+128);
+// dV [256, 384), dK [384, 512).
+constexpr int kThreadsW = 320;
+constexpr int kStagesW = 2;
+
+enum : int {
+  WB_KV = 0,
+  WB_QF = 1,                     // [kStagesW]
+  WB_QE = WB_QF + kStagesW,      // [kStagesW]
+  WB_SDP = WB_QE + kStagesW,     // [2]
+  WB_P = WB_SDP + 2,             // [2] 128 arrivals
+  WB_DQ = WB_P + 2,              // [2]
+  WB_FREE = WB_DQ + 2,           // [2] 128 arrivals
+  WB_ROW = WB_FREE + 2,          // [2] 128 arrivals
+  WB_DRAIN = WB_ROW + 2,
+  WB_COUNT = WB_DRAIN + 1
+};
+
+struct BwdWideSmem {
+  static constexpr int kKV = 128 * 128 * 2;    // K or V tile, fp16
+  static constexpr int kQT = 64 * 128 * 2;     // Q or dO sub-tile
+  static constexpr int kPT = 128 * 64 * 2;     // P^T or dS^T buffer
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kKV;
+  static constexpr int kQ = kV + kKV;                   // [kStagesW]
+  static constexpr int kDO = kQ + kStagesW * kQT;       // [kStagesW]
+  static constexpr int kPt = kDO + kStagesW * kQT;      // [2]
+  static constexpr int kDSt = kPt + 2 * kPT;            // [2]
+  static constexpr int kRow = kDSt + 2 * kPT;           // [2][lse2|delta][64] f32
+  static constexpr int kBar = kRow + 2 * 2 * 64 * 4;
+  static constexpr int kMisc = kBar + WB_COUNT * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+__global__ void __launch_bounds__(kThreadsW, 1)
+    step_bwd_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using L = BwdWideSmem;
+  constexpr int D = 128;
+  constexpr int NS = kStagesW;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_u32 + pad;
+  const uint32_t sK = sbase + L::kK;
+  const uint32_t sV = sbase + L::kV;
+  const uint32_t sQ = sbase + L::kQ;
+  const uint32_t sDO = sbase + L::kDO;
+  const uint32_t sPt = sbase + L::kPt;
+  const uint32_t sDSt = sbase + L::kDSt;
+  float* s_row = reinterpret_cast<float*>(smem + L::kRow);  // [b][lse2 | delta][64]
+  const uint32_t bar0 = sbase + L::kBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x / p.Hkv;
+  const int kh = blockIdx.x % p.Hkv;
+  const WorkItem w = p.items[item];
+  const int n_sub = 2 * (w.hi - w.lo);  // 64-row query sub-tiles per head
+  const int n_iter = n_sub * p.G;
+  const int64_t kv_row0 = static_cast<int64_t>(w.kv_owner) * p.n_kv + static_cast<int64_t>(w.tile) * 128;
+  const int32_t kpos0 = __ldg(p.kv_tile_pos + static_cast<int64_t>(w.kv_owner) * p.n_kt + w.tile);
+  const int32_t* q_tile_pos = p.q_tile_pos + static_cast<int64_t>(w.q_owner) * p.n_qt;
+  const int64_t q_row_base = static_cast<int64_t>(w.q_owner) * p.n_q + static_cast<int64_t>(w.lo) * 128;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < WB_COUNT; ++i) {
+      const bool many = (i >= WB_P && i < WB_P + 2) || (i >= WB_FREE && i < WB_FREE + 2) ||
+                        (i >= WB_ROW && i < WB_ROW + 2);
+      ptx::mbar_init(bar(i), many ? 128u : 1u);
+    }
+    *s_abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tDV = tmem + 256;
+  const uint32_t tDK = tmem + 384;
+
+  if (n_iter > 0 && warp == 8 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::prefetch_tmap(&tm_do);
+    ptx::mbar_arrive_expect_tx(bar(WB_KV), 2 * L::kKV);
+    for (int b = 0; b < 2; ++b) {
+      ptx::tma_load_3d(sK + b * 16384, &tm_k, bar(WB_KV), b * 64, kh, static_cast<int>(kv_row0));
+      ptx::tma_load_3d(sV + b * 16384, &tm_v, bar(WB_KV), b * 64, kh, static_cast<int>(kv_row0));
+    }
+    int issued = 0;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % NS;
+      if (it >= NS) {
+        if (!ptx::mbar_wait(bar(WB_QE + s), ((it / NS) - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, 0x2100 + it);
+          break;
+        }
+      }
+      const int h = kh * p.G + it / n_sub;
+      const int row = static_cast<int>(q_row_base + static_cast<int64_t>(it % n_sub) * 64);
+      ptx::mbar_arrive_expect_tx(bar(WB_QF + s), 2 * L::kQT);
+      for (int b = 0; b < 2; ++b) {
+        ptx::tma_load_3d(sQ + s * L::kQT + b * 8192, &tm_q, bar(WB_QF + s), b * 64, h, row);
+        ptx::tma_load_3d(sDO + s * L::kQT + b * 8192, &tm_do, bar(WB_QF + s), b * 64, h, row);
+      }
+      issued = it + 1;
+    }
+    const volatile int never = 0;
+    ptx::mbar_wait(bar(WB_KV), 0, &never, p.wait_limit_ns);
+    for (int it = issued > NS ? issued - NS : 0; it < issued; ++it)
+      ptx::mbar_wait(bar(WB_QF + it % NS), (it / NS) & 1, &never, p.wait_limit_ns);
+  } else if (n_iter > 0 && warp == 9 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_sdp = ptx::idesc_fp16(128, 64, 0, 0);   // K-major A and B
+    constexpr uint32_t idesc_kv = ptx::idesc_fp16(128, 128, 0, 1);   // A K-major, B MN-major
+    constexpr uint32_t idesc_dq = ptx::idesc_fp16(128, 64, 1, 1);    // A and B MN-major
+    bool ok = ptx::mbar_wait(bar(WB_KV), 0, s_abort, p.wait_limit_ns);
+    if (!ok) ptx::record_timeout(p.status, s_abort, 0x2200);
+    // dV, dK and dQ^T of iteration i (the second half of an iteration)
+    auto tail = [&](int i) -> bool {
+      const int b = i & 1;
+      const int s = i % NS;
+      if (!ptx::mbar_wait(bar(WB_P + b), (i >> 1) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x2300 + i);
+        return false;
+      }
+      ptx::tc_fence_after();
+      const uint32_t pt = sPt + b * L::kPT;
+      const uint32_t dst = sDSt + b * L::kPT;
+      const uint32_t q_tile = sQ + s * L::kQT;
+      const uint32_t do_tile = sDO + s * L::kQT;
+      // dV += P^T dO, dK += dS^T Q: K = 64 queries. A: [128 keys][64 q] K-major
+      // (one 128-byte swizzle column). B: [64 q][128 d] MN-major, d 64..127 at
+      // +8 KB, 8-query groups at 1 KB.
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+        ptx::mma_ss(tDV, ptx::sdesc_sw128(pt + kk * 32, 16, 1024),
+                         ptx::sdesc_sw128(do_tile + kk * 2048, 8192, 1024), idesc_kv, acc);
+        ptx::mma_ss(tDK, ptx::sdesc_sw128(dst + kk * 32, 16, 1024),
+                         ptx::sdesc_sw128(q_tile + kk * 2048, 8192, 1024), idesc_kv, acc);
+      }
+      ptx::mma_commit(bar(WB_QE + s));
+      // dQ^T = K^T dS^T: M = d, N = 64 q, K = 128 keys. A = K read MN-major
+      // (d contiguous: d 64..127 at +16 KB, 8-key groups at 1 KB); B = dS^T
+      // read MN-major (q contiguous, one 64-wide atom, 8-key groups at 1 KB).
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        ptx::mma_ss(tmem + 128 * b, ptx::sdesc_sw128(sK + kk * 2048, 16384, 1024),
+                         ptx::sdesc_sw128(dst + kk * 2048, 16, 1024), idesc_dq,
+                         kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(WB_DQ + b));
+      return true;
+    };
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int b = it & 1;
+      const int s = it % NS;
+      if (!ptx::mbar_wait(bar(WB_QF + s), (it / NS) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x2400 + it);
+        ok = false;
+        break;
+      }
+      if (it >= 2 && !ptx::mbar_wait(bar(WB_FREE + b), ((it >> 1) - 1) & 1, s_abort,
+                                     p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x2500 + it);
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t q_tile = sQ + s * L::kQT;
+      const uint32_t do_tile = sDO + s * L::kQT;
+      // S^T = K Q^T and dP^T = V dO^T: K = d = 128; A [128][128] K-major in two
+      // 64-column blocks of 16 KB, B [64][128] K-major in two blocks of 8 KB.
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t boff = (kk >> 2) * 8192 + (kk & 3) * 32;
+        ptx::mma_ss(tmem + 128 * b, ptx::sdesc_sw128(sK + aoff, 16, 1024),
+                         ptx::sdesc_sw128(q_tile + boff, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+        ptx::mma_ss(tmem + 128 * b + 64, ptx::sdesc_sw128(sV + aoff, 16, 1024),
+                         ptx::sdesc_sw128(do_tile + boff, 16, 1024), idesc_sdp,
+                         kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(WB_SDP + b));
+      if (it >= 1 && !tail(it - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok) tail(n_iter - 1);
+    ptx::mma_commit(bar(WB_DRAIN));
+    const volatile int never = 0;
+    ptx::mbar_wait(bar(WB_DRAIN), 0, &never, p.wait_limit_ns);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute
+    const int wg = warp >> 2;                 // warpgroup = buffer parity it handles
+    const int t = threadIdx.x & 127;          // key row (P/dS) and d column (dQ^T)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int32_t kpos = kpos0 + t;
+    const int32_t dend = doc_end(p.cu, p.n_cu, kpos);
+    const uint32_t tS = tmem + 128 * wg;
+    const uint32_t tDP = tS + 64;
+    float* lse2 = s_row + wg * 128;
+    float* dlt = lse2 + 64;
+    const uint32_t pt = sPt + wg * L::kPT;
+    const uint32_t dst = sDSt + wg * L::kPT;
+    bool ok = true;
+    for (int it = wg; it < n_iter; it += 2) {
+      const int k = it >> 1;
+      const int h = kh * p.G + it / n_sub;
+      const int sub = it % n_sub;
+      const int64_t q_row0 = q_row_base + static_cast<int64_t>(sub) * 64;
+      const int32_t qpos0 = __ldg(q_tile_pos + w.lo + (sub >> 1)) + (sub & 1) * 64;
+      if (t < 64) {
+        lse2[t] = __ldg(p.lse + static_cast<int64_t>(h) * p.T_q + q_row0 + t) * kLog2e;
+        dlt[t] = __ldg(p.delta + static_cast<int64_t>(h) * p.T_q + q_row0 + t);
+      }
+      ptx::mbar_arrive(bar(WB_ROW + wg));
+      if (!ptx::mbar_wait(bar(WB_ROW + wg), k & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x2600 + it);
+        ok = false;
+      }
+      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ptx::doc_start(p.cu, p.n_cu, qpos0 + 63));
+      const int lo_i = kpos - qpos0;
+      const int hi_i = dend - 1 - qpos0;
+      if (ok && !ptx::mbar_wait(bar(WB_SDP + wg), k & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x2700 + it);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float sv[32], dp[32];
+        ptx::tmem_ld32(tS + lane_base + c * 32, sv);
+        ptx::tmem_ld32(tDP + lane_base + c * 32, dp);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int i = c * 32 + x;
+          const bool vis = full || (i >= lo_i && i <= hi_i);
+          const float pv = vis ? ptx::ex2(fmaf(sv[x], p.scale_log2, -lse2[i])) : 0.f;
+          sv[x] = pv;
+          dp[x] = pv * (dp[x] - dlt[i]);
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int chunk = c * 4 + ch;  // 16-byte chunk of the 128-byte row
+          const uint32_t off = static_cast<uint32_t>(t * 128 + (((chunk ^ t) & 7) << 4));
+          const float* a = sv + ch * 8;
+          const float* g = dp + ch * 8;
+          ptx::st_shared_v4(pt + off, ptx::pack_f16(a[0], a[1]), ptx::pack_f16(a[2], a[3]),
+                            ptx::pack_f16(a[4], a[5]), ptx::pack_f16(a[6], a[7]));
+          ptx::st_shared_v4(dst + off, ptx::pack_f16(g[0], g[1]), ptx::pack_f16(g[2], g[3]),
+                            ptx::pack_f16(g[4], g[5]), ptx::pack_f16(g[6], g[7]));
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(WB_P + wg));
+      if (!ptx::mbar_wait(bar(WB_DQ + wg), k & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x2800 + it);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ptx::tc_fence_after();
+      // dQ^T: lane t = column t of d; column qi = query row qi of the sub-tile.
+      float* dq_col = p.dq + (q_row0 * p.Hq + h) * D + t;
+      const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float v[32];
+        ptx::tmem_ld32(tS + lane_base + c * 32, v);
+#pragma unroll
+        for (int x = 0; x < 32; ++x)
+          atomicAdd(dq_col + (c * 32 + x) * row_stride, v[x] * p.scale);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(WB_FREE + wg));
+    }
+    // dK (warpgroup 0) and dV (warpgroup 1) once every MMA has finished
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && n_iter > 0) {
+      const volatile int never = 0;
+      const bool done = ptx::mbar_wait(bar(WB_DRAIN), 0, &never, p.wait_limit_ns);
+      if (__all_sync(0xffffffffu, done)) {
+        ptx::tc_fence_after();
+        float* dst_row = (wg == 0 ? p.dk : p.dv) + ((kv_row0 + t) * p.Hkv + kh) * D;
+        const uint32_t src = wg == 0 ? tDK : tDV;
+        const float mul = wg == 0 ? p.scale : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float a[32];
+          ptx::tmem_ld32(src + lane_base + c * 32, a);
+          float4* d4 = reinterpret_cast<float4*>(dst_row + c * 32);
+#pragma unroll
+          for (int x4 = 0; x4 < 8; ++x4) {
+            float4 u = d4[x4];
+            u.x += a[x4 * 4] * mul;
+            u.y += a[x4 * 4 + 1] * mul;
+            u.z += a[x4 * 4 + 2] * mul;
+            u.w += a[x4 * 4 + 3] * mul;
+            d4[x4] = u;
+          }
+        }
+      } else {
+        ptx::record_timeout(p.status, s_abort, 0x2900);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 size_t step_bwd_smem_bytes(int d) {
-  return d == 128 ? BwdSmem<128>::kAlloc : BwdSmem<64>::kAlloc;
+  return d == 128 ? BwdWideSmem::kAlloc : BwdSmem<64>::kAlloc;
 }
+
+int step_bwd_q_box_rows(int d) { return d == 128 ? 64 : 128; }
 
 cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
@@ -384,12 +737,12 @@ cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
   cudaError_t err;
   if (d == 128) {
     if (!attr_done[1]) {
-      err = cudaFuncSetAttribute(step_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      err = cudaFuncSetAttribute(step_bwd_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
       if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_bwd attr: ") + cudaGetErrorString(err));
       attr_done[1] = true;
     }
-    step_bwd_kernel<128><<<grid, kThreads, smem, s>>>(tq, tk, tv, tdo, p);
+    step_bwd_wide_kernel<<<grid, kThreadsW, smem, s>>>(tq, tk, tv, tdo, p);
   } else {
     if (!attr_done[0]) {
       err = cudaFuncSetAttribute(step_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // B = V [keys x d], d contiguous (MN-major): 8-key groups at 1024 B,
         // 64-column blocks at 16 KB
         const uint64_t b = ptx::sdesc_sw128(v_tile + kk * 2048, 16384, 1024);
-        ptx::mma_bf16_ss(tO, a, b, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_ss(tO, a, b, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
       }
       ptx::mma_commit(bar(BAR_O));
       ptx::mma_commit(bar(BAR_EMPTY + s));
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
         const uint64_t a = ptx::sdesc_sw128(sQ + off, 16, 1024);
         const uint64_t b = ptx::sdesc_sw128(k_tile + off, 16, 1024);
-        ptx::mma_bf16_ss(tS[j & 1], a, b, idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_ss(tS[j & 1], a, b, idesc_s, kk > 0 ? 1u : 0u);
       }
       ptx::mma_commit(bar(BAR_S + (j & 1)));
       if (j >= 1 && !issue_pv(j - 1)) {
