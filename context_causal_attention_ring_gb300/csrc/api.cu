@@ -347,7 +347,11 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const
   const bool all_items = (mode == CP_ATTN_WRITE_PARTIAL) || fp.first || fp.o_final != nullptr;
   const int n_items = all_items ? (p->fwd_off[step + 1] - p->fwd_off[step]) : p->fwd_nonempty[step];
   if (n_items == 0) return CP_ATTN_OK;
-  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_items) * p->Hq));
+  // one CTA per (item, query head), or per (item, pair of heads of a group)
+  const int hpc = step_fwd_heads_per_cta(p->d);
+  const int G = p->Hq / p->Hkv;
+  const int64_t units = hpc == 1 ? p->Hq : static_cast<int64_t>(p->Hkv) * ((G + 1) / 2);
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_items) * units));
   return launch_step_fwd(p->d, grid, step_fwd_smem_bytes(p->d), static_cast<cudaStream_t>(stream),
                          tq, tk, tv, fp);
 }

@@ -55,6 +55,8 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, const FwdParams& p);
 size_t step_fwd_smem_bytes(int d);
+// Query heads one forward CTA handles (d = 128 pairs the heads of a group).
+int step_fwd_heads_per_cta(int d);
 
 cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,

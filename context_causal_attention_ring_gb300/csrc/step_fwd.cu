@@ -381,11 +381,363 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ===========================================================================
+// d = 128: two query heads per CTA in ping-pong.
+//
+// A CTA takes one query tile and two query heads A and B of the same KV head
+// (so both see exactly the same K/V tiles and the same mask). Softmax
+// warpgroup A works on S_A(j) while the tensor core runs O_B += P_B V(j-1) and
+// S_B(j), and the other way round, so exponentials and MMAs overlap. P is
+// written back into its own S columns of TMEM as bf16 pairs and feeds
+// O += P V as the A operand read from tensor memory (no shared-memory copy).
+// Warps: 0-3 softmax head A, 4-7 softmax head B, 8 TMA producer, 9 TMEM
+// owner + MMA issuer (320 threads).
+// TMEM columns: S_A [0,128) (P_A in [0,64)), S_B [128,256), O_A [256,384),
+// O_B [384,512).
+constexpr int kThreadsP = 320;
+constexpr int kStagesP = 2;
+
+enum : int {
+  PB_Q = 0,
+  PB_K = 1,                     // [kStagesP]
+  PB_V = PB_K + kStagesP,       // [kStagesP]
+  PB_E = PB_V + kStagesP,       // [kStagesP] stage free
+  PB_S = PB_E + kStagesP,       // [2] S of head slot ready
+  PB_P = PB_S + 2,              // [2] P of head slot written (128 arrivals)
+  PB_O = PB_P + 2,              // [2] final O of head slot ready
+  PB_DRAIN = PB_O + 2,
+  PB_COUNT = PB_DRAIN + 1
+};
+
+struct FwdPairSmem {
+  static constexpr int kTile = 128 * 128 * 2;
+  static constexpr int kQ = 0;                          // [2 heads]
+  static constexpr int kK = kQ + 2 * kTile;             // [kStagesP]
+  static constexpr int kV = kK + kStagesP * kTile;      // [kStagesP]
+  static constexpr int kBar = kV + kStagesP * kTile;
+  static constexpr int kMisc = kBar + PB_COUNT * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+__global__ void __launch_bounds__(kThreadsP, 1)
+    step_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = FwdPairSmem;
+  constexpr int D = 128;
+  constexpr int NS = kStagesP;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_u32 + pad;
+  const uint32_t sQ = sbase + L::kQ;
+  const uint32_t sK = sbase + L::kK;
+  const uint32_t sV = sbase + L::kV;
+  const uint32_t bar0 = sbase + L::kBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_pairs = (p.G + 1) >> 1;
+  const int Hkv = p.Hq / p.G;
+  const int item = blockIdx.x / (Hkv * n_pairs);
+  const int rem = blockIdx.x % (Hkv * n_pairs);
+  const int kh = rem / n_pairs;
+  const int hp = rem % n_pairs;
+  const int hA = kh * p.G + 2 * hp;
+  const int nh = (p.G - 2 * hp) >= 2 ? 2 : 1;
+  const WorkItem w = p.items[item];
+  const int n_tiles = w.hi - w.lo;
+  const int64_t q_row0 = static_cast<int64_t>(w.q_owner) * p.n_q + static_cast<int64_t>(w.tile) * 128;
+  const int32_t qpos0 = __ldg(p.q_tile_pos + static_cast<int64_t>(w.q_owner) * p.n_qt + w.tile);
+  const int64_t kv_row_base = static_cast<int64_t>(w.kv_owner) * p.n_kv;
+  const int32_t* kv_tile_pos = p.kv_tile_pos + static_cast<int64_t>(w.kv_owner) * p.n_kt;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < PB_COUNT; ++i)
+      ptx::mbar_init(bar(i), (i == PB_P || i == PB_P + 1) ? 128u : 1u);
+    *s_abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (n_tiles > 0 && warp == 8 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::mbar_arrive_expect_tx(bar(PB_Q), nh * L::kTile);
+    for (int hs = 0; hs < nh; ++hs)
+      for (int b = 0; b < 2; ++b)
+        ptx::tma_load_3d(sQ + hs * L::kTile + b * 16384, &tm_q, bar(PB_Q), b * 64, hA + hs,
+                         static_cast<int>(q_row0));
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % NS;
+      if (j >= NS) {
+        if (!ptx::mbar_wait(bar(PB_E + s), ((j / NS) - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, 0x3100 + j);
+          break;
+        }
+      }
+      const int row = static_cast<int>(kv_row_base + static_cast<int64_t>(w.lo + j) * 128);
+      ptx::mbar_arrive_expect_tx(bar(PB_K + s), L::kTile);
+      for (int b = 0; b < 2; ++b)
+        ptx::tma_load_3d(sK + s * L::kTile + b * 16384, &tm_k, bar(PB_K + s), b * 64, kh, row);
+      ptx::mbar_arrive_expect_tx(bar(PB_V + s), L::kTile);
+      for (int b = 0; b < 2; ++b)
+        ptx::tma_load_3d(sV + s * L::kTile + b * 16384, &tm_v, bar(PB_V + s), b * 64, kh, row);
+      issued = j + 1;
+    }
+    const volatile int never = 0;
+    ptx::mbar_wait(bar(PB_Q), 0, &never, p.wait_limit_ns);
+    for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) {
+      ptx::mbar_wait(bar(PB_K + j % NS), (j / NS) & 1, &never, p.wait_limit_ns);
+      ptx::mbar_wait(bar(PB_V + j % NS), (j / NS) & 1, &never, p.wait_limit_ns);
+    }
+  } else if (n_tiles > 0 && warp == 9 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
+    bool ok = ptx::mbar_wait(bar(PB_Q), 0, s_abort, p.wait_limit_ns);
+    if (!ok) ptx::record_timeout(p.status, s_abort, 0x3200);
+    auto issue_s = [&](int j, int hs) {
+      const uint32_t k_tile = sK + (j % NS) * L::kTile;
+      const uint32_t q_tile = sQ + hs * L::kTile;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::mma_ss(tmem + 128 * hs, ptx::sdesc_sw128(q_tile + off, 16, 1024),
+                    ptx::sdesc_sw128(k_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(bar(PB_S + hs));
+    };
+    auto issue_o = [&](int j, int hs) -> bool {
+      if (!ptx::mbar_wait(bar(PB_P + hs), j & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x3300 + j);
+        return false;
+      }
+      ptx::tc_fence_after();
+      const uint32_t v_tile = sV + (j % NS) * L::kTile;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        // A = P (bf16 pairs in the head's S columns), 16 keys = 8 columns
+        ptx::mma_ts(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
+                    ptx::sdesc_sw128(v_tile + kk * 2048, 16384, 1024), idesc_o,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      return true;
+    };
+    auto wait_kv = [&](int bar_base, int j, int where) -> bool {
+      if (!ptx::mbar_wait(bar(bar_base + j % NS), (j / NS) & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, where + j);
+        return false;
+      }
+      ptx::tc_fence_after();
+      return true;
+    };
+    if (ok && wait_kv(PB_K, 0, 0x3400)) {
+      issue_s(0, 0);
+      if (nh == 2) issue_s(0, 1);
+    } else {
+      ok = false;
+    }
+    for (int j = 1; ok && j < n_tiles; ++j) {
+      if (!wait_kv(PB_K, j, 0x3400) || !wait_kv(PB_V, j - 1, 0x3500)) { ok = false; break; }
+      if (!issue_o(j - 1, 0)) { ok = false; break; }
+      issue_s(j, 0);  // executes after the O MMA above has read P_A (in-order pipe)
+      if (nh == 2) {
+        if (!issue_o(j - 1, 1)) { ok = false; break; }
+        issue_s(j, 1);
+      }
+      ptx::mma_commit(bar(PB_E + (j - 1) % NS));
+    }
+    if (ok && wait_kv(PB_V, n_tiles - 1, 0x3500)) {
+      if (issue_o(n_tiles - 1, 0)) {
+        ptx::mma_commit(bar(PB_O + 0));
+        if (nh == 2 && issue_o(n_tiles - 1, 1)) ptx::mma_commit(bar(PB_O + 1));
+      }
+      ptx::mma_commit(bar(PB_E + (n_tiles - 1) % NS));
+    }
+    ptx::mma_commit(bar(PB_DRAIN));
+    const volatile int never = 0;
+    ptx::mbar_wait(bar(PB_DRAIN), 0, &never, p.wait_limit_ns);
+  } else if (warp < 8 && (warp >> 2) < nh) {
+    // ------------------------------------------------------------ softmax
+    const int hs = warp >> 2;
+    const int h = hA + hs;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 128 * hs;
+    const uint32_t tO = tmem + 256 + 128 * hs;
+    const int32_t my_pos = qpos0 + r;
+    const int32_t my_ds = ptx::doc_start(p.cu, p.n_cu, my_pos);
+    const int32_t ds_last = ptx::doc_start(p.cu, p.n_cu, qpos0 + 127);
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int32_t kpos0 = __ldg(kv_tile_pos + w.lo + j);
+      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ds_last);
+      if (!ptx::mbar_wait(bar(PB_S + hs), j & 1, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x3600 + j);
+        ok = false;
+      }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // S(j) complete implies O += P V of tile j-1 complete (issued before it)
+      ptx::tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        ptx::tmem_ld32(tS + lane_base + c * 32, *reinterpret_cast<float(*)[32]>(s + c * 32));
+      if (!full) {
+        const int lo = my_ds - kpos0;
+        const int hi = my_pos - kpos0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < lo || c > hi) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * p.scale_log2;
+      float alpha = 1.f;
+      if (m_tile > m_used + kRescaleThreshold) {
+        alpha = ptx::ex2(m_used - m_tile);
+        l *= alpha;
+        m_used = m_tile;
+      }
+      const float base = (m_used == -INFINITY) ? 0.f : m_used;
+      float rowsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        s[c] = ptx::ex2(fmaf(s[c], p.scale_log2, -base));
+        rowsum += s[c];
+      }
+      l += rowsum;
+      // P as bf16 pairs into this head's S columns [0, 64)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) pk[x] = ptx::pack_bf16(s[c * 32 + 2 * x], s[c * 32 + 2 * x + 1]);
+        ptx::tmem_st16(tS + lane_base + c * 16, pk);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          ptx::tmem_ld32(tO + lane_base + c * 32, o);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] *= alpha;
+          ptx::tmem_st32(tO + lane_base + c * 32, o);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(PB_P + hs));
+    }
+    if (ok && n_tiles > 0) {
+      if (!ptx::mbar_wait(bar(PB_O + hs), 0, s_abort, p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x3700);
+        ok = false;
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      ptx::tc_fence_after();
+      const int64_t g = q_row0 + r;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float lse_t = l > 0.f ? (m_used + ptx::lg2(l)) * kLn2 : -INFINITY;
+      const int64_t row_off = (g * p.Hq + h) * D;
+      const int64_t lse_off = static_cast<int64_t>(h) * p.T_q + g;
+      float w_old = 0.f, w_new = 1.f, lse_out = lse_t;
+      const bool merge = (p.mode == CP_ATTN_ACCUMULATE) && !p.first;
+      float* o_dst = p.o_part;
+      float* lse_dst = p.lse_part;
+      if (p.mode == CP_ATTN_WRITE_PARTIAL) {
+        o_dst += static_cast<int64_t>(w.kv_owner) * p.T_q * p.Hq * D;
+        lse_dst += static_cast<int64_t>(w.kv_owner) * p.Hq * p.T_q;
+      }
+      if (merge) {
+        const float a = lse_dst[lse_off] * kLog2e;
+        const float b = lse_t * kLog2e;
+        const float M = fmaxf(a, b);
+        if (M == -INFINITY) {
+          w_old = 0.f;
+          w_new = 0.f;
+          lse_out = -INFINITY;
+        } else {
+          const float ea = ptx::ex2(a - M), eb = ptx::ex2(b - M);
+          const float sum = ea + eb;
+          w_old = ea / sum;
+          w_new = eb / sum;
+          lse_out = (M + ptx::lg2(sum)) * kLn2;
+        }
+      }
+      lse_dst[lse_off] = lse_out;
+      float4* od = reinterpret_cast<float4*>(o_dst + row_off);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (n_tiles > 0) {
+          ptx::tmem_ld32(tO + lane_base + c * 32, o);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        }
+#pragma unroll
+        for (int x4 = 0; x4 < 8; ++x4) {
+          float4 v;
+          v.x = o[x4 * 4 + 0] * inv_l;
+          v.y = o[x4 * 4 + 1] * inv_l;
+          v.z = o[x4 * 4 + 2] * inv_l;
+          v.w = o[x4 * 4 + 3] * inv_l;
+          if (merge) {
+            const float4 u = od[c * 8 + x4];
+            v.x = u.x * w_old + v.x * w_new;
+            v.y = u.y * w_old + v.y * w_new;
+            v.z = u.z * w_old + v.z * w_new;
+            v.w = u.w * w_old + v.w * w_new;
+          }
+          od[c * 8 + x4] = v;
+          if (p.o_final) {
+            uint2 pk;
+            pk.x = ptx::pack_bf16(v.x, v.y);
+            pk.y = ptx::pack_bf16(v.z, v.w);
+            *reinterpret_cast<uint2*>(p.o_final + row_off + c * 32 + x4 * 4) = pk;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 size_t step_fwd_smem_bytes(int d) {
-  return d == 128 ? FwdSmem<128>::kAlloc : FwdSmem<64>::kAlloc;
+  return d == 128 ? FwdPairSmem::kAlloc : FwdSmem<64>::kAlloc;
 }
+
+int step_fwd_heads_per_cta(int d) { return d == 128 ? 2 : 1; }
 
 cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
@@ -394,12 +746,12 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
   cudaError_t err;
   if (d == 128) {
     if (!attr_done[1]) {
-      err = cudaFuncSetAttribute(step_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      err = cudaFuncSetAttribute(step_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
       if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd attr: ") + cudaGetErrorString(err));
       attr_done[1] = true;
     }
-    step_fwd_kernel<128><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+    step_fwd_pair_kernel<<<grid, kThreadsP, smem, s>>>(tq, tk, tv, p);
   } else {
     if (!attr_done[0]) {
       err = cudaFuncSetAttribute(step_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
