@@ -366,9 +366,10 @@ cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops
   if (!half_ops || !lse || !delta || !dq_acc || !dk_acc || !dv_acc)
     return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: null tensor pointer");
   if ((reinterpret_cast<uintptr_t>(half_ops) & 255u) || !aligned16(dq_acc) ||
-      !aligned16(dk_acc) || !aligned16(dv_acc))
+      !aligned16(dk_acc) || !aligned16(dv_acc) || !aligned16(lse) || !aligned16(delta))
     return fail(CP_ATTN_ERR_INVALID_ARG,
-                "step_bwd: half_ops must be 256-byte and accumulators 16-byte aligned");
+                "step_bwd: half_ops must be 256-byte aligned; accumulators, lse and delta "
+                "16-byte aligned");
   const HalfOps ho = half_ops_layout(p);
   const char* hb = static_cast<const char*>(half_ops);
   CUtensorMap tq, tk, tv, tdo;

@@ -7,7 +7,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/cp_attn.h"
+#include "cp_attn.h"
 
 namespace cpa {
 

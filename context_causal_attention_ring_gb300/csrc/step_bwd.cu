@@ -376,8 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Per iteration (one 64-row query sub-tile of one head of the group):
 //   S^T  = K Q^T    (M = 128 keys, N = 64)   TMEM buffer b = it & 1
 //   dP^T = V dO^T   (M = 128 keys, N = 64)   TMEM buffer b
-//   P^T, dS^T (fp16) -> shared-memory buffer b   by compute warpgroup b
-//   dV += P^T dO,  dK += dS^T Q              (M = 128 keys, N = 128, K = 64)
+//   P^T (fp16) -> back into buffer b's S^T columns of TMEM, dS^T (fp16) ->
+//   shared-memory buffer b, by compute warpgroup b
+//   dV += P^T dO (P^T read from TMEM), dK += dS^T Q   (M = 128 keys, N = 128)
 //   dQ^T = K^T dS^T (M = 128 = d, N = 64)   TMEM, in buffer b's S^T columns
 // Two compute warpgroups take alternate iterations, so one warpgroup's
 // exponentials and its dQ read-out overlap the other's MMAs, and both TMEM
@@ -387,10 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // instruction.
 // Warps: 0-3 compute warpgroup 0, 4-7 compute warpgroup 1, 8 TMA producer,
 // 9 TMEM owner + MMA issuer (320 threads).
-// TMEM columns: buffer b: S^T/dQ^T [128b, 128b+64), dP^T [128b+64, 128b+128);
-// dV [256, 384), dK [384, 512).
+// TMEM columns: buffer b: S^T (then P^T in its first 32 columns, then dQ^T)
+// [128b, 128b+64), dP^T [128b+64, 128b+128); dV [256, 384), dK [384, 512).
+// Q/dO (and the sub-tile's LSE/delta rows) come through a 3-stage TMA ring:
+// a stage is free only after that iteration's dV/dK MMAs, so two stages would
+// leave the next load's latency exposed every iteration.
 constexpr int kThreadsW = 320;
-constexpr int kStagesW = 2;
+constexpr int kStagesW = 3;
 
 enum : int {
   WB_KV = 0,
@@ -400,23 +404,21 @@ enum : int {
   WB_P = WB_SDP + 2,             // [2] 128 arrivals
   WB_DQ = WB_P + 2,              // [2]
   WB_FREE = WB_DQ + 2,           // [2] 128 arrivals
-  WB_ROW = WB_FREE + 2,          // [2] 128 arrivals
-  WB_DRAIN = WB_ROW + 2,
+  WB_DRAIN = WB_FREE + 2,
   WB_COUNT = WB_DRAIN + 1
 };
 
 struct BwdWideSmem {
   static constexpr int kKV = 128 * 128 * 2;    // K or V tile, fp16
   static constexpr int kQT = 64 * 128 * 2;     // Q or dO sub-tile
-  static constexpr int kPT = 128 * 64 * 2;     // P^T or dS^T buffer
+  static constexpr int kPT = 128 * 64 * 2;     // dS^T buffer
   static constexpr int kK = 0;
   static constexpr int kV = kK + kKV;
   static constexpr int kQ = kV + kKV;                   // [kStagesW]
   static constexpr int kDO = kQ + kStagesW * kQT;       // [kStagesW]
-  static constexpr int kPt = kDO + kStagesW * kQT;      // [2]
-  static constexpr int kDSt = kPt + 2 * kPT;            // [2]
-  static constexpr int kRow = kDSt + 2 * kPT;           // [2][lse2|delta][64] f32
-  static constexpr int kBar = kRow + 2 * 2 * 64 * 4;
+  static constexpr int kDSt = kDO + kStagesW * kQT;     // [2]
+  static constexpr int kRow = kDSt + 2 * kPT;           // [kStagesW][lse|delta][64] f32
+  static constexpr int kBar = kRow + kStagesW * 2 * 64 * 4;
   static constexpr int kMisc = kBar + WB_COUNT * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -439,9 +441,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   const uint32_t sV = sbase + L::kV;
   const uint32_t sQ = sbase + L::kQ;
   const uint32_t sDO = sbase + L::kDO;
-  const uint32_t sPt = sbase + L::kPt;
   const uint32_t sDSt = sbase + L::kDSt;
-  float* s_row = reinterpret_cast<float*>(smem + L::kRow);  // [b][lse2 | delta][64]
+  const uint32_t sRow = sbase + L::kRow;
+  const float* s_row = reinterpret_cast<const float*>(smem + L::kRow);  // [stage][lse | delta][64]
   const uint32_t bar0 = sbase + L::kBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -461,8 +463,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < WB_COUNT; ++i) {
-      const bool many = (i >= WB_P && i < WB_P + 2) || (i >= WB_FREE && i < WB_FREE + 2) ||
-                        (i >= WB_ROW && i < WB_ROW + 2);
+      const bool many = (i >= WB_P && i < WB_P + 2) || (i >= WB_FREE && i < WB_FREE + 2);
       ptx::mbar_init(bar(i), many ? 128u : 1u);
     }
     *s_abort = 0;
@@ -501,100 +502,104 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       }
       const int h = kh * p.G + it / n_sub;
       const int row = static_cast<int>(q_row_base + static_cast<int64_t>(it % n_sub) * 64);
-      ptx::mbar_arrive_expect_tx(bar(WB_QF + s), 2 * L::kQT);
+      ptx::mbar_arrive_expect_tx(bar(WB_QF + s), 2 * L::kQT + 2 * 64 * 4);
       for (int b = 0; b < 2; ++b) {
         ptx::tma_load_3d(sQ + s * L::kQT + b * 8192, &tm_q, bar(WB_QF + s), b * 64, h, row);
         ptx::tma_load_3d(sDO + s * L::kQT + b * 8192, &tm_do, bar(WB_QF + s), b * 64, h, row);
       }
+      // the sub-tile's 64 LSE and delta values (256 bytes each, contiguous)
+      const int64_t row_off = static_cast<int64_t>(h) * p.T_q + row;
+      ptx::bulk_load(sRow + s * 512, p.lse + row_off, 256, bar(WB_QF + s));
+      ptx::bulk_load(sRow + s * 512 + 256, p.delta + row_off, 256, bar(WB_QF + s));
       issued = it + 1;
     }
     const volatile int never = 0;
     ptx::mbar_wait(bar(WB_KV), 0, &never, p.wait_limit_ns);
     for (int it = issued > NS ? issued - NS : 0; it < issued; ++it)
       ptx::mbar_wait(bar(WB_QF + it % NS), (it / NS) & 1, &never, p.wait_limit_ns);
-  } else if (n_iter > 0 && warp == 9 && lane == 0) {
+  } else if (n_iter > 0 && warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop so that descriptors stay warp-uniform;
+    // lane 0 alone issues each tcgen05 instruction.
+    const uint32_t leader = lane == 0 ? 1u : 0u;
     constexpr uint32_t idesc_sdp = ptx::idesc_fp16(128, 64, 0, 0);   // K-major A and B
     constexpr uint32_t idesc_kv = ptx::idesc_fp16(128, 128, 0, 1);   // A K-major, B MN-major
     constexpr uint32_t idesc_dq = ptx::idesc_fp16(128, 64, 1, 1);    // A and B MN-major
-    bool ok = ptx::mbar_wait(bar(WB_KV), 0, s_abort, p.wait_limit_ns);
-    if (!ok) ptx::record_timeout(p.status, s_abort, 0x2200);
+    // K and V as K-major A ([128][128] in two 64-column blocks of 16 KB), and
+    // K as MN-major A for dQ^T (d contiguous: d 64..127 at +16 KB).
+    const uint64_t dK = ptx::sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV = ptx::sdesc_sw128(sV, 16, 1024);
+    const uint64_t dK_mn = ptx::sdesc_sw128(sK, 16384, 1024);
+    auto wait_all = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+      const bool w_ok = ptx::mbar_wait(b_, parity, s_abort, p.wait_limit_ns);
+      if (!w_ok) ptx::record_timeout(p.status, s_abort, where);
+      return __all_sync(0xffffffffu, w_ok);
+    };
+    bool ok = wait_all(bar(WB_KV), 0, 0x2200);
     // dV, dK and dQ^T of iteration i (the second half of an iteration)
     auto tail = [&](int i) -> bool {
       const int b = i & 1;
       const int s = i % NS;
-      if (!ptx::mbar_wait(bar(WB_P + b), (i >> 1) & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x2300 + i);
-        return false;
-      }
+      if (!wait_all(bar(WB_P + b), (i >> 1) & 1, 0x2300 + i)) return false;
       ptx::tc_fence_after();
-      const uint32_t pt = sPt + b * L::kPT;
-      const uint32_t dst = sDSt + b * L::kPT;
-      const uint32_t q_tile = sQ + s * L::kQT;
-      const uint32_t do_tile = sDO + s * L::kQT;
-      // dV += P^T dO, dK += dS^T Q: K = 64 queries. A: [128 keys][64 q] K-major
-      // (one 128-byte swizzle column). B: [64 q][128 d] MN-major, d 64..127 at
-      // +8 KB, 8-query groups at 1 KB.
+      // dS^T buffer: [128 keys][64 q] fp16, one 128-byte swizzle column; read
+      // K-major as A of dK and MN-major as B of dQ^T (same descriptor bits).
+      const uint64_t dDS = ptx::sdesc_sw128(sDSt + b * L::kPT, 16, 1024);
+      // Q / dO sub-tile [64 q][128 d] as MN-major B: d 64..127 at +8 KB
+      const uint64_t dQm = ptx::sdesc_sw128(sQ + s * L::kQT, 8192, 1024);
+      const uint64_t dDOm = ptx::sdesc_sw128(sDO + s * L::kQT, 8192, 1024);
+      // dV += P^T dO (P^T read from TMEM: fp16 pairs in buffer b's first 32
+      // columns, 16 queries = 8 columns) and dK += dS^T Q; K = 64 queries.
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-        ptx::mma_ss(tDV, ptx::sdesc_sw128(pt + kk * 32, 16, 1024),
-                         ptx::sdesc_sw128(do_tile + kk * 2048, 8192, 1024), idesc_kv, acc);
-        ptx::mma_ss(tDK, ptx::sdesc_sw128(dst + kk * 32, 16, 1024),
-                         ptx::sdesc_sw128(q_tile + kk * 2048, 8192, 1024), idesc_kv, acc);
+        ptx::mma_ts_w(tDV, tmem + 128 * b + kk * 8, ptx::sdesc_add(dDOm, kk * 2048), idesc_kv,
+                      acc, leader);
+        ptx::mma_ss_w(tDK, ptx::sdesc_add(dDS, kk * 32), ptx::sdesc_add(dQm, kk * 2048),
+                      idesc_kv, acc, leader);
       }
-      ptx::mma_commit(bar(WB_QE + s));
-      // dQ^T = K^T dS^T: M = d, N = 64 q, K = 128 keys. A = K read MN-major
-      // (d contiguous: d 64..127 at +16 KB, 8-key groups at 1 KB); B = dS^T
-      // read MN-major (q contiguous, one 64-wide atom, 8-key groups at 1 KB).
+      ptx::mma_commit_w(bar(WB_QE + s), leader);
+      // dQ^T = K^T dS^T: M = d, N = 64 q, K = 128 keys.
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        ptx::mma_ss(tmem + 128 * b, ptx::sdesc_sw128(sK + kk * 2048, 16384, 1024),
-                         ptx::sdesc_sw128(dst + kk * 2048, 16, 1024), idesc_dq,
-                         kk > 0 ? 1u : 0u);
-      }
-      ptx::mma_commit(bar(WB_DQ + b));
+      for (int kk = 0; kk < 8; ++kk)
+        ptx::mma_ss_w(tmem + 128 * b, ptx::sdesc_add(dK_mn, kk * 2048),
+                      ptx::sdesc_add(dDS, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u, leader);
+      ptx::mma_commit_w(bar(WB_DQ + b), leader);
       return true;
     };
     for (int it = 0; ok && it < n_iter; ++it) {
       const int b = it & 1;
       const int s = it % NS;
-      if (!ptx::mbar_wait(bar(WB_QF + s), (it / NS) & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x2400 + it);
-        ok = false;
-        break;
-      }
-      if (it >= 2 && !ptx::mbar_wait(bar(WB_FREE + b), ((it >> 1) - 1) & 1, s_abort,
-                                     p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x2500 + it);
+      if (!wait_all(bar(WB_QF + s), (it / NS) & 1, 0x2400 + it)) { ok = false; break; }
+      if (it >= 2 && !wait_all(bar(WB_FREE + b), ((it >> 1) - 1) & 1, 0x2500 + it)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t q_tile = sQ + s * L::kQT;
-      const uint32_t do_tile = sDO + s * L::kQT;
-      // S^T = K Q^T and dP^T = V dO^T: K = d = 128; A [128][128] K-major in two
-      // 64-column blocks of 16 KB, B [64][128] K-major in two blocks of 8 KB.
+      // S^T = K Q^T and dP^T = V dO^T: K = d = 128; B [64][128] K-major in two
+      // blocks of 8 KB.
+      const uint64_t dQk = ptx::sdesc_sw128(sQ + s * L::kQT, 16, 1024);
+      const uint64_t dDOk = ptx::sdesc_sw128(sDO + s * L::kQT, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
         const uint32_t boff = (kk >> 2) * 8192 + (kk & 3) * 32;
-        ptx::mma_ss(tmem + 128 * b, ptx::sdesc_sw128(sK + aoff, 16, 1024),
-                         ptx::sdesc_sw128(q_tile + boff, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
-        ptx::mma_ss(tmem + 128 * b + 64, ptx::sdesc_sw128(sV + aoff, 16, 1024),
-                         ptx::sdesc_sw128(do_tile + boff, 16, 1024), idesc_sdp,
-                         kk > 0 ? 1u : 0u);
+        ptx::mma_ss_w(tmem + 128 * b, ptx::sdesc_add(dK, aoff), ptx::sdesc_add(dQk, boff),
+                      idesc_sdp, kk > 0 ? 1u : 0u, leader);
+        ptx::mma_ss_w(tmem + 128 * b + 64, ptx::sdesc_add(dV, aoff),
+                      ptx::sdesc_add(dDOk, boff), idesc_sdp, kk > 0 ? 1u : 0u, leader);
       }
-      ptx::mma_commit(bar(WB_SDP + b));
+      ptx::mma_commit_w(bar(WB_SDP + b), leader);
       if (it >= 1 && !tail(it - 1)) {
         ok = false;
         break;
       }
     }
     if (ok) tail(n_iter - 1);
-    ptx::mma_commit(bar(WB_DRAIN));
+    ptx::mma_commit_w(bar(WB_DRAIN), leader);
     const volatile int never = 0;
     ptx::mbar_wait(bar(WB_DRAIN), 0, &never, p.wait_limit_ns);
+    __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ compute
     const int wg = warp >> 2;                 // warpgroup = buffer parity it handles
@@ -604,9 +609,6 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     const int32_t dend = doc_end(p.cu, p.n_cu, kpos);
     const uint32_t tS = tmem + 128 * wg;
     const uint32_t tDP = tS + 64;
-    float* lse2 = s_row + wg * 128;
-    float* dlt = lse2 + 64;
-    const uint32_t pt = sPt + wg * L::kPT;
     const uint32_t dst = sDSt + wg * L::kPT;
     bool ok = true;
     for (int it = wg; it < n_iter; it += 2) {
@@ -615,12 +617,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       const int sub = it % n_sub;
       const int64_t q_row0 = q_row_base + static_cast<int64_t>(sub) * 64;
       const int32_t qpos0 = __ldg(q_tile_pos + w.lo + (sub >> 1)) + (sub & 1) * 64;
-      if (t < 64) {
-        lse2[t] = __ldg(p.lse + static_cast<int64_t>(h) * p.T_q + q_row0 + t) * kLog2e;
-        dlt[t] = __ldg(p.delta + static_cast<int64_t>(h) * p.T_q + q_row0 + t);
-      }
-      ptx::mbar_arrive(bar(WB_ROW + wg));
-      if (!ptx::mbar_wait(bar(WB_ROW + wg), k & 1, s_abort, p.wait_limit_ns)) {
+      // LSE and delta of the sub-tile arrive with its Q/dO stage
+      const float* lse = s_row + (it % NS) * 128;
+      const float* dlt = lse + 64;
+      if (!ptx::mbar_wait(bar(WB_QF + it % NS), (it / NS) & 1, s_abort, p.wait_limit_ns)) {
         ptx::record_timeout(p.status, s_abort, 0x2600 + it);
         ok = false;
       }
@@ -635,25 +635,51 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       ptx::tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
-        float sv[32], dp[32];
-        ptx::tmem_ld32(tS + lane_base + c * 32, sv);
-        ptx::tmem_ld32(tDP + lane_base + c * 32, dp);
+        float sv[32], dp[32], l2[32], dl[32];
+        ptx::tmem_ld32x2(tS + lane_base + c * 32, tDP + lane_base + c * 32, sv, dp);
+        // this chunk's LSE (to base 2) and delta, 16 bytes at a time
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int i = c * 32 + x;
-          const bool vis = full || (i >= lo_i && i <= hi_i);
-          const float pv = vis ? ptx::ex2(fmaf(sv[x], p.scale_log2, -lse2[i])) : 0.f;
-          sv[x] = pv;
-          dp[x] = pv * (dp[x] - dlt[i]);
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 a = reinterpret_cast<const float4*>(lse + c * 32)[k4];
+          const float4 d4 = reinterpret_cast<const float4*>(dlt + c * 32)[k4];
+          l2[4 * k4] = a.x * kLog2e;
+          l2[4 * k4 + 1] = a.y * kLog2e;
+          l2[4 * k4 + 2] = a.z * kLog2e;
+          l2[4 * k4 + 3] = a.w * kLog2e;
+          dl[4 * k4] = d4.x;
+          dl[4 * k4 + 1] = d4.y;
+          dl[4 * k4 + 2] = d4.z;
+          dl[4 * k4 + 3] = d4.w;
         }
+        if (full) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const float pv = ptx::ex2(fmaf(sv[x], p.scale_log2, -l2[x]));
+            sv[x] = pv;
+            dp[x] = pv * (dp[x] - dl[x]);
+          }
+        } else {
+          // branch-free mask: an invisible pair gets exponent -inf, i.e. P = 0
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int i = c * 32 + x;
+            const bool vis = i >= lo_i && i <= hi_i;
+            const float arg = vis ? fmaf(sv[x], p.scale_log2, -l2[x]) : -INFINITY;
+            const float pv = ptx::ex2(arg);
+            sv[x] = pv;
+            dp[x] = pv * (dp[x] - dl[x]);
+          }
+        }
+        // P^T as fp16 pairs into S^T columns [16c, 16c + 16) (already read)
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) pk[x] = ptx::pack_f16(sv[2 * x], sv[2 * x + 1]);
+        ptx::tmem_st16(tS + lane_base + c * 16, pk);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int chunk = c * 4 + ch;  // 16-byte chunk of the 128-byte row
           const uint32_t off = static_cast<uint32_t>(t * 128 + (((chunk ^ t) & 7) << 4));
-          const float* a = sv + ch * 8;
           const float* g = dp + ch * 8;
-          ptx::st_shared_v4(pt + off, ptx::pack_f16(a[0], a[1]), ptx::pack_f16(a[2], a[3]),
-                            ptx::pack_f16(a[4], a[5]), ptx::pack_f16(a[6], a[7]));
           ptx::st_shared_v4(dst + off, ptx::pack_f16(g[0], g[1]), ptx::pack_f16(g[2], g[3]),
                             ptx::pack_f16(g[4], g[5]), ptx::pack_f16(g[6], g[7]));
         }
@@ -670,16 +696,15 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       // dQ^T: lane t = column t of d; column qi = query row qi of the sub-tile.
       float* dq_col = p.dq + (q_row0 * p.Hq + h) * D + t;
       const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        ptx::tmem_ld32(tS + lane_base + c * 32, v);
+      {
+        float v[64];
+        ptx::tmem_ld64(tS + lane_base, v);
+        // TMEM columns are free once read: let the next S^T/dP^T in
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(WB_FREE + wg));
 #pragma unroll
-        for (int x = 0; x < 32; ++x)
-          atomicAdd(dq_col + (c * 32 + x) * row_stride, v[x] * p.scale);
+        for (int x = 0; x < 64; ++x) atomicAdd(dq_col + x * row_stride, v[x] * p.scale);
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(WB_FREE + wg));
     }
     // dK (warpgroup 0) and dV (warpgroup 1) once every MMA has finished
     ok = __all_sync(0xffffffffu, ok);

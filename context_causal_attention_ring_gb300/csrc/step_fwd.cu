@@ -506,44 +506,48 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       ptx::mbar_wait(bar(PB_K + j % NS), (j / NS) & 1, &never, p.wait_limit_ns);
       ptx::mbar_wait(bar(PB_V + j % NS), (j / NS) & 1, &never, p.wait_limit_ns);
     }
-  } else if (n_tiles > 0 && warp == 9 && lane == 0) {
+  } else if (n_tiles > 0 && warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop so that descriptors stay warp-uniform;
+    // lane 0 alone issues each tcgen05 instruction.
+    const uint32_t leader = lane == 0 ? 1u : 0u;
     constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
-    bool ok = ptx::mbar_wait(bar(PB_Q), 0, s_abort, p.wait_limit_ns);
-    if (!ok) ptx::record_timeout(p.status, s_abort, 0x3200);
+    const uint64_t dQ0 = ptx::sdesc_sw128(sQ, 16, 1024);
+    auto wait_all = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+      const bool w_ok = ptx::mbar_wait(b_, parity, s_abort, p.wait_limit_ns);
+      if (!w_ok) ptx::record_timeout(p.status, s_abort, where);
+      return __all_sync(0xffffffffu, w_ok);
+    };
+    bool ok = wait_all(bar(PB_Q), 0, 0x3200);
     auto issue_s = [&](int j, int hs) {
-      const uint32_t k_tile = sK + (j % NS) * L::kTile;
-      const uint32_t q_tile = sQ + hs * L::kTile;
+      // S = Q K^T: both K-major, two 64-column blocks of 16 KB each
+      const uint64_t dk = ptx::sdesc_sw128(sK + (j % NS) * L::kTile, 16, 1024);
+      const uint64_t dq = ptx::sdesc_add(dQ0, hs * L::kTile);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_ss(tmem + 128 * hs, ptx::sdesc_sw128(q_tile + off, 16, 1024),
-                    ptx::sdesc_sw128(k_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_ss_w(tmem + 128 * hs, ptx::sdesc_add(dq, off), ptx::sdesc_add(dk, off), idesc_s,
+                      kk > 0 ? 1u : 0u, leader);
       }
-      ptx::mma_commit(bar(PB_S + hs));
+      ptx::mma_commit_w(bar(PB_S + hs), leader);
     };
     auto issue_o = [&](int j, int hs) -> bool {
-      if (!ptx::mbar_wait(bar(PB_P + hs), j & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x3300 + j);
-        return false;
-      }
+      if (!wait_all(bar(PB_P + hs), j & 1, 0x3300 + j)) return false;
       ptx::tc_fence_after();
-      const uint32_t v_tile = sV + (j % NS) * L::kTile;
+      // B = V [keys][d] MN-major: 8-key groups at 1 KB, d 64..127 at +16 KB
+      const uint64_t dv = ptx::sdesc_sw128(sV + (j % NS) * L::kTile, 16384, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         // A = P (bf16 pairs in the head's S columns), 16 keys = 8 columns
-        ptx::mma_ts(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
-                    ptx::sdesc_sw128(v_tile + kk * 2048, 16384, 1024), idesc_o,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_ts_w(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
+                      ptx::sdesc_add(dv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
+                      leader);
       }
       return true;
     };
     auto wait_kv = [&](int bar_base, int j, int where) -> bool {
-      if (!ptx::mbar_wait(bar(bar_base + j % NS), (j / NS) & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, where + j);
-        return false;
-      }
+      if (!wait_all(bar(bar_base + j % NS), (j / NS) & 1, where + j)) return false;
       ptx::tc_fence_after();
       return true;
     };
@@ -554,25 +558,28 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       ok = false;
     }
     for (int j = 1; ok && j < n_tiles; ++j) {
-      if (!wait_kv(PB_K, j, 0x3400) || !wait_kv(PB_V, j - 1, 0x3500)) { ok = false; break; }
+      // O(j-1) only needs V(j-1): do not hold it behind the load of K(j)
+      if (!wait_kv(PB_V, j - 1, 0x3500)) { ok = false; break; }
       if (!issue_o(j - 1, 0)) { ok = false; break; }
+      if (!wait_kv(PB_K, j, 0x3400)) { ok = false; break; }
       issue_s(j, 0);  // executes after the O MMA above has read P_A (in-order pipe)
       if (nh == 2) {
         if (!issue_o(j - 1, 1)) { ok = false; break; }
         issue_s(j, 1);
       }
-      ptx::mma_commit(bar(PB_E + (j - 1) % NS));
+      ptx::mma_commit_w(bar(PB_E + (j - 1) % NS), leader);
     }
     if (ok && wait_kv(PB_V, n_tiles - 1, 0x3500)) {
       if (issue_o(n_tiles - 1, 0)) {
-        ptx::mma_commit(bar(PB_O + 0));
-        if (nh == 2 && issue_o(n_tiles - 1, 1)) ptx::mma_commit(bar(PB_O + 1));
+        ptx::mma_commit_w(bar(PB_O + 0), leader);
+        if (nh == 2 && issue_o(n_tiles - 1, 1)) ptx::mma_commit_w(bar(PB_O + 1), leader);
       }
-      ptx::mma_commit(bar(PB_E + (n_tiles - 1) % NS));
+      ptx::mma_commit_w(bar(PB_E + (n_tiles - 1) % NS), leader);
     }
-    ptx::mma_commit(bar(PB_DRAIN));
+    ptx::mma_commit_w(bar(PB_DRAIN), leader);
     const volatile int never = 0;
     ptx::mbar_wait(bar(PB_DRAIN), 0, &never, p.wait_limit_ns);
+    __syncwarp();
   } else if (warp < 8 && (warp >> 2) < nh) {
     // ------------------------------------------------------------ softmax
     const int hs = warp >> 2;
@@ -587,8 +594,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    int32_t kpos_next = n_tiles > 0 ? __ldg(kv_tile_pos + w.lo) : 0;
     for (int j = 0; j < n_tiles; ++j) {
-      const int32_t kpos0 = __ldg(kv_tile_pos + w.lo + j);
+      const int32_t kpos0 = kpos_next;
+      if (j + 1 < n_tiles) kpos_next = __ldg(kv_tile_pos + w.lo + j + 1);
       const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ds_last);
       if (!ptx::mbar_wait(bar(PB_S + hs), j & 1, s_abort, p.wait_limit_ns)) {
         ptx::record_timeout(p.status, s_abort, 0x3600 + j);
@@ -598,9 +607,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       // S(j) complete implies O += P V of tile j-1 complete (issued before it)
       ptx::tc_fence_after();
       float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        ptx::tmem_ld32(tS + lane_base + c * 32, *reinterpret_cast<float(*)[32]>(s + c * 32));
+      ptx::tmem_ld64x2(tS + lane_base, tS + lane_base + 64, *reinterpret_cast<float(*)[64]>(s),
+                       *reinterpret_cast<float(*)[64]>(s + 64));
       if (!full) {
         const int lo = my_ds - kpos0;
         const int hi = my_pos - kpos0;
