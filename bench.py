@@ -33,6 +33,29 @@ sys.path.insert(0, ROOT)
 from workloads import WORKLOADS, bf16_bits_to_f64, make_inputs  # noqa: E402
 
 METRIC = "causal attn TFLOPS fwd/bwd (unmasked FLOPs) and % of GB300 dense BF16 peak"
+
+# DRAM traffic per launch from the ncu captures summarised in profiles/, valid
+# only while the kernel source is the one that was profiled.
+PROFILED_TRAFFIC = {
+    "step_bwd": ("context_causal_attention_ring_gb300/csrc/step_bwd.cu",
+                 "6f4d0850f80fc96fec82177a9f73c535d58c41a81f370fc2da2e2c3c0c62432d", 3.083181e9),
+    "step_fwd": ("context_causal_attention_ring_gb300/csrc/step_fwd.cu",
+                 "962bcc022a36eb265601159221af02a28b2d626978a903101d90dc92b2e555b7", 1.288470e9),
+}
+
+
+def _profiled_traffic(kernel):
+    import hashlib
+    if kernel not in PROFILED_TRAFFIC:
+        return None
+    rel, digest, nbytes = PROFILED_TRAFFIC[kernel]
+    try:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() == digest:
+                return nbytes
+    except OSError:
+        pass
+    return None
 UNIT = "TFLOPS"
 
 
@@ -264,7 +287,7 @@ def run_ours(args, w):
         dom, dom_flops, dom_ms = "step_fwd", fwd_flops, sum(fwd_ms) / args.steps
     achieved = (dom_flops / R) / (dom_ms / R * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": _profiled_traffic(dom),
                 "peak_kind": f"bf16_tflops_sustained ({peak_kind}): timed inside a long loop",
                 "flops_per_launch": dom_flops / R}
 
