@@ -22,6 +22,7 @@
 // more than 8, so exponentials stay below 2^8 -- the result is the same
 // softmax; only the reference point of the exponentials moves.
 #include <cmath>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -396,6 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // O_B [384,512).
 constexpr int kThreadsP = 320;
 constexpr int kStagesP = 2;
+// Of every 8 column pairs of a full tile, this many take their exponentials
+// on the FMA pipe (the rest on MUFU).
+#ifndef CPA_FWD_EMU_PAIRS
+#define CPA_FWD_EMU_PAIRS 0
+#endif
+constexpr int kEmuPairs = CPA_FWD_EMU_PAIRS;
 
 enum : int {
   PB_Q = 0,
@@ -616,10 +623,19 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         for (int c = 0; c < 128; ++c)
           if (c < lo || c > hi) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row maximum: eight independent chains of three-input maxima
+      float mk[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      const float m_tile = mx * p.scale_log2;
+      for (int x = 0; x < 8; ++x) mk[x] = ptx::max3(s[2 * x], s[2 * x + 1], s[16 + 2 * x]);
+#pragma unroll
+      for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          mk[x] = c + 16 < 128 ? ptx::max3(mk[x], s[c + 2 * x + 1], s[c + 16 + 2 * x])
+                               : fmaxf(mk[x], s[c + 2 * x + 1]);
+      }
+      const float mx = fmaxf(ptx::max3(mk[0], mk[1], mk[2]), ptx::max3(mk[3], mk[4], mk[5]));
+      const float m_tile = ptx::max3(mx, mk[6], mk[7]) * p.scale_log2;
       float alpha = 1.f;
       if (m_tile > m_used + kRescaleThreshold) {
         alpha = ptx::ex2(m_used - m_tile);
@@ -627,21 +643,42 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         m_used = m_tile;
       }
       const float base = (m_used == -INFINITY) ? 0.f : m_used;
-      float rowsum = 0.f;
+      // P = 2^(s * scale_log2 - base), two columns per instruction, packed
+      // to bf16 pairs and stored into this head's S columns [0, 64) chunk by
+      // chunk; on full tiles (no -inf) a share of the pairs may go to the
+      // FMA pipe
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nb2 = make_float2(-base, -base);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
+      auto exp_pack_store = [&](auto emu_pairs) {
+        constexpr int kEmu = decltype(emu_pairs)::value;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = ptx::ex2(fmaf(s[c], p.scale_log2, -base));
-        rowsum += s[c];
-      }
-      l += rowsum;
-      // P as bf16 pairs into this head's S columns [0, 64)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) pk[x] = ptx::pack_bf16(s[c * 32 + 2 * x], s[c * 32 + 2 * x + 1]);
-        ptx::tmem_st16(tS + lane_base + c * 16, pk);
-      }
+          for (int x = 0; x < 16; ++x) {
+            const int i = c * 16 + x;
+            float2 e = ptx::fma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nb2);
+            if (((i * kEmu) & 7) < kEmu) {
+              e = ptx::exp2_poly2(e);
+            } else {
+              e.x = ptx::ex2(e.x);
+              e.y = ptx::ex2(e.y);
+            }
+            acc[x & 3] = ptx::add2(acc[x & 3], e);
+            pk[x] = ptx::pack_bf16(e.x, e.y);
+          }
+          ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
+        }
+      };
+      if (full) exp_pack_store(std::integral_constant<int, kEmuPairs>{});
+      else exp_pack_store(std::integral_constant<int, 0>{});
+      const float2 acc01 = ptx::add2(acc[0], acc[1]);
+      const float2 acc23 = ptx::add2(acc[2], acc[3]);
+      const float2 accs = ptx::add2(acc01, acc23);
+      l += accs.x + accs.y;
+      ptx::tmem_wait_st();
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
