@@ -391,12 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S_B(j), and the other way round, so exponentials and MMAs overlap. P is
 // written back into its own S columns of TMEM as bf16 pairs and feeds
 // O += P V as the A operand read from tensor memory (no shared-memory copy).
-// Warps: 0-3 softmax head A, 4-7 softmax head B, 8 TMA producer, 9 TMEM
-// owner + MMA issuer (320 threads).
+// K and V stream through separate rings with their own producer warps: a K
+// stage is released once both heads' S MMAs have read it, a V stage once both
+// O MMAs have, so the next tiles are requested well before they are needed.
+// Warps: 0-3 softmax head A, 4-7 softmax head B, 8 Q + K loads, 9 TMEM owner
+// + MMA issuer, 10 V loads (352 threads).
 // TMEM columns: S_A [0,128) (P_A in [0,64)), S_B [128,256), O_A [256,384),
 // O_B [384,512).
-constexpr int kThreadsP = 320;
-constexpr int kStagesP = 2;
+constexpr int kThreadsP = 352;
+constexpr int kKStagesP = 3;
+constexpr int kVStagesP = 2;
 // Of every 8 column pairs of a full tile, this many take their exponentials
 // on the FMA pipe (the rest on MUFU).
 #ifndef CPA_FWD_EMU_PAIRS
@@ -406,12 +410,13 @@ constexpr int kEmuPairs = CPA_FWD_EMU_PAIRS;
 
 enum : int {
   PB_Q = 0,
-  PB_K = 1,                     // [kStagesP]
-  PB_V = PB_K + kStagesP,       // [kStagesP]
-  PB_E = PB_V + kStagesP,       // [kStagesP] stage free
-  PB_S = PB_E + kStagesP,       // [2] S of head slot ready
-  PB_P = PB_S + 2,              // [2] P of head slot written (128 arrivals)
-  PB_O = PB_P + 2,              // [2] final O of head slot ready
+  PB_K = 1,                      // [kKStagesP] K tile landed
+  PB_V = PB_K + kKStagesP,       // [kVStagesP] V tile landed
+  PB_KE = PB_V + kVStagesP,      // [kKStagesP] K stage free
+  PB_VE = PB_KE + kKStagesP,     // [kVStagesP] V stage free
+  PB_S = PB_VE + kVStagesP,      // [2] S of head slot ready
+  PB_P = PB_S + 2,               // [2] P of head slot written (128 arrivals)
+  PB_O = PB_P + 2,               // [2] final O of head slot ready
   PB_DRAIN = PB_O + 2,
   PB_COUNT = PB_DRAIN + 1
 };
@@ -419,13 +424,37 @@ enum : int {
 struct FwdPairSmem {
   static constexpr int kTile = 128 * 128 * 2;
   static constexpr int kQ = 0;                          // [2 heads]
-  static constexpr int kK = kQ + 2 * kTile;             // [kStagesP]
-  static constexpr int kV = kK + kStagesP * kTile;      // [kStagesP]
-  static constexpr int kBar = kV + kStagesP * kTile;
+  static constexpr int kK = kQ + 2 * kTile;             // [kKStagesP]
+  static constexpr int kV = kK + kKStagesP * kTile;     // [kVStagesP]
+  static constexpr int kBar = kV + kVStagesP * kTile;
   static constexpr int kMisc = kBar + PB_COUNT * 8;
   static constexpr int kBytes = kMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;
+  // The dynamic shared-memory window starts 1 KB-aligned (checked by the
+  // kernel), so no alignment slack is reserved.
+  static constexpr int kAlloc = kBytes;
 };
+static_assert(FwdPairSmem::kAlloc <= 232448, "pair kernel shared memory");
+
+// Waits, by every lane of a warp, for N barrier phases; the usual case (all
+// complete) is settled by one round of non-blocking tests in flight
+// together. Returns false (agreed across the warp) on a timeout or abort.
+template <int N>
+__device__ __forceinline__ bool wait_phases(const uint32_t (&bars)[N], const uint32_t (&par)[N],
+                                            volatile int* abort_flag, uint64_t limit_ns,
+                                            int32_t* status, int where) {
+  bool done = true;
+#pragma unroll
+  for (int i = 0; i < N; ++i) done = ptx::mbar_test_wait(bars[i], par[i]) && done;
+  if (!__all_sync(0xffffffffu, done)) {
+    bool w_ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) w_ok = w_ok && ptx::mbar_wait(bars[i], par[i], abort_flag, limit_ns);
+    if (!w_ok) ptx::record_timeout(status, abort_flag, where);
+    if (!__all_sync(0xffffffffu, w_ok)) return false;
+  }
+  ptx::tc_fence_after();
+  return true;
+}
 
 __global__ void __launch_bounds__(kThreadsP, 1)
     step_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -433,12 +462,19 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                          const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using L = FwdPairSmem;
   constexpr int D = 128;
-  constexpr int NS = kStagesP;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
-  const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
-  uint8_t* smem = smem_raw + pad;
-  const uint32_t sbase = raw_u32 + pad;
+  constexpr int KS = kKStagesP;
+  constexpr int VS = kVStagesP;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = ptx::smem_u32(smem);
+  if (sbase & 1023u) {
+    // the 128-byte swizzled tiles need a 1 KB-aligned window: report, do nothing
+    if (threadIdx.x == 0 &&
+        atomicCAS(p.status, 0, static_cast<int>(CP_ATTN_ERR_UNSUPPORTED)) == 0) {
+      p.status[1] = static_cast<int>(blockIdx.x);
+      p.status[2] = 0x3F00;
+    }
+    return;
+  }
   const uint32_t sQ = sbase + L::kQ;
   const uint32_t sK = sbase + L::kK;
   const uint32_t sV = sbase + L::kV;
@@ -479,40 +515,44 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (n_tiles > 0 && warp == 8 && lane == 0) {
-    // ------------------------------------------------------------ producer
-    ptx::prefetch_tmap(&tm_q);
-    ptx::prefetch_tmap(&tm_k);
-    ptx::prefetch_tmap(&tm_v);
-    ptx::mbar_arrive_expect_tx(bar(PB_Q), nh * L::kTile);
-    for (int hs = 0; hs < nh; ++hs)
-      for (int b = 0; b < 2; ++b)
-        ptx::tma_load_3d(sQ + hs * L::kTile + b * 16384, &tm_q, bar(PB_Q), b * 64, hA + hs,
-                         static_cast<int>(q_row0));
+  if (n_tiles > 0 && (warp == 8 || warp == 10) && lane == 0) {
+    // ------------------------------------------------------------ producers
+    // warp 8: Q once, then K through its ring; warp 10: V through its ring
+    const bool is_k = warp == 8;
+    const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    const int NS = is_k ? KS : VS;
+    const int full_bar = is_k ? PB_K : PB_V;
+    const int free_bar = is_k ? PB_KE : PB_VE;
+    const uint32_t ring = is_k ? sK : sV;
+    ptx::prefetch_tmap(tm);
+    if (is_k) {
+      ptx::prefetch_tmap(&tm_q);
+      ptx::mbar_arrive_expect_tx(bar(PB_Q), nh * L::kTile);
+      for (int hs = 0; hs < nh; ++hs)
+        for (int b = 0; b < 2; ++b)
+          ptx::tma_load_3d(sQ + hs * L::kTile + b * 16384, &tm_q, bar(PB_Q), b * 64, hA + hs,
+                           static_cast<int>(q_row0));
+    }
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % NS;
       if (j >= NS) {
-        if (!ptx::mbar_wait(bar(PB_E + s), ((j / NS) - 1) & 1, s_abort, p.wait_limit_ns)) {
-          ptx::record_timeout(p.status, s_abort, 0x3100 + j);
+        if (!ptx::mbar_wait(bar(free_bar + s), ((j / NS) - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, (is_k ? 0x3100 : 0x3800) + j);
           break;
         }
       }
       const int row = static_cast<int>(kv_row_base + static_cast<int64_t>(w.lo + j) * 128);
-      ptx::mbar_arrive_expect_tx(bar(PB_K + s), L::kTile);
+      ptx::mbar_arrive_expect_tx(bar(full_bar + s), L::kTile);
       for (int b = 0; b < 2; ++b)
-        ptx::tma_load_3d(sK + s * L::kTile + b * 16384, &tm_k, bar(PB_K + s), b * 64, kh, row);
-      ptx::mbar_arrive_expect_tx(bar(PB_V + s), L::kTile);
-      for (int b = 0; b < 2; ++b)
-        ptx::tma_load_3d(sV + s * L::kTile + b * 16384, &tm_v, bar(PB_V + s), b * 64, kh, row);
+        ptx::tma_load_3d(ring + s * L::kTile + b * 16384, tm, bar(full_bar + s), b * 64, kh, row);
       issued = j + 1;
     }
+    // every issued copy must land before the CTA may exit
     const volatile int never = 0;
-    ptx::mbar_wait(bar(PB_Q), 0, &never, p.wait_limit_ns);
-    for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) {
-      ptx::mbar_wait(bar(PB_K + j % NS), (j / NS) & 1, &never, p.wait_limit_ns);
-      ptx::mbar_wait(bar(PB_V + j % NS), (j / NS) & 1, &never, p.wait_limit_ns);
-    }
+    if (is_k) ptx::mbar_wait(bar(PB_Q), 0, &never, p.wait_limit_ns);
+    for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
+      ptx::mbar_wait(bar(full_bar + j % NS), (j / NS) & 1, &never, p.wait_limit_ns);
   } else if (n_tiles > 0 && warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop so that descriptors stay warp-uniform;
@@ -521,15 +561,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
     const uint64_t dQ0 = ptx::sdesc_sw128(sQ, 16, 1024);
-    auto wait_all = [&](uint32_t b_, uint32_t parity, int where) -> bool {
-      const bool w_ok = ptx::mbar_wait(b_, parity, s_abort, p.wait_limit_ns);
-      if (!w_ok) ptx::record_timeout(p.status, s_abort, where);
-      return __all_sync(0xffffffffu, w_ok);
+    auto wait_set = [&](const auto& bars, const auto& par, int where) -> bool {
+      return wait_phases(bars, par, s_abort, p.wait_limit_ns, p.status, where);
     };
-    bool ok = wait_all(bar(PB_Q), 0, 0x3200);
     auto issue_s = [&](int j, int hs) {
       // S = Q K^T: both K-major, two 64-column blocks of 16 KB each
-      const uint64_t dk = ptx::sdesc_sw128(sK + (j % NS) * L::kTile, 16, 1024);
+      const uint64_t dk = ptx::sdesc_sw128(sK + (j % KS) * L::kTile, 16, 1024);
       const uint64_t dq = ptx::sdesc_add(dQ0, hs * L::kTile);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -539,11 +576,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       ptx::mma_commit_w(bar(PB_S + hs), leader);
     };
-    auto issue_o = [&](int j, int hs) -> bool {
-      if (!wait_all(bar(PB_P + hs), j & 1, 0x3300 + j)) return false;
-      ptx::tc_fence_after();
+    auto issue_o = [&](int j, int hs) {
       // B = V [keys][d] MN-major: 8-key groups at 1 KB, d 64..127 at +16 KB
-      const uint64_t dv = ptx::sdesc_sw128(sV + (j % NS) * L::kTile, 16384, 1024);
+      const uint64_t dv = ptx::sdesc_sw128(sV + (j % VS) * L::kTile, 16384, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         // A = P (bf16 pairs in the head's S columns), 16 keys = 8 columns
@@ -551,37 +586,46 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                       ptx::sdesc_add(dv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
                       leader);
       }
-      return true;
     };
-    auto wait_kv = [&](int bar_base, int j, int where) -> bool {
-      if (!wait_all(bar(bar_base + j % NS), (j / NS) & 1, where + j)) return false;
-      ptx::tc_fence_after();
-      return true;
-    };
-    if (ok && wait_kv(PB_K, 0, 0x3400)) {
+    bool ok;
+    {
+      const uint32_t b[2] = {bar(PB_Q), bar(PB_K)};
+      const uint32_t ph[2] = {0u, 0u};
+      ok = wait_set(b, ph, 0x3200);
+    }
+    if (ok) {
       issue_s(0, 0);
       if (nh == 2) issue_s(0, 1);
-    } else {
-      ok = false;
+      ptx::mma_commit_w(bar(PB_KE + 0), leader);
     }
-    for (int j = 1; ok && j < n_tiles; ++j) {
-      // O(j-1) only needs V(j-1): do not hold it behind the load of K(j)
-      if (!wait_kv(PB_V, j - 1, 0x3500)) { ok = false; break; }
-      if (!issue_o(j - 1, 0)) { ok = false; break; }
-      if (!wait_kv(PB_K, j, 0x3400)) { ok = false; break; }
-      issue_s(j, 0);  // executes after the O MMA above has read P_A (in-order pipe)
+    for (int j = 1; ok && j <= n_tiles; ++j) {
+      // head A: O(j-1) then S(j) (S(j) overwrites P(j-1): the pipe is in order)
+      const int jp = j - 1;
+      const bool more = j < n_tiles;
+      {
+        // after the last tile there is no K(j): test V(j-1) twice instead
+        const uint32_t b[3] = {bar(PB_P + 0), bar(PB_V + jp % VS),
+                               more ? bar(PB_K + j % KS) : bar(PB_V + jp % VS)};
+        const uint32_t ph[3] = {static_cast<uint32_t>(jp & 1), static_cast<uint32_t>((jp / VS) & 1),
+                                more ? static_cast<uint32_t>((j / KS) & 1)
+                                     : static_cast<uint32_t>((jp / VS) & 1)};
+        if (!wait_set(b, ph, 0x3300 + j)) { ok = false; break; }
+      }
+      issue_o(jp, 0);
+      if (more) issue_s(j, 0);
+      else ptx::mma_commit_w(bar(PB_O + 0), leader);
       if (nh == 2) {
-        if (!issue_o(j - 1, 1)) { ok = false; break; }
-        issue_s(j, 1);
+        const uint32_t b[1] = {bar(PB_P + 1)};
+        const uint32_t ph[1] = {static_cast<uint32_t>(jp & 1)};
+        if (!wait_set(b, ph, 0x3500 + j)) { ok = false; break; }
+        issue_o(jp, 1);
       }
-      ptx::mma_commit_w(bar(PB_E + (j - 1) % NS), leader);
-    }
-    if (ok && wait_kv(PB_V, n_tiles - 1, 0x3500)) {
-      if (issue_o(n_tiles - 1, 0)) {
-        ptx::mma_commit_w(bar(PB_O + 0), leader);
-        if (nh == 2 && issue_o(n_tiles - 1, 1)) ptx::mma_commit_w(bar(PB_O + 1), leader);
+      ptx::mma_commit_w(bar(PB_VE + jp % VS), leader);
+      if (nh == 2) {
+        if (more) issue_s(j, 1);
+        else ptx::mma_commit_w(bar(PB_O + 1), leader);
       }
-      ptx::mma_commit_w(bar(PB_E + (n_tiles - 1) % NS), leader);
+      if (more) ptx::mma_commit_w(bar(PB_KE + j % KS), leader);
     }
     ptx::mma_commit_w(bar(PB_DRAIN), leader);
     const volatile int never = 0;
@@ -704,7 +748,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const int64_t g = q_row0 + r;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const float lse_t = l > 0.f ? (m_used + ptx::lg2(l)) * kLn2 : -INFINITY;
-      const int64_t row_off = (g * p.Hq + h) * D;
       const int64_t lse_off = static_cast<int64_t>(h) * p.T_q + g;
       float w_old = 0.f, w_new = 1.f, lse_out = lse_t;
       const bool merge = (p.mode == CP_ATTN_ACCUMULATE) && !p.first;
@@ -730,37 +773,69 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           lse_out = (M + ptx::lg2(sum)) * kLn2;
         }
       }
-      lse_dst[lse_off] = lse_out;
-      float4* od = reinterpret_cast<float4*>(o_dst + row_off);
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        if (n_tiles > 0) {
-          ptx::tmem_ld32(tO + lane_base + c * 32, o);
-        } else {
+      // A merge with nothing new (no visible tile) leaves O and LSE as they are.
+      const bool keep_old = merge && n_tiles == 0;
+      if (!keep_old) lse_dst[lse_off] = lse_out;
+      if (!(keep_old && p.o_final == nullptr)) {
+        // O rows leave through shared memory so that global accesses are
+        // coalesced: per 32-column chunk the warp stages its 32 rows (each
+        // thread its own row, 16-byte units XOR-swizzled by row), then
+        // writes 4 rows per instruction, 128 contiguous bytes per row.
+        // Staging uses this head's Q tile, free once its S MMAs are done.
+        ptx::fence_proxy_async_smem();
+        uint8_t* stage = smem + L::kQ + hs * L::kTile + (warp & 3) * 8192;
+        const int sub = lane >> 3;  // row within a group of four
+        const int q4 = lane & 7;    // 16-byte unit within the chunk
+        const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
+        const int64_t base_off = ((q_row0 + (warp & 3) * 32) * p.Hq + h) * D + q4 * 4;
+        // per-row weights of the rows this lane writes: new = a * o + b * old
+        const float a_row = inv_l * w_new;
+        float a_r[8], b_r[8];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        for (int it = 0; it < 8; ++it) {
+          a_r[it] = __shfl_sync(0xffffffffu, a_row, it * 4 + sub);
+          b_r[it] = __shfl_sync(0xffffffffu, w_old, it * 4 + sub);
         }
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          if (n_tiles > 0) {
+            ptx::tmem_ld32(tO + lane_base + c * 32, o);
+          } else {
 #pragma unroll
-        for (int x4 = 0; x4 < 8; ++x4) {
-          float4 v;
-          v.x = o[x4 * 4 + 0] * inv_l;
-          v.y = o[x4 * 4 + 1] * inv_l;
-          v.z = o[x4 * 4 + 2] * inv_l;
-          v.w = o[x4 * 4 + 3] * inv_l;
-          if (merge) {
-            const float4 u = od[c * 8 + x4];
-            v.x = u.x * w_old + v.x * w_new;
-            v.y = u.y * w_old + v.y * w_new;
-            v.z = u.z * w_old + v.z * w_new;
-            v.w = u.w * w_old + v.w * w_new;
+            for (int x = 0; x < 32; ++x) o[x] = 0.f;
           }
-          od[c * 8 + x4] = v;
-          if (p.o_final) {
-            uint2 pk;
-            pk.x = ptx::pack_bf16(v.x, v.y);
-            pk.y = ptx::pack_bf16(v.z, v.w);
-            *reinterpret_cast<uint2*>(p.o_final + row_off + c * 32 + x4 * 4) = pk;
+          uint8_t* buf = stage + (c & 1) * 4096;
+#pragma unroll
+          for (int x4 = 0; x4 < 8; ++x4)
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((x4 ^ (lane & 7)) << 4)) =
+                make_float4(o[4 * x4], o[4 * x4 + 1], o[4 * x4 + 2], o[4 * x4 + 3]);
+          __syncwarp();
+          float4 old[8];
+          if (merge) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it)
+              old[it] = *reinterpret_cast<const float4*>(o_dst + base_off + (it * 4 + sub) * row_stride + c * 32);
+          }
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int row = it * 4 + sub;
+            const float4 t = *reinterpret_cast<const float4*>(buf + row * 128 + ((q4 ^ (row & 7)) << 4));
+            float4 v = make_float4(t.x * a_r[it], t.y * a_r[it], t.z * a_r[it], t.w * a_r[it]);
+            if (merge) {
+              v.x = fmaf(old[it].x, b_r[it], v.x);
+              v.y = fmaf(old[it].y, b_r[it], v.y);
+              v.z = fmaf(old[it].z, b_r[it], v.z);
+              v.w = fmaf(old[it].w, b_r[it], v.w);
+            }
+            const int64_t off = base_off + row * row_stride + c * 32;
+            if (!keep_old) *reinterpret_cast<float4*>(o_dst + off) = v;
+            if (p.o_final) {
+              uint2 pk;
+              pk.x = ptx::pack_bf16(v.x, v.y);
+              pk.y = ptx::pack_bf16(v.z, v.w);
+              *reinterpret_cast<uint2*>(p.o_final + off) = pk;
+            }
           }
         }
       }
