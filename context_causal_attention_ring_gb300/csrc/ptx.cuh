@@ -476,5 +476,26 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
   }
 }
 
+// Waits, by every lane of a warp, for N barrier phases; the usual case (all
+// complete) is settled by one round of non-blocking tests in flight
+// together. Returns false (agreed across the warp) on a timeout or abort.
+template <int N>
+__device__ __forceinline__ bool wait_phases(const uint32_t (&bars)[N], const uint32_t (&par)[N],
+                                            volatile int* abort_flag, uint64_t limit_ns,
+                                            int32_t* status, int where) {
+  bool done = true;
+#pragma unroll
+  for (int i = 0; i < N; ++i) done = mbar_test_wait(bars[i], par[i]) && done;
+  if (!__all_sync(0xffffffffu, done)) {
+    bool w_ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) w_ok = w_ok && mbar_wait(bars[i], par[i], abort_flag, limit_ns);
+    if (!w_ok) record_timeout(status, abort_flag, where);
+    if (!__all_sync(0xffffffffu, w_ok)) return false;
+  }
+  tc_fence_after();
+  return true;
+}
+
 }  // namespace ptx
 }  // namespace cpa

@@ -378,18 +378,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   dP^T = V dO^T   (M = 128 keys, N = 64)   TMEM buffer b
 //   P^T (fp16) -> back into buffer b's S^T columns of TMEM, dS^T (fp16) ->
 //   shared-memory buffer b, by compute warpgroup b
+//   dQ^T = K^T dS^T (M = 128 = d, N = 64)   TMEM, in buffer b's dP^T columns
 //   dV += P^T dO (P^T read from TMEM), dK += dS^T Q   (M = 128 keys, N = 128)
-//   dQ^T = K^T dS^T (M = 128 = d, N = 64)   TMEM, in buffer b's S^T columns
 // Two compute warpgroups take alternate iterations, so one warpgroup's
 // exponentials and its dQ read-out overlap the other's MMAs, and both TMEM
-// buffers and both shared-memory buffers alternate with them. dQ comes out
+// buffers and both shared-memory buffers alternate with them. The MMA warp
+// issues S^T/dP^T of iteration it+1 before the dQ^T/dV/dK of iteration it,
+// and dQ^T before dV/dK, so the read-out of dQ^T that frees a buffer runs
+// while the tensor core still has dV/dK queued. dQ comes out
 // transposed (TMEM lane = column of d), so each warp's fp32 reduction into
 // dq covers 32 consecutive floats of one query row: one 128-byte line per
 // instruction.
 // Warps: 0-3 compute warpgroup 0, 4-7 compute warpgroup 1, 8 TMA producer,
 // 9 TMEM owner + MMA issuer (320 threads).
-// TMEM columns: buffer b: S^T (then P^T in its first 32 columns, then dQ^T)
-// [128b, 128b+64), dP^T [128b+64, 128b+128); dV [256, 384), dK [384, 512).
+// TMEM columns: buffer b: S^T (then P^T in its first 32 columns)
+// [128b, 128b+64), dP^T (then dQ^T) [128b+64, 128b+128); dV [256, 384),
+// dK [384, 512).
 // Q/dO (and the sub-tile's LSE/delta rows) come through a 3-stage TMA ring:
 // a stage is free only after that iteration's dV/dK MMAs, so two stages would
 // leave the next load's latency exposed every iteration.
@@ -536,7 +540,39 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       return __all_sync(0xffffffffu, w_ok);
     };
     bool ok = wait_all(bar(WB_KV), 0, 0x2200);
-    // dV, dK and dQ^T of iteration i (the second half of an iteration)
+    // First half of iteration it: S^T = K Q^T and dP^T = V dO^T into buffer
+    // it & 1, once its Q/dO stage has landed and the buffer's previous dQ^T
+    // has been read out.
+    auto head = [&](int it) -> bool {
+      const int b = it & 1;
+      const int s = it % NS;
+      {
+        // the stage's Q/dO and the buffer's previous dQ^T read-out (none
+        // before the third iteration: test the stage twice instead)
+        const uint32_t bs[2] = {bar(WB_QF + s), it >= 2 ? bar(WB_FREE + b) : bar(WB_QF + s)};
+        const uint32_t ph[2] = {static_cast<uint32_t>((it / NS) & 1),
+                                it >= 2 ? static_cast<uint32_t>(((it >> 1) - 1) & 1)
+                                        : static_cast<uint32_t>((it / NS) & 1)};
+        if (!ptx::wait_phases(bs, ph, s_abort, p.wait_limit_ns, p.status, 0x2400 + it)) return false;
+      }
+      // K = d = 128; B [64][128] K-major in two blocks of 8 KB.
+      const uint64_t dQk = ptx::sdesc_sw128(sQ + s * L::kQT, 16, 1024);
+      const uint64_t dDOk = ptx::sdesc_sw128(sDO + s * L::kQT, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t boff = (kk >> 2) * 8192 + (kk & 3) * 32;
+        ptx::mma_ss_w(tmem + 128 * b, ptx::sdesc_add(dK, aoff), ptx::sdesc_add(dQk, boff),
+                      idesc_sdp, kk > 0 ? 1u : 0u, leader);
+        ptx::mma_ss_w(tmem + 128 * b + 64, ptx::sdesc_add(dV, aoff),
+                      ptx::sdesc_add(dDOk, boff), idesc_sdp, kk > 0 ? 1u : 0u, leader);
+      }
+      ptx::mma_commit_w(bar(WB_SDP + b), leader);
+      return true;
+    };
+    // Second half of iteration i, once its P^T and dS^T are written: dQ^T
+    // first (the compute warps read it out while dV and dK run), then dV and
+    // dK, after which the Q/dO stage is free.
     auto tail = [&](int i) -> bool {
       const int b = i & 1;
       const int s = i % NS;
@@ -545,6 +581,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       // dS^T buffer: [128 keys][64 q] fp16, one 128-byte swizzle column; read
       // K-major as A of dK and MN-major as B of dQ^T (same descriptor bits).
       const uint64_t dDS = ptx::sdesc_sw128(sDSt + b * L::kPT, 16, 1024);
+      // dQ^T = K^T dS^T: M = d, N = 64 q, K = 128 keys, into the dP^T
+      // columns of the buffer (already read by the compute warps).
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        ptx::mma_ss_w(tmem + 128 * b + 64, ptx::sdesc_add(dK_mn, kk * 2048),
+                      ptx::sdesc_add(dDS, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u, leader);
+      ptx::mma_commit_w(bar(WB_DQ + b), leader);
       // Q / dO sub-tile [64 q][128 d] as MN-major B: d 64..127 at +8 KB
       const uint64_t dQm = ptx::sdesc_sw128(sQ + s * L::kQT, 8192, 1024);
       const uint64_t dDOm = ptx::sdesc_sw128(sDO + s * L::kQT, 8192, 1024);
@@ -559,43 +602,15 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                       idesc_kv, acc, leader);
       }
       ptx::mma_commit_w(bar(WB_QE + s), leader);
-      // dQ^T = K^T dS^T: M = d, N = 64 q, K = 128 keys.
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        ptx::mma_ss_w(tmem + 128 * b, ptx::sdesc_add(dK_mn, kk * 2048),
-                      ptx::sdesc_add(dDS, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u, leader);
-      ptx::mma_commit_w(bar(WB_DQ + b), leader);
       return true;
     };
+    // S^T/dP^T of the next iteration go in before the tail of this one, so
+    // that the other warpgroup computes while this tail runs.
+    if (ok) ok = head(0);
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int b = it & 1;
-      const int s = it % NS;
-      if (!wait_all(bar(WB_QF + s), (it / NS) & 1, 0x2400 + it)) { ok = false; break; }
-      if (it >= 2 && !wait_all(bar(WB_FREE + b), ((it >> 1) - 1) & 1, 0x2500 + it)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      // S^T = K Q^T and dP^T = V dO^T: K = d = 128; B [64][128] K-major in two
-      // blocks of 8 KB.
-      const uint64_t dQk = ptx::sdesc_sw128(sQ + s * L::kQT, 16, 1024);
-      const uint64_t dDOk = ptx::sdesc_sw128(sDO + s * L::kQT, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t boff = (kk >> 2) * 8192 + (kk & 3) * 32;
-        ptx::mma_ss_w(tmem + 128 * b, ptx::sdesc_add(dK, aoff), ptx::sdesc_add(dQk, boff),
-                      idesc_sdp, kk > 0 ? 1u : 0u, leader);
-        ptx::mma_ss_w(tmem + 128 * b + 64, ptx::sdesc_add(dV, aoff),
-                      ptx::sdesc_add(dDOk, boff), idesc_sdp, kk > 0 ? 1u : 0u, leader);
-      }
-      ptx::mma_commit_w(bar(WB_SDP + b), leader);
-      if (it >= 1 && !tail(it - 1)) {
-        ok = false;
-        break;
-      }
+      if (it + 1 < n_iter && !head(it + 1)) { ok = false; break; }
+      if (!tail(it)) { ok = false; break; }
     }
-    if (ok) tail(n_iter - 1);
     ptx::mma_commit_w(bar(WB_DRAIN), leader);
     const volatile int never = 0;
     ptx::mbar_wait(bar(WB_DRAIN), 0, &never, p.wait_limit_ns);
@@ -698,7 +713,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
       {
         float v[64];
-        ptx::tmem_ld64(tS + lane_base, v);
+        ptx::tmem_ld64(tDP + lane_base, v);
         // TMEM columns are free once read: let the next S^T/dP^T in
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(WB_FREE + wg));
@@ -713,22 +728,42 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       const bool done = ptx::mbar_wait(bar(WB_DRAIN), 0, &never, p.wait_limit_ns);
       if (__all_sync(0xffffffffu, done)) {
         ptx::tc_fence_after();
-        float* dst_row = (wg == 0 ? p.dk : p.dv) + ((kv_row0 + t) * p.Hkv + kh) * D;
+        // Rows leave through shared memory so that the global read-modify-
+        // write is coalesced: per 32-column chunk the warp stages its 32 rows
+        // (each thread its own row, 16-byte units XOR-swizzled by row), then
+        // updates 4 rows per instruction, 128 contiguous bytes per row. The
+        // Q/dO stages are free once every MMA has finished.
+        ptx::fence_proxy_async_smem();
+        float* dst = wg == 0 ? p.dk : p.dv;
         const uint32_t src = wg == 0 ? tDK : tDV;
         const float mul = wg == 0 ? p.scale : 1.f;
+        uint8_t* stage = smem + L::kQ + warp * 8192;
+        const int sub = lane >> 3;  // row within a group of four
+        const int q4 = lane & 7;    // 16-byte unit within the chunk
+        const int64_t row_stride = static_cast<int64_t>(p.Hkv) * D;
+        const int64_t base_off = ((kv_row0 + (warp & 3) * 32) * p.Hkv + kh) * D + q4 * 4;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float a[32];
           ptx::tmem_ld32(src + lane_base + c * 32, a);
-          float4* d4 = reinterpret_cast<float4*>(dst_row + c * 32);
+          uint8_t* buf = stage + (c & 1) * 4096;
 #pragma unroll
-          for (int x4 = 0; x4 < 8; ++x4) {
-            float4 u = d4[x4];
-            u.x += a[x4 * 4] * mul;
-            u.y += a[x4 * 4 + 1] * mul;
-            u.z += a[x4 * 4 + 2] * mul;
-            u.w += a[x4 * 4 + 3] * mul;
-            d4[x4] = u;
+          for (int x4 = 0; x4 < 8; ++x4)
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((x4 ^ (lane & 7)) << 4)) =
+                make_float4(a[4 * x4] * mul, a[4 * x4 + 1] * mul, a[4 * x4 + 2] * mul,
+                            a[4 * x4 + 3] * mul);
+          __syncwarp();
+          float4 old[8];
+#pragma unroll
+          for (int it = 0; it < 8; ++it)
+            old[it] = *reinterpret_cast<const float4*>(dst + base_off + (it * 4 + sub) * row_stride + c * 32);
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int row = it * 4 + sub;
+            const float4 t4 = *reinterpret_cast<const float4*>(buf + row * 128 + ((q4 ^ (row & 7)) << 4));
+            const float4 v = make_float4(old[it].x + t4.x, old[it].y + t4.y, old[it].z + t4.z,
+                                         old[it].w + t4.w);
+            *reinterpret_cast<float4*>(dst + base_off + row * row_stride + c * 32) = v;
           }
         }
       } else {

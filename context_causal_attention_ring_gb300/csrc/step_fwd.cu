@@ -435,27 +435,6 @@ struct FwdPairSmem {
 };
 static_assert(FwdPairSmem::kAlloc <= 232448, "pair kernel shared memory");
 
-// Waits, by every lane of a warp, for N barrier phases; the usual case (all
-// complete) is settled by one round of non-blocking tests in flight
-// together. Returns false (agreed across the warp) on a timeout or abort.
-template <int N>
-__device__ __forceinline__ bool wait_phases(const uint32_t (&bars)[N], const uint32_t (&par)[N],
-                                            volatile int* abort_flag, uint64_t limit_ns,
-                                            int32_t* status, int where) {
-  bool done = true;
-#pragma unroll
-  for (int i = 0; i < N; ++i) done = ptx::mbar_test_wait(bars[i], par[i]) && done;
-  if (!__all_sync(0xffffffffu, done)) {
-    bool w_ok = true;
-#pragma unroll
-    for (int i = 0; i < N; ++i) w_ok = w_ok && ptx::mbar_wait(bars[i], par[i], abort_flag, limit_ns);
-    if (!w_ok) ptx::record_timeout(status, abort_flag, where);
-    if (!__all_sync(0xffffffffu, w_ok)) return false;
-  }
-  ptx::tc_fence_after();
-  return true;
-}
-
 __global__ void __launch_bounds__(kThreadsP, 1)
     step_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -562,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
     const uint64_t dQ0 = ptx::sdesc_sw128(sQ, 16, 1024);
     auto wait_set = [&](const auto& bars, const auto& par, int where) -> bool {
-      return wait_phases(bars, par, s_abort, p.wait_limit_ns, p.status, where);
+      return ptx::wait_phases(bars, par, s_abort, p.wait_limit_ns, p.status, where);
     };
     auto issue_s = [&](int j, int hs) {
       // S = Q K^T: both K-major, two 64-column blocks of 16 KB each
