@@ -38,9 +38,9 @@ METRIC = "causal attn TFLOPS fwd/bwd (unmasked FLOPs) and % of GB300 dense BF16 
 # only while the kernel source is the one that was profiled.
 PROFILED_TRAFFIC = {
     "step_bwd": ("context_causal_attention_ring_gb300/csrc/step_bwd.cu",
-                 "6f4d0850f80fc96fec82177a9f73c535d58c41a81f370fc2da2e2c3c0c62432d", 3.083181e9),
+                 "22ed59fda2fd3373194af78d5665db1864e5145353b020c033f97cdd07cbd383", 3.094209e9),
     "step_fwd": ("context_causal_attention_ring_gb300/csrc/step_fwd.cu",
-                 "962bcc022a36eb265601159221af02a28b2d626978a903101d90dc92b2e555b7", 1.288470e9),
+                 "35a5e784cbe8ba5fe94de81997be1ed9d3c60e89e1ac1b3b0159662189ad572f", 1.293699e9),
 }
 
 

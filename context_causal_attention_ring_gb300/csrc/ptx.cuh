@@ -411,30 +411,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// 2^x for a pair of finite x <= 128 on the FMA pipe instead of MUFU, so that
-// the two pipes share the exponentials of a softmax. Cody-Waite style split
-// x = n + f with n = round(x) (the 1.5 * 2^23 addition rounds to an integer
-// and leaves n in the low mantissa bits), f in [-1/2, 1/2]; 2^f by a cubic
-// fitted here by the Remez exchange algorithm for minimax relative error
-// (max relative error 7.5e-5, far below the bf16 rounding of P); 2^n is
-// added to the exponent field. x is clamped at -125 so that the result
-// stays a normal number (2^-125 instead of a smaller value or zero). Not
-// for -inf inputs (masked scores): those use ex2.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -125.0f);
-  x.y = fmaxf(x.y, -125.0f);
-  const float2 t = add2(x, make_float2(kShift, kShift));
-  const float2 n = sub2(t, make_float2(kShift, kShift));
-  const float2 f = sub2(x, n);
-  float2 p = fma2(make_float2(0.0551716691f, 0.0551716691f), f,
-                  make_float2(0.242611122f, 0.242611122f));
-  p = fma2(p, f, make_float2(0.693260985f, 0.693260985f));
-  p = fma2(p, f, make_float2(0.999928074f, 0.999928074f));
-  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -22,7 +22,6 @@
 // more than 8, so exponentials stay below 2^8 -- the result is the same
 // softmax; only the reference point of the exponentials moves.
 #include <cmath>
-#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -401,12 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kThreadsP = 352;
 constexpr int kKStagesP = 3;
 constexpr int kVStagesP = 2;
-// Of every 8 column pairs of a full tile, this many take their exponentials
-// on the FMA pipe (the rest on MUFU).
-#ifndef CPA_FWD_EMU_PAIRS
-#define CPA_FWD_EMU_PAIRS 0
-#endif
-constexpr int kEmuPairs = CPA_FWD_EMU_PAIRS;
 
 enum : int {
   PB_Q = 0,
@@ -668,35 +661,25 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const float base = (m_used == -INFINITY) ? 0.f : m_used;
       // P = 2^(s * scale_log2 - base), two columns per instruction, packed
       // to bf16 pairs and stored into this head's S columns [0, 64) chunk by
-      // chunk; on full tiles (no -inf) a share of the pairs may go to the
-      // FMA pipe
+      // chunk
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       const float2 nb2 = make_float2(-base, -base);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
-      auto exp_pack_store = [&](auto emu_pairs) {
-        constexpr int kEmu = decltype(emu_pairs)::value;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int i = c * 16 + x;
-            float2 e = ptx::fma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nb2);
-            if (((i * kEmu) & 7) < kEmu) {
-              e = ptx::exp2_poly2(e);
-            } else {
-              e.x = ptx::ex2(e.x);
-              e.y = ptx::ex2(e.y);
-            }
-            acc[x & 3] = ptx::add2(acc[x & 3], e);
-            pk[x] = ptx::pack_bf16(e.x, e.y);
-          }
-          ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
+        for (int x = 0; x < 16; ++x) {
+          const int i = c * 16 + x;
+          float2 e = ptx::fma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nb2);
+          e.x = ptx::ex2(e.x);
+          e.y = ptx::ex2(e.y);
+          acc[x & 3] = ptx::add2(acc[x & 3], e);
+          pk[x] = ptx::pack_bf16(e.x, e.y);
         }
-      };
-      if (full) exp_pack_store(std::integral_constant<int, kEmuPairs>{});
-      else exp_pack_store(std::integral_constant<int, 0>{});
+        ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
+      }
       const float2 acc01 = ptx::add2(acc[0], acc[1]);
       const float2 acc23 = ptx::add2(acc[2], acc[3]);
       const float2 accs = ptx::add2(acc01, acc23);
