@@ -6,7 +6,7 @@ there is no CPU fallback.
 """
 from ._abi import (  # noqa: F401
     ACCUMULATE, CpAttnError, LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG, OP_BACKWARD,
-    OP_FORWARD, PASS_KV, PASS_Q, Plan, TENSOR_KV, TENSOR_Q, TO_NATURAL,
+    OP_FORWARD, PASS_KV, PASS_Q, VARIANT_AUTO, Plan, TENSOR_KV, TENSOR_Q, TO_NATURAL,
     TO_RANK_MAJOR, WRITE_PARTIAL, exported_symbols, launch_count, lib_path,
-    load, merge_lse, status_string,
+    load, merge_lse, select_variant, status_string,
 )

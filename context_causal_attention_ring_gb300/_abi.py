@@ -20,14 +20,15 @@ from . import build as _build
 (OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT,
  ERR_RANGE) = range(8)
 LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG = 0, 1
-PASS_KV, PASS_Q = 0, 1
+PASS_KV, PASS_Q, VARIANT_AUTO = 0, 1, 2
 WRITE_PARTIAL, ACCUMULATE = 0, 1
 OP_FORWARD, OP_BACKWARD = 0, 1
 TENSOR_Q, TENSOR_KV = 0, 1
 TO_RANK_MAJOR, TO_NATURAL = 0, 1
 
 LAYOUTS = {"contiguous": LAYOUT_CONTIGUOUS, "zigzag": LAYOUT_ZIGZAG}
-VARIANTS = {"pass_kv": PASS_KV, "pass_q": PASS_Q}
+VARIANTS = {"pass_kv": PASS_KV, "pass_q": PASS_Q, "auto": VARIANT_AUTO}
+VARIANT_NAMES = {PASS_KV: "pass_kv", PASS_Q: "pass_q"}
 
 
 class CpAttnError(RuntimeError):
@@ -49,6 +50,7 @@ class _PlanDesc(ctypes.Structure):
         ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)),
         ("n_docs", ctypes.c_int),
         ("softmax_scale", ctypes.c_float),
+        ("window", ctypes.c_int64),
     ]
 
 
@@ -59,6 +61,7 @@ _SIG = {
     "cp_attn_plan": (_I, [ctypes.POINTER(_P), _I64, _I, _I, _I, _I, _I, _I,
                           ctypes.POINTER(ctypes.c_int32), _I]),
     "cp_attn_plan_ex": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_PlanDesc)]),
+    "cp_attn_select_variant": (_I, [_I64, _I64, _I, _I, ctypes.POINTER(_I)]),
     "cp_attn_plan_destroy": (None, [_P]),
     "cp_attn_plan_info": (_I, [_P, ctypes.POINTER(_I64), _I]),
     "cp_attn_plan_positions": (_I, [_P, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
@@ -146,13 +149,22 @@ def _check(status: int):
         raise CpAttnError(status, msg.decode() if msg else "")
 
 
+def select_variant(n_new: int, n_cached: int, n_q_heads: int, n_kv_heads: int) -> str:
+    """Pass KV or Pass Q for a prefill of n_new tokens after n_cached cached
+    ones (cp_attn_select_variant)."""
+    out = _I()
+    _check(load().cp_attn_select_variant(int(n_new), int(n_cached), int(n_q_heads),
+                                         int(n_kv_heads), ctypes.byref(out)))
+    return VARIANT_NAMES[out.value]
+
+
 class Plan:
     """Owner of a cp_attn_plan_t (host and device tables)."""
 
     def __init__(self, seq_len: int, cp: int, n_q_heads: int, n_kv_heads: int,
                  head_dim: int, layout: str = "zigzag", variant: str = "pass_kv",
                  cu_seqlens=None, kv_prefix_len: int = 0,
-                 softmax_scale: float = 0.0):
+                 softmax_scale: float = 0.0, window: int = 0):
         lib = load()
         self._keep = None
         desc = _PlanDesc()
@@ -170,16 +182,19 @@ class Plan:
             desc.cu_seqlens = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
             desc.n_docs = len(cu) - 1
         desc.softmax_scale = float(softmax_scale)
+        desc.window = int(window)
         h = _P()
         _check(lib.cp_attn_plan_ex(ctypes.byref(h), ctypes.byref(desc)))
         self.handle = h
-        info = (_I64 * 12)()
-        _check(lib.cp_attn_plan_info(h, info, 12))
+        info = (_I64 * 14)()
+        _check(lib.cp_attn_plan_info(h, info, 14))
         (self.T_q, self.T_kv, self.n_q, self.n_kv, self.R, self.Hq, self.Hkv,
-         self.d, self.n_qt, self.n_kt, self.n_docs, on_dev) = [int(x) for x in info]
+         self.d, self.n_qt, self.n_kt, self.n_docs, on_dev, var,
+         self.window) = [int(x) for x in info]
         self.on_device = bool(on_dev)
         self.layout = layout
-        self.variant = variant
+        # the ring ordering in use ("auto" resolved by the library)
+        self.variant = VARIANT_NAMES[var]
         self.kv_prefix_len = int(kv_prefix_len)
 
     def close(self):

@@ -222,12 +222,21 @@ void cp_attn_plan_destroy(cp_attn_plan_t plan) {
   delete plan;
 }
 
+cp_attn_status cp_attn_select_variant(int64_t n_new, int64_t n_cached, int n_q_heads,
+                                      int n_kv_heads, cp_attn_variant* out) {
+  clear_error();
+  if (!out || n_new <= 0 || n_cached < 0 || n_q_heads <= 0 || n_kv_heads <= 0)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "select_variant: bad arguments");
+  *out = select_variant_rule(n_new, n_cached, n_q_heads, n_kv_heads);
+  return CP_ATTN_OK;
+}
+
 cp_attn_status cp_attn_plan_info(cp_attn_plan_t p, int64_t* info, int n) {
   clear_error();
-  if (!p || !info || n < 0 || n > 12) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_info: bad arguments");
-  const int64_t v[12] = {p->T_q, p->T_kv, p->n_q, p->n_kv, p->R, p->Hq, p->Hkv, p->d,
+  if (!p || !info || n < 0 || n > 14) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_info: bad arguments");
+  const int64_t v[14] = {p->T_q, p->T_kv, p->n_q, p->n_kv, p->R, p->Hq, p->Hkv, p->d,
                          p->n_qt, p->n_kt, static_cast<int64_t>(p->cu.size()) - 1,
-                         p->on_device ? 1 : 0};
+                         p->on_device ? 1 : 0, static_cast<int64_t>(p->variant), p->window};
   for (int i = 0; i < n; ++i) info[i] = v[i];
   return CP_ATTN_OK;
 }
@@ -327,6 +336,7 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const
   fp.kv_tile_pos = p->d_kv_tile_pos;
   fp.cu = p->d_cu;
   fp.n_cu = static_cast<int>(p->cu.size());
+  fp.window = static_cast<int32_t>(p->window);
   fp.n_qt = p->n_qt;
   fp.n_kt = p->n_kt;
   fp.n_q = p->n_q;
@@ -386,6 +396,7 @@ cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops
   bp.kv_tile_pos = p->d_kv_tile_pos;
   bp.cu = p->d_cu;
   bp.n_cu = static_cast<int>(p->cu.size());
+  bp.window = static_cast<int32_t>(p->window);
   bp.n_qt = p->n_qt;
   bp.n_kt = p->n_kt;
   bp.n_q = p->n_q;

@@ -43,6 +43,7 @@ struct cp_attn_plan_s {
   cp_attn_layout layout = CP_ATTN_LAYOUT_ZIGZAG;
   cp_attn_variant variant = CP_ATTN_PASS_KV;
   float scale = 0.f;
+  int64_t window = 0;       // sliding window in tokens, 0 = none
   std::vector<int32_t> cu;  // document offsets (at least {0, P+N})
   // sizes
   int64_t n_q = 0, n_kv = 0, T_q = 0, T_kv = 0;
@@ -78,6 +79,11 @@ void clear_error();
 // planner (plan.cpp)
 cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc);
 int64_t doc_start_host(const std::vector<int32_t>& cu, int64_t pos);
+// First key visible to the query at `pos` (document start or window start).
+int64_t row_lo_host(const cp_attn_plan_s* p, int64_t pos);
+// Pass Q iff its ring message (the new tokens' Q) is smaller than Pass KV's
+// (K and V of all tokens).
+cp_attn_variant select_variant_rule(int64_t n_new, int64_t n_cached, int hq, int hkv);
 int tile_class(const cp_attn_plan_s* p, int qa_rank, int qt, int kb_rank, int kt);
 int64_t tile_visible_pairs(const cp_attn_plan_s* p, int qa_rank, int qt, int kb_rank,
                            int kt);

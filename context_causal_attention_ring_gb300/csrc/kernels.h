@@ -18,6 +18,7 @@ struct FwdParams {
   const int32_t* kv_tile_pos; // [R][n_kt]
   const int32_t* cu;          // document offsets
   int n_cu;                   // n_docs + 1
+  int32_t window;             // sliding window in tokens, 0 = none
   int n_qt, n_kt;
   int64_t n_q, n_kv, T_q;
   int Hq, G;
@@ -37,6 +38,7 @@ struct BwdParams {
   const int32_t* kv_tile_pos;
   const int32_t* cu;
   int n_cu;
+  int32_t window;             // sliding window in tokens, 0 = none
   int n_qt, n_kt;
   int64_t n_q, n_kv, T_q, T_kv;
   int Hq, Hkv, G;

@@ -11,10 +11,14 @@
 //
 // Block classes use a closed form on the contiguous position ranges of a
 // tile (every tile lies inside one chunk because chunks are multiples of 128
-// tokens). With ds(q) = start of q's document, a query q sees the keys in
-// [ds(q), q]. For queries [qa, qb] and keys [ka, kb]:
-//   non-empty  <=>  ka <= qb  and  kb >= ds(qa)
-//   full       <=>  kb <= qa  and  ka >= ds(qb)
+// tokens). A query q sees the keys in [lo(q), q], where lo(q) is the start of
+// q's document, or q - W + 1 with a sliding window of W tokens when that is
+// later (the window masks of the models that "mix sliding-window and global
+// layers", section "What's next" of the MaxText post). lo is nondecreasing in
+// q, so for queries [qa, qb] and keys [ka, kb], with q* = max(qa, ka):
+//   non-empty  <=>  q* <= qb  and  lo(q*) <= kb
+//   full       <=>  kb <= qa  and  ka >= lo(qb)
+// (without a window, lo(q*) <= kb reduces to ds(qa) <= kb.)
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -43,15 +47,26 @@ static void shard(int64_t n_tokens, int R, cp_attn_layout layout, int64_t offset
   }
 }
 
+int64_t row_lo_host(const cp_attn_plan_s* p, int64_t pos) {
+  const int64_t ds = doc_start_host(p->cu, pos);
+  return p->window > 0 ? std::max(ds, pos - p->window + 1) : ds;
+}
+
+cp_attn_variant select_variant_rule(int64_t n_new, int64_t n_cached, int hq, int hkv) {
+  // Pass Q sends T_new*Hq*d elements per hop, Pass KV 2*T_total*Hkv*d.
+  const double q_msg = static_cast<double>(n_new) * hq;
+  const double kv_msg = 2.0 * static_cast<double>(n_new + n_cached) * hkv;
+  return q_msg < kv_msg ? CP_ATTN_PASS_Q : CP_ATTN_PASS_KV;
+}
+
 int tile_class(const cp_attn_plan_s* p, int qr, int qt, int kr, int kt) {
   const int64_t qa = p->q_tile_pos[static_cast<size_t>(qr) * p->n_qt + qt];
   const int64_t qb = qa + kTile - 1;
   const int64_t ka = p->kv_tile_pos[static_cast<size_t>(kr) * p->n_kt + kt];
   const int64_t kb = ka + kTile - 1;
-  const int64_t ds_qa = doc_start_host(p->cu, qa);
-  if (!(ka <= qb && kb >= ds_qa)) return 0;
-  const int64_t ds_qb = doc_start_host(p->cu, qb);
-  if (kb <= qa && ka >= ds_qb) return 2;
+  const int64_t qs = std::max(qa, ka);
+  if (!(qs <= qb && row_lo_host(p, qs) <= kb)) return 0;
+  if (kb <= qa && ka >= row_lo_host(p, qb)) return 2;
   return 1;
 }
 
@@ -65,7 +80,7 @@ int64_t tile_visible_pairs(const cp_attn_plan_s* p, int qr, int qt, int kr, int 
   int64_t n = 0;
   for (int i = 0; i < kTile; ++i) {
     const int64_t q = qa + i;
-    const int64_t lo = std::max(ka, doc_start_host(p->cu, q));
+    const int64_t lo = std::max(ka, row_lo_host(p, q));
     const int64_t hi = std::min(kb, q);
     if (hi >= lo) n += hi - lo + 1;
   }
@@ -84,8 +99,10 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
     return fail(CP_ATTN_ERR_UNSUPPORTED, "plan: head_dim must be 64 or 128");
   if (desc->layout != CP_ATTN_LAYOUT_ZIGZAG && desc->layout != CP_ATTN_LAYOUT_CONTIGUOUS)
     return fail(CP_ATTN_ERR_INVALID_ARG, "plan: unknown layout");
-  if (desc->variant != CP_ATTN_PASS_KV && desc->variant != CP_ATTN_PASS_Q)
+  if (desc->variant != CP_ATTN_PASS_KV && desc->variant != CP_ATTN_PASS_Q &&
+      desc->variant != CP_ATTN_VARIANT_AUTO)
     return fail(CP_ATTN_ERR_INVALID_ARG, "plan: unknown variant");
+  if (desc->window < 0) return fail(CP_ATTN_ERR_SHAPE, "plan: window must be >= 0");
   const int64_t unit = (desc->layout == CP_ATTN_LAYOUT_ZIGZAG ? 2LL * R : 1LL * R) * kTile;
   if (N % unit != 0 || P % unit != 0)
     return fail(CP_ATTN_ERR_SHAPE,
@@ -103,7 +120,11 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
   p->Hkv = desc->n_kv_heads;
   p->d = desc->head_dim;
   p->layout = desc->layout;
-  p->variant = desc->variant;
+  p->variant = desc->variant == CP_ATTN_VARIANT_AUTO
+                   ? select_variant_rule(N, P, desc->n_q_heads, desc->n_kv_heads)
+                   : desc->variant;
+  // a window as long as the whole sequence masks nothing
+  p->window = desc->window >= N + P ? 0 : desc->window;
   p->scale = desc->softmax_scale > 0.f ? desc->softmax_scale
                                        : static_cast<float>(1.0 / std::sqrt(static_cast<double>(p->d)));
   // documents

@@ -441,6 +441,15 @@ __device__ __forceinline__ int32_t doc_start(const int32_t* __restrict__ cu, int
   return __ldg(cu + lo);
 }
 
+// First key visible to the query at global position `pos`: the start of its
+// document, or pos - window + 1 when a sliding window (window > 0) starts
+// later.
+__device__ __forceinline__ int32_t row_lo(const int32_t* __restrict__ cu, int n_cu,
+                                          int32_t window, int32_t pos) {
+  const int32_t ds = doc_start(cu, n_cu, pos);
+  return window > 0 ? max(ds, pos - window + 1) : ds;
+}
+
 // Marks the CTA as aborting and records the first timeout of the launch in
 // the status word: [0] = CP_ATTN_ERR_TIMEOUT, [1] = block, [2] = where.
 __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* abort_flag,

@@ -251,7 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = threadIdx.x;  // key row (P/dS) and query row (dQ read-out)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int32_t kpos = kpos0 + j;
-    const int32_t dend = doc_end(p.cu, p.n_cu, kpos);
+    // one past the last query that sees this key: its document end, or the
+    // end of the key's sliding window when that is earlier
+    const int32_t dend = p.window > 0 ? min(doc_end(p.cu, p.n_cu, kpos), kpos + p.window)
+                                      : doc_end(p.cu, p.n_cu, kpos);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int h = kh * p.G + it / n_qtiles;
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::record_timeout(p.status, s_abort, 0x1800 + it);
         ok = false;
       }
-      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ptx::doc_start(p.cu, p.n_cu, qpos0 + 127));
+      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ptx::row_lo(p.cu, p.n_cu, p.window, qpos0 + 127));
       const int lo_i = kpos - qpos0;        // first visible query column
       const int hi_i = dend - 1 - qpos0;    // last visible query column
       if (!ptx::mbar_wait(bar(BAR_S), it & 1, s_abort, p.wait_limit_ns) ||
@@ -621,7 +624,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     const int t = threadIdx.x & 127;          // key row (P/dS) and d column (dQ^T)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int32_t kpos = kpos0 + t;
-    const int32_t dend = doc_end(p.cu, p.n_cu, kpos);
+    // one past the last query that sees this key: its document end, or the
+    // end of the key's sliding window when that is earlier
+    const int32_t dend = p.window > 0 ? min(doc_end(p.cu, p.n_cu, kpos), kpos + p.window)
+                                      : doc_end(p.cu, p.n_cu, kpos);
     const uint32_t tS = tmem + 128 * wg;
     const uint32_t tDP = tS + 64;
     const uint32_t dst = sDSt + wg * L::kPT;
@@ -639,7 +645,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         ptx::record_timeout(p.status, s_abort, 0x2600 + it);
         ok = false;
       }
-      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ptx::doc_start(p.cu, p.n_cu, qpos0 + 63));
+      const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ptx::row_lo(p.cu, p.n_cu, p.window, qpos0 + 63));
       const int lo_i = kpos - qpos0;
       const int hi_i = dend - 1 - qpos0;
       if (ok && !ptx::mbar_wait(bar(WB_SDP + wg), k & 1, s_abort, p.wait_limit_ns)) {

@@ -221,8 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x;  // query row within the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int32_t my_pos = qpos0 + r;
-    const int32_t my_ds = ptx::doc_start(p.cu, p.n_cu, my_pos);
-    const int32_t ds_last = ptx::doc_start(p.cu, p.n_cu, qpos0 + 127);
+    // first visible key of a row: its document start, or the start of its
+    // sliding window when that is later
+    const int32_t my_ds = ptx::row_lo(p.cu, p.n_cu, p.window, my_pos);
+    const int32_t ds_last = ptx::row_lo(p.cu, p.n_cu, p.window, qpos0 + 127);
     float m_used = -INFINITY;  // reference point of the exponentials (base 2)
     float l = 0.f;
     bool ok = true;
@@ -612,8 +614,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const uint32_t tS = tmem + 128 * hs;
     const uint32_t tO = tmem + 256 + 128 * hs;
     const int32_t my_pos = qpos0 + r;
-    const int32_t my_ds = ptx::doc_start(p.cu, p.n_cu, my_pos);
-    const int32_t ds_last = ptx::doc_start(p.cu, p.n_cu, qpos0 + 127);
+    // first visible key of a row: its document start, or the start of its
+    // sliding window when that is later
+    const int32_t my_ds = ptx::row_lo(p.cu, p.n_cu, p.window, my_pos);
+    const int32_t ds_last = ptx::row_lo(p.cu, p.n_cu, p.window, qpos0 + 127);
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;

@@ -65,10 +65,13 @@ typedef enum cp_attn_layout {
 /* Ring ordering ("Ring Attention Algorithms"): PASS_KV keeps Q on its rank
  * and moves KV (at step t rank r holds the KV of rank (r-t) mod R);
  * PASS_Q keeps KV and moves Q (at step t rank r holds the Q of rank
- * (r-t) mod R), then returns partial outputs to their owners and merges. */
+ * (r-t) mod R), then returns partial outputs to their owners and merges.
+ * VARIANT_AUTO (plan descriptors only) picks one of the two at plan time
+ * with cp_attn_select_variant; cp_attn_plan_info reports the choice. */
 typedef enum cp_attn_variant {
   CP_ATTN_PASS_KV = 0,
-  CP_ATTN_PASS_Q = 1
+  CP_ATTN_PASS_Q = 1,
+  CP_ATTN_VARIANT_AUTO = 2
 } cp_attn_variant;
 
 /* Epilogue of cp_attn_step_fwd.
@@ -123,6 +126,13 @@ typedef struct cp_attn_plan_desc {
                                 and not after it. Copied by the plan. */
   int n_docs;
   float softmax_scale;    /* 0 selects 1/sqrt(head_dim) */
+  int64_t window;         /* sliding window W in tokens, 0 for none: a key k
+                             is then visible to query q only if q - k < W
+                             (on top of the document and causal rules). The
+                             window layers of models that "mix sliding-window
+                             and global layers" ("Announcing Long-Context
+                             Training on TPUs with MaxText Context
+                             Parallelism", section "What's next"). */
 } cp_attn_plan_desc;
 
 /* Build a plan: per-rank positions (zigzag or contiguous), the per-step
@@ -137,12 +147,27 @@ cp_attn_status cp_attn_plan(cp_attn_plan_t* out, int64_t seq_len, int cp,
                             cp_attn_layout layout, cp_attn_variant variant,
                             const int32_t* cu_seqlens, int n_docs);
 cp_attn_status cp_attn_plan_ex(cp_attn_plan_t* out, const cp_attn_plan_desc* desc);
+
+/* Pass KV or Pass Q for a prefill of n_new tokens after n_cached cached
+ * ones ("Ring Attention Algorithms": Pass KV suits full prefill and partial
+ * prefill with a low to medium KV-cache hit rate, Pass Q a high hit rate or
+ * decode). The rule compares the per-hop ring messages: Pass Q moves the new
+ * tokens' Q (n_new*Hq*d elements), Pass KV the K and V of all tokens
+ * (2*(n_new+n_cached)*Hkv*d). PASS_Q iff the first is strictly smaller,
+ * i.e. n_new/(n_new+n_cached) < 2*Hkv/Hq. (One page places the crossover at
+ * a ~10% cache *miss* rate with the opposite direction; this library follows
+ * the message-size argument and the qualitative statements, which agree.)
+ * ERR_INVALID_ARG for n_new <= 0, n_cached < 0, non-positive head counts or
+ * a NULL out. */
+cp_attn_status cp_attn_select_variant(int64_t n_new, int64_t n_cached, int n_q_heads,
+                                      int n_kv_heads, cp_attn_variant* out);
 void cp_attn_plan_destroy(cp_attn_plan_t plan);
 
-/* Sizes of a plan, written to info[0..n-1] (n <= 12):
+/* Sizes of a plan, written to info[0..n-1] (n <= 14):
  * 0 T_q (= R*n_q), 1 T_kv (= R*n_kv), 2 n_q (query rows per rank),
  * 3 n_kv (KV rows per rank), 4 R, 5 Hq, 6 Hkv, 7 d, 8 q tiles per rank,
- * 9 kv tiles per rank, 10 n_docs, 11 has device tables (0/1). */
+ * 9 kv tiles per rank, 10 n_docs, 11 has device tables (0/1),
+ * 12 ring ordering (cp_attn_variant, AUTO resolved), 13 window. */
 cp_attn_status cp_attn_plan_info(cp_attn_plan_t plan, int64_t* info, int n);
 
 /* Host queries (bit-exact plan artefacts; no device needed).

@@ -41,6 +41,15 @@ Readings where the pages are silent (each is listed in the design doc):
   global position P + i (P = cached length).
 * Backward: the standard softmax gradient with the global (merged) LSE, so
   each ring step's share uses P = exp(S - LSE_global).
+* Sliding window ([MaxText] "What's next": models that mix sliding-window
+  and global layers): with a window of W tokens a key is visible only if
+  it is also fewer than W positions behind the query (q - k < W); W = 0
+  means no window.
+* Pass KV or Pass Q ([CP-Inference] "Ring Attention Algorithms" and "Context
+  Parallelism (CP) vs. Tensor Parallelism (TP)"): the ring message of Pass Q
+  is the new tokens' Q (T_new * Hq * d), that of Pass KV the K and V of all
+  tokens (2 * T_total * Hkv * d); the cheaper one is chosen (Pass Q only
+  when strictly smaller).
 """
 from __future__ import annotations
 
@@ -64,6 +73,7 @@ __all__ = [
     "sampled_forward",
     "sampled_dq",
     "sampled_dkdv",
+    "select_variant",
     "TILE",
 ]
 
@@ -157,17 +167,25 @@ def doc_index(pos: np.ndarray, cu_seqlens) -> np.ndarray:
     return np.searchsorted(cu, pos, side="right") - 1
 
 
-def visible_mask(qpos, kpos, cu_seqlens=None) -> np.ndarray:
+def _vis(qp, qd, kp, kd, window):
+    """Visibility of keys (kp, kd) from queries (qp, qd): same document, not
+    after the query, and (with a window) fewer than `window` positions
+    behind it."""
+    v = (kp[None, :] <= qp[:, None]) & (kd[None, :] == qd[:, None])
+    if window:
+        v &= (qp[:, None] - kp[None, :]) < window
+    return v
+
+
+def visible_mask(qpos, kpos, cu_seqlens=None, *, window: int = 0) -> np.ndarray:
     """vis[i, j]: key at kpos[j] is visible from the query at qpos[i]."""
     qpos = np.asarray(qpos, dtype=np.int64)
     kpos = np.asarray(kpos, dtype=np.int64)
-    causal = kpos[None, :] <= qpos[:, None]
-    same_doc = doc_index(kpos, cu_seqlens)[None, :] == \
-        doc_index(qpos, cu_seqlens)[:, None]
-    return causal & same_doc
+    return _vis(qpos, doc_index(qpos, cu_seqlens), kpos, doc_index(kpos, cu_seqlens),
+                window)
 
 
-def block_mask(q_pos, kv_pos, cu_seqlens=None, tile: int = TILE):
+def block_mask(q_pos, kv_pos, cu_seqlens=None, tile: int = TILE, *, window: int = 0):
     """Tile class per (q_owner, kv_owner, q_tile, kv_tile), by brute force.
 
     EMPTY (0) if no (query, key) pair of the tile is visible, FULL (2) if all
@@ -181,7 +199,7 @@ def block_mask(q_pos, kv_pos, cu_seqlens=None, tile: int = TILE):
     out = np.zeros((R, R, nq // tile, nk // tile), dtype=np.uint8)
     for a in range(R):
         for b in range(R):
-            vis = visible_mask(q_pos[a], kv_pos[b], cu_seqlens)
+            vis = visible_mask(q_pos[a], kv_pos[b], cu_seqlens, window=window)
             v4 = vis.reshape(nq // tile, tile, nk // tile, tile)
             anyv = v4.any(axis=(1, 3))
             allv = v4.all(axis=(1, 3))
@@ -189,9 +207,9 @@ def block_mask(q_pos, kv_pos, cu_seqlens=None, tile: int = TILE):
     return out
 
 
-def count_visible(qpos, kpos, cu_seqlens=None) -> int:
+def count_visible(qpos, kpos, cu_seqlens=None, *, window: int = 0) -> int:
     """Number of visible (query, key) pairs (per query head)."""
-    return int(visible_mask(qpos, kpos, cu_seqlens).sum())
+    return int(visible_mask(qpos, kpos, cu_seqlens, window=window).sum())
 
 
 # ---------------------------------------------------------------------------
@@ -216,7 +234,7 @@ def _per_head(x):
 
 
 def partial_attention(q, k, v, qpos, kpos, cu_seqlens=None, scale=None,
-                      row_block: int = 512):
+                      row_block: int = 512, *, window: int = 0):
     """Softmax attention of queries ``q`` over keys ``k``/values ``v``.
 
     q: [n, Hq, d], k and v: [m, Hkv, d]. Returns O [n, Hq, d] and LSE [Hq, n]
@@ -246,11 +264,12 @@ def partial_attention(q, k, v, qpos, kpos, cu_seqlens=None, scale=None,
         qp = qpos[r0:r1]
         qd = qdoc[r0:r1]
         keep = (kpos <= qp.max()) & (kdoc >= qd.min()) & (kdoc <= qd.max())
+        if window:
+            keep &= kpos > qp.min() - window
         ksel, kidx = _key_index(keep)
         if kidx.size == 0:
             continue
-        vis = (kpos[kidx][None, :] <= qp[:, None]) & \
-              (kdoc[kidx][None, :] == qd[:, None])
+        vis = _vis(qp, qd, kpos[kidx], kdoc[kidx], window)
         has = vis.any(axis=1)
         for h in range(Hq):
             kh = h // G
@@ -267,9 +286,9 @@ def partial_attention(q, k, v, qpos, kpos, cu_seqlens=None, scale=None,
     return O, LSE
 
 
-def attention(q, k, v, qpos, kpos, cu_seqlens=None, scale=None):
+def attention(q, k, v, qpos, kpos, cu_seqlens=None, scale=None, *, window: int = 0):
     """Monolithic (no context parallelism) causal attention over all keys."""
-    return partial_attention(q, k, v, qpos, kpos, cu_seqlens, scale)
+    return partial_attention(q, k, v, qpos, kpos, cu_seqlens, scale, window=window)
 
 
 def lse_merge(parts):
@@ -295,7 +314,7 @@ def _split(x, R):
 
 
 def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
-                 variant: str = "pass_kv"):
+                 variant: str = "pass_kv", *, window: int = 0):
     """Explicit ring over R virtual ranks; inputs in rank-major order.
 
     q: [R*n_q, Hq, d] (rank r's queries are rows r*n_q ...), k/v:
@@ -316,7 +335,7 @@ def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
             for r in range(R):
                 qo, ko = sched[t][r]
                 part = partial_attention(Q[qo], K[ko], V[ko], q_pos[qo],
-                                         kv_pos[ko], cu_seqlens, scale)
+                                         kv_pos[ko], cu_seqlens, scale, window=window)
                 acc[qo] = part if acc[qo] is None else lse_merge([acc[qo], part])
         outs = acc
     else:
@@ -326,7 +345,7 @@ def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
                 qo, ko = sched[t][r]
                 slots[qo][ko] = partial_attention(Q[qo], K[ko], V[ko],
                                                   q_pos[qo], kv_pos[ko],
-                                                  cu_seqlens, scale)
+                                                  cu_seqlens, scale, window=window)
         outs = [lse_merge(slots[qo]) for qo in range(R)]
     O = np.concatenate([o for o, _ in outs], axis=0)
     LSE = np.concatenate([l for _, l in outs], axis=1)
@@ -337,7 +356,8 @@ def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
 # Backward  (softmax gradient with recomputed probabilities)
 # ---------------------------------------------------------------------------
 def _pair_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens, scale,
-                   dq, dk, dv, row_block: int = 512, want_dkdv: bool = True):
+                   dq, dk, dv, row_block: int = 512, want_dkdv: bool = True,
+                   window: int = 0):
     """Add one (query set, key set) share of the gradients into dq/dk/dv.
 
     P = exp(scale q.k - LSE) on visible pairs (LSE = the merged, global one),
@@ -360,11 +380,12 @@ def _pair_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens, scale,
         qp = qpos[r0:r1]
         qd = qdoc[r0:r1]
         keep = (kpos <= qp.max()) & (kdoc >= qd.min()) & (kdoc <= qd.max())
+        if window:
+            keep &= kpos > qp.min() - window
         ksel, kidx = _key_index(keep)
         if kidx.size == 0:
             continue
-        vis = (kpos[kidx][None, :] <= qp[:, None]) & \
-              (kdoc[kidx][None, :] == qd[:, None])
+        vis = _vis(qp, qd, kpos[kidx], kdoc[kidx], window)
         for h in range(Hq):
             kh = h // G
             kk = kh_[kh][ksel]
@@ -381,7 +402,7 @@ def _pair_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens, scale,
 
 
 def attention_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens=None,
-                       scale=None):
+                       scale=None, *, window: int = 0):
     """Gradients of monolithic attention. o/lse are the forward results."""
     q, k, v, dout, o, lse = map(_as_f64, (q, k, v, dout, o, lse))
     d = q.shape[2]
@@ -391,12 +412,12 @@ def attention_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens=None,
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     _pair_backward(q, k, v, dout, o, lse, qpos, kpos, cu_seqlens, scale,
-                   dq, dk, dv)
+                   dq, dk, dv, window=window)
     return dq, dk, dv
 
 
 def ring_backward(q, k, v, dout, o, lse, q_pos, kv_pos, cu_seqlens=None,
-                  scale=None, variant: str = "pass_kv", steps=None):
+                  scale=None, variant: str = "pass_kv", steps=None, *, window: int = 0):
     """Explicit ring backward: each step adds the share of the pair it holds.
 
     Rank-major inputs as in ``ring_forward``; o and lse are the merged
@@ -425,7 +446,7 @@ def ring_backward(q, k, v, dout, o, lse, q_pos, kv_pos, cu_seqlens=None,
             dv_p = np.zeros((nk,) + v.shape[1:])
             _pair_backward(q[qs], k[ks], v[ks], dout[qs], o[qs], lse[:, qs],
                            q_pos[qo], kv_pos[ko], cu_seqlens, scale,
-                           dq_p, dk_p, dv_p)
+                           dq_p, dk_p, dv_p, window=window)
             dq[qs] += dq_p
             dk[ks] += dk_p
             dv[ks] += dv_p
@@ -436,35 +457,36 @@ def ring_backward(q, k, v, dout, o, lse, q_pos, kv_pos, cu_seqlens=None,
 # Sampled rows for workloads too large for the full oracle
 # ---------------------------------------------------------------------------
 def sampled_forward(q, k, v, rows, qpos, kpos, cu_seqlens=None, scale=None,
-                    row_block: int = 32):
+                    row_block: int = 32, *, window: int = 0):
     """O [len(rows), Hq, d] and LSE [Hq, len(rows)] at the given query rows,
     each an exact full-prefix softmax over all of that row's visible keys."""
     rows = np.asarray(rows, dtype=np.int64)
     return partial_attention(_as_f64(np.asarray(q)[rows]), k, v,
                              np.asarray(qpos)[rows], kpos, cu_seqlens, scale,
-                             row_block=row_block)
+                             row_block=row_block, window=window)
 
 
 def sampled_dq(q, k, v, dout, rows, qpos, kpos, cu_seqlens=None, scale=None,
-               row_block: int = 32):
+               row_block: int = 32, *, window: int = 0):
     """dQ at the given rows, using the oracle's own O and LSE of those rows."""
     d = q.shape[2]
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     rows = np.asarray(rows, dtype=np.int64)
     o, lse = sampled_forward(q, k, v, rows, qpos, kpos, cu_seqlens, scale,
-                             row_block)
+                             row_block, window=window)
     q_rows = _as_f64(np.asarray(q)[rows])
     dout_rows = _as_f64(np.asarray(dout)[rows])
     dq = np.zeros_like(q_rows)
     _pair_backward(q_rows, k, v, dout_rows, o, lse,
                    np.asarray(qpos)[rows], kpos, cu_seqlens, scale,
-                   dq, None, None, row_block=row_block, want_dkdv=False)
+                   dq, None, None, row_block=row_block, want_dkdv=False,
+                   window=window)
     return dq
 
 
 def sampled_dkdv(q, k, v, dout, key_rows, qpos, kpos, cu_seqlens=None,
-                 scale=None):
+                 scale=None, *, window: int = 0):
     """dK and dV at the given key rows.
 
     Only the queries that can see one of those keys contribute; for each of
@@ -479,14 +501,29 @@ def sampled_dkdv(q, k, v, dout, key_rows, qpos, kpos, cu_seqlens=None,
     kpos = np.asarray(kpos, dtype=np.int64)
     key_rows = np.asarray(key_rows, dtype=np.int64)
     kp = kpos[key_rows]
-    vis = visible_mask(qpos, kp, cu_seqlens)
+    vis = visible_mask(qpos, kp, cu_seqlens, window=window)
     qrows = np.nonzero(vis.any(axis=1))[0]
-    o, lse = sampled_forward(q, k, v, qrows, qpos, kpos, cu_seqlens, scale)
+    o, lse = sampled_forward(q, k, v, qrows, qpos, kpos, cu_seqlens, scale,
+                             window=window)
     kk = _as_f64(np.asarray(k)[key_rows])
     vv = _as_f64(np.asarray(v)[key_rows])
     dq = np.zeros((len(qrows),) + q.shape[1:])
     dk = np.zeros_like(kk)
     dv = np.zeros_like(vv)
     _pair_backward(_as_f64(q[qrows]), kk, vv, _as_f64(np.asarray(dout)[qrows]),
-                   o, lse, qpos[qrows], kp, cu_seqlens, scale, dq, dk, dv)
+                   o, lse, qpos[qrows], kp, cu_seqlens, scale, dq, dk, dv,
+                   window=window)
     return dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Ring ordering choice  ([CP-Inference] "Ring Attention Algorithms")
+# ---------------------------------------------------------------------------
+def select_variant(n_new: int, n_cached: int, n_q_heads: int, n_kv_heads: int) -> str:
+    """"pass_q" when the per-hop message of Pass Q (the Q of the n_new new
+    tokens: n_new * Hq * d elements) is strictly smaller than that of Pass KV
+    (K and V of all n_new + n_cached tokens: 2 * (n_new + n_cached) * Hkv * d),
+    else "pass_kv". The head dimension d is common to both and drops out."""
+    q_msg = n_new * n_q_heads
+    kv_msg = 2 * (n_new + n_cached) * n_kv_heads
+    return "pass_q" if q_msg < kv_msg else "pass_kv"

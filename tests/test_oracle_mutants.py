@@ -13,6 +13,7 @@ import pytest
 import oracle
 import oracle.ring_attention as ra
 import test_oracle_pins as pins
+import test_oracle_window_variant as wv
 
 
 def _mutant(func, old, new):
@@ -28,16 +29,22 @@ CASES = [
     # (function, original text, planted text, pins that should catch it)
     ("partial_attention", "kh = h // G", "kh = h % Hkv",
      [pins.test_cp1_equals_library_causal_sdpa]),
-    ("partial_attention", "(kpos[kidx][None, :] <= qp[:, None])",
-     "(kpos[kidx][None, :] < qp[:, None])",
-     [lambda: pins.test_forward_matches_brute_force(None)]),
+    ("_vis", "(kp[None, :] <= qp[:, None])", "(kp[None, :] < qp[:, None])",
+     [lambda: pins.test_forward_matches_brute_force(None),
+      pins.test_worked_example_load_balance]),
+    ("_vis", "< window", "<= window",
+     [lambda: wv.test_window_forward_matches_brute_force(3, None)]),
+    ("_vis", "(kd[None, :] == qd[:, None])", "(kd[None, :] <= qd[:, None])",
+     [lambda: pins.test_forward_matches_brute_force([0, 5, 6, 13, 20])]),
+    ("select_variant", "q_msg < kv_msg", "q_msg <= kv_msg",
+     [wv.test_select_variant_crossover_is_the_message_size_tie]),
+    ("select_variant", "2 * (n_new + n_cached) * n_kv_heads", "2 * n_cached * n_kv_heads",
+     [wv.test_select_variant_follows_the_pages,
+      wv.test_select_variant_crossover_is_the_message_size_tie]),
     ("partial_attention", "mx_safe + np.log(l_safe)", "np.log(l_safe)",
      [lambda: pins.test_forward_matches_brute_force(None)]),
     ("partial_attention", "np.exp(s - mx_safe[:, None])", "np.exp(s)",
      [lambda: pins.test_forward_matches_brute_force(None)]),
-    ("visible_mask", "kpos[None, :] <= qpos[:, None]",
-     "kpos[None, :] < qpos[:, None]",
-     [pins.test_worked_example_load_balance]),
     ("doc_index", 'side="right"', 'side="left"',
      [lambda: pins.test_forward_matches_brute_force([0, 5, 6, 13, 20])]),
     ("rank_chunks", "[r, 2 * R - 1 - r]", "[r, R + r]",
