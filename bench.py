@@ -326,6 +326,64 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_variant_sweep(args):
+    """Pass KV against Pass Q for partial prefill at several KV-cache hit
+    rates (405B-shaped heads: 128 query / 8 KV heads, d = 128, R = 8, 65536
+    tokens in all): the forward time of each ordering on this GPU, the
+    library's choice (cp_attn_select_variant) and the per-hop ring message
+    each ordering would send. On one GPU the ring is emulated, so the times
+    show the compute side only; the messages show the communication side the
+    choice is made on."""
+    import torch
+    import context_causal_attention_ring_gb300 as cpa
+    from workloads import Workload
+
+    torch.cuda.set_device(0)
+    R, Hq, Hkv, d, total = 8, 128, 8, 128, 65536
+    rows = []
+    for n_new in (65536, 32768, 16384, 8192, 4096, 2048):
+        w = Workload(f"sweep_{n_new}", n_new, Hq, Hkv, d, R, kv_prefix_len=total - n_new)
+        inp = make_inputs(w, with_dout=False)
+        dev_bf16 = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+        qn, kn, vn = (dev_bf16(x) for x in (inp.q, inp.k, inp.v))
+        del inp
+        row = {"n_new": n_new, "n_cached": total - n_new, "hit_rate": 1 - n_new / total,
+               "chosen": cpa.select_variant(n_new, total - n_new, Hq, Hkv),
+               "q_msg_bytes_per_hop": n_new // R * Hq * d * 2,
+               "kv_msg_bytes_per_hop": 2 * (total // R) * Hkv * d * 2}
+        for variant in ("pass_kv", "pass_q"):
+            plan = cpa.Plan(n_new, R, Hq, Hkv, d, variant=variant, kv_prefix_len=total - n_new)
+            q, k, v = torch.empty_like(qn), torch.empty_like(kn), torch.empty_like(vn)
+            plan.layout_apply(cpa.TENSOR_Q, cpa.TO_RANK_MAJOR, qn, q)
+            plan.layout_apply(cpa.TENSOR_KV, cpa.TO_RANK_MAJOR, kn, k)
+            plan.layout_apply(cpa.TENSOR_KV, cpa.TO_RANK_MAJOR, vn, v)
+            o = torch.empty_like(q)
+            lse = torch.empty((Hq, plan.T_q), dtype=torch.float32, device="cuda")
+            ws = torch.empty(plan.workspace_size(cpa.OP_FORWARD), dtype=torch.uint8, device="cuda")
+            for _ in range(max(1, args.warmup)):
+                plan.forward(q, k, v, o, lse, ws)
+            times = []
+            for _ in range(max(3, args.steps)):
+                e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+                e0.record()
+                plan.forward(q, k, v, o, lse, ws)
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            plan.sync_status()
+            flops = 4.0 * d * Hq * plan.visible_pairs()
+            ms = statistics.median(times)
+            row[variant] = {"fwd_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+            del q, k, v, o, lse, ws, plan
+            torch.cuda.empty_cache()
+        rows.append(row)
+        del qn, kn, vn
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "pass_kv_vs_pass_q_forward", "unit": "ms", "config": {
+        "workload": "405B-shaped partial prefill sweep", "total_tokens": total, "cp": R,
+        "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d}, "rows": rows}), flush=True)
+
+
 def run_e2e(args, plan, inp, dev, stream, flops, ws):
     import torch
     import context_causal_attention_ring_gb300 as cpa
@@ -402,7 +460,12 @@ def main():
                     help="profiling aid: override the workload's query heads")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="profiling aid: override the workload's KV heads")
+    ap.add_argument("--variant-sweep", action="store_true",
+                    help="time Pass KV against Pass Q at several KV-cache hit rates")
     args = ap.parse_args()
+    if args.variant_sweep:
+        run_variant_sweep(args)
+        return
     w = WORKLOADS[args.workload]
     if args.q_heads or args.kv_heads:
         import dataclasses
