@@ -19,14 +19,15 @@ from . import build as _build
 # enums (match include/cp_attn.h)
 (OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT,
  ERR_RANGE) = range(8)
-LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG = 0, 1
+LAYOUT_CONTIGUOUS, LAYOUT_ZIGZAG, LAYOUT_USP = 0, 1, 2
+SPLIT_HEADS, GATHER_HEADS = 0, 1
 PASS_KV, PASS_Q, VARIANT_AUTO = 0, 1, 2
 WRITE_PARTIAL, ACCUMULATE = 0, 1
 OP_FORWARD, OP_BACKWARD = 0, 1
 TENSOR_Q, TENSOR_KV = 0, 1
 TO_RANK_MAJOR, TO_NATURAL = 0, 1
 
-LAYOUTS = {"contiguous": LAYOUT_CONTIGUOUS, "zigzag": LAYOUT_ZIGZAG}
+LAYOUTS = {"contiguous": LAYOUT_CONTIGUOUS, "zigzag": LAYOUT_ZIGZAG, "usp": LAYOUT_USP}
 VARIANTS = {"pass_kv": PASS_KV, "pass_q": PASS_Q, "auto": VARIANT_AUTO}
 VARIANT_NAMES = {PASS_KV: "pass_kv", PASS_Q: "pass_q"}
 
@@ -51,6 +52,7 @@ class _PlanDesc(ctypes.Structure):
         ("n_docs", ctypes.c_int),
         ("softmax_scale", ctypes.c_float),
         ("window", ctypes.c_int64),
+        ("a2a", ctypes.c_int),
     ]
 
 
@@ -62,6 +64,7 @@ _SIG = {
                           ctypes.POINTER(ctypes.c_int32), _I]),
     "cp_attn_plan_ex": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_PlanDesc)]),
     "cp_attn_select_variant": (_I, [_I64, _I64, _I, _I, ctypes.POINTER(_I)]),
+    "cp_attn_head_a2a": (_I, [_I64, _I, _I64, _I, _I, _P, _P, _P]),
     "cp_attn_plan_destroy": (None, [_P]),
     "cp_attn_plan_info": (_I, [_P, ctypes.POINTER(_I64), _I]),
     "cp_attn_plan_positions": (_I, [_P, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
@@ -158,13 +161,26 @@ def select_variant(n_new: int, n_cached: int, n_q_heads: int, n_kv_heads: int) -
     return VARIANT_NAMES[out.value]
 
 
+def head_a2a(x, out, a2a: int, direction: int, heads: Optional[int] = None, stream=None):
+    """Sequence <-> head all-to-all (cp_attn_head_a2a). SPLIT_HEADS: x
+    [rows, heads, d] -> out [a2a, rows, heads/a2a, d]; GATHER_HEADS: the
+    inverse (x is then [a2a, rows, heads/a2a, d])."""
+    if direction == SPLIT_HEADS:
+        rows, heads, d = x.shape
+    else:
+        u, rows, hs, d = x.shape
+        heads = u * hs
+    _check(load().cp_attn_head_a2a(int(rows), int(heads), int(d * x.element_size()), int(a2a),
+                                   int(direction), _ptr(x), _ptr(out), _stream(stream)))
+
+
 class Plan:
     """Owner of a cp_attn_plan_t (host and device tables)."""
 
     def __init__(self, seq_len: int, cp: int, n_q_heads: int, n_kv_heads: int,
                  head_dim: int, layout: str = "zigzag", variant: str = "pass_kv",
                  cu_seqlens=None, kv_prefix_len: int = 0,
-                 softmax_scale: float = 0.0, window: int = 0):
+                 softmax_scale: float = 0.0, window: int = 0, a2a: int = 1):
         lib = load()
         self._keep = None
         desc = _PlanDesc()
@@ -183,14 +199,15 @@ class Plan:
             desc.n_docs = len(cu) - 1
         desc.softmax_scale = float(softmax_scale)
         desc.window = int(window)
+        desc.a2a = int(a2a)
         h = _P()
         _check(lib.cp_attn_plan_ex(ctypes.byref(h), ctypes.byref(desc)))
         self.handle = h
-        info = (_I64 * 14)()
-        _check(lib.cp_attn_plan_info(h, info, 14))
+        info = (_I64 * 15)()
+        _check(lib.cp_attn_plan_info(h, info, 15))
         (self.T_q, self.T_kv, self.n_q, self.n_kv, self.R, self.Hq, self.Hkv,
          self.d, self.n_qt, self.n_kt, self.n_docs, on_dev, var,
-         self.window) = [int(x) for x in info]
+         self.window, self.a2a) = [int(x) for x in info]
         self.on_device = bool(on_dev)
         self.layout = layout
         # the ring ordering in use ("auto" resolved by the library)

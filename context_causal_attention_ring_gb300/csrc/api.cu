@@ -233,10 +233,11 @@ cp_attn_status cp_attn_select_variant(int64_t n_new, int64_t n_cached, int n_q_h
 
 cp_attn_status cp_attn_plan_info(cp_attn_plan_t p, int64_t* info, int n) {
   clear_error();
-  if (!p || !info || n < 0 || n > 14) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_info: bad arguments");
-  const int64_t v[14] = {p->T_q, p->T_kv, p->n_q, p->n_kv, p->R, p->Hq, p->Hkv, p->d,
+  if (!p || !info || n < 0 || n > 15) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_info: bad arguments");
+  const int64_t v[15] = {p->T_q, p->T_kv, p->n_q, p->n_kv, p->R, p->Hq, p->Hkv, p->d,
                          p->n_qt, p->n_kt, static_cast<int64_t>(p->cu.size()) - 1,
-                         p->on_device ? 1 : 0, static_cast<int64_t>(p->variant), p->window};
+                         p->on_device ? 1 : 0, static_cast<int64_t>(p->variant), p->window,
+                         p->a2a};
   for (int i = 0; i < n; ++i) info[i] = v[i];
   return CP_ATTN_OK;
 }
@@ -563,6 +564,28 @@ cp_attn_status cp_attn_layout_apply(cp_attn_plan_t p, cp_attn_tensor_kind kind,
   }
   return launch_permute_rows(map, rows, row_bytes, direction == CP_ATTN_TO_NATURAL ? 1 : 0, in, out,
                              static_cast<cudaStream_t>(stream));
+}
+
+cp_attn_status cp_attn_head_a2a(int64_t rows, int heads, int64_t head_bytes, int a2a,
+                                cp_attn_a2a_direction direction, const void* in, void* out,
+                                void* stream) {
+  clear_error();
+  if (!in || !out) return fail(CP_ATTN_ERR_INVALID_ARG, "head_a2a: null pointer");
+  if (rows < 0 || heads <= 0 || a2a <= 0 || heads % a2a != 0)
+    return fail(CP_ATTN_ERR_SHAPE, "head_a2a: heads must be a positive multiple of a2a");
+  if (head_bytes <= 0 || head_bytes % 16)
+    return fail(CP_ATTN_ERR_SHAPE, "head_a2a: head_bytes must be a positive multiple of 16");
+  if (!aligned16(in) || !aligned16(out))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "head_a2a: pointers must be 16-byte aligned");
+  if (direction != CP_ATTN_SPLIT_HEADS && direction != CP_ATTN_GATHER_HEADS)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "head_a2a: bad direction");
+  const int64_t bytes = rows * heads * head_bytes;
+  const char* ci = static_cast<const char*>(in);
+  const char* co = static_cast<const char*>(out);
+  if (ci < co + bytes && co < ci + bytes)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "head_a2a: in and out overlap");
+  return launch_head_a2a(rows, heads, head_bytes, a2a, direction == CP_ATTN_GATHER_HEADS ? 1 : 0,
+                         in, out, static_cast<cudaStream_t>(stream));
 }
 
 cp_attn_status cp_attn_selftest_wait_timeout(cp_attn_plan_t p, uint64_t limit_ns, void* stream) {

@@ -106,6 +106,30 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
   }
 }
 
+// K7 sequence <-> head all-to-all. Split: element (t, h, x) of [rows][heads]
+// [vec] moves to sub-rank u = h / hs at [u][t][h % hs][x] (hs = heads / a2a);
+// gather is the inverse. One 16-byte vector per thread, grid-stride; reads
+// (split) or writes (gather) walk the source/destination rows in order, and
+// every head row of `vec` vectors stays contiguous on both sides.
+__global__ void __launch_bounds__(256) head_a2a_kernel(int64_t rows, int heads, int hs,
+                                                       int64_t vec, int gather,
+                                                       const uint4* __restrict__ in,
+                                                       uint4* __restrict__ out) {
+  const int64_t total = rows * heads * vec;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    // idx enumerates the [rows][heads][vec] side
+    const int64_t x = idx % vec;
+    const int64_t th = idx / vec;
+    const int h = static_cast<int>(th % heads);
+    const int64_t t = th / heads;
+    const int u = h / hs;
+    const int64_t other = ((static_cast<int64_t>(u) * rows + t) * hs + (h - u * hs)) * vec + x;
+    if (gather) out[idx] = __ldg(in + other);
+    else out[other] = __ldg(in + idx);
+  }
+}
+
 // delta[h][t] = sum_x dO[t,h,x] * O[t,h,x], one warp per (t, h); lanes read
 // 4 elements at a time. O is bf16 or fp32.
 template <typename OT>
@@ -246,6 +270,17 @@ cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t
   permute_rows_kernel<<<grid_for(rows * vpr, 256, 152 * 16), 256, 0, s>>>(
       row_map, rows, vpr, to_natural, static_cast<const uint4*>(in), static_cast<uint4*>(out));
   return check_launch("permute_rows");
+}
+
+cp_attn_status launch_head_a2a(int64_t rows, int heads, int64_t head_bytes, int a2a, int gather,
+                               const void* in, void* out, cudaStream_t s) {
+  const int64_t vec = head_bytes / 16;
+  const int64_t total = rows * heads * vec;
+  if (total == 0) return CP_ATTN_OK;
+  head_a2a_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, s>>>(
+      rows, heads, heads / a2a, vec, gather, static_cast<const uint4*>(in),
+      static_cast<uint4*>(out));
+  return check_launch("head_a2a");
 }
 
 cp_attn_status launch_bwd_preprocess(int64_t rows, int heads, int d, const __nv_bfloat16* o,

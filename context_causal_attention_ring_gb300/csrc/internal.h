@@ -41,6 +41,7 @@ struct cp_attn_plan_s {
   int64_t P = 0;   // cached prefix
   int R = 0, Hq = 0, Hkv = 0, d = 0;
   cp_attn_layout layout = CP_ATTN_LAYOUT_ZIGZAG;
+  int a2a = 1;              // USP all-to-all group size
   cp_attn_variant variant = CP_ATTN_PASS_KV;
   float scale = 0.f;
   int64_t window = 0;       // sliding window in tokens, 0 = none

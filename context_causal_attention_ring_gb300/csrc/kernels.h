@@ -74,6 +74,10 @@ cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
                                 __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
                                 cudaStream_t s);
 
+// Sequence <-> head all-to-all (gather = 0: split heads, 1: gather them).
+cp_attn_status launch_head_a2a(int64_t rows, int heads, int64_t head_bytes, int a2a, int gather,
+                               const void* in, void* out, cudaStream_t s);
+
 cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t row_bytes,
                                    int to_natural, const void* in, void* out, cudaStream_t s);
 

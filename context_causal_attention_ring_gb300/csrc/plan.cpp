@@ -34,13 +34,21 @@ int64_t doc_start_host(const std::vector<int32_t>& cu, int64_t pos) {
   return static_cast<int64_t>(*(it - 1));
 }
 
-static void shard(int64_t n_tokens, int R, cp_attn_layout layout, int64_t offset,
+static void shard(int64_t n_tokens, int R, cp_attn_layout layout, int a2a, int64_t offset,
                   int r, std::vector<int64_t>& out) {
-  if (layout == CP_ATTN_LAYOUT_ZIGZAG) {
-    const int64_t c = n_tokens / (2 * R);
-    const int64_t chunks[2] = {r, 2 * R - 1 - r};
-    for (int64_t ch : chunks)
-      for (int64_t i = 0; i < c; ++i) out.push_back(offset + ch * c + i);
+  if (layout == CP_ATTN_LAYOUT_ZIGZAG || layout == CP_ATTN_LAYOUT_USP) {
+    // USP: ring rank r pools the zigzag pairs of devices r*a2a .. r*a2a+a2a-1
+    // of D = a2a*R devices, in ascending position order: chunks
+    // r*a2a .. r*a2a+a2a-1, then 2D-r*a2a-a2a .. 2D-1-r*a2a (zigzag is the
+    // case a2a = 1)
+    const int64_t U = layout == CP_ATTN_LAYOUT_USP ? a2a : 1;
+    const int64_t D = U * R;
+    const int64_t c = n_tokens / (2 * D);
+    for (int half = 0; half < 2; ++half)
+      for (int64_t u = 0; u < U; ++u) {
+        const int64_t ch = half == 0 ? r * U + u : 2 * D - r * U - U + u;
+        for (int64_t i = 0; i < c; ++i) out.push_back(offset + ch * c + i);
+      }
   } else {
     const int64_t c = n_tokens / R;
     for (int64_t i = 0; i < c; ++i) out.push_back(offset + r * c + i);
@@ -97,13 +105,16 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
     return fail(CP_ATTN_ERR_SHAPE, "plan: n_q_heads must be a positive multiple of n_kv_heads");
   if (desc->head_dim != 64 && desc->head_dim != 128)
     return fail(CP_ATTN_ERR_UNSUPPORTED, "plan: head_dim must be 64 or 128");
-  if (desc->layout != CP_ATTN_LAYOUT_ZIGZAG && desc->layout != CP_ATTN_LAYOUT_CONTIGUOUS)
+  if (desc->layout != CP_ATTN_LAYOUT_ZIGZAG && desc->layout != CP_ATTN_LAYOUT_CONTIGUOUS &&
+      desc->layout != CP_ATTN_LAYOUT_USP)
     return fail(CP_ATTN_ERR_INVALID_ARG, "plan: unknown layout");
+  const int a2a = desc->layout == CP_ATTN_LAYOUT_USP ? desc->a2a : 1;
+  if (a2a < 1) return fail(CP_ATTN_ERR_SHAPE, "plan: a2a must be >= 1");
   if (desc->variant != CP_ATTN_PASS_KV && desc->variant != CP_ATTN_PASS_Q &&
       desc->variant != CP_ATTN_VARIANT_AUTO)
     return fail(CP_ATTN_ERR_INVALID_ARG, "plan: unknown variant");
   if (desc->window < 0) return fail(CP_ATTN_ERR_SHAPE, "plan: window must be >= 0");
-  const int64_t unit = (desc->layout == CP_ATTN_LAYOUT_ZIGZAG ? 2LL * R : 1LL * R) * kTile;
+  const int64_t unit = (desc->layout == CP_ATTN_LAYOUT_CONTIGUOUS ? 1LL * R : 2LL * R * a2a) * kTile;
   if (N % unit != 0 || P % unit != 0)
     return fail(CP_ATTN_ERR_SHAPE,
                 "plan: seq_len and kv_prefix_len must be multiples of " +
@@ -120,6 +131,7 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
   p->Hkv = desc->n_kv_heads;
   p->d = desc->head_dim;
   p->layout = desc->layout;
+  p->a2a = a2a;
   p->variant = desc->variant == CP_ATTN_VARIANT_AUTO
                    ? select_variant_rule(N, P, desc->n_q_heads, desc->n_kv_heads)
                    : desc->variant;
@@ -151,10 +163,10 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
   p->n_kt = static_cast<int>(p->n_kv / kTile);
   p->q_pos.clear();
   p->kv_pos.clear();
-  for (int r = 0; r < R; ++r) shard(N, R, p->layout, P, r, p->q_pos);
+  for (int r = 0; r < R; ++r) shard(N, R, p->layout, p->a2a, P, r, p->q_pos);
   for (int r = 0; r < R; ++r) {
-    if (P > 0) shard(P, R, p->layout, 0, r, p->kv_pos);
-    shard(N, R, p->layout, P, r, p->kv_pos);
+    if (P > 0) shard(P, R, p->layout, p->a2a, 0, r, p->kv_pos);
+    shard(N, R, p->layout, p->a2a, P, r, p->kv_pos);
   }
   p->q_tile_pos.resize(static_cast<size_t>(R) * p->n_qt);
   p->kv_tile_pos.resize(static_cast<size_t>(R) * p->n_kt);

@@ -56,10 +56,22 @@ typedef enum cp_attn_status {
 
 /* Chunk layout ("Load Balancing in CP"): ZIGZAG cuts the sequence into 2R
  * chunks and gives rank r chunks r and 2R-1-r (in that order); CONTIGUOUS
- * gives rank r the r-th of R equal chunks (no compute balancing). */
+ * gives rank r the r-th of R equal chunks (no compute balancing).
+ * USP ("A2A + P2P (USP)" in the MaxText post): D = a2a * R devices each hold
+ * their zigzag pair of 2D chunks; an all-to-all inside each group of a2a
+ * consecutive devices pools the group's tokens (and splits its heads, see
+ * cp_attn_head_a2a), so ring rank r holds the chunks of devices
+ * r*a2a .. r*a2a + a2a - 1, kept in ascending position order, and the ring
+ * has R steps of a2a-times longer chunks. On one GPU the token half of that
+ * all-to-all is part of the plan's layout permutation (cp_attn_layout_apply
+ * goes straight from natural order to the pooled order). With R = 1 this is pure Ulysses ("All-to-All
+ * (Ulysses)"): one rank holds the whole sequence for its heads. A USP plan
+ * describes the ring of one head group (n_q_heads and n_kv_heads are the
+ * heads each device keeps after the all-to-all). */
 typedef enum cp_attn_layout {
   CP_ATTN_LAYOUT_CONTIGUOUS = 0,
-  CP_ATTN_LAYOUT_ZIGZAG = 1
+  CP_ATTN_LAYOUT_ZIGZAG = 1,
+  CP_ATTN_LAYOUT_USP = 2
 } cp_attn_layout;
 
 /* Ring ordering ("Ring Attention Algorithms"): PASS_KV keeps Q on its rank
@@ -133,14 +145,17 @@ typedef struct cp_attn_plan_desc {
                              and global layers" ("Announcing Long-Context
                              Training on TPUs with MaxText Context
                              Parallelism", section "What's next"). */
+  int a2a;                /* USP layout: all-to-all group size (devices per
+                             ring rank), >= 1; ignored (treated as 1) by the
+                             other layouts */
 } cp_attn_plan_desc;
 
 /* Build a plan: per-rank positions (zigzag or contiguous), the per-step
  * (q_owner, kv_owner) schedule, the 128x128 block classes and the per-step
  * work lists, uploaded to the current CUDA device if there is one (a plan
  * made without a device serves the host-side queries only).
- * Chunk rule: zigzag needs N and P to be multiples of 256*R; contiguous
- * needs multiples of 128*R. Returns ERR_SHAPE otherwise. On success *out
+ * Chunk rule: zigzag needs N and P to be multiples of 256*R; USP multiples
+ * of 256*R*a2a; contiguous multiples of 128*R. Returns ERR_SHAPE otherwise. On success *out
  * owns host and device tables until cp_attn_plan_destroy. */
 cp_attn_status cp_attn_plan(cp_attn_plan_t* out, int64_t seq_len, int cp,
                             int n_q_heads, int n_kv_heads, int head_dim,
@@ -163,11 +178,12 @@ cp_attn_status cp_attn_select_variant(int64_t n_new, int64_t n_cached, int n_q_h
                                       int n_kv_heads, cp_attn_variant* out);
 void cp_attn_plan_destroy(cp_attn_plan_t plan);
 
-/* Sizes of a plan, written to info[0..n-1] (n <= 14):
+/* Sizes of a plan, written to info[0..n-1] (n <= 15):
  * 0 T_q (= R*n_q), 1 T_kv (= R*n_kv), 2 n_q (query rows per rank),
  * 3 n_kv (KV rows per rank), 4 R, 5 Hq, 6 Hkv, 7 d, 8 q tiles per rank,
  * 9 kv tiles per rank, 10 n_docs, 11 has device tables (0/1),
- * 12 ring ordering (cp_attn_variant, AUTO resolved), 13 window. */
+ * 12 ring ordering (cp_attn_variant, AUTO resolved), 13 window,
+ * 14 a2a (1 unless USP). */
 cp_attn_status cp_attn_plan_info(cp_attn_plan_t plan, int64_t* info, int n);
 
 /* Host queries (bit-exact plan artefacts; no device needed).
@@ -305,6 +321,29 @@ cp_attn_status cp_attn_backward(cp_attn_plan_t plan, const void* q, const void* 
 cp_attn_status cp_attn_layout_apply(cp_attn_plan_t plan, cp_attn_tensor_kind kind,
                                     cp_attn_direction direction, const void* in,
                                     void* out, int64_t row_bytes, void* stream);
+
+/* Sequence <-> head all-to-all of Ulysses / USP ("All-to-All (Ulysses)" and
+ * "A2A + P2P (USP)" in the MaxText post), emulated on one GPU that holds
+ * every device's buffer (kernel K7, a strided copy at HBM bandwidth).
+ * SPLIT_HEADS (before attention): in [rows, heads, head_bytes] with rows in
+ *   device order (each device's tokens, every head) -> out [a2a][rows]
+ *   [heads/a2a][head_bytes]: the tensor of sub-rank u is the one every
+ *   device u of a group holds after the exchange (the group's tokens for
+ *   heads [u*heads/a2a, (u+1)*heads/a2a)), gathered over the groups in ring
+ *   order. Each sub-rank then runs its own ring (a USP plan with heads/a2a
+ *   heads) on out[u].
+ * GATHER_HEADS (after attention): the inverse, out[u] -> [rows, heads, ...].
+ * head_bytes: bytes of one head's row (d * element size), a multiple of 16;
+ * heads must be a multiple of a2a. LSE [heads, rows] needs no exchange: the
+ * rows of sub-rank u's heads are already contiguous. `in` and `out` must
+ * not overlap. */
+typedef enum cp_attn_a2a_direction {
+  CP_ATTN_SPLIT_HEADS = 0,
+  CP_ATTN_GATHER_HEADS = 1
+} cp_attn_a2a_direction;
+cp_attn_status cp_attn_head_a2a(int64_t rows, int heads, int64_t head_bytes, int a2a,
+                                cp_attn_a2a_direction direction, const void* in, void* out,
+                                void* stream);
 
 /* Synchronise `stream`, then read and clear the plan's device status word.
  * Returns CP_ATTN_OK or the first device-side error (ERR_TIMEOUT). */

@@ -74,6 +74,8 @@ __all__ = [
     "sampled_dq",
     "sampled_dkdv",
     "select_variant",
+    "head_split",
+    "head_gather",
     "TILE",
 ]
 
@@ -84,25 +86,35 @@ EMPTY, PARTIAL, FULL = 0, 1, 2
 # ---------------------------------------------------------------------------
 # Chunk plan  ([CP-Inference] "Load Balancing in CP")
 # ---------------------------------------------------------------------------
-def rank_chunks(R: int, layout: str = "zigzag"):
+def rank_chunks(R: int, layout: str = "zigzag", a2a: int = 1):
     """Chunk indices held by each rank, in the rank's local order.
 
     zigzag: the sequence is cut into 2R chunks and rank r takes chunks r and
     2R-1-r. contiguous: R chunks, rank r takes chunk r (no balancing).
+    usp ([MaxText] "A2A + P2P (USP)"): D = a2a * R devices, each holding its
+    zigzag pair of 2D chunks; an all-to-all within each group of a2a
+    consecutive devices pools the group's tokens, so ring rank r holds the
+    chunks of devices r*a2a, ..., r*a2a + a2a - 1. The receiving devices may
+    place the pooled chunks in any order; they are kept in ascending
+    position order, so every rank's positions increase along its rows.
     """
     if layout == "zigzag":
         return [[r, 2 * R - 1 - r] for r in range(R)]
     if layout == "contiguous":
         return [[r] for r in range(R)]
+    if layout == "usp":
+        D = a2a * R
+        return [sorted(c for d in range(r * a2a, (r + 1) * a2a) for c in (d, 2 * D - 1 - d))
+                for r in range(R)]
     raise ValueError(layout)
 
 
 def shard_positions(n_tokens: int, R: int, layout: str = "zigzag",
-                    offset: int = 0):
+                    offset: int = 0, a2a: int = 1):
     """Global positions held by each rank, in local order, for a run of
     ``n_tokens`` tokens starting at global position ``offset``."""
-    chunks = rank_chunks(R, layout)
-    n_chunks = 2 * R if layout == "zigzag" else R
+    chunks = rank_chunks(R, layout, a2a)
+    n_chunks = {"zigzag": 2 * R, "contiguous": R, "usp": 2 * R * a2a}[layout]
     assert n_tokens % n_chunks == 0
     c = n_tokens // n_chunks
     out = []
@@ -114,7 +126,7 @@ def shard_positions(n_tokens: int, R: int, layout: str = "zigzag",
 
 
 def plan_positions(seq_len: int, R: int, layout: str = "zigzag",
-                   kv_prefix_len: int = 0):
+                   kv_prefix_len: int = 0, a2a: int = 1):
     """Per-rank global positions of the query tokens and of the KV tokens.
 
     Full prefill: Q and KV are the same tokens. Partial prefill (a cached
@@ -123,11 +135,11 @@ def plan_positions(seq_len: int, R: int, layout: str = "zigzag",
     and the new tokens (the queries) sit at positions P, P+1, ...
     """
     P = int(kv_prefix_len)
-    q_pos = shard_positions(seq_len, R, layout, offset=P)
+    q_pos = shard_positions(seq_len, R, layout, offset=P, a2a=a2a)
     if P == 0:
         kv_pos = [p.copy() for p in q_pos]
     else:
-        cache = shard_positions(P, R, layout, offset=0)
+        cache = shard_positions(P, R, layout, offset=0, a2a=a2a)
         kv_pos = [np.concatenate([cache[r], q_pos[r]]) for r in range(R)]
     return q_pos, kv_pos
 
@@ -527,3 +539,26 @@ def select_variant(n_new: int, n_cached: int, n_q_heads: int, n_kv_heads: int) -
     q_msg = n_new * n_q_heads
     kv_msg = 2 * (n_new + n_cached) * n_kv_heads
     return "pass_q" if q_msg < kv_msg else "pass_kv"
+
+
+# ---------------------------------------------------------------------------
+# Sequence <-> head all-to-all  ([MaxText] "All-to-All (Ulysses)", "A2A + P2P")
+# ---------------------------------------------------------------------------
+def head_split(x, a2a: int):
+    """The all-to-all before attention, seen from one GPU holding every
+    device's buffer. x: [T, H, e] with rows in device order (each device's
+    tokens, all heads). Device u of a group keeps heads [u*H/a2a, (u+1)*H/a2a)
+    and receives the group's other tokens for them; gathered over all groups,
+    sub-rank u's tensor is x[:, its heads, :]. Returns [a2a, T, H/a2a, e]."""
+    x = np.asarray(x)
+    T, H = x.shape[0], x.shape[1]
+    assert H % a2a == 0
+    hs = H // a2a
+    return np.stack([x[:, u * hs:(u + 1) * hs] for u in range(a2a)])
+
+
+def head_gather(y):
+    """The all-to-all after attention: the inverse of head_split. y:
+    [a2a, T, H/a2a, e] -> [T, H, e]."""
+    y = np.asarray(y)
+    return np.concatenate([y[u] for u in range(y.shape[0])], axis=1)

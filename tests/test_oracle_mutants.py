@@ -14,6 +14,7 @@ import oracle
 import oracle.ring_attention as ra
 import test_oracle_pins as pins
 import test_oracle_window_variant as wv
+import test_oracle_usp as usp
 
 
 def _mutant(func, old, new):
@@ -49,6 +50,11 @@ CASES = [
      [lambda: pins.test_forward_matches_brute_force([0, 5, 6, 13, 20])]),
     ("rank_chunks", "[r, 2 * R - 1 - r]", "[r, R + r]",
      [pins.test_worked_example_load_balance]),
+    ("rank_chunks", "for c in (d, 2 * D - 1 - d)", "for c in (d, D + d)",
+     [usp.test_usp_figure_pairs_of_devices,
+      lambda: usp.test_usp_ranks_balanced_and_increasing(2, 2)]),
+    ("head_split", "x[:, u * hs:(u + 1) * hs]", "x[:, u:u + hs]",
+     [usp.test_head_split_moves_heads_not_tokens]),
     ("ring_schedule", "row.append((r, other))", "row.append((r, r))",
      [lambda: pins.test_ring_equals_monolithic("pass_kv", "zigzag", False)]),
     ("lse_merge", "np.exp(lses - LSE_safe[None])", "np.exp(lses - M_safe[None])",

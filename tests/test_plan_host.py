@@ -135,7 +135,7 @@ def test_plan_rejects_bad_arguments(kw, status):
 
 def test_header_declarations_are_exported():
     hdr = open(os.path.join(ROOT, "include", "cp_attn.h")).read()
-    declared = sorted(set(re.findall(r"\b(cp_attn_[a-z_]+)\s*\(", hdr)))
+    declared = sorted(set(re.findall(r"\b(cp_attn_[a-z0-9_]+)\s*\(", hdr)))
     lib = cpa.load()
     for name in declared:
         assert hasattr(lib, name), name

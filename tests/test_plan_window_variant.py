@@ -63,3 +63,25 @@ def test_select_variant_rejects_bad_arguments():
     for args in ((0, 10, 8, 1), (10, -1, 8, 1), (10, 10, 0, 1), (10, 10, 8, 0)):
         with pytest.raises(cpa.CpAttnError):
             cpa.select_variant(*args)
+
+
+@pytest.mark.parametrize("R,U,P", [(2, 2, 0), (4, 2, 0), (1, 4, 0), (2, 4, 4096), (3, 2, 0), (8, 1, 0)])
+def test_usp_plan_bit_exact(R, U, P):
+    N = 256 * R * U * 2
+    cu = np.array([0, 300, N + P - 129, N + P], dtype=np.int32)
+    p = cpa.Plan(N, R, 4, 2, 128, layout="usp", a2a=U, kv_prefix_len=P, cu_seqlens=cu)
+    assert (p.R, p.a2a) == (R, U)
+    q_pos, kv_pos = oracle.plan_positions(N, R, "usp", kv_prefix_len=P, a2a=U)
+    for r in range(R):
+        assert np.array_equal(p.positions(cpa.TENSOR_Q, r), q_pos[r])
+        assert np.array_equal(p.positions(cpa.TENSOR_KV, r), kv_pos[r])
+    assert np.array_equal(p.block_mask(), oracle.block_mask(q_pos, kv_pos, cu))
+    allk = np.concatenate(kv_pos)
+    assert p.visible_pairs() == sum(oracle.count_visible(x, allk, cu) for x in q_pos)
+
+
+def test_usp_plan_rejects_bad_chunks():
+    with pytest.raises(cpa.CpAttnError):
+        cpa.Plan(512, 2, 4, 2, 128, layout="usp", a2a=2)   # needs 1024-token multiples
+    with pytest.raises(cpa.CpAttnError):
+        cpa.Plan(2048, 2, 4, 2, 128, layout="usp", a2a=0)
