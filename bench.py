@@ -384,6 +384,101 @@ def run_variant_sweep(args):
         "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d}, "rows": rows}), flush=True)
 
 
+def run_usp_sweep(args):
+    """The 32768-token 32/8-head layer on D = 8 emulated devices, as a plain
+    zigzag ring (a2a = 1, 8 steps), USP with a2a = 2 and 4 (4 and 2 steps of
+    longer chunks) and pure Ulysses (a2a = 8, one step). Per arrangement: the
+    forward and backward time of all a2a head-group rings, and the head
+    all-to-all kernel's bandwidth on Q."""
+    import torch
+    import context_causal_attention_ring_gb300 as cpa
+
+    torch.cuda.set_device(0)
+    w = WORKLOADS["llama3_8b_layer"]
+    N, Hq, Hkv, d, D = w.seq_len, w.n_q_heads, w.n_kv_heads, w.head_dim, w.cp
+    inp = make_inputs(w)
+    dev_bf16 = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+    qn, kn, vn, don = (dev_bf16(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    del inp
+    peaks, _ = _peaks()
+    rows = []
+    for U in (1, 2, 4, 8):
+        R = D // U
+        hq, hkv = Hq // U, Hkv // U
+        plan = cpa.Plan(N, R, hq, hkv, d, layout="usp", a2a=U)
+        T = plan.T_q
+
+        def pooled(x, heads, kind):
+            y = torch.empty_like(x)
+            plan.layout_apply(kind, cpa.TO_RANK_MAJOR, x, y, row_bytes=heads * d * 2)
+            s_ = torch.empty((U, T, heads // U, d), dtype=x.dtype, device="cuda")
+            cpa.head_a2a(y, s_, U, cpa.SPLIT_HEADS)
+            return y, s_
+
+        qy, qs = pooled(qn, Hq, cpa.TENSOR_Q)
+        _, ks = pooled(kn, Hkv, cpa.TENSOR_KV)
+        _, vs = pooled(vn, Hkv, cpa.TENSOR_KV)
+        _, dos = pooled(don, Hq, cpa.TENSOR_Q)
+        os_ = torch.empty_like(qs)
+        lse = torch.empty((Hq, T), dtype=torch.float32, device="cuda")
+        dqs = torch.empty((U, T, hq, d), device="cuda")
+        dks = torch.empty((U, T, hkv, d), device="cuda")
+        dvs = torch.empty_like(dks)
+        wsf = torch.empty(plan.workspace_size(cpa.OP_FORWARD), dtype=torch.uint8, device="cuda")
+        wsb = torch.empty(plan.workspace_size(cpa.OP_BACKWARD), dtype=torch.uint8, device="cuda")
+
+        def fwd():
+            for u in range(U):
+                plan.forward(qs[u], ks[u], vs[u], os_[u], lse[u * hq:(u + 1) * hq], wsf)
+
+        def bwd():
+            for u in range(U):
+                plan.backward(qs[u], ks[u], vs[u], os_[u], lse[u * hq:(u + 1) * hq], dos[u],
+                              dqs[u], dks[u], dvs[u], wsb, o_f32=wsf)
+
+        def a2a():
+            cpa.head_a2a(qy, qs, U, cpa.SPLIT_HEADS)
+
+        def timed(fn, n):
+            for _ in range(max(1, args.warmup)):
+                fn()
+            ts = []
+            for _ in range(n):
+                e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            return statistics.median(ts)
+
+        # the backward of each head group needs its own forward's fp32 O:
+        # time them as a pair, and the forward alone
+        f_ms = timed(fwd, max(3, args.steps))
+
+        def fb():
+            for u in range(U):
+                plan.forward(qs[u], ks[u], vs[u], os_[u], lse[u * hq:(u + 1) * hq], wsf)
+                plan.backward(qs[u], ks[u], vs[u], os_[u], lse[u * hq:(u + 1) * hq], dos[u],
+                              dqs[u], dks[u], dvs[u], wsb, o_f32=wsf)
+
+        fb_ms = timed(fb, max(3, args.steps))
+        a_ms = timed(a2a, max(3, args.steps))
+        plan.sync_status()
+        flops = 4.0 * d * Hq * plan.visible_pairs()
+        a2a_bytes = 2 * T * Hq * d * 2
+        rows.append({"a2a": U, "ring_steps": R, "chunk_tokens": N // (2 * D) * U,
+                     "fwd_ms": f_ms, "fwd_tflops": flops / (f_ms * 1e-3) / 1e12,
+                     "fwd_bwd_ms": fb_ms, "fwd_bwd_tflops": 3.5 * flops / (fb_ms * 1e-3) / 1e12,
+                     "head_a2a_q_ms": a_ms, "head_a2a_q_gbs": a2a_bytes / (a_ms * 1e-3) / 1e9,
+                     "head_a2a_frac_of_hbm": a2a_bytes / (a_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]})
+        del plan, qy, qs, ks, vs, dos, os_, lse, dqs, dks, dvs, wsf, wsb
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "usp_arrangements", "unit": "ms", "config": {
+        "workload": w.name, "seq_len": N, "devices": D, "n_q_heads": Hq, "n_kv_heads": Hkv,
+        "head_dim": d}, "rows": rows}), flush=True)
+
+
 def run_e2e(args, plan, inp, dev, stream, flops, ws):
     import torch
     import context_causal_attention_ring_gb300 as cpa
@@ -462,9 +557,14 @@ def main():
                     help="profiling aid: override the workload's KV heads")
     ap.add_argument("--variant-sweep", action="store_true",
                     help="time Pass KV against Pass Q at several KV-cache hit rates")
+    ap.add_argument("--usp-sweep", action="store_true",
+                    help="time the layer as zigzag ring, USP and pure Ulysses arrangements")
     args = ap.parse_args()
     if args.variant_sweep:
         run_variant_sweep(args)
+        return
+    if args.usp_sweep:
+        run_usp_sweep(args)
         return
     w = WORKLOADS[args.workload]
     if args.q_heads or args.kv_heads:
