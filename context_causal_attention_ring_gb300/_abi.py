@@ -56,6 +56,18 @@ class _PlanDesc(ctypes.Structure):
     ]
 
 
+class _DecodeDesc(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int),
+        ("cp", ctypes.c_int),
+        ("kv_len", ctypes.c_int64),
+        ("n_q_heads", ctypes.c_int),
+        ("n_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("softmax_scale", ctypes.c_float),
+    ]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _I64 = ctypes.c_int64
@@ -65,6 +77,8 @@ _SIG = {
     "cp_attn_plan_ex": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_PlanDesc)]),
     "cp_attn_select_variant": (_I, [_I64, _I64, _I, _I, ctypes.POINTER(_I)]),
     "cp_attn_head_a2a": (_I, [_I64, _I, _I64, _I, _I, _P, _P, _P]),
+    "cp_attn_decode_workspace_size": (_I, [ctypes.POINTER(_DecodeDesc), ctypes.POINTER(ctypes.c_size_t)]),
+    "cp_attn_decode": (_I, [ctypes.POINTER(_DecodeDesc), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_plan_destroy": (None, [_P]),
     "cp_attn_plan_info": (_I, [_P, ctypes.POINTER(_I64), _I]),
     "cp_attn_plan_positions": (_I, [_P, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
@@ -159,6 +173,33 @@ def select_variant(n_new: int, n_cached: int, n_q_heads: int, n_kv_heads: int) -
     _check(load().cp_attn_select_variant(int(n_new), int(n_cached), int(n_q_heads),
                                          int(n_kv_heads), ctypes.byref(out)))
     return VARIANT_NAMES[out.value]
+
+
+def _decode_desc(batch, cp, kv_len, n_q_heads, n_kv_heads, head_dim, softmax_scale=0.0):
+    d = _DecodeDesc()
+    d.batch, d.cp, d.kv_len = int(batch), int(cp), int(kv_len)
+    d.n_q_heads, d.n_kv_heads, d.head_dim = int(n_q_heads), int(n_kv_heads), int(head_dim)
+    d.softmax_scale = float(softmax_scale)
+    return d
+
+
+def decode_workspace_size(batch, cp, kv_len, n_q_heads, n_kv_heads, head_dim) -> int:
+    """Workspace bytes of cp_attn_decode."""
+    out = ctypes.c_size_t()
+    desc = _decode_desc(batch, cp, kv_len, n_q_heads, n_kv_heads, head_dim)
+    _check(load().cp_attn_decode_workspace_size(ctypes.byref(desc), ctypes.byref(out)))
+    return int(out.value)
+
+
+def decode(q, k, v, o, lse, workspace, cp: int, softmax_scale: float = 0.0, stream=None):
+    """One-row decode over the emulated ring (cp_attn_decode). q [B, Hq, d],
+    k and v [B, kv_len, Hkv, d] bf16; o [B, Hq, d] bf16; lse [Hq, B] fp32."""
+    B, Hq, d = q.shape
+    kv_len, Hkv = k.shape[1], k.shape[2]
+    desc = _decode_desc(B, cp, kv_len, Hq, Hkv, d, softmax_scale)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().cp_attn_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                 _ptr(lse), _ptr(workspace), int(nbytes), _stream(stream)))
 
 
 def head_a2a(x, out, a2a: int, direction: int, heads: Optional[int] = None, stream=None):

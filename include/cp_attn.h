@@ -345,6 +345,36 @@ cp_attn_status cp_attn_head_a2a(int64_t rows, int heads, int64_t head_bytes, int
                                 cp_attn_a2a_direction direction, const void* in, void* out,
                                 void* stream);
 
+/* One-row decode over the emulated ring (kernel K8, then the K4 merge):
+ * Pass Q for decode ("Context Parallelism for Scalable Million-Token
+ * Inference": "Attention Compute Patterns in Multi-Turn Chat" -- decode is a
+ * single-row attention of the new token over every earlier token -- and
+ * "Ring Attention Algorithms" -- for decode the KV stays on its rank, the
+ * query visits each rank, and the partial outputs are merged). Each of
+ * `batch` sequences has one new query row and kv_len keys (its cached tokens
+ * plus its own new token, appended by the caller), all visible to that row.
+ * Rank r holds keys [r*kv_len/cp, (r+1)*kv_len/cp) of every sequence; each
+ * rank's shard is split further into runs of 64-512 keys so the grid fills
+ * the GPU, and the merge combines every run's partial.
+ * q: bf16 [batch, Hq, d]; k, v: bf16 [batch, kv_len, Hkv, d]; o: bf16
+ * [batch, Hq, d]; lse: fp32 [Hq, batch] (natural log, scale applied).
+ * workspace: cp_attn_decode_workspace_size bytes (fp32 partials), 16-byte
+ * aligned like every pointer. Supported: head_dim 64 or 128, at most 16 query
+ * heads per KV head, kv_len a multiple of 64*cp. */
+typedef struct cp_attn_decode_desc {
+  int batch;           /* sequences, one new row each */
+  int cp;              /* ring size R: ranks sharing each sequence's keys */
+  int64_t kv_len;      /* keys per sequence */
+  int n_q_heads;
+  int n_kv_heads;
+  int head_dim;
+  float softmax_scale; /* 0 selects 1/sqrt(head_dim) */
+} cp_attn_decode_desc;
+cp_attn_status cp_attn_decode_workspace_size(const cp_attn_decode_desc* desc, size_t* bytes);
+cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, const void* k,
+                              const void* v, void* o, float* lse, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the plan's device status word.
  * Returns CP_ATTN_OK or the first device-side error (ERR_TIMEOUT). */
 cp_attn_status cp_attn_sync_status(cp_attn_plan_t plan, void* stream);

@@ -76,6 +76,7 @@ __all__ = [
     "select_variant",
     "head_split",
     "head_gather",
+    "decode",
     "TILE",
 ]
 
@@ -562,3 +563,31 @@ def head_gather(y):
     [a2a, T, H/a2a, e] -> [T, H, e]."""
     y = np.asarray(y)
     return np.concatenate([y[u] for u in range(y.shape[0])], axis=1)
+
+
+# ---------------------------------------------------------------------------
+# Decode  ([CP-Inference] "Attention Compute Patterns in Multi-Turn Chat",
+# "Ring Attention Algorithms": Pass Q for decode)
+# ---------------------------------------------------------------------------
+def decode(q, k, v, R: int, scale=None):
+    """One new query row per sequence attending to all of its keys.
+
+    q: [B, Hq, d]; k, v: [B, T, Hkv, d], where the new token is the last of
+    the T keys, so every key is visible. Rank r holds keys
+    [r*T/R, (r+1)*T/R) of each sequence; the row visits every rank, each rank
+    computes its partial attention, and the partials are merged. Returns
+    O [B, Hq, d] and LSE [Hq, B]."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, T = k.shape[0], k.shape[1]
+    assert T % R == 0
+    n = T // R
+    O = np.zeros(q.shape)
+    LSE = np.zeros((q.shape[1], B))
+    for b in range(B):
+        parts = [partial_attention(q[b:b + 1], k[b, r * n:(r + 1) * n], v[b, r * n:(r + 1) * n],
+                                   [T - 1], np.arange(r * n, (r + 1) * n), None, scale)
+                 for r in range(R)]
+        o, l = lse_merge(parts)
+        O[b] = o[0]
+        LSE[:, b] = l[:, 0]
+    return O, LSE

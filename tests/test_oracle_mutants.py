@@ -15,6 +15,7 @@ import oracle.ring_attention as ra
 import test_oracle_pins as pins
 import test_oracle_window_variant as wv
 import test_oracle_usp as usp
+import test_oracle_decode as dec
 
 
 def _mutant(func, old, new):
@@ -55,6 +56,10 @@ CASES = [
       lambda: usp.test_usp_ranks_balanced_and_increasing(2, 2)]),
     ("head_split", "x[:, u * hs:(u + 1) * hs]", "x[:, u:u + hs]",
      [usp.test_head_split_moves_heads_not_tokens]),
+    ("decode", "[T - 1], np.arange(r * n, (r + 1) * n)", "[n - 1], np.arange(r * n, (r + 1) * n)",
+     [lambda: dec.test_decode_is_the_last_row_of_causal_attention(2)]),
+    ("decode", "v[b, r * n:(r + 1) * n]", "v[b, 0:n]",
+     [lambda: dec.test_decode_is_the_last_row_of_causal_attention(4)]),
     ("ring_schedule", "row.append((r, other))", "row.append((r, r))",
      [lambda: pins.test_ring_equals_monolithic("pass_kv", "zigzag", False)]),
     ("lse_merge", "np.exp(lses - LSE_safe[None])", "np.exp(lses - M_safe[None])",

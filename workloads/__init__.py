@@ -44,6 +44,7 @@ __all__ = [
     "doc_lengths",
     "cu_seqlens_from_lengths",
     "sample_rows",
+    "make_decode_inputs",
 ]
 
 
@@ -205,3 +206,17 @@ def make_inputs(w: Workload, with_dout: Optional[bool] = None,
     return Inputs(q=q, k=k, v=v, dout=dout, cu_seqlens=cu,
                   meta=dict(workload=w.name, seq_len=n_new,
                             kv_prefix_len=prefix))
+
+
+def make_decode_inputs(batch: int, kv_len: int, n_q_heads: int, n_kv_heads: int,
+                       head_dim: int, seed: int = 0, qk_scale: float = 1.0):
+    """Decode inputs: one new query row per sequence, q [batch, Hq, d], and
+    each sequence's keys and values k, v [batch, kv_len, Hkv, d] (bf16 bits,
+    standard normals; Q and K multiplied by qk_scale)."""
+    rng = np.random.default_rng(seed)
+    q = draw_bf16(rng, (batch, n_q_heads, head_dim), qk_scale)
+    k = draw_bf16(rng, (batch * kv_len, n_kv_heads, head_dim), qk_scale).reshape(
+        batch, kv_len, n_kv_heads, head_dim)
+    v = draw_bf16(rng, (batch * kv_len, n_kv_heads, head_dim)).reshape(
+        batch, kv_len, n_kv_heads, head_dim)
+    return q, k, v
