@@ -479,6 +479,56 @@ def run_usp_sweep(args):
         "head_dim": d}, "rows": rows}), flush=True)
 
 
+def run_decode_bench(args):
+    """One-row decode over the emulated ring (cp_attn_decode: K8 partials and
+    the K4 merge) on two shapes: a 405B-shaped row (128 / 8 heads) over 131072
+    keys on 8 ranks, and a batch of 16 sequences with 8B-shaped heads (32 / 8)
+    over 32768 keys each. Both read more K/V than the L2 holds. The roofline
+    is HBM: algorithmic bytes = K + V + q + o (+ the LSE), once."""
+    import torch
+    import context_causal_attention_ring_gb300 as cpa
+    from workloads import make_decode_inputs
+
+    torch.cuda.set_device(0)
+    peaks, peak_kind = _peaks()
+    rows = []
+    for name, B, T, Hq, Hkv, d, R in (("405b_row_131072", 1, 131072, 128, 8, 128, 8),
+                                      ("8b_batch16_32768", 16, 32768, 32, 8, 128, 8)):
+        q, k, v = make_decode_inputs(B, T, Hq, Hkv, d, seed=3)
+        dev_bf16 = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(
+            torch.bfloat16).cuda()
+        qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+        del q, k, v
+        o = torch.empty_like(qd)
+        lse = torch.empty((Hq, B), dtype=torch.float32, device="cuda")
+        ws = torch.empty(cpa.decode_workspace_size(B, R, T, Hq, Hkv, d), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(max(3, args.warmup)):
+            cpa.decode(qd, kd, vd, o, lse, ws, R)
+        n = max(20, args.steps)
+        ev = [(torch.cuda.Event(True), torch.cuda.Event(True)) for _ in range(n)]
+        n0 = cpa.launch_count()
+        for e0, e1 in ev:
+            e0.record()
+            cpa.decode(qd, kd, vd, o, lse, ws, R)
+            e1.record()
+        torch.cuda.synchronize()
+        launches = (cpa.launch_count() - n0) // n
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        kv_bytes = 2 * B * T * Hkv * d * 2
+        algo = kv_bytes + 2 * B * Hq * d * 2 + Hq * B * 4
+        gbs = algo / (ms * 1e-3) / 1e9
+        rows.append({"workload": name, "batch": B, "kv_len": T, "n_q_heads": Hq,
+                     "n_kv_heads": Hkv, "head_dim": d, "cp": R, "ms": ms,
+                     "algorithmic_bytes": algo, "achieved_gbs": gbs,
+                     "frac_of_hbm": gbs / peaks["hbm_gbs"], "launches_per_call": launches})
+        del qd, kd, vd, o, lse, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "decode_hbm_bandwidth", "unit": "GB/s",
+                      "peak": peaks["hbm_gbs"], "peak_kind": f"hbm_gbs ({peak_kind})",
+                      "rows": rows}), flush=True)
+
+
 def run_e2e(args, plan, inp, dev, stream, flops, ws):
     import torch
     import context_causal_attention_ring_gb300 as cpa
@@ -559,7 +609,12 @@ def main():
                     help="time Pass KV against Pass Q at several KV-cache hit rates")
     ap.add_argument("--usp-sweep", action="store_true",
                     help="time the layer as zigzag ring, USP and pure Ulysses arrangements")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the one-row decode against the HBM roofline")
     args = ap.parse_args()
+    if args.decode:
+        run_decode_bench(args)
+        return
     if args.variant_sweep:
         run_variant_sweep(args)
         return

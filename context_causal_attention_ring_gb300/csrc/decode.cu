@@ -14,11 +14,12 @@
 // G * L * d * 4 FLOP), so it runs on the CUDA cores, not the tensor cores:
 //   1. scores s[j][h] = scale * q_h . k_j, K staged through shared memory in
 //      64-key tiles (cp.async, double-buffered, 16-byte units XOR-swizzled
-//      by row), one thread per (key, group of heads);
-//   2. per head: max over the L keys, p = 2^(s - max), sum;
-//   3. O_h = sum_j p[j][h] v_j, V staged the same way, each warp taking
-//      every 8th key and each lane 4 (or 2) columns of d; the warps' sums
-//      meet in shared memory;
+//      by row), one thread per (one or two keys, group of heads);
+//   2. per head (half a warp each): max over the L keys, p = 2^(s - max),
+//      sum;
+//   3. O_h = sum_j p[j][h] v_j, V staged the same way, each warp taking 8
+//      consecutive keys of a tile and each lane 4 (or 2) columns of d; the
+//      warps' sums meet in shared memory;
 //   4. O_h / l_h and LSE_h = ln l_h + max to the partial slots.
 // The partials then go through the LSE merge (K4).
 #include <cmath>
@@ -55,10 +56,9 @@ struct DecSmem {
   static constexpr int kTileBytes = kDecTile * kRowBytes;
   static constexpr int kQ = 0;                                  // [kDecMaxG][D] f32
   static constexpr int kKV = kQ + kDecMaxG * D * 4;             // [2][kDecTile][D] bf16
-  static constexpr int kS = kKV + 2 * kTileBytes;               // [kDecMaxL][kDecMaxG] f32
+  static constexpr int kS = kKV + 2 * kTileBytes;               // [kDecMaxG][kDecMaxL] f32
   static constexpr int kO = kS + kDecMaxL * kDecMaxG * 4;       // [kDecMaxG][D] f32
-  static constexpr int kRed = kO + kDecMaxG * D * 4;            // [8][kDecMaxG] f32
-  static constexpr int kStat = kRed + 8 * kDecMaxG * 4;         // max[G], sum[G]
+  static constexpr int kStat = kO + kDecMaxG * D * 4;           // max[G], sum[G]
   static constexpr int kBytes = kStat + 2 * kDecMaxG * 4;
 };
 
@@ -89,14 +89,13 @@ __device__ __forceinline__ void stage_tile(uint32_t tile, const __nv_bfloat16* s
   cp_async_commit();
 }
 
-template <int D, int HPG>  // HPG: query heads per thread in the score phase
+template <int D, int HPG>  // HPG: query heads per thread-key in the score phase (1, 2, 4)
 __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecParams p) {
   using S = DecSmem<D>;
   extern __shared__ __align__(16) uint8_t smem[];
   float* q_s = reinterpret_cast<float*>(smem + S::kQ);
   float* s_s = reinterpret_cast<float*>(smem + S::kS);
   float* o_s = reinterpret_cast<float*>(smem + S::kO);
-  float* red = reinterpret_cast<float*>(smem + S::kRed);
   float* st_max = reinterpret_cast<float*>(smem + S::kStat);
   float* st_sum = st_max + kDecMaxG;
   const uint32_t kv_s = ptx::smem_u32(smem + S::kKV);
@@ -123,11 +122,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecPa
     o_s[i] = 0.f;
   }
 
-  // ---- 1. scores: thread = (key j of the tile, group hg of HPG heads)
-  const int j = t & (kDecTile - 1);
-  const int hg = t >> 6;  // 4 groups of 64 threads
+  // ---- 1. scores: thread = (KPT keys of the tile, group g of HPT heads).
+  // KPT = 1 for up to 4 heads per group; 2 above, so that each 16-byte load
+  // of K or of Q serves more FMAs.
+  constexpr int KPT = HPG == 1 ? 1 : 2;
+  constexpr int HPT = HPG == 1 ? 1 : HPG / 2;
+  constexpr int kSlots = kDecTile / KPT;     // key slots per head group
+  const int j0 = t % kSlots;
+  const int g = t / kSlots;                  // a warp shares its group: Q reads broadcast
   for (int tile = 0; tile < n_tiles; ++tile) {
-    const uint32_t cur = kv_s + (tile & 1) * S::kTileBytes;
     if (tile + 1 < n_tiles) {
       stage_tile<D>(kv_s + ((tile + 1) & 1) * S::kTileBytes, p.k, p, b, kh,
                     key0 + (tile + 1) * kDecTile);
@@ -136,83 +139,72 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecPa
       cp_async_wait<0>();
     }
     __syncthreads();
-    float2 acc[HPG];
+    float2 acc[KPT][HPT];
 #pragma unroll
-    for (int i = 0; i < HPG; ++i) acc[i] = make_float2(0.f, 0.f);
-    const uint8_t* row = smem + S::kKV + (tile & 1) * S::kTileBytes + j * S::kRowBytes;
+    for (int a2 = 0; a2 < KPT; ++a2)
+#pragma unroll
+      for (int i = 0; i < HPT; ++i) acc[a2][i] = make_float2(0.f, 0.f);
+    const uint8_t* tb = smem + S::kKV + (tile & 1) * S::kTileBytes;
 #pragma unroll 4
     for (int c = 0; c < D / 8; ++c) {
-      const uint4 kr = *reinterpret_cast<const uint4*>(row + ((c ^ (j & 7)) << 4));
-      const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kr);
-      float2 kf[4];
+      float2 kf[KPT][4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) kf[x] = __bfloat1622float2(k2[x]);
+      for (int a2 = 0; a2 < KPT; ++a2) {
+        const int j = j0 + a2 * kSlots;
+        const uint4 kr = *reinterpret_cast<const uint4*>(tb + j * S::kRowBytes + ((c ^ (j & 7)) << 4));
+        const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kr);
 #pragma unroll
-      for (int i = 0; i < HPG; ++i) {
-        const float4* qr = reinterpret_cast<const float4*>(q_s + (hg * HPG + i) * D + c * 8);
+        for (int x = 0; x < 4; ++x) kf[a2][x] = __bfloat1622float2(k2[x]);
+      }
+#pragma unroll
+      for (int i = 0; i < HPT; ++i) {
+        const float4* qr = reinterpret_cast<const float4*>(q_s + (g * HPT + i) * D + c * 8);
         const float4 qa = qr[0], qb = qr[1];
-        acc[i] = ptx::fma2(make_float2(qa.x, qa.y), kf[0], acc[i]);
-        acc[i] = ptx::fma2(make_float2(qa.z, qa.w), kf[1], acc[i]);
-        acc[i] = ptx::fma2(make_float2(qb.x, qb.y), kf[2], acc[i]);
-        acc[i] = ptx::fma2(make_float2(qb.z, qb.w), kf[3], acc[i]);
+#pragma unroll
+        for (int a2 = 0; a2 < KPT; ++a2) {
+          acc[a2][i] = ptx::fma2(make_float2(qa.x, qa.y), kf[a2][0], acc[a2][i]);
+          acc[a2][i] = ptx::fma2(make_float2(qa.z, qa.w), kf[a2][1], acc[a2][i]);
+          acc[a2][i] = ptx::fma2(make_float2(qb.x, qb.y), kf[a2][2], acc[a2][i]);
+          acc[a2][i] = ptx::fma2(make_float2(qb.z, qb.w), kf[a2][3], acc[a2][i]);
+        }
       }
     }
 #pragma unroll
-    for (int i = 0; i < HPG; ++i)
-      if (hg * HPG + i < G) s_s[(tile * kDecTile + j) * kDecMaxG + hg * HPG + i] = acc[i].x + acc[i].y;
+    for (int i = 0; i < HPT; ++i)
+#pragma unroll
+      for (int a2 = 0; a2 < KPT; ++a2)
+        if (g * HPT + i < G)
+          s_s[(g * HPT + i) * kDecMaxL + tile * kDecTile + j0 + a2 * kSlots] =
+              acc[a2][i].x + acc[a2][i].y;
     __syncthreads();  // the tile buffer is reloaded two tiles on
   }
   // prefetch the first V tile while the softmax runs
   stage_tile<D>(kv_s, p.v, p, b, kh, key0);
 
-  // ---- 2. per head: max, p = 2^(s - max), sum (thread t owns keys t, t+256)
+  // ---- 2. per head: max, p = 2^(s - max), sum. Head h belongs to the 16
+  // threads 16h .. 16h+15 (half a warp), each scanning every 16th key, so
+  // both reductions stay inside the half-warp.
   {
-    float mx[kDecMaxG];
+    const int h = t >> 4;
+    const int sub = t & 15;
+    float* row = s_s + h * kDecMaxL;
+    float m = -INFINITY;
+    if (h < G)
+      for (int k = sub; k < p.L; k += 16) m = fmaxf(m, row[k]);
 #pragma unroll
-    for (int h = 0; h < kDecMaxG; ++h) mx[h] = -INFINITY;
-    for (int k = t; k < p.L; k += kDecThreads)
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+    if (h < G)
+      for (int k = sub; k < p.L; k += 16) {
+        const float e = ptx::ex2(row[k] - m);
+        row[k] = e;
+        sum += e;
+      }
 #pragma unroll
-      for (int h = 0; h < kDecMaxG; ++h)
-        if (h < G) mx[h] = fmaxf(mx[h], s_s[k * kDecMaxG + h]);
-#pragma unroll
-    for (int h = 0; h < kDecMaxG; ++h) {
-      if (h >= G) break;
-      float m = mx[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) red[warp * kDecMaxG + h] = m;
-    }
-    __syncthreads();
-    if (t < G) {
-      float m = red[t];
-      for (int w = 1; w < kDecThreads / 32; ++w) m = fmaxf(m, red[w * kDecMaxG + t]);
-      st_max[t] = m;
-    }
-    __syncthreads();
-    float sm[kDecMaxG];
-#pragma unroll
-    for (int h = 0; h < kDecMaxG; ++h) sm[h] = 0.f;
-    for (int k = t; k < p.L; k += kDecThreads)
-#pragma unroll
-      for (int h = 0; h < kDecMaxG; ++h)
-        if (h < G) {
-          const float e = ptx::ex2(s_s[k * kDecMaxG + h] - st_max[h]);
-          s_s[k * kDecMaxG + h] = e;
-          sm[h] += e;
-        }
-#pragma unroll
-    for (int h = 0; h < kDecMaxG; ++h) {
-      if (h >= G) break;
-      float s = sm[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) red[warp * kDecMaxG + h] = s;
-    }
-    __syncthreads();
-    if (t < G) {
-      float s = 0.f;
-      for (int w = 0; w < kDecThreads / 32; ++w) s += red[w * kDecMaxG + t];
-      st_sum[t] = s;
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (sub == 0 && h < G) {
+      st_max[h] = m;
+      st_sum[h] = sum;
     }
   }
 
@@ -234,33 +226,39 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecPa
     }
     __syncthreads();
     const uint8_t* base = smem + S::kKV + (tile & 1) * S::kTileBytes;
-    for (int jj = warp; jj < kDecTile; jj += kDecThreads / 32) {
+    // warp w takes keys 8w .. 8w+7 of the tile: their p of one head are two
+    // 16-byte loads (all lanes read the same address)
+    constexpr int kKeysPerWarp = kDecTile / (kDecThreads / 32);
+    float vf[kKeysPerWarp][kCols];
+#pragma unroll
+    for (int kk = 0; kk < kKeysPerWarp; ++kk) {
+      const int jj = warp * kKeysPerWarp + kk;
       // this lane's kCols columns: byte offset lane*kCols*2 of the row
       const int off = lane * kCols * 2;
       const int unit = off >> 4;
       const uint8_t* src = base + jj * S::kRowBytes + (((unit ^ (jj & 7)) << 4) | (off & 15));
-      float vf[kCols];
       if constexpr (kCols == 4) {
         const uint2 raw = *reinterpret_cast<const uint2*>(src);
         const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
         const float2 a = __bfloat1622float2(v2[0]), c = __bfloat1622float2(v2[1]);
-        vf[0] = a.x; vf[1] = a.y; vf[2] = c.x; vf[3] = c.y;
+        vf[kk][0] = a.x; vf[kk][1] = a.y; vf[kk][2] = c.x; vf[kk][3] = c.y;
       } else {
         const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
         const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw));
-        vf[0] = a.x; vf[1] = a.y;
+        vf[kk][0] = a.x; vf[kk][1] = a.y;
       }
-      const float4* pr = reinterpret_cast<const float4*>(s_s + (tile * kDecTile + jj) * kDecMaxG);
+    }
+    const float* pc = s_s + tile * kDecTile + warp * kKeysPerWarp;  // head h at h * kDecMaxL
 #pragma unroll
-      for (int h4 = 0; h4 < kDecMaxG / 4; ++h4) {
-        if (h4 * 4 >= G) break;
-        const float4 pv = pr[h4];
-        const float ph[4] = {pv.x, pv.y, pv.z, pv.w};
+    for (int h = 0; h < kDecMaxG; ++h) {
+      if (h >= G) break;
+      const float4 p0 = *reinterpret_cast<const float4*>(pc + h * kDecMaxL);
+      const float4 p1 = *reinterpret_cast<const float4*>(pc + h * kDecMaxL + 4);
+      const float ph[kKeysPerWarp] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+      for (int kk = 0; kk < kKeysPerWarp; ++kk)
 #pragma unroll
-          for (int x = 0; x < kCols; ++x) acc[h4 * 4 + i][x] = fmaf(ph[i], vf[x], acc[h4 * 4 + i][x]);
-      }
+        for (int x = 0; x < kCols; ++x) acc[h][x] = fmaf(ph[kk], vf[kk][x], acc[h][x]);
     }
     __syncthreads();
   }
