@@ -622,9 +622,19 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     float l = 0.f;
     bool ok = true;
     int32_t kpos_next = n_tiles > 0 ? __ldg(kv_tile_pos + w.lo) : 0;
+    // The epilogue reads this row's fp32 running output back (merge): ask L2
+    // for it a few tiles before the end so those reads do not wait on HBM.
+    const bool will_merge = p.mode == CP_ATTN_ACCUMULATE && !p.first;
+    const int prefetch_at = n_tiles > 3 ? n_tiles - 3 : 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int32_t kpos0 = kpos_next;
       if (j + 1 < n_tiles) kpos_next = __ldg(kv_tile_pos + w.lo + j + 1);
+      if (will_merge && j == prefetch_at) {
+        const float* row = p.o_part + ((q_row0 + r) * p.Hq + h) * D;
+#pragma unroll
+        for (int x = 0; x < D * 4 / 128; ++x)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(row + x * 32)));
+      }
       const bool full = (kpos0 + 127 <= qpos0) && (kpos0 >= ds_last);
       if (!ptx::mbar_wait(bar(PB_S + hs), j & 1, s_abort, p.wait_limit_ns)) {
         ptx::record_timeout(p.status, s_abort, 0x3600 + j);
@@ -762,7 +772,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           a_r[it] = __shfl_sync(0xffffffffu, a_row, it * 4 + sub);
           b_r[it] = __shfl_sync(0xffffffffu, w_old, it * 4 + sub);
         }
-#pragma unroll 1
+        // the running output's rows of chunk c + 1 are requested while chunk
+        // c is combined, so the read-backs overlap
+        float4 old[8], old_next[8];
+        auto load_old = [&](float4 (&dst)[8], int c) {
+#pragma unroll
+          for (int it = 0; it < 8; ++it)
+            dst[it] = *reinterpret_cast<const float4*>(o_dst + base_off + (it * 4 + sub) * row_stride + c * 32);
+        };
+        if (merge) load_old(old, 0);
+#pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           if (n_tiles > 0) {
@@ -771,18 +790,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 #pragma unroll
             for (int x = 0; x < 32; ++x) o[x] = 0.f;
           }
+          if (merge && c + 1 < D / 32) load_old(old_next, c + 1);
           uint8_t* buf = stage + (c & 1) * 4096;
 #pragma unroll
           for (int x4 = 0; x4 < 8; ++x4)
             *reinterpret_cast<float4*>(buf + lane * 128 + ((x4 ^ (lane & 7)) << 4)) =
                 make_float4(o[4 * x4], o[4 * x4 + 1], o[4 * x4 + 2], o[4 * x4 + 3]);
           __syncwarp();
-          float4 old[8];
-          if (merge) {
-#pragma unroll
-            for (int it = 0; it < 8; ++it)
-              old[it] = *reinterpret_cast<const float4*>(o_dst + base_off + (it * 4 + sub) * row_stride + c * 32);
-          }
 #pragma unroll
           for (int it = 0; it < 8; ++it) {
             const int row = it * 4 + sub;
@@ -802,6 +816,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
               pk.y = ptx::pack_bf16(v.z, v.w);
               *reinterpret_cast<uint2*>(p.o_final + off) = pk;
             }
+          }
+          if (merge && c + 1 < D / 32) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) old[it] = old_next[it];
           }
         }
       }
