@@ -527,8 +527,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   } else if (n_iter > 0 && warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop so that descriptors stay warp-uniform;
-    // lane 0 alone issues each tcgen05 instruction.
-    const uint32_t leader = lane == 0 ? 1u : 0u;
+    // one elected lane issues each tcgen05 instruction.
+    const uint32_t leader = ptx::elect_one();
     constexpr uint32_t idesc_sdp = ptx::idesc_fp16(128, 64, 0, 0);   // K-major A and B
     constexpr uint32_t idesc_kv = ptx::idesc_fp16(128, 128, 0, 1);   // A K-major, B MN-major
     constexpr uint32_t idesc_dq = ptx::idesc_fp16(128, 64, 1, 1);    // A and B MN-major

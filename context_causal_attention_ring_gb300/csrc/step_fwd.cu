@@ -530,8 +530,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   } else if (n_tiles > 0 && warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop so that descriptors stay warp-uniform;
-    // lane 0 alone issues each tcgen05 instruction.
-    const uint32_t leader = lane == 0 ? 1u : 0u;
+    // one elected lane issues each tcgen05 instruction.
+    const uint32_t leader = ptx::elect_one();
     constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
     const uint64_t dQ0 = ptx::sdesc_sw128(sQ, 16, 1024);
