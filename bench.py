@@ -221,6 +221,8 @@ def run_ours(args, w):
     dk = torch.empty((plan.T_kv, Hkv, d), dtype=torch.float32, device=dev)
     dv = torch.empty_like(dk)
 
+    # consecutive ring steps on this stream are each other's only producers
+    plan.set_chaining(True)
     pairs = [plan.visible_pairs(t) for t in range(R)]
     fwd_flops = 4.0 * d * Hq * sum(pairs)
     bwd_flops = 2.5 * fwd_flops

@@ -80,6 +80,7 @@ _SIG = {
     "cp_attn_decode_workspace_size": (_I, [ctypes.POINTER(_DecodeDesc), ctypes.POINTER(ctypes.c_size_t)]),
     "cp_attn_decode": (_I, [ctypes.POINTER(_DecodeDesc), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_plan_destroy": (None, [_P]),
+    "cp_attn_plan_set_chaining": (_I, [_P, _I]),
     "cp_attn_plan_info": (_I, [_P, ctypes.POINTER(_I64), _I]),
     "cp_attn_plan_positions": (_I, [_P, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
     "cp_attn_plan_schedule": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
@@ -297,6 +298,9 @@ class Plan:
         return int(out.value)
 
     # ------------------------------------------------------------ device calls
+    def set_chaining(self, enable: bool):
+        _check(load().cp_attn_plan_set_chaining(self.handle, 1 if enable else 0))
+
     def step_fwd(self, step, q, k, v, o_part, lse_part, mode, o_final=None, stream=None):
         _check(load().cp_attn_step_fwd(self.handle, step, _ptr(q), _ptr(k), _ptr(v),
                                        _ptr(o_part), _ptr(lse_part), mode, _ptr(o_final),

@@ -312,10 +312,16 @@ cp_attn_status cp_attn_half_ops_size(cp_attn_plan_t p, size_t* bytes) {
   return CP_ATTN_OK;
 }
 
-cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const void* k,
-                                const void* v, float* o_part, float* lse_part,
-                                cp_attn_merge_mode mode, void* o_final, void* stream) {
-  clear_error();
+namespace {
+
+// One forward ring step. chained: launch it so that it may overlap the tail of
+// the kernel before it, which must be an earlier step of the same ring.
+// *launched tells whether a kernel went out (a step without work launches none).
+cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const void* k,
+                             const void* v, float* o_part, float* lse_part,
+                             cp_attn_merge_mode mode, void* o_final, void* stream, bool chained,
+                             bool* launched) {
+  *launched = false;
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
   if (step < 0 || step >= p->R) return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd: step out of range");
@@ -358,19 +364,21 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const
   const bool all_items = (mode == CP_ATTN_WRITE_PARTIAL) || fp.first || fp.o_final != nullptr;
   const int n_items = all_items ? (p->fwd_off[step + 1] - p->fwd_off[step]) : p->fwd_nonempty[step];
   if (n_items == 0) return CP_ATTN_OK;
+  *launched = true;
   // one CTA per (item, query head), or per (item, pair of heads of a group)
   const int hpc = step_fwd_heads_per_cta(p->d);
   const int G = p->Hq / p->Hkv;
   const int64_t units = hpc == 1 ? p->Hq : static_cast<int64_t>(p->Hkv) * ((G + 1) / 2);
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_items) * units));
   return launch_step_fwd(p->d, grid, step_fwd_smem_bytes(p->d), static_cast<cudaStream_t>(stream),
-                         tq, tk, tv, fp);
+                         tq, tk, tv, fp, chained);
 }
 
-cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops,
-                                const float* lse, const float* delta, float* dq_acc,
-                                float* dk_acc, float* dv_acc, void* stream) {
-  clear_error();
+// One backward ring step; chained and *launched as for step_fwd_impl.
+cp_attn_status step_bwd_impl(cp_attn_plan_t p, int step, const void* half_ops, const float* lse,
+                             const float* delta, float* dq_acc, float* dk_acc, float* dv_acc,
+                             void* stream, bool chained, bool* launched) {
+  *launched = false;
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
   if (step < 0 || step >= p->R) return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: step out of range");
@@ -418,9 +426,38 @@ cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops
   bp.wait_limit_ns = kWaitLimitNs;
   const int n_items = p->bwd_off[step + 1] - p->bwd_off[step];
   if (n_items == 0) return CP_ATTN_OK;
+  *launched = true;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_items) * p->Hkv));
   return launch_step_bwd(p->d, grid, step_bwd_smem_bytes(p->d), static_cast<cudaStream_t>(stream),
-                         tq, tk, tv, tdo, bp);
+                         tq, tk, tv, tdo, bp, chained);
+}
+
+}  // namespace
+
+cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const void* k,
+                                const void* v, float* o_part, float* lse_part,
+                                cp_attn_merge_mode mode, void* o_final, void* stream) {
+  clear_error();
+  bool launched = false;
+  return step_fwd_impl(p, step, q, k, v, o_part, lse_part, mode, o_final, stream,
+                       p && p->chain_steps && step > 0, &launched);
+}
+
+cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops,
+                                const float* lse, const float* delta, float* dq_acc,
+                                float* dk_acc, float* dv_acc, void* stream) {
+  clear_error();
+  bool launched = false;
+  return step_bwd_impl(p, step, half_ops, lse, delta, dq_acc, dk_acc, dv_acc, stream,
+                       p && p->chain_steps && step > 0, &launched);
+}
+
+cp_attn_status cp_attn_plan_set_chaining(cp_attn_plan_t p, int enable) {
+  clear_error();
+  if (!p) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_set_chaining: null plan");
+  if (enable != 0 && enable != 1) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_set_chaining: enable must be 0 or 1");
+  p->chain_steps = enable;
+  return CP_ATTN_OK;
 }
 
 cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* q, const void* k,
@@ -489,10 +526,14 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, c
   float* ws = static_cast<float*>(workspace);
   if (p->variant == CP_ATTN_PASS_KV) {
     // Q stays, KV moves; merge "as it goes" into the fp32 accumulator
+    // each step after the first that launches overlaps the tail of the one before
+    bool prev = false;
     for (int t = 0; t < p->R; ++t) {
-      st = cp_attn_step_fwd(p, t, q, k, v, ws, lse, CP_ATTN_ACCUMULATE, t == p->R - 1 ? o : nullptr,
-                            stream);
+      bool launched = false;
+      st = step_fwd_impl(p, t, q, k, v, ws, lse, CP_ATTN_ACCUMULATE, t == p->R - 1 ? o : nullptr,
+                         stream, prev, &launched);
       if (st != CP_ATTN_OK) return st;
+      prev = prev || launched;
     }
     return CP_ATTN_OK;
   }
@@ -503,9 +544,13 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, c
   const int64_t l_slot = p->T_q * p->Hq;
   const size_t o_bytes = (static_cast<size_t>(o_slot) * p->R * sizeof(float) + 255) & ~static_cast<size_t>(255);
   float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  bool prev = false;
   for (int t = 0; t < p->R; ++t) {
-    st = cp_attn_step_fwd(p, t, q, k, v, ws, ws_lse, CP_ATTN_WRITE_PARTIAL, nullptr, stream);
+    bool launched = false;
+    st = step_fwd_impl(p, t, q, k, v, ws, ws_lse, CP_ATTN_WRITE_PARTIAL, nullptr, stream, prev,
+                       &launched);
     if (st != CP_ATTN_OK) return st;
+    prev = prev || launched;
   }
   // The merge also leaves the fp32 result in slot 0 (each (row, head) is read
   // completely by one warp before that warp writes it).
@@ -533,9 +578,12 @@ cp_attn_status cp_attn_backward(cp_attn_plan_t p, const void* q, const void* k, 
                                    stream)) !=
       CP_ATTN_OK)
     return st;
+  bool prev = false;
   for (int t = 0; t < p->R; ++t) {
-    st = cp_attn_step_bwd(p, t, half_ops, lse, delta, dq, dk, dv, stream);
+    bool launched = false;
+    st = step_bwd_impl(p, t, half_ops, lse, delta, dq, dk, dv, stream, prev, &launched);
     if (st != CP_ATTN_OK) return st;
+    prev = prev || launched;
   }
   return CP_ATTN_OK;
 }

@@ -69,6 +69,8 @@ struct cp_attn_plan_s {
   int32_t* d_status = nullptr;
   int32_t* d_row_q = nullptr;   // rank-major row -> natural row (queries)
   int32_t* d_row_kv = nullptr;  // rank-major row -> natural row (keys)
+  // per-step calls of steps >= 1 launch chained to the kernel before them
+  int chain_steps = 0;
 };
 
 namespace cpa {

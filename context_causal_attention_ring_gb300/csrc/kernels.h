@@ -53,9 +53,12 @@ struct BwdParams {
   uint64_t wait_limit_ns;
 };
 
+// chained: launch with programmatic stream serialization, so that the grid
+// may start while the kernel before it (the previous ring step) drains; the
+// d = 128 kernels wait for it before their accumulator read-modify-write.
 cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
-                               const CUtensorMap& tv, const FwdParams& p);
+                               const CUtensorMap& tv, const FwdParams& p, bool chained);
 size_t step_fwd_smem_bytes(int d);
 // Query heads one forward CTA handles (d = 128 pairs the heads of a group).
 int step_fwd_heads_per_cta(int d);
@@ -63,7 +66,7 @@ int step_fwd_heads_per_cta(int d);
 cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, const CUtensorMap& tdo,
-                               const BwdParams& p);
+                               const BwdParams& p, bool chained);
 size_t step_bwd_smem_bytes(int d);
 // Rows of the Q / dO tensor-map box the backward kernel for head_dim d uses.
 int step_bwd_q_box_rows(int d);

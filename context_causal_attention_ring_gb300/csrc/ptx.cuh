@@ -87,6 +87,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch. grid_dep_launch lets the next kernel of the
+// stream (when it was launched with programmatic stream serialization) start
+// once every CTA of this grid has executed it or exited. grid_dep_wait blocks
+// until the grids this one depends on have completed and their writes are
+// visible; it returns at once for a normally launched grid.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -484,6 +484,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  // the next ring step may start on SMs this grid leaves idle
+  if (threadIdx.x == 0) ptx::grid_dep_launch();
   const uint32_t tDV = tmem + 256;
   const uint32_t tDK = tmem + 384;
 
@@ -733,6 +735,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       const volatile int never = 0;
       const bool done = ptx::mbar_wait(bar(WB_DRAIN), 0, &never, p.wait_limit_ns);
       if (__all_sync(0xffffffffu, done)) {
+        // the previous ring step (when this grid was launched chained to it)
+        // has finished its read-modify-write of the same dK / dV rows
+        ptx::grid_dep_wait();
         ptx::tc_fence_after();
         // Rows leave through shared memory so that the global read-modify-
         // write is coalesced: per 32-column chunk the warp stages its 32 rows
@@ -798,7 +803,7 @@ int step_bwd_q_box_rows(int d) { return d == 128 ? 64 : 128; }
 cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, const CUtensorMap& tdo,
-                               const BwdParams& p) {
+                               const BwdParams& p, bool chained) {
   static bool attr_done[2] = {false, false};
   cudaError_t err;
   if (d == 128) {
@@ -808,7 +813,18 @@ cp_attn_status launch_step_bwd(int d, dim3 grid, size_t smem, cudaStream_t s,
       if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_bwd attr: ") + cudaGetErrorString(err));
       attr_done[1] = true;
     }
-    step_bwd_wide_kernel<<<grid, kThreadsW, smem, s>>>(tq, tk, tv, tdo, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreadsW);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    err = cudaLaunchKernelEx(&cfg, step_bwd_wide_kernel, tq, tk, tv, tdo, p);
+    if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_bwd launch: ") + cudaGetErrorString(err));
   } else {
     if (!attr_done[0]) {
       err = cudaFuncSetAttribute(step_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,

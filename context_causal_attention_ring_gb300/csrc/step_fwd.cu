@@ -488,6 +488,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  // the next ring step may start on SMs this grid leaves idle
+  if (threadIdx.x == 0) ptx::grid_dep_launch();
 
   if (n_tiles > 0 && (warp == 8 || warp == 10) && lane == 0) {
     // ------------------------------------------------------------ producers
@@ -720,6 +722,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
+      // the previous ring step (when this grid was launched chained to it)
+      // has finished with the running output and LSE rows read below
+      ptx::grid_dep_wait();
       ptx::tc_fence_after();
       const int64_t g = q_row0 + r;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -845,7 +850,7 @@ int step_fwd_heads_per_cta(int d) { return d == 128 ? 2 : 1; }
 
 cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
-                               const CUtensorMap& tv, const FwdParams& p) {
+                               const CUtensorMap& tv, const FwdParams& p, bool chained) {
   static bool attr_done[2] = {false, false};
   cudaError_t err;
   if (d == 128) {
@@ -855,7 +860,18 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
       if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd attr: ") + cudaGetErrorString(err));
       attr_done[1] = true;
     }
-    step_fwd_pair_kernel<<<grid, kThreadsP, smem, s>>>(tq, tk, tv, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreadsP);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    err = cudaLaunchKernelEx(&cfg, step_fwd_pair_kernel, tq, tk, tv, p);
+    if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd launch: ") + cudaGetErrorString(err));
   } else {
     if (!attr_done[0]) {
       err = cudaFuncSetAttribute(step_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -221,6 +221,22 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
                                 cp_attn_merge_mode mode, void* o_final,
                                 void* stream);
 
+/* Chained ring steps (programmatic dependent launch). With enable = 1,
+ * cp_attn_step_fwd and cp_attn_step_bwd launch every step >= 1 so that it
+ * may start on SMs left idle while the kernel before it on the stream drains;
+ * the step waits for that kernel to finish before it reads or writes the
+ * running output and LSE (forward, ACCUMULATE) or dK and dV (backward). Its
+ * other inputs are read before that wait, so the caller promises that the
+ * kernel launched just before step t >= 1 on the same stream is an earlier
+ * step of the same ring on the same buffers, and that nothing written
+ * between them is read by the step. cp_attn_forward and cp_attn_backward
+ * always chain their own steps. enable = 0 (the default) launches every step
+ * normally. The pages' ring runs one kernel per step on each rank; chaining
+ * only lets consecutive steps of the emulated ring overlap at their edges.
+ * Affects the head_dim 128 kernels. ERR_INVALID_ARG for a NULL plan or
+ * enable outside {0, 1}. */
+cp_attn_status cp_attn_plan_set_chaining(cp_attn_plan_t plan, int enable);
+
 /* Bytes of the fp16 operand copies used by the backward step: exact IEEE
  * fp16 copies of q, k, v and dout, in that order, each starting on a
  * 256-byte boundary. The backward MMAs run on fp16 operands so that the

@@ -95,13 +95,17 @@ def test_step_partials_each_pair(d, Hq, Hkv):
             assert np.all(O[ko, qs][empty.T] == 0.0)
 
 
-def test_running_accumulator_fp32():
+@pytest.mark.parametrize("chained", [False, True])
+def test_running_accumulator_fp32(chained):
     """ACCUMULATE: the fp32 running merge after all steps equals monolithic
-    attention at 1e-2 without any bf16 rounding of the result."""
+    attention at 1e-2 without any bf16 rounding of the result, with the steps
+    launched normally and chained (each step overlapping the previous one's
+    tail until its read-modify-write of the accumulator)."""
     w = Workload("acc", 2048, 4, 1, 128, 4)
     inp = make_inputs(w)
     plan = _plan(w)
     run = DeviceRun(plan, inp)
+    plan.set_chaining(chained)
     o_acc = torch.full((plan.T_q, 4, 128), float("nan"), device="cuda")
     lse = torch.full((4, plan.T_q), float("nan"), device="cuda")
     for t in range(plan.R):

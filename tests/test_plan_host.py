@@ -140,3 +140,13 @@ def test_header_declarations_are_exported():
     for name in declared:
         assert hasattr(lib, name), name
     assert set(declared) == set(cpa.exported_symbols())
+
+
+def test_step_chaining_flag_is_validated():
+    """cp_attn_plan_set_chaining takes 0 or 1 and needs a plan (host only)."""
+    plan = _plan(N=1024, R=4)
+    plan.set_chaining(True)
+    plan.set_chaining(False)
+    lib = cpa.load()
+    assert lib.cp_attn_plan_set_chaining(plan.handle, 2) == 1  # CP_ATTN_ERR_INVALID_ARG
+    assert lib.cp_attn_plan_set_chaining(None, 1) == 1  # CP_ATTN_ERR_INVALID_ARG
