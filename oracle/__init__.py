@@ -6,6 +6,9 @@ restatement of what the pages define. Only the tests, the smoke check of
 The CUDA library never calls it, and it shares no code with the CUDA path:
 the only common module is ``workloads`` (seeded random inputs).
 
+``oracle.fp8`` holds the E4M3 format and the per-tensor FP8 quantization of
+the FP8 path; its attention is ``attention`` on the dequantized values.
+
 Parity status per function (see the pins in ``tests/test_oracle_*.py``):
 every public function here is pinned against something other than itself
 (a worked example printed on the pages, closed forms, brute force on tiny
