@@ -531,6 +531,87 @@ def run_decode_bench(args):
                       "rows": rows}), flush=True)
 
 
+def run_fp8_bench(args):
+    """FP8 (E4M3) against bf16 on the 405B-shaped prefill (131072 new tokens,
+    128 query / 8 KV heads, d = 128, CP = 8 zigzag), both orderings, forward
+    only: the ring of K1 steps (cp_attn_forward_fp8 / cp_attn_forward), each
+    timed with CUDA events after warm-up; the quantization kernels (absmax,
+    quantize, V^T) are timed apart. TFLOPS count unmasked FLOPs (4 d per
+    visible pair per query head). The FP8 roofline peak is the measured bf16
+    burst peak times the nominal fp8 / bf16 ratio (2)."""
+    import torch
+    import context_causal_attention_ring_gb300 as cpa
+
+    torch.cuda.set_device(0)
+    peaks, peak_kind = _peaks()
+    w = WORKLOADS["prefill_405b_full"]
+    inp = make_inputs(w, with_dout=False)
+    dev = torch.device("cuda:0")
+    rows = []
+    for variant in ("pass_kv", "pass_q"):
+        plan = cpa.Plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                        layout=w.layout, variant=variant)
+        R, Hq, Hkv, d = plan.R, plan.Hq, plan.Hkv, plan.d
+        flops = 4.0 * d * Hq * plan.visible_pairs()
+        bf = {}
+        for name, bits in (("q", inp.q), ("k", inp.k), ("v", inp.v)):
+            x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+            y = torch.empty_like(x)
+            plan.layout_apply(cpa.TENSOR_Q if name == "q" else cpa.TENSOR_KV, cpa.TO_RANK_MAJOR,
+                              x, y)
+            bf[name] = y
+            del x
+        T_q, T_kv = plan.T_q, plan.T_kv
+        amax = torch.zeros(4, dtype=torch.float32, device=dev)
+        scales = torch.zeros(4, dtype=torch.float32, device=dev)
+        q8 = torch.empty((T_q, Hq, d), dtype=torch.uint8, device=dev)
+        k8 = torch.empty((T_kv, Hkv, d), dtype=torch.uint8, device=dev)
+        vt8 = torch.empty((Hkv, d, T_kv), dtype=torch.uint8, device=dev)
+
+        def quantize():
+            for i, (x, out, rws, hh, tr) in enumerate(((bf["q"], q8, T_q, Hq, False),
+                                                        (bf["k"], k8, T_kv, Hkv, False),
+                                                        (bf["v"], vt8, T_kv, Hkv, True))):
+                cpa.fp8_absmax(x, rws * hh * d, amax[i:i + 1])
+                cpa.fp8_quantize(x, rws, hh, d, amax[i:i + 1], out, scales[i:i + 1], transpose=tr)
+
+        o = torch.empty((T_q, Hq, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((Hq, T_q), dtype=torch.float32, device=dev)
+        ws = torch.empty(plan.workspace_size(cpa.OP_FORWARD), dtype=torch.uint8, device=dev)
+        calls = {"fp8": lambda: plan.forward_fp8(q8, k8, vt8, scales, o, lse, ws),
+                 "bf16": lambda: plan.forward(bf["q"], bf["k"], bf["v"], o, lse, ws),
+                 "quantize": quantize}
+        res = {}
+        for name, fn in calls.items():
+            for _ in range(max(3, args.warmup)):
+                if name == "fp8":
+                    quantize()
+                fn()
+            n = max(5, min(args.steps, 10))
+            ev = [(torch.cuda.Event(True), torch.cuda.Event(True)) for _ in range(n)]
+            for e0, e1 in ev:
+                e0.record()
+                fn()
+                e1.record()
+            torch.cuda.synchronize()
+            res[name] = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        plan.sync_status()
+        qbytes = 2 * (T_q * Hq * d * 2 + 2 * T_kv * Hkv * d * 2) + T_q * Hq * d + 2 * T_kv * Hkv * d
+        rows.append({"variant": variant, "flops": flops,
+                     "fp8_ms": res["fp8"], "fp8_tflops": flops / (res["fp8"] * 1e-3) / 1e12,
+                     "bf16_ms": res["bf16"], "bf16_tflops": flops / (res["bf16"] * 1e-3) / 1e12,
+                     "quantize_ms": res["quantize"],
+                     "quantize_gbs": qbytes / (res["quantize"] * 1e-3) / 1e9})
+        del bf, q8, k8, vt8, o, lse, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "fp8 vs bf16 forward TFLOPS (unmasked FLOPs)",
+                      "workload": "prefill_405b_full: 131072 tokens, 128/8 heads, d=128, CP=8 zigzag",
+                      "fp8_peak_tflops": 2 * peaks["bf16_tflops"],
+                      "bf16_peak_tflops": peaks["bf16_tflops"],
+                      "peak_kind": f"bf16_tflops burst ({peak_kind}); fp8 = 2 x bf16 (nominal ratio)",
+                      "hbm_gbs": peaks["hbm_gbs"], "rows": rows}), flush=True)
+
+
 def run_e2e(args, plan, inp, dev, stream, flops, ws):
     """End to end through the public whole-op calls with host buffers. Every
     step copies its inputs from pinned host memory, runs the layout
@@ -648,9 +729,14 @@ def main():
                     help="time Pass KV against Pass Q at several KV-cache hit rates")
     ap.add_argument("--usp-sweep", action="store_true",
                     help="time the layer as zigzag ring, USP and pure Ulysses arrangements")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 (E4M3) forward against bf16 on the 405B-shaped prefill")
     ap.add_argument("--decode", action="store_true",
                     help="time the one-row decode against the HBM roofline")
     args = ap.parse_args()
+    if args.fp8:
+        run_fp8_bench(args)
+        return
     if args.decode:
         run_decode_bench(args)
         return

@@ -81,6 +81,10 @@ _SIG = {
     "cp_attn_decode": (_I, [ctypes.POINTER(_DecodeDesc), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_plan_destroy": (None, [_P]),
     "cp_attn_plan_set_chaining": (_I, [_P, _I]),
+    "cp_attn_fp8_absmax": (_I, [_P, _I64, _P, _P]),
+    "cp_attn_fp8_quantize": (_I, [_P, _I64, _I, _I, _P, _I, _P, _P, _P]),
+    "cp_attn_step_fwd_fp8": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
+    "cp_attn_forward_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_plan_info": (_I, [_P, ctypes.POINTER(_I64), _I]),
     "cp_attn_plan_positions": (_I, [_P, _I, _I, ctypes.POINTER(ctypes.c_int32)]),
     "cp_attn_plan_schedule": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
@@ -306,6 +310,20 @@ class Plan:
                                        _ptr(o_part), _ptr(lse_part), mode, _ptr(o_final),
                                        _stream(stream)))
 
+    def step_fwd_fp8(self, step, q8, k8, vt8, scales, o_part, lse_part, mode, o_final=None,
+                     stream=None):
+        _check(load().cp_attn_step_fwd_fp8(self.handle, step, _ptr(q8), _ptr(k8), _ptr(vt8),
+                                           _ptr(scales), _ptr(o_part), _ptr(lse_part), mode,
+                                           _ptr(o_final), _stream(stream)))
+
+    def forward_fp8(self, q8, k8, vt8, scales, o, lse, workspace, workspace_bytes=None,
+                    stream=None):
+        if workspace_bytes is None:
+            workspace_bytes = workspace.numel() * workspace.element_size()
+        _check(load().cp_attn_forward_fp8(self.handle, _ptr(q8), _ptr(k8), _ptr(vt8),
+                                          _ptr(scales), _ptr(o), _ptr(lse), _ptr(workspace),
+                                          int(workspace_bytes), _stream(stream)))
+
     def half_ops_size(self) -> int:
         out = ctypes.c_size_t()
         _check(load().cp_attn_half_ops_size(self.handle, ctypes.byref(out)))
@@ -347,6 +365,19 @@ class Plan:
 
     def sync_status(self, stream=None):
         _check(load().cp_attn_sync_status(self.handle, _stream(stream)))
+
+
+def fp8_absmax(x, n, amax, stream=None):
+    """amax (device fp32) = max |x| over n bf16 values of x."""
+    _check(load().cp_attn_fp8_absmax(_ptr(x), int(n), _ptr(amax), _stream(stream)))
+
+
+def fp8_quantize(x, rows, heads, head_dim, amax, out, scale=None, transpose=False, stream=None):
+    """E4M3 codes of x (bf16 [rows][heads][head_dim]) into out, same layout or
+    [heads][head_dim][rows]; scale (device fp32) receives amax / 448."""
+    _check(load().cp_attn_fp8_quantize(_ptr(x), int(rows), int(heads), int(head_dim), _ptr(amax),
+                                       1 if transpose else 0, _ptr(out), _ptr(scale),
+                                       _stream(stream)))
 
 
 def merge_lse(n_parts, rows, heads, head_dim, o_parts, part_stride, lse_parts,

@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libcp_attn.so")
 STAMP = os.path.join(BUILD, "stamp.txt")
 
 SOURCES = ["api.cu", "plan.cpp", "step_fwd.cu", "step_bwd.cu", "hbm_kernels.cu",
-           "noalloc.cu", "decode.cu"]
+           "noalloc.cu", "decode.cu", "fp8.cu"]
 HEADERS = ["internal.h", "kernels.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

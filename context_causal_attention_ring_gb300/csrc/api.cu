@@ -61,6 +61,46 @@ cp_attn_status tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int hea
   return tmap_3d(m, base, rows, heads, d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
+// One-byte elements. rows layout: [rows][heads][d] viewed as (d, heads, rows)
+// with a box of d x 1 x 128; transposed layout: [heads][d][rows] viewed as
+// (rows, d, heads) with a box of 128 x d x 1. Either box lands in shared
+// memory as 128-byte rows with the 128-byte swizzle (d = 128).
+cp_attn_status tmap_u8(CUtensorMap* m, const void* base, int64_t rows, int heads, int d,
+                       bool transposed) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(CP_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  if (!transposed) {
+    dims[0] = static_cast<cuuint64_t>(d);
+    dims[1] = static_cast<cuuint64_t>(heads);
+    dims[2] = static_cast<cuuint64_t>(rows);
+    strides[0] = static_cast<cuuint64_t>(d);
+    strides[1] = static_cast<cuuint64_t>(heads) * d;
+    box[0] = static_cast<cuuint32_t>(d);
+    box[1] = 1;
+    box[2] = 128;
+  } else {
+    dims[0] = static_cast<cuuint64_t>(rows);
+    dims[1] = static_cast<cuuint64_t>(d);
+    dims[2] = static_cast<cuuint64_t>(heads);
+    strides[0] = static_cast<cuuint64_t>(rows);
+    strides[1] = static_cast<cuuint64_t>(rows) * d;
+    box[0] = 128;
+    box[1] = static_cast<cuuint32_t>(d);
+    box[2] = 1;
+  }
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(CP_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed with code " + std::to_string(r));
+  return CP_ATTN_OK;
+}
+
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Offsets of the fp16 copies of q, k, v, dout inside the half-operand buffer.
@@ -317,10 +357,12 @@ namespace {
 // One forward ring step. chained: launch it so that it may overlap the tail of
 // the kernel before it, which must be an earlier step of the same ring.
 // *launched tells whether a kernel went out (a step without work launches none).
+// scales != NULL selects the E4M3 kernel: q, k E4M3 [T][H][128], v then
+// holds V^T E4M3 [Hkv][128][T_kv], scales the device descale factors.
 cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const void* k,
                              const void* v, float* o_part, float* lse_part,
                              cp_attn_merge_mode mode, void* o_final, void* stream, bool chained,
-                             bool* launched) {
+                             bool* launched, const float* scales = nullptr) {
   *launched = false;
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
@@ -332,10 +374,21 @@ cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const vo
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) ||
       (o_final && !aligned16(o_final)))
     return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd: tensors must be 16-byte aligned");
+  const bool fp8 = scales != nullptr;
+  if (fp8 && p->d != 128)
+    return fail(CP_ATTN_ERR_UNSUPPORTED, "step_fwd_fp8: head_dim must be 128");
+  if (fp8 && !aligned16(scales))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd_fp8: scales must be 16-byte aligned");
   CUtensorMap tq, tk, tv;
-  if ((st = tmap_bf16(&tq, q, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
-  if ((st = tmap_bf16(&tk, k, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
-  if ((st = tmap_bf16(&tv, v, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+  if (fp8) {
+    if ((st = tmap_u8(&tq, q, p->T_q, p->Hq, p->d, false)) != CP_ATTN_OK) return st;
+    if ((st = tmap_u8(&tk, k, p->T_kv, p->Hkv, p->d, false)) != CP_ATTN_OK) return st;
+    if ((st = tmap_u8(&tv, v, p->T_kv, p->Hkv, p->d, true)) != CP_ATTN_OK) return st;
+  } else {
+    if ((st = tmap_bf16(&tq, q, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
+    if ((st = tmap_bf16(&tk, k, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+    if ((st = tmap_bf16(&tv, v, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+  }
   FwdParams fp;
   std::memset(&fp, 0, sizeof(fp));
   fp.items = p->d_fwd + p->fwd_off[step];
@@ -357,6 +410,7 @@ cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const vo
   fp.o_part = o_part;
   fp.lse_part = lse_part;
   fp.o_final = mode == CP_ATTN_ACCUMULATE ? static_cast<__nv_bfloat16*>(o_final) : nullptr;
+  fp.scales = scales;
   fp.status = p->d_status;
   fp.wait_limit_ns = kWaitLimitNs;
   // Items without visible tiles still run when every row must be written:
@@ -370,6 +424,9 @@ cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const vo
   const int G = p->Hq / p->Hkv;
   const int64_t units = hpc == 1 ? p->Hq : static_cast<int64_t>(p->Hkv) * ((G + 1) / 2);
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_items) * units));
+  if (fp8)
+    return launch_step_fwd_fp8(grid, step_fwd_fp8_smem_bytes(), static_cast<cudaStream_t>(stream),
+                               tq, tk, tv, fp, chained);
   return launch_step_fwd(p->d, grid, step_fwd_smem_bytes(p->d), static_cast<cudaStream_t>(stream),
                          tq, tk, tv, fp, chained);
 }
@@ -458,6 +515,46 @@ cp_attn_status cp_attn_plan_set_chaining(cp_attn_plan_t p, int enable) {
   if (enable != 0 && enable != 1) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_set_chaining: enable must be 0 or 1");
   p->chain_steps = enable;
   return CP_ATTN_OK;
+}
+
+cp_attn_status cp_attn_step_fwd_fp8(cp_attn_plan_t p, int step, const void* q8, const void* k8,
+                                    const void* vt8, const float* scales, float* o_part,
+                                    float* lse_part, cp_attn_merge_mode mode, void* o_final,
+                                    void* stream) {
+  clear_error();
+  if (!scales) return fail(CP_ATTN_ERR_INVALID_ARG, "step_fwd_fp8: null scales");
+  bool launched = false;
+  return step_fwd_impl(p, step, q8, k8, vt8, o_part, lse_part, mode, o_final, stream,
+                       p && p->chain_steps && step > 0, &launched, scales);
+}
+
+cp_attn_status cp_attn_fp8_absmax(const void* x, int64_t n, float* amax, void* stream) {
+  clear_error();
+  if (!x || !amax) return fail(CP_ATTN_ERR_INVALID_ARG, "fp8_absmax: null pointer");
+  if (n < 0 || n % 8) return fail(CP_ATTN_ERR_SHAPE, "fp8_absmax: n must be a non-negative multiple of 8");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(amax) & 3u))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "fp8_absmax: x must be 16-byte and amax 4-byte aligned");
+  return launch_fp8_absmax(x, n, reinterpret_cast<unsigned int*>(amax),
+                           static_cast<cudaStream_t>(stream));
+}
+
+cp_attn_status cp_attn_fp8_quantize(const void* x, int64_t rows, int heads, int head_dim,
+                                    const float* amax, int transpose, void* out, float* scale,
+                                    void* stream) {
+  clear_error();
+  if (!x || !amax || !out) return fail(CP_ATTN_ERR_INVALID_ARG, "fp8_quantize: null pointer");
+  if (rows < 0 || heads <= 0 || (head_dim != 64 && head_dim != 128))
+    return fail(CP_ATTN_ERR_SHAPE, "fp8_quantize: head_dim must be 64 or 128, heads positive");
+  if (transpose != 0 && transpose != 1)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "fp8_quantize: transpose must be 0 or 1");
+  if (transpose && rows % 64)
+    return fail(CP_ATTN_ERR_SHAPE, "fp8_quantize: transposed output needs rows % 64 == 0");
+  if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(amax) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "fp8_quantize: misaligned pointer");
+  return launch_fp8_quantize(x, rows, heads, head_dim,
+                             reinterpret_cast<const unsigned int*>(amax), transpose, out, scale,
+                             static_cast<cudaStream_t>(stream));
 }
 
 cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* q, const void* k,
@@ -554,6 +651,47 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, c
   }
   // The merge also leaves the fp32 result in slot 0 (each (row, head) is read
   // completely by one warp before that warp writes it).
+  return cp_attn_merge_lse(p->R, p->T_q, p->Hq, p->d, ws, o_slot, ws_lse, l_slot, o, ws, lse,
+                           stream);
+}
+
+cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t p, const void* q8, const void* k8,
+                                   const void* vt8, const float* scales, void* o, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  if (!scales) return fail(CP_ATTN_ERR_INVALID_ARG, "forward_fp8: null scales");
+  size_t need = 0;
+  cp_attn_workspace_size(p, CP_ATTN_OP_FORWARD, &need);
+  if (!workspace || workspace_bytes < need)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "forward_fp8: workspace smaller than cp_attn_workspace_size");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "forward_fp8: workspace must be 256-byte aligned");
+  if (!o || !lse) return fail(CP_ATTN_ERR_INVALID_ARG, "forward_fp8: null output");
+  float* ws = static_cast<float*>(workspace);
+  bool prev = false;
+  if (p->variant == CP_ATTN_PASS_KV) {
+    for (int t = 0; t < p->R; ++t) {
+      bool launched = false;
+      st = step_fwd_impl(p, t, q8, k8, vt8, ws, lse, CP_ATTN_ACCUMULATE,
+                         t == p->R - 1 ? o : nullptr, stream, prev, &launched, scales);
+      if (st != CP_ATTN_OK) return st;
+      prev = prev || launched;
+    }
+    return CP_ATTN_OK;
+  }
+  const int64_t o_slot = p->T_q * p->Hq * p->d;
+  const int64_t l_slot = p->T_q * p->Hq;
+  const size_t o_bytes = (static_cast<size_t>(o_slot) * p->R * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  for (int t = 0; t < p->R; ++t) {
+    bool launched = false;
+    st = step_fwd_impl(p, t, q8, k8, vt8, ws, ws_lse, CP_ATTN_WRITE_PARTIAL, nullptr, stream,
+                       prev, &launched, scales);
+    if (st != CP_ATTN_OK) return st;
+    prev = prev || launched;
+  }
   return cp_attn_merge_lse(p->R, p->T_q, p->Hq, p->d, ws, o_slot, ws_lse, l_slot, o, ws, lse,
                            stream);
 }

@@ -28,6 +28,7 @@ struct FwdParams {
   float* o_part;
   float* lse_part;
   __nv_bfloat16* o_final;     // optional
+  const float* scales;        // E4M3 kernel: device [3] descale factors of q, k, v
   int32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -60,6 +61,24 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, const FwdParams& p, bool chained);
 size_t step_fwd_smem_bytes(int d);
+
+// E4M3 forward step (head_dim 128): q, k E4M3 [tokens][heads][128] maps
+// (128-byte boxes), tvt the V^T map E4M3 [heads][128][tokens]; p.scales set.
+cp_attn_status launch_step_fwd_fp8(dim3 grid, size_t smem, cudaStream_t s,
+                                   const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tvt, const FwdParams& p, bool chained);
+size_t step_fwd_fp8_smem_bytes();
+
+// Per-tensor E4M3 quantization (fp8.cu). absmax: *amax_bits = bits of
+// max |x| over n bf16 values (n a multiple of 8; zeroed first on the stream).
+cp_attn_status launch_fp8_absmax(const void* x, int64_t n, unsigned int* amax_bits,
+                                 cudaStream_t s);
+// quantize: x bf16 [rows][heads][d] -> E4M3 in the same layout, or (transpose)
+// [heads][d][rows] with rows a multiple of 64; *scale (if not NULL) gets the
+// descale factor amax / 448.
+cp_attn_status launch_fp8_quantize(const void* x, int64_t rows, int heads, int d,
+                                   const unsigned int* amax_bits, int transpose, void* out,
+                                   float* scale, cudaStream_t s);
 // Query heads one forward CTA handles (d = 128 pairs the heads of a group).
 int step_fwd_heads_per_cta(int d);
 

@@ -402,42 +402,66 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kThreadsP = 352;
 constexpr int kKStagesP = 3;
 constexpr int kVStagesP = 2;
+// E4M3 tiles are half the size: deeper rings in about two thirds of the space
+constexpr int kKStagesF8 = 4;
+constexpr int kVStagesF8 = 3;
+constexpr int kKStagesMax = 4;
+constexpr int kVStagesMax = 3;
 
 enum : int {
   PB_Q = 0,
-  PB_K = 1,                      // [kKStagesP] K tile landed
-  PB_V = PB_K + kKStagesP,       // [kVStagesP] V tile landed
-  PB_KE = PB_V + kVStagesP,      // [kKStagesP] K stage free
-  PB_VE = PB_KE + kKStagesP,     // [kVStagesP] V stage free
-  PB_S = PB_VE + kVStagesP,      // [2] S of head slot ready
+  PB_K = 1,                      // [kKStagesMax] K tile landed
+  PB_V = PB_K + kKStagesMax,     // [kVStagesMax] V tile landed
+  PB_KE = PB_V + kVStagesMax,    // [kKStagesMax] K stage free
+  PB_VE = PB_KE + kKStagesMax,   // [kVStagesMax] V stage free
+  PB_S = PB_VE + kVStagesMax,    // [2] S of head slot ready
   PB_P = PB_S + 2,               // [2] P of head slot written (128 arrivals)
   PB_O = PB_P + 2,               // [2] final O of head slot ready
   PB_DRAIN = PB_O + 2,
   PB_COUNT = PB_DRAIN + 1
 };
 
-struct FwdPairSmem {
-  static constexpr int kTile = 128 * 128 * 2;
+// F8: E4M3 operands (one byte per element), else bf16.
+template <bool F8>
+struct FwdPairSmemT {
+  static constexpr int kKS = F8 ? kKStagesF8 : kKStagesP;
+  static constexpr int kVS = F8 ? kVStagesF8 : kVStagesP;
+  static constexpr int kTile = 128 * 128 * (F8 ? 1 : 2);
   static constexpr int kQ = 0;                          // [2 heads]
-  static constexpr int kK = kQ + 2 * kTile;             // [kKStagesP]
-  static constexpr int kV = kK + kKStagesP * kTile;     // [kVStagesP]
-  static constexpr int kBar = kV + kVStagesP * kTile;
+  static constexpr int kK = kQ + 2 * kTile;             // [kKS]
+  static constexpr int kV = kK + kKS * kTile;           // [kVS]
+  static constexpr int kBar = kV + kVS * kTile;
   static constexpr int kMisc = kBar + PB_COUNT * 8;
   static constexpr int kBytes = kMisc + 16;
   // The dynamic shared-memory window starts 1 KB-aligned (checked by the
   // kernel), so no alignment slack is reserved.
   static constexpr int kAlloc = kBytes;
+  // The epilogue stages each head's output rows through 32 KB starting at
+  // kQ + 32 KB * head: Q and K space, which only the S MMAs read, and those
+  // have all completed when a head's last O MMA has.
+  static_assert(2 * 32768 <= kV, "epilogue staging must not reach the V ring");
+  static_assert(kAlloc > 232448 / 2, "one CTA per SM (each takes all of TMEM)");
 };
+using FwdPairSmem = FwdPairSmemT<false>;
 static_assert(FwdPairSmem::kAlloc <= 232448, "pair kernel shared memory");
+static_assert(FwdPairSmemT<true>::kAlloc <= 232448, "pair kernel shared memory");
 
+// F8: Q and K are E4M3 [tokens][heads][d] and tm_v maps V^T, E4M3
+// [heads][d][tokens] (keys contiguous, the K-major B operand of O = P V); the
+// MMAs are kind::f8f6f4 with K = 32, P goes to TMEM as E4M3 (scaled by 2^8 so
+// that probabilities down to 2^-14 stay normal), the running maximum moves
+// whenever it grows (so P * 2^8 <= 256 < 448), and the per-tensor descale
+// factors p.scales[0..2] (q, k, v) multiply the scores and the output.
+template <bool F8>
 __global__ void __launch_bounds__(kThreadsP, 1)
     step_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = FwdPairSmem;
+  using L = FwdPairSmemT<F8>;
   constexpr int D = 128;
-  constexpr int KS = kKStagesP;
-  constexpr int VS = kVStagesP;
+  constexpr int KS = L::kKS;
+  constexpr int VS = L::kVS;
+  constexpr int kBoxes = F8 ? 1 : 2;  // 128-byte-wide TMA boxes per 128-row tile
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
   if (sbase & 1023u) {
@@ -505,7 +529,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       ptx::prefetch_tmap(&tm_q);
       ptx::mbar_arrive_expect_tx(bar(PB_Q), nh * L::kTile);
       for (int hs = 0; hs < nh; ++hs)
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < kBoxes; ++b)
           ptx::tma_load_3d(sQ + hs * L::kTile + b * 16384, &tm_q, bar(PB_Q), b * 64, hA + hs,
                            static_cast<int>(q_row0));
     }
@@ -520,8 +544,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       const int row = static_cast<int>(kv_row_base + static_cast<int64_t>(w.lo + j) * 128);
       ptx::mbar_arrive_expect_tx(bar(full_bar + s), L::kTile);
-      for (int b = 0; b < 2; ++b)
-        ptx::tma_load_3d(ring + s * L::kTile + b * 16384, tm, bar(full_bar + s), b * 64, kh, row);
+      if (F8 && !is_k) {
+        // V^T box: 128 keys (bytes) x 128 d rows of head kh
+        ptx::tma_load_3d(ring + s * L::kTile, tm, bar(full_bar + s), row, 0, kh);
+      } else {
+        for (int b = 0; b < kBoxes; ++b)
+          ptx::tma_load_3d(ring + s * L::kTile + b * 16384, tm, bar(full_bar + s), b * 64, kh, row);
+      }
       issued = j + 1;
     }
     // every issued copy must land before the CTA may exit
@@ -534,8 +563,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // The whole warp runs the loop so that descriptors stay warp-uniform;
     // one elected lane issues each tcgen05 instruction.
     const uint32_t leader = ptx::elect_one();
-    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
-    constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
+    // kind::f8f6f4 format code 0 is E4M3; kind::f16 code 1 is bf16
+    constexpr uint32_t idesc_s = F8 ? ptx::idesc_f16kind(128, 128, 0, 0, 0u)
+                                    : ptx::idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idesc_o = F8 ? ptx::idesc_f16kind(128, D, 0, 0, 0u)
+                                    : ptx::idesc_bf16(128, D, 0, 1);
     const uint64_t dQ0 = ptx::sdesc_sw128(sQ, 16, 1024);
     auto wait_set = [&](const auto& bars, const auto& par, int where) -> bool {
       return ptx::wait_phases(bars, par, s_abort, p.wait_limit_ns, p.status, where);
@@ -544,23 +576,42 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       // S = Q K^T: both K-major, two 64-column blocks of 16 KB each
       const uint64_t dk = ptx::sdesc_sw128(sK + (j % KS) * L::kTile, 16, 1024);
       const uint64_t dq = ptx::sdesc_add(dQ0, hs * L::kTile);
+      if constexpr (F8) {
+        // d = 128 bytes: one swizzle atom, K = 32 elements (32 bytes) per MMA
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_ss_w(tmem + 128 * hs, ptx::sdesc_add(dq, off), ptx::sdesc_add(dk, off), idesc_s,
-                      kk > 0 ? 1u : 0u, leader);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_ss_f8_w(tmem + 128 * hs, ptx::sdesc_add(dq, kk * 32),
+                           ptx::sdesc_add(dk, kk * 32), idesc_s, kk > 0 ? 1u : 0u, leader);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::mma_ss_w(tmem + 128 * hs, ptx::sdesc_add(dq, off), ptx::sdesc_add(dk, off), idesc_s,
+                        kk > 0 ? 1u : 0u, leader);
+        }
       }
       ptx::mma_commit_w(bar(PB_S + hs), leader);
     };
     auto issue_o = [&](int j, int hs) {
-      // B = V [keys][d] MN-major: 8-key groups at 1 KB, d 64..127 at +16 KB
-      const uint64_t dv = ptx::sdesc_sw128(sV + (j % VS) * L::kTile, 16384, 1024);
+      if constexpr (F8) {
+        // B = V^T [d][keys] K-major (one swizzle atom); A = P, four E4M3 per
+        // column in the head's S columns: 32 keys = 8 columns per MMA
+        const uint64_t dv = ptx::sdesc_sw128(sV + (j % VS) * L::kTile, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        // A = P (bf16 pairs in the head's S columns), 16 keys = 8 columns
-        ptx::mma_ts_w(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
-                      ptx::sdesc_add(dv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
-                      leader);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_ts_f8_w(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
+                           ptx::sdesc_add(dv, kk * 32), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
+                           leader);
+      } else {
+        // B = V [keys][d] MN-major: 8-key groups at 1 KB, d 64..127 at +16 KB
+        const uint64_t dv = ptx::sdesc_sw128(sV + (j % VS) * L::kTile, 16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // A = P (bf16 pairs in the head's S columns), 16 keys = 8 columns
+          ptx::mma_ts_w(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
+                        ptx::sdesc_add(dv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
+                        leader);
+        }
       }
     };
     bool ok;
@@ -623,6 +674,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    // E4M3 scores carry the q and k descale factors
+    const float scale_log2 = F8 ? p.scale_log2 * (__ldg(p.scales) * __ldg(p.scales + 1))
+                                : p.scale_log2;
+    constexpr float kThreshold = F8 ? 0.f : kRescaleThreshold;
+    constexpr float kPExp = F8 ? 8.f : 0.f;  // P is stored as 2^kPExp * p
     int32_t kpos_next = n_tiles > 0 ? __ldg(kv_tile_pos + w.lo) : 0;
     // The epilogue reads this row's fp32 running output back (merge): ask L2
     // for it a few tiles before the end so those reads do not wait on HBM.
@@ -667,34 +723,55 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                                : fmaxf(mk[x], s[c + 2 * x + 1]);
       }
       const float mx = fmaxf(ptx::max3(mk[0], mk[1], mk[2]), ptx::max3(mk[3], mk[4], mk[5]));
-      const float m_tile = ptx::max3(mx, mk[6], mk[7]) * p.scale_log2;
+      const float m_tile = ptx::max3(mx, mk[6], mk[7]) * scale_log2;
       float alpha = 1.f;
-      if (m_tile > m_used + kRescaleThreshold) {
+      if (m_tile > m_used + kThreshold) {
         alpha = ptx::ex2(m_used - m_tile);
         l *= alpha;
         m_used = m_tile;
       }
       const float base = (m_used == -INFINITY) ? 0.f : m_used;
-      // P = 2^(s * scale_log2 - base), two columns per instruction, packed
-      // to bf16 pairs and stored into this head's S columns [0, 64) chunk by
-      // chunk
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-      const float2 nb2 = make_float2(-base, -base);
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 nb2 = make_float2(kPExp - base, kPExp - base);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
+      if constexpr (F8) {
+        // four keys per column: 64 keys = 16 columns per chunk
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int i = c * 16 + x;
-          float2 e = ptx::fma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nb2);
-          e.x = ptx::ex2(e.x);
-          e.y = ptx::ex2(e.y);
-          acc[x & 3] = ptx::add2(acc[x & 3], e);
-          pk[x] = ptx::pack_bf16(e.x, e.y);
+          for (int x = 0; x < 16; ++x) {
+            const int i = c * 64 + 4 * x;
+            float2 e0 = ptx::fma2(make_float2(s[i], s[i + 1]), sc2, nb2);
+            float2 e1 = ptx::fma2(make_float2(s[i + 2], s[i + 3]), sc2, nb2);
+            e0.x = ptx::ex2(e0.x);
+            e0.y = ptx::ex2(e0.y);
+            e1.x = ptx::ex2(e1.x);
+            e1.y = ptx::ex2(e1.y);
+            acc[x & 3] = ptx::add2(acc[x & 3], ptx::add2(e0, e1));
+            pk[x] = ptx::pack_e4m3x4(e0.x, e0.y, e1.x, e1.y);
+          }
+          ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
         }
-        ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
+      } else {
+        // P = 2^(s * scale_log2 - base), two columns per instruction, packed
+        // to bf16 pairs and stored into this head's S columns [0, 64) chunk
+        // by chunk
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const int i = c * 16 + x;
+            float2 e = ptx::fma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, nb2);
+            e.x = ptx::ex2(e.x);
+            e.y = ptx::ex2(e.y);
+            acc[x & 3] = ptx::add2(acc[x & 3], e);
+            pk[x] = ptx::pack_bf16(e.x, e.y);
+          }
+          ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
+        }
       }
       const float2 acc01 = ptx::add2(acc[0], acc[1]);
       const float2 acc23 = ptx::add2(acc[2], acc[3]);
@@ -727,8 +804,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       ptx::grid_dep_wait();
       ptx::tc_fence_after();
       const int64_t g = q_row0 + r;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const float lse_t = l > 0.f ? (m_used + ptx::lg2(l)) * kLn2 : -INFINITY;
+      // l and O carry the 2^kPExp of P; E4M3 V carries its descale factor
+      const float inv_l = l > 0.f ? (F8 ? __ldg(p.scales + 2) : 1.f) / l : 0.f;
+      const float lse_t = l > 0.f ? (m_used + ptx::lg2(l) - kPExp) * kLn2 : -INFINITY;
       const int64_t lse_off = static_cast<int64_t>(h) * p.T_q + g;
       float w_old = 0.f, w_new = 1.f, lse_out = lse_t;
       const bool merge = (p.mode == CP_ATTN_ACCUMULATE) && !p.first;
@@ -764,7 +842,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         // writes 4 rows per instruction, 128 contiguous bytes per row.
         // Staging uses this head's Q tile, free once its S MMAs are done.
         ptx::fence_proxy_async_smem();
-        uint8_t* stage = smem + L::kQ + hs * L::kTile + (warp & 3) * 8192;
+        uint8_t* stage = smem + L::kQ + hs * 32768 + (warp & 3) * 8192;
         const int sub = lane >> 3;  // row within a group of four
         const int q4 = lane & 7;    // 16-byte unit within the chunk
         const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
@@ -855,7 +933,7 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
   cudaError_t err;
   if (d == 128) {
     if (!attr_done[1]) {
-      err = cudaFuncSetAttribute(step_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      err = cudaFuncSetAttribute(step_fwd_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
       if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd attr: ") + cudaGetErrorString(err));
       attr_done[1] = true;
@@ -870,7 +948,7 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = chained ? 1 : 0;
-    err = cudaLaunchKernelEx(&cfg, step_fwd_pair_kernel, tq, tk, tv, p);
+    err = cudaLaunchKernelEx(&cfg, step_fwd_pair_kernel<false>, tq, tk, tv, p);
     if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd launch: ") + cudaGetErrorString(err));
   } else {
     if (!attr_done[0]) {
@@ -883,6 +961,35 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
   }
   err = cudaGetLastError();
   if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd launch: ") + cudaGetErrorString(err));
+  count_launch();
+  return CP_ATTN_OK;
+}
+
+size_t step_fwd_fp8_smem_bytes() { return FwdPairSmemT<true>::kAlloc; }
+
+cp_attn_status launch_step_fwd_fp8(dim3 grid, size_t smem, cudaStream_t s,
+                                   const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tvt, const FwdParams& p, bool chained) {
+  static bool attr_done = false;
+  cudaError_t err;
+  if (!attr_done) {
+    err = cudaFuncSetAttribute(step_fwd_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd_fp8 attr: ") + cudaGetErrorString(err));
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreadsP);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = chained ? 1 : 0;
+  err = cudaLaunchKernelEx(&cfg, step_fwd_pair_kernel<true>, tq, tk, tvt, p);
+  if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd_fp8 launch: ") + cudaGetErrorString(err));
   count_launch();
   return CP_ATTN_OK;
 }

@@ -237,6 +237,49 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
  * enable outside {0, 1}. */
 cp_attn_status cp_attn_plan_set_chaining(cp_attn_plan_t plan, int enable);
 
+/* ---------------------------------------------------------------- FP8
+ * The pages' benchmark model (Llama 3 405B) is quantized to FP8 throughout
+ * ("Experimental Setup & Results", Model and Quantization). The format is
+ * E4M3 (OCP 8-bit floating point: bias 7, three mantissa bits, largest
+ * finite 448, no infinities) with one scale per tensor: with amax = max|x|,
+ * x is stored as RN-even(fp32(x) * fp32(448/amax)) clamped to +-448 and
+ * stands for code * fp32(amax/448) (scale 1 for an all-zero tensor). The
+ * attention computed is the same as the bf16 path's, on those values.
+ *
+ * cp_attn_fp8_absmax: *amax (device fp32) = max |x| over n bf16 values
+ *   (device, 16-byte aligned, n a multiple of 8). Overwrites *amax; NaNs
+ *   are ignored.
+ * cp_attn_fp8_quantize: x bf16 [rows][heads][head_dim] (device) -> out E4M3
+ *   (device, 16-byte aligned), in the same layout (transpose = 0) or as
+ *   [heads][head_dim][rows] (transpose = 1, rows % 64 == 0: the V^T layout
+ *   the FP8 step reads), using the *amax of a preceding cp_attn_fp8_absmax;
+ *   *scale (device, may be NULL) receives the descale factor amax/448.
+ *   head_dim 64 or 128. ERR_SHAPE / ERR_INVALID_ARG on bad sizes, pointers
+ *   or alignment.
+ * cp_attn_step_fwd_fp8: cp_attn_step_fwd with E4M3 inputs, head_dim 128:
+ *   q8 [T_q][Hq][128], k8 [T_kv][Hkv][128], vt8 the V^T layout
+ *   [Hkv][128][T_kv], all in the plan's rank-major token order (apply
+ *   cp_attn_layout_apply to the bf16 tensors before quantizing); scales a
+ *   device array of three floats, the descale factors of q, k and v
+ *   (16-byte aligned). P is rounded to E4M3 (after scaling by 2^8) for the
+ *   P V product; the row sums, the LSE and all accumulation stay fp32.
+ *   Outputs, modes and errors as cp_attn_step_fwd; ERR_UNSUPPORTED for
+ *   head_dim != 128.
+ * cp_attn_forward_fp8: cp_attn_forward over those inputs (same workspace).
+ *   The plan's chaining flag (cp_attn_plan_set_chaining) applies to
+ *   cp_attn_step_fwd_fp8 as to cp_attn_step_fwd. */
+cp_attn_status cp_attn_fp8_absmax(const void* x, int64_t n, float* amax, void* stream);
+cp_attn_status cp_attn_fp8_quantize(const void* x, int64_t rows, int heads, int head_dim,
+                                    const float* amax, int transpose, void* out, float* scale,
+                                    void* stream);
+cp_attn_status cp_attn_step_fwd_fp8(cp_attn_plan_t plan, int step, const void* q8,
+                                    const void* k8, const void* vt8, const float* scales,
+                                    float* o_part, float* lse_part, cp_attn_merge_mode mode,
+                                    void* o_final, void* stream);
+cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t plan, const void* q8, const void* k8,
+                                   const void* vt8, const float* scales, void* o, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of the fp16 operand copies used by the backward step: exact IEEE
  * fp16 copies of q, k, v and dout, in that order, each starting on a
  * 256-byte boundary. The backward MMAs run on fp16 operands so that the

@@ -26,7 +26,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_per_tensor", "dequantize"]
+__all__ = ["E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_per_tensor", "dequantize",
+           "pv_rounding_bound"]
 
 E4M3_MAX = 448.0
 _BIAS = 7
@@ -75,12 +76,15 @@ def e4m3_encode(x) -> np.ndarray:
     return code.astype(np.uint8)
 
 
-def quantize_per_tensor(x):
+def quantize_per_tensor(x, amax=None):
     """(codes, scale, inv): per-tensor E4M3 quantization of the values x
     (exact in fp32, e.g. bf16 inputs). scale = fp32(amax / 448) is the
-    dequantization factor, inv = fp32(448 / amax) the quantization one."""
+    dequantization factor, inv = fp32(448 / amax) the quantization one.
+    ``amax`` gives max |x| of the whole tensor when x is only part of it."""
     x = np.asarray(x, dtype=np.float64)
-    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    if amax is None:
+        amax = np.max(np.abs(x)) if x.size else 0.0
+    amax = np.float32(amax)
     if amax == 0:
         inv = np.float32(1.0)
         scale = np.float32(1.0)
@@ -94,3 +98,58 @@ def quantize_per_tensor(x):
 def dequantize(codes, scale) -> np.ndarray:
     """The value each code stands for: code * scale, in fp64."""
     return e4m3_decode(codes) * np.float64(scale)
+
+
+def pv_rounding_bound(q, k, v, qpos, kpos, cu_seqlens=None, scale=None, *, window: int = 0,
+                      p_exp: int = 8, row_block: int = 256):
+    """Largest change of each output element O[n, Hq, d] that E4M3 rounding
+    of the probabilities can cause when the P V product takes them in E4M3.
+
+    The FP8 step keeps the row sums in fp32 and rounds each numerator
+    P_k = 2^p_exp * 2^(s_k - m) (s in log2 units, m <= the row maximum M the
+    kernel holds when it meets key k) to E4M3 before P V. A normal P_k
+    (>= 2^-6) moves by at most 2^-4 P_k, which after normalisation is
+    2^-4 p_k (p the softmax probability); a subnormal one by at most half
+    the subnormal spacing, 2^-10, which after normalisation is at most
+    2^-10 / (2^p_exp L) with L = sum_k 2^(s_k - M). A key can be subnormal
+    only if 2^(s_k - M) < 2^(-6 - p_exp), and for such a key 2^-4 p_k is
+    below 2^(-10 - p_exp) / L as well. So, per element,
+      bound = 2^-4 sum_{k normal} p_k |v_k| + 2^(-10 - p_exp) / L * sum_{k sub} |v_k|
+    where "sub" are the keys with 2^(s_k - M) < 2^(-6 - p_exp). The worst
+    admissible rounding reaches it when the kernel's maximum is M throughout.
+    Rows without visible keys get 0.
+    """
+    from .ring_attention import _as_f64, _per_head, _vis, doc_index
+    q = _as_f64(q)
+    n, Hq, d = q.shape
+    m, Hkv, _ = np.shape(k)
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kh_ = _per_head(k)
+    vh_ = [np.abs(x) for x in _per_head(v)]
+    qpos = np.asarray(qpos, dtype=np.int64)
+    kpos = np.asarray(kpos, dtype=np.int64)
+    qdoc = doc_index(qpos, cu_seqlens)
+    kdoc = doc_index(kpos, cu_seqlens)
+    B = np.zeros((n, Hq, d))
+    rel = 2.0 ** -4
+    sub_abs = 2.0 ** (-10 - p_exp)
+    sub_below = 2.0 ** (-6 - p_exp)
+    for r0 in range(0, n, row_block):
+        r1 = min(n, r0 + row_block)
+        vis = _vis(qpos[r0:r1], qdoc[r0:r1], kpos, kdoc, window)
+        has = vis.any(axis=1)
+        for h in range(Hq):
+            kh = h // G
+            s = scale * (q[r0:r1, h, :] @ kh_[kh].T)
+            s = np.where(vis, s, -np.inf)
+            mx = np.where(has, s.max(axis=1), 0.0)
+            e = np.exp(s - mx[:, None])                 # 2^(s - M) in log2 terms
+            L = np.where(has, e.sum(axis=1), 1.0)
+            p = e / L[:, None]
+            sub = (e < sub_below) & vis
+            b = rel * (np.where(sub, 0.0, p) @ vh_[kh]) + \
+                (sub_abs / L)[:, None] * (sub.astype(np.float64) @ vh_[kh])
+            B[r0:r1, h, :] = np.where(has[:, None], b, 0.0)
+    return B

@@ -125,3 +125,41 @@ def test_planted_encoder_mistake_is_caught(old, new, monkeypatch):
         except (AssertionError, ValueError, OverflowError):
             caught += 1
     assert caught > 0
+
+
+def _worst_case_change(q, k, v, scale, p_exp=8):
+    """Output change when every numerator 2^p_exp * 2^(s - M) of a causal
+    row moves by the largest E4M3 rounding error, in the direction of its
+    value's sign, column by column (one head, all keys visible up to the
+    row). Written out directly: normal numerators by 2^-4 of themselves,
+    subnormal ones by 2^-10."""
+    n, d = q.shape
+    s = scale * (q @ k.T)
+    s = np.where(np.tril(np.ones((n, n), dtype=bool)), s, -np.inf)
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    P = 2.0 ** p_exp * e
+    L = e.sum(axis=1)
+    out = np.zeros((n, d))
+    for j in range(d):
+        sg = np.sign(v[:, j])[None, :]
+        Pt = np.where(P < 2.0 ** -6, P + 2.0 ** -10 * sg, P * (1 + 2.0 ** -4 * sg))
+        Pt = np.where(e > 0, Pt, 0.0)
+        out[:, j] = np.abs((Pt - P) @ v[:, j]) / (2.0 ** p_exp * L)
+    return out
+
+
+@pytest.mark.parametrize("spread", [0.3, 9.0])
+def test_pv_rounding_bound_is_reached_by_the_worst_rounding(spread):
+    """The bound equals the change caused by the worst admissible rounding
+    (every numerator moved by its largest error towards its value's sign):
+    with close scores (all numerators normal) and with spread-out ones (many
+    subnormal)."""
+    rng = np.random.default_rng(11)
+    n, d = 48, 8
+    q = rng.standard_normal((n, 1, d)) * spread
+    k = rng.standard_normal((n, 1, d))
+    v = rng.standard_normal((n, 1, d))
+    pos = np.arange(n)
+    B = f8.pv_rounding_bound(q, k, v, pos, pos, scale=1.0 / np.sqrt(d))[:, 0, :]
+    W = _worst_case_change(q[:, 0], k[:, 0], v[:, 0], 1.0 / np.sqrt(d))
+    np.testing.assert_allclose(B, W, rtol=1e-9, atol=1e-15)
