@@ -38,9 +38,9 @@ METRIC = "causal attn TFLOPS fwd/bwd (unmasked FLOPs) and % of GB300 dense BF16 
 # only while the kernel source is the one that was profiled.
 PROFILED_TRAFFIC = {
     "step_bwd": ("context_causal_attention_ring_gb300/csrc/step_bwd.cu",
-                 "22ed59fda2fd3373194af78d5665db1864e5145353b020c033f97cdd07cbd383", 3.094209e9),
+                 "bb08c296ea737c1e0859b8dc93e1670e4c445e2eacc8f2e67a1ec2c7300cc727", 3.100231e9),
     "step_fwd": ("context_causal_attention_ring_gb300/csrc/step_fwd.cu",
-                 "35a5e784cbe8ba5fe94de81997be1ed9d3c60e89e1ac1b3b0159662189ad572f", 1.293699e9),
+                 "9f265fea77a8e823b62a3ac07383f5921ac0a1824df8c31409ef5ab60ea3c0b9", 1.295524e9),
 }
 
 
@@ -544,13 +544,13 @@ def run_fp8_bench(args):
 
     torch.cuda.set_device(0)
     peaks, peak_kind = _peaks()
-    w = WORKLOADS["prefill_405b_full"]
+    w = WORKLOADS[args.fp8_workload]
     inp = make_inputs(w, with_dout=False)
     dev = torch.device("cuda:0")
     rows = []
     for variant in ("pass_kv", "pass_q"):
         plan = cpa.Plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim,
-                        layout=w.layout, variant=variant)
+                        layout=w.layout, variant=variant, kv_prefix_len=w.kv_prefix_len)
         R, Hq, Hkv, d = plan.R, plan.Hq, plan.Hkv, plan.d
         flops = 4.0 * d * Hq * plan.visible_pairs()
         bf = {}
@@ -605,7 +605,9 @@ def run_fp8_bench(args):
         del bf, q8, k8, vt8, o, lse, ws
         torch.cuda.empty_cache()
     print(json.dumps({"metric": "fp8 vs bf16 forward TFLOPS (unmasked FLOPs)",
-                      "workload": "prefill_405b_full: 131072 tokens, 128/8 heads, d=128, CP=8 zigzag",
+                      "workload": f"{w.name}: {w.seq_len} new tokens after {w.kv_prefix_len} cached, "
+                                  f"{w.n_q_heads}/{w.n_kv_heads} heads, d={w.head_dim}, "
+                                  f"CP={w.cp} {w.layout}",
                       "fp8_peak_tflops": 2 * peaks["bf16_tflops"],
                       "bf16_peak_tflops": peaks["bf16_tflops"],
                       "peak_kind": f"bf16_tflops burst ({peak_kind}); fp8 = 2 x bf16 (nominal ratio)",
@@ -731,6 +733,8 @@ def main():
                     help="time the layer as zigzag ring, USP and pure Ulysses arrangements")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) forward against bf16 on the 405B-shaped prefill")
+    ap.add_argument("--fp8-workload", default="prefill_405b_full", choices=sorted(WORKLOADS),
+                    help="workload of --fp8")
     ap.add_argument("--decode", action="store_true",
                     help="time the one-row decode against the HBM roofline")
     args = ap.parse_args()
