@@ -160,7 +160,7 @@ def run_reference(args, w):
     if rank != 0:
         return
     heads = int(os.environ.get("CP_BENCH_CPU_HEADS", "4"))
-    inp = make_inputs(w)
+    inp = make_inputs(w, with_dout=True)  # the step times forward and backward
     cpu_oracle_sample(w, 1, inp)  # warm-up (page-in, BLAS threads)
     vals, times = [], []
     desc = ""
@@ -200,7 +200,7 @@ def run_ours(args, w):
 
     plan = cpa.Plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim,
                     layout=w.layout, variant="pass_kv", kv_prefix_len=w.kv_prefix_len)
-    inp = make_inputs(w)
+    inp = make_inputs(w, with_dout=True)  # the step times forward and backward
 
     def dev_bf16(bits):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -276,6 +276,10 @@ def run_ours(args, w):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
+    q_mib = plan.T_q * Hq * d * 2 / 2**20
+    l2_note = (f"inputs larger than L2 (Q {q_mib:.0f} MiB, dO {q_mib:.0f} MiB)"
+               if 2 * q_mib > 129 else
+               f"inputs fit in L2 (Q {q_mib:.1f} MiB): a launch-bound small case, warm L2")
     value = ws * (fwd_flops + bwd_flops) / (ms_per_step * 1e-3) / 1e12
     fwd_tflops = fwd_flops / (statistics.median(fwd_ms) * 1e-3) / 1e12
     bwd_tflops = bwd_flops / (statistics.median(bwd_ms) * 1e-3) / 1e12
@@ -314,7 +318,7 @@ def run_ours(args, w):
             "config": {"workload": w.name, "seq_len": w.seq_len, "cp": w.cp,
                        "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d,
                        "layout": w.layout, "variant": "pass_kv", "parallelism": f"replicas{ws}",
-                       "l2": "inputs larger than L2 (Q 256 MiB, dO 256 MiB)",
+                       "l2": l2_note,
                        "flops_per_step": fwd_flops + bwd_flops},
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
             "fwd_ms": statistics.median(fwd_ms), "bwd_ms": statistics.median(bwd_ms),
@@ -398,7 +402,7 @@ def run_usp_sweep(args):
     torch.cuda.set_device(0)
     w = WORKLOADS["llama3_8b_layer"]
     N, Hq, Hkv, d, D = w.seq_len, w.n_q_heads, w.n_kv_heads, w.head_dim, w.cp
-    inp = make_inputs(w)
+    inp = make_inputs(w, with_dout=True)  # the step times forward and backward
     dev_bf16 = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
     qn, kn, vn, don = (dev_bf16(x) for x in (inp.q, inp.k, inp.v, inp.dout))
     del inp

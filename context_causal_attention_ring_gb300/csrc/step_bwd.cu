@@ -173,19 +173,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_wait(bar(BAR_KV), 0, &never, p.wait_limit_ns);
     for (int it = issued > NS ? issued - NS : 0; it < issued; ++it)
       ptx::mbar_wait(bar(BAR_QF + it % NS), (it / NS) & 1, &never, p.wait_limit_ns);
-  } else if (n_iter > 0 && warp == 5 && lane == 0) {
+  } else if (n_iter > 0 && warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop; one elected lane issues each tcgen05
+    // instruction, and every wait's outcome is agreed across the warp.
+    const uint32_t leader = ptx::elect_one();
+    auto wait_w = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+      const bool w_ok = ptx::mbar_wait(b_, parity, s_abort, p.wait_limit_ns);
+      if (!w_ok && leader) ptx::record_timeout(p.status, s_abort, where);
+      return __all_sync(0xffffffffu, w_ok);
+    };
     constexpr uint32_t idesc_s = ptx::idesc_fp16(128, 128, 0, 0);  // K-major A and B
     constexpr uint32_t idesc_kb = ptx::idesc_fp16(128, D, 0, 1);   // A K-major, B MN-major
     constexpr uint32_t idesc_q = ptx::idesc_fp16(128, D, 1, 1);    // A and B MN-major
-    bool ok = ptx::mbar_wait(bar(BAR_KV), 0, s_abort, p.wait_limit_ns);
-    if (!ok) ptx::record_timeout(p.status, s_abort, 0x1200);
+    bool ok = wait_w(bar(BAR_KV), 0, 0x1200);
     for (int it = 0; ok && it < n_iter; ++it) {
       const int s = it % NS;
       const uint32_t q_tile = sQ + s * L::kTileBytes;
       const uint32_t do_tile = sDO + s * L::kTileBytes;
-      if (!ptx::mbar_wait(bar(BAR_QF + s), (it / NS) & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x1300 + it);
+      if (!wait_w(bar(BAR_QF + s), (it / NS) & 1, 0x1300 + it)) {
         ok = false;
         break;
       }
@@ -194,13 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_ss(tS, ptx::sdesc_sw128(sK + off, 16, 1024),
-                         ptx::sdesc_sw128(q_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_ss_w(tS, ptx::sdesc_sw128(sK + off, 16, 1024),
+                         ptx::sdesc_sw128(q_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u, leader);
       }
-      ptx::mma_commit(bar(BAR_S));
+      ptx::mma_commit_w(bar(BAR_S), leader);
       if (it > 0) {
-        if (!ptx::mbar_wait(bar(BAR_DQFREE), (it - 1) & 1, s_abort, p.wait_limit_ns)) {
-          ptx::record_timeout(p.status, s_abort, 0x1400 + it);
+        if (!wait_w(bar(BAR_DQFREE), (it - 1) & 1, 0x1400 + it)) {
           ok = false;
           break;
         }
@@ -210,12 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_ss(tDP, ptx::sdesc_sw128(sV + off, 16, 1024),
-                         ptx::sdesc_sw128(do_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_ss_w(tDP, ptx::sdesc_sw128(sV + off, 16, 1024),
+                         ptx::sdesc_sw128(do_tile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u, leader);
       }
-      ptx::mma_commit(bar(BAR_DP));
-      if (!ptx::mbar_wait(bar(BAR_P), it & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x1500 + it);
+      ptx::mma_commit_w(bar(BAR_DP), leader);
+      if (!wait_w(bar(BAR_P), it & 1, 0x1500 + it)) {
         ok = false;
         break;
       }
@@ -227,23 +231,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
         const uint32_t boff = kk * 2048;
         const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-        ptx::mma_ss(tDV, ptx::sdesc_sw128(sPt + aoff, 16, 1024),
-                         ptx::sdesc_sw128(do_tile + boff, 16384, 1024), idesc_kb, acc);
-        ptx::mma_ss(tDK, ptx::sdesc_sw128(sDSt + aoff, 16, 1024),
-                         ptx::sdesc_sw128(q_tile + boff, 16384, 1024), idesc_kb, acc);
+        ptx::mma_ss_w(tDV, ptx::sdesc_sw128(sPt + aoff, 16, 1024),
+                         ptx::sdesc_sw128(do_tile + boff, 16384, 1024), idesc_kb, acc, leader);
+        ptx::mma_ss_w(tDK, ptx::sdesc_sw128(sDSt + aoff, 16, 1024),
+                         ptx::sdesc_sw128(q_tile + boff, 16384, 1024), idesc_kb, acc, leader);
       }
-      ptx::mma_commit(bar(BAR_QE + s));
+      ptx::mma_commit_w(bar(BAR_QE + s), leader);
       // dQ = dS K: M = queries, N = d, K = keys. A = dS read from dS^T
       // ([keys][queries]) as MN-major; B = K ([keys][d]) MN-major.
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        ptx::mma_ss(tDP, ptx::sdesc_sw128(sDSt + kk * 2048, 16384, 1024),
+        ptx::mma_ss_w(tDP, ptx::sdesc_sw128(sDSt + kk * 2048, 16384, 1024),
                          ptx::sdesc_sw128(sK + kk * 2048, 16384, 1024), idesc_q,
-                         kk > 0 ? 1u : 0u);
+                         kk > 0 ? 1u : 0u, leader);
       }
-      ptx::mma_commit(bar(BAR_DQ));
+      ptx::mma_commit_w(bar(BAR_DQ), leader);
     }
-    ptx::mma_commit(bar(BAR_DRAIN));
+    ptx::mma_commit_w(bar(BAR_DRAIN), leader);
     const volatile int never = 0;
     ptx::mbar_wait(bar(BAR_DRAIN), 0, &never, p.wait_limit_ns);
   } else if (warp < 4) {

@@ -158,20 +158,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_wait(bar(BAR_V + j % kStages), (j / kStages) & 1, &never, p.wait_limit_ns);
       }
     }
-  } else if (n_tiles > 0 && warp == 5 && lane == 0) {
+  } else if (n_tiles > 0 && warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop; one elected lane issues each tcgen05
+    // instruction, and every wait's outcome is agreed across the warp.
+    const uint32_t leader = ptx::elect_one();
+    auto wait_w = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+      const bool w_ok = ptx::mbar_wait(b_, parity, s_abort, p.wait_limit_ns);
+      if (!w_ok && leader) ptx::record_timeout(p.status, s_abort, where);
+      return __all_sync(0xffffffffu, w_ok);
+    };
     constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
-    bool ok = ptx::mbar_wait(bar(BAR_Q), 0, s_abort, p.wait_limit_ns);
-    if (!ok) ptx::record_timeout(p.status, s_abort, 0x200);
+    bool ok = wait_w(bar(BAR_Q), 0, 0x200);
     auto issue_pv = [&](int i) -> bool {
-      if (!ptx::mbar_wait(bar(BAR_P), i & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x300 + i);
+      if (!wait_w(bar(BAR_P), i & 1, 0x300 + i)) {
         return false;
       }
       const int s = i % kStages;
-      if (!ptx::mbar_wait(bar(BAR_V + s), (i / kStages) & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x400 + i);
+      if (!wait_w(bar(BAR_V + s), (i / kStages) & 1, 0x400 + i)) {
         return false;
       }
       ptx::tc_fence_after();
@@ -183,16 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // B = V [keys x d], d contiguous (MN-major): 8-key groups at 1024 B,
         // 64-column blocks at 16 KB
         const uint64_t b = ptx::sdesc_sw128(v_tile + kk * 2048, 16384, 1024);
-        ptx::mma_ss(tO, a, b, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_ss_w(tO, a, b, idesc_o, (i > 0 || kk > 0) ? 1u : 0u, leader);
       }
-      ptx::mma_commit(bar(BAR_O));
-      ptx::mma_commit(bar(BAR_EMPTY + s));
+      ptx::mma_commit_w(bar(BAR_O), leader);
+      ptx::mma_commit_w(bar(BAR_EMPTY + s), leader);
       return true;
     };
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int s = j % kStages;
-      if (!ptx::mbar_wait(bar(BAR_K + s), (j / kStages) & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x500 + j);
+      if (!wait_w(bar(BAR_K + s), (j / kStages) & 1, 0x500 + j)) {
         ok = false;
         break;
       }
@@ -203,9 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
         const uint64_t a = ptx::sdesc_sw128(sQ + off, 16, 1024);
         const uint64_t b = ptx::sdesc_sw128(k_tile + off, 16, 1024);
-        ptx::mma_ss(tS[j & 1], a, b, idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_ss_w(tS[j & 1], a, b, idesc_s, kk > 0 ? 1u : 0u, leader);
       }
-      ptx::mma_commit(bar(BAR_S + (j & 1)));
+      ptx::mma_commit_w(bar(BAR_S + (j & 1)), leader);
       if (j >= 1 && !issue_pv(j - 1)) {
         ok = false;
         break;
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) issue_pv(n_tiles - 1);
     // Drain: wait for every MMA this thread issued.
-    ptx::mma_commit(bar(BAR_DRAIN));
+    ptx::mma_commit_w(bar(BAR_DRAIN), leader);
     const volatile int never = 0;
     ptx::mbar_wait(bar(BAR_DRAIN), 0, &never, p.wait_limit_ns);
   } else if (warp < 4) {

@@ -108,11 +108,12 @@ def _check_o(O, O_ref, B, what):
     return float(err.max()), float(B.max())
 
 
-def _run_and_check(w, variant="pass_kv", layout="zigzag", cu=None, chained_steps=False):
+def _run_and_check(w, variant="pass_kv", layout="zigzag", cu=None, chained_steps=False,
+                   window=0):
     inp = make_inputs(w, with_dout=False)
     P, N = w.kv_prefix_len, w.seq_len
     plan = cpa.Plan(N, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim, layout=layout,
-                    variant=variant, cu_seqlens=cu, kv_prefix_len=P)
+                    variant=variant, cu_seqlens=cu, kv_prefix_len=P, window=window)
     run = Fp8Run(plan, inp)
     if chained_steps:
         # per-step ACCUMULATE calls, chained
@@ -128,8 +129,8 @@ def _run_and_check(w, variant="pass_kv", layout="zigzag", cu=None, chained_steps
         o, lse, _ = run.forward()
     qd, kd, vd = _oracle_inputs(inp)
     qpos, kpos = P + np.arange(N), np.arange(P + N)
-    O_ref, L_ref = oracle.attention(qd, kd, vd, qpos, kpos, cu)
-    B = f8.pv_rounding_bound(qd, kd, vd, qpos, kpos, cu)
+    O_ref, L_ref = oracle.attention(qd, kd, vd, qpos, kpos, cu, window=window)
+    B = f8.pv_rounding_bound(qd, kd, vd, qpos, kpos, cu, window=window)
     O = run.base.to_natural_rows(bf16_to_f64(o))
     L = run.base.to_natural_rows(f32_to_f64(lse), axis=1)
     what = f"fp8 {w.name} {variant}/{layout}"
@@ -156,6 +157,13 @@ def test_fp8_forward_gqa_and_scale(qk_scale):
 def test_fp8_partial_prefill(variant):
     w = Workload("fp8pp", 1024, 8, 2, 128, 2, kv_prefix_len=3072)
     _run_and_check(w, variant)
+
+
+@pytest.mark.parametrize("window", [100, 1000])
+def test_fp8_sliding_window_with_documents(window):
+    w = Workload("fp8win", 2048, 4, 2, 128, 4)
+    cu = np.array([0, 700, 1500, 2048], dtype=np.int32)
+    _run_and_check(w, cu=cu, window=window)
 
 
 def test_fp8_chained_per_step_calls():
