@@ -452,9 +452,10 @@ static_assert(FwdPairSmemT<true>::kAlloc <= 232448, "pair kernel shared memory")
 
 // F8: Q and K are E4M3 [tokens][heads][d] and tm_v maps V^T, E4M3
 // [heads][d][tokens] (keys contiguous, the K-major B operand of O = P V); the
-// MMAs are kind::f8f6f4 with K = 32, P goes to TMEM as E4M3 (scaled by 2^8 so
-// that probabilities down to 2^-14 stay normal), the running maximum moves
-// whenever it grows (so P * 2^8 <= 256 < 448), and the per-tensor descale
+// MMAs are kind::f8f6f4 with K = 32, P goes to TMEM as E4M3 scaled by 2^4
+// (probabilities down to 2^-10 of the running maximum stay normal), the
+// running maximum moves when it grows by more than 2^4 (so P * 2^4 <= 2^8 =
+// 256 < 448, the largest E4M3 value), and the per-tensor descale
 // factors p.scales[0..2] (q, k, v) multiply the scores and the output.
 template <bool F8>
 __global__ void __launch_bounds__(kThreadsP, 1)
@@ -681,8 +682,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // E4M3 scores carry the q and k descale factors
     const float scale_log2 = F8 ? p.scale_log2 * (__ldg(p.scales) * __ldg(p.scales + 1))
                                 : p.scale_log2;
-    constexpr float kThreshold = F8 ? 0.f : kRescaleThreshold;
-    constexpr float kPExp = F8 ? 8.f : 0.f;  // P is stored as 2^kPExp * p
+    constexpr float kThreshold = F8 ? 4.f : kRescaleThreshold;
+    constexpr float kPExp = F8 ? 4.f : 0.f;  // P is stored as 2^kPExp * p
     int32_t kpos_next = n_tiles > 0 ? __ldg(kv_tile_pos + w.lo) : 0;
     // The epilogue reads this row's fp32 running output back (merge): ask L2
     // for it a few tiles before the end so those reads do not wait on HBM.

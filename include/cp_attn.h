@@ -261,7 +261,7 @@ cp_attn_status cp_attn_plan_set_chaining(cp_attn_plan_t plan, int enable);
  *   [Hkv][128][T_kv], all in the plan's rank-major token order (apply
  *   cp_attn_layout_apply to the bf16 tensors before quantizing); scales a
  *   device array of three floats, the descale factors of q, k and v
- *   (16-byte aligned). P is rounded to E4M3 (after scaling by 2^8) for the
+ *   (16-byte aligned). P is rounded to E4M3 (after scaling by 2^4) for the
  *   P V product; the row sums, the LSE and all accumulation stay fp32.
  *   Outputs, modes and errors as cp_attn_step_fwd; ERR_UNSUPPORTED for
  *   head_dim != 128.

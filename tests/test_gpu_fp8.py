@@ -26,6 +26,8 @@ if cuda_ok():
     import context_causal_attention_ring_gb300 as cpa
 
 FP32_SLACK = 2e-4
+# the FP8 step scales P by 2^P_EXP before rounding it to E4M3
+P_EXP = 4
 
 
 def _quantize_dev(x, rows, heads, d, transpose=False):
@@ -130,7 +132,7 @@ def _run_and_check(w, variant="pass_kv", layout="zigzag", cu=None, chained_steps
     qd, kd, vd = _oracle_inputs(inp)
     qpos, kpos = P + np.arange(N), np.arange(P + N)
     O_ref, L_ref = oracle.attention(qd, kd, vd, qpos, kpos, cu, window=window)
-    B = f8.pv_rounding_bound(qd, kd, vd, qpos, kpos, cu, window=window)
+    B = f8.pv_rounding_bound(qd, kd, vd, qpos, kpos, cu, window=window, p_exp=P_EXP)
     O = run.base.to_natural_rows(bf16_to_f64(o))
     L = run.base.to_natural_rows(f32_to_f64(lse), axis=1)
     what = f"fp8 {w.name} {variant}/{layout}"
@@ -204,7 +206,7 @@ def test_fp8_prefill_405b_sampled(name):
     qd = f8.dequantize(cq, sq)
     qpos, kpos = P + rows, np.arange(P + N)
     O_ref, L_ref = oracle.sampled_forward(qd, kd, vd, np.arange(len(rows)), qpos, kpos)
-    B = f8.pv_rounding_bound(qd, kd, vd, qpos, kpos, row_block=4)
+    B = f8.pv_rounding_bound(qd, kd, vd, qpos, kpos, row_block=4, p_exp=P_EXP)
     del kd, vd
     for variant in ("pass_kv", "pass_q"):
         plan = cpa.Plan(N, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim, variant=variant,
