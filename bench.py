@@ -76,6 +76,24 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The maximum of a per-rank float over all ranks of the default process
+    group (the value itself when there is no group or a single rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(n_ranks: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job rate: every rank runs its own replica of the step, so the
+    job processes n_ranks times one rank's FLOPs in the slowest rank's time."""
+    return n_ranks * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -270,17 +288,13 @@ def run_ours(args, w):
     pre_ms = [e[1].elapsed_time(e[2]) for e in events]
     bwd_ms = [e[2].elapsed_time(e[3]) for e in events]
     step_ms = [e[0].elapsed_time(e[3]) for e in events]
-    total_ms = events[0][0].elapsed_time(events[-1][3])
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(events[0][0].elapsed_time(events[-1][3]), dev)
     ms_per_step = total_ms / args.steps
     q_mib = plan.T_q * Hq * d * 2 / 2**20
     l2_note = (f"inputs larger than L2 (Q {q_mib:.0f} MiB, dO {q_mib:.0f} MiB)"
                if 2 * q_mib > 129 else
                f"inputs fit in L2 (Q {q_mib:.1f} MiB): a launch-bound small case, warm L2")
-    value = ws * (fwd_flops + bwd_flops) / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(ws, fwd_flops + bwd_flops, ms_per_step)
     fwd_tflops = fwd_flops / (statistics.median(fwd_ms) * 1e-3) / 1e12
     bwd_tflops = bwd_flops / (statistics.median(bwd_ms) * 1e-3) / 1e12
 
@@ -705,13 +719,8 @@ def run_e2e(args, plan, inp, dev, stream, flops, ws):
     e1.record(stream)
     torch.cuda.synchronize()
     plan.sync_status(stream)
-    ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": ws * flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    return {"value": whole_job_tflops(ws, flops, ms), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "path": "pinned host -> device, layout to rank-major, cp_attn_forward, "
                     "cp_attn_backward, layout to natural, device -> pinned host; "
