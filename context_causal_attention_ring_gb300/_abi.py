@@ -81,6 +81,7 @@ _SIG = {
     "cp_attn_decode": (_I, [ctypes.POINTER(_DecodeDesc), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_plan_destroy": (None, [_P]),
     "cp_attn_plan_set_chaining": (_I, [_P, _I]),
+    "cp_attn_decode_sync_status": (_I, [_P]),
     "cp_attn_fp8_absmax": (_I, [_P, _I64, _P, _P]),
     "cp_attn_fp8_quantize": (_I, [_P, _I64, _I, _I, _P, _I, _P, _P, _P]),
     "cp_attn_step_fwd_fp8": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
@@ -205,6 +206,11 @@ def decode(q, k, v, o, lse, workspace, cp: int, softmax_scale: float = 0.0, stre
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().cp_attn_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                  _ptr(lse), _ptr(workspace), int(nbytes), _stream(stream)))
+
+
+def decode_sync_status(stream=None):
+    """Synchronise the stream and raise on a device-side error of the decode."""
+    _check(load().cp_attn_decode_sync_status(_stream(stream)))
 
 
 def head_a2a(x, out, a2a: int, direction: int, heads: Optional[int] = None, stream=None):

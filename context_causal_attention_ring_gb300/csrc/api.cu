@@ -197,6 +197,13 @@ void free_plan_device(cp_attn_plan_s* p) {
   p->on_device = false;
 }
 
+// [rows, heads, d] bf16 tensor map with 64 x 1 x 128 boxes (the step kernels'
+// view), for kernels outside this file.
+cp_attn_status encode_bf16_rows_map(CUtensorMap* m, const void* base, int64_t rows, int heads,
+                                    int d) {
+  return tmap_bf16(m, base, rows, heads, d);
+}
+
 }  // namespace cpa
 
 using namespace cpa;

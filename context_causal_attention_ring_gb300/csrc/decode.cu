@@ -23,7 +23,11 @@
 //   4. O_h / l_h and LSE_h = ln l_h + max to the partial slots.
 // The partials then go through the LSE merge (K4).
 #include <cmath>
+#include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -281,13 +285,370 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecPa
         (st_max[t] + ptx::lg2(st_sum[t])) * kLn2d;
 }
 
-// Keys per CTA: the largest of 512, 256, 128, 64 that divides the shard and
-// still leaves about four CTAs per SM; 64 if none does.
-int pick_part_len(int64_t shard, int64_t ctas_per_part) {
-  const int64_t want = 152 * 4;
+// K9: the same partial attention on the tensor cores (head_dim 128, runs of
+// 128, 256 or 512 keys). The G <= 16 query heads of a KV head form the
+// N = 16 side of two products per 128-key tile, both accumulated in TMEM:
+//   S^T  = K Q^T    (M = 128 keys, N = 16 heads, K = d)
+//   O^T += V^T P^T  (M = d, N = 16 heads, K = keys)
+// The K tiles and then the V tiles of the run stream through a two-slot TMA
+// ring. The whole run's scores fit in TMEM (16 columns per tile), so the
+// softmax is one pass between the two products: per head, the maximum and
+// the sum over the run, reduced across the four softmax warps through shared
+// memory. P goes to shared memory in bf16 as the B operand of O^T. Query rows
+// past G are zero and their columns are ignored.
+// Warps: 0-3 softmax and epilogue (thread = key of a tile, then column of d),
+// 4 TMA producer, 5 TMEM owner and MMA issuer. About 85 KB of shared memory,
+// so two CTAs share an SM.
+constexpr int kTcThreads = 192;
+constexpr int kTcN = 16;                    // MMA N: the query heads, padded
+constexpr int kTcMaxTiles = kDecMaxL / 128;
+
+enum : int {
+  TB_FULL = 0,    // [2] tile of the slot landed
+  TB_EMPTY = 2,   // [2] slot read by its MMAs
+  TB_S = 4,       // all scores of the run in TMEM
+  TB_P = 5,       // 128 arrivals: P in shared memory
+  TB_O = 6,       // O^T complete
+  TB_RED = 7,     // 128 arrivals per phase: the warps' partial maxima, then sums
+  TB_COUNT = 8
+};
+
+struct DecTcSmem {
+  static constexpr int kTile = 128 * 128 * 2;               // a K or V tile
+  static constexpr int kRing = 0;                           // [2]
+  static constexpr int kQ = kRing + 2 * kTile;              // [16][128] bf16: 2 blocks of 2 KB
+  static constexpr int kP = kQ + kTcN * 128 * 2;            // [16][512] bf16: 8 blocks of 2 KB
+  static constexpr int kRed = kP + kTcN * kDecMaxL * 2;     // [max | sum][4 warps][16] f32
+  static constexpr int kBar = kRed + 2 * 4 * kTcN * 4;
+  static constexpr int kMisc = kBar + TB_COUNT * 8;
+  static constexpr int kBytes = kMisc + 16;
+};
+
+struct DecTcParams {
+  const __nv_bfloat16* q;  // [B][Hq][128]
+  float* o_part;           // [parts][B][Hq][128]
+  float* lse_part;         // [parts][Hq][B]
+  int B, Hq, Hkv, G;
+  int64_t kv_len;
+  int L;                   // keys per part: 128, 256 or 512
+  float scale_log2;
+  int32_t* status;         // [4] device status word
+  uint64_t wait_limit_ns;
+};
+
+// Byte offset of element (row, col) of a K-major bf16 operand with 16 rows:
+// 64-column blocks of 16 x 128 bytes (2 KB), 16-byte units XOR-swizzled by
+// row (the 128-byte swizzle).
+__device__ __forceinline__ uint32_t kmaj16_off(int row, int col) {
+  const int chunk = ((col & 63) >> 3) ^ (row & 7);
+  return static_cast<uint32_t>((col >> 6) * 2048 + row * 128 + (chunk << 4) + ((col & 7) << 1));
+}
+
+__global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const DecTcParams p) {
+  using S = DecTcSmem;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = ptx::smem_u32(smem);
+  if (sbase & 1023u) {
+    // the 128-byte swizzled tiles need a 1 KB-aligned window: report, do nothing
+    if (threadIdx.x == 0 &&
+        atomicCAS(p.status, 0, static_cast<int>(CP_ATTN_ERR_UNSUPPORTED)) == 0) {
+      p.status[1] = static_cast<int>(blockIdx.x);
+      p.status[2] = 0x9F00;
+    }
+    return;
+  }
+  const uint32_t sRing = sbase + S::kRing;
+  const uint32_t sQ = sbase + S::kQ;
+  const uint32_t sP = sbase + S::kP;
+  float* red = reinterpret_cast<float*>(smem + S::kRed);
+  const uint32_t bar0 = sbase + S::kBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::kMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::kMisc + 4);
+
+  const int part = blockIdx.x;
+  const int kh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.G;
+  const int nt = p.L / 128;
+  const int row0 = static_cast<int>(static_cast<int64_t>(b) * p.kv_len +
+                                    static_cast<int64_t>(part) * p.L);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TB_COUNT; ++i)
+      ptx::mbar_init(bar(i), (i == TB_P || i == TB_RED) ? 128u : 1u);
+    *s_abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 128);
+    ptx::tmem_relinquish();
+  }
+  if (warp < 4) {
+    // the group's query rows as the K-major B operand of S^T; rows past G zero
+    for (int c = threadIdx.x; c < kTcN * 16; c += 128) {
+      const int h = c >> 4;
+      const int d0 = (c & 15) * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (h < G)
+        v = __ldg(reinterpret_cast<const uint4*>(
+            p.q + (static_cast<int64_t>(b) * p.Hq + kh * G + h) * 128 + d0));
+      *reinterpret_cast<uint4*>(smem + S::kQ + kmaj16_off(h, d0)) = v;
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const volatile int never = 0;
+
+  if (warp == 4 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    int issued = 0;
+    for (int i = 0; i < 2 * nt; ++i) {
+      const int slot = i & 1;
+      if (i >= 2 && !ptx::mbar_wait(bar(TB_EMPTY + slot), ((i >> 1) - 1) & 1, s_abort,
+                                    p.wait_limit_ns)) {
+        ptx::record_timeout(p.status, s_abort, 0x9100 + i);
+        break;
+      }
+      const CUtensorMap* tm = i < nt ? &tm_k : &tm_v;
+      const int row = row0 + (i % nt) * 128;
+      ptx::mbar_arrive_expect_tx(bar(TB_FULL + slot), S::kTile);
+      for (int blk = 0; blk < 2; ++blk)
+        ptx::tma_load_3d(sRing + slot * S::kTile + blk * 16384, tm, bar(TB_FULL + slot), blk * 64,
+                         kh, row);
+      issued = i + 1;
+    }
+    // every issued copy must land before the CTA may exit
+    for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+      ptx::mbar_wait(bar(TB_FULL + (i & 1)), (i >> 1) & 1, &never, p.wait_limit_ns);
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t leader = ptx::elect_one();
+    auto wait_w = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+      const bool w_ok = ptx::mbar_wait(b_, parity, s_abort, p.wait_limit_ns);
+      if (!w_ok && leader) ptx::record_timeout(p.status, s_abort, where);
+      return __all_sync(0xffffffffu, w_ok);
+    };
+    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, kTcN, 0, 0);  // K-major A and B
+    constexpr uint32_t idesc_o = ptx::idesc_bf16(128, kTcN, 1, 0);  // A (V^T) MN-major
+    const uint64_t dQ = ptx::sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dP = ptx::sdesc_sw128(sP, 16, 1024);
+    bool ok = true;
+    for (int t = 0; ok && t < nt; ++t) {
+      const int slot = t & 1;
+      if (!wait_w(bar(TB_FULL + slot), (t >> 1) & 1, 0x9200 + t)) { ok = false; break; }
+      ptx::tc_fence_after();
+      // K tile [128 keys][128 d] in two 64-column blocks of 16 KB
+      const uint64_t dK = ptx::sdesc_sw128(sRing + slot * S::kTile, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        ptx::mma_ss_w(tmem + kTcN * t, ptx::sdesc_add(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
+                      ptx::sdesc_add(dQ, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s,
+                      kk > 0 ? 1u : 0u, leader);
+      ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
+    }
+    ptx::mma_commit_w(bar(TB_S), leader);
+    if (ok) ok = wait_w(bar(TB_P), 0, 0x9300);
+    if (ok) ptx::tc_fence_after();
+    for (int t = 0; ok && t < nt; ++t) {
+      const int i = nt + t;
+      const int slot = i & 1;
+      if (!wait_w(bar(TB_FULL + slot), (i >> 1) & 1, 0x9400 + t)) { ok = false; break; }
+      ptx::tc_fence_after();
+      // V tile as the MN-major A of O^T (M = d: d 64..127 at +16 KB; K = keys,
+      // 16 keys = 2 KB per step); P as the K-major B, 64 keys per 2 KB block
+      const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16384, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        ptx::mma_ss_w(tmem + 64, ptx::sdesc_add(dV, kk * 2048),
+                      ptx::sdesc_add(dP, (2 * t + (kk >> 2)) * 2048 + (kk & 3) * 32), idesc_o,
+                      (t > 0 || kk > 0) ? 1u : 0u, leader);
+      ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
+    }
+    ptx::mma_commit_w(bar(TB_O), leader);
+    ptx::mbar_wait(bar(TB_O), 0, &never, p.wait_limit_ns);
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = threadIdx.x;  // key of each tile, then column of d
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = ptx::mbar_wait(bar(TB_S), 0, s_abort, p.wait_limit_ns);
+    if (!ok) ptx::record_timeout(p.status, s_abort, 0x9500);
+    float x[kTcMaxTiles][kTcN];
+    float M[kTcN], l[kTcN];
+    if (__all_sync(0xffffffffu, ok)) {
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int i = 0; i < kTcMaxTiles; ++i) {
+        if (i < nt) {
+          uint32_t r[16];
+          ptx::tmem_ld16(tmem + lane_base + kTcN * i, r);
+#pragma unroll
+          for (int h = 0; h < kTcN; ++h) x[i][h] = __uint_as_float(r[h]) * p.scale_log2;
+        } else {
+#pragma unroll
+          for (int h = 0; h < kTcN; ++h) x[i][h] = -INFINITY;
+        }
+      }
+      // per head: maximum over the thread's keys, the warp, then the 4 warps
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) {
+        float m = x[0][h];
+#pragma unroll
+        for (int i = 1; i < kTcMaxTiles; ++i) m = fmaxf(m, x[i][h]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        M[h] = m;
+      }
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h)
+        if (lane == h) red[warp * kTcN + h] = M[h];
+      ptx::mbar_arrive(bar(TB_RED));
+      ok = ptx::mbar_wait(bar(TB_RED), 0, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9600);
+    }
+    if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h)
+        M[h] = fmaxf(fmaxf(red[h], red[kTcN + h]), fmaxf(red[2 * kTcN + h], red[3 * kTcN + h]));
+      // P = 2^(x - M) (bf16 into shared memory) and the per-head sums
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) {
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kTcMaxTiles; ++i) {
+          if (i < nt) {
+            const float e = ptx::ex2(x[i][h] - M[h]);
+            sum += e;
+            *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h, i * 128 + t)) =
+                __float2bfloat16_rn(e);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        l[h] = sum;
+      }
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h)
+        if (lane == h) red[4 * kTcN + warp * kTcN + h] = l[h];
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(bar(TB_P));
+      ptx::mbar_arrive(bar(TB_RED));
+      ok = ptx::mbar_wait(bar(TB_RED), 1, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9700);
+    }
+    if (__all_sync(0xffffffffu, ok)) {
+      const float* rs = red + 4 * kTcN;
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) l[h] = (rs[h] + rs[kTcN + h]) + (rs[2 * kTcN + h] + rs[3 * kTcN + h]);
+      ok = ptx::mbar_wait(bar(TB_O), 0, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9800);
+    }
+    if (__all_sync(0xffffffffu, ok)) {
+      ptx::tc_fence_after();
+      // O^T: TMEM lane = column t of d, column h = query head
+      uint32_t r[16];
+      ptx::tmem_ld16(tmem + lane_base + 64, r);
+      const int64_t obase = (static_cast<int64_t>(part) * p.B + b) * p.Hq + kh * G;
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) {
+        if (h < G) {
+          p.o_part[(obase + h) * 128 + t] = __uint_as_float(r[h]) / l[h];
+          if (t == h)
+            p.lse_part[(static_cast<int64_t>(part) * p.Hq + kh * G + h) * p.B + b] =
+                (M[h] + ptx::lg2(l[h])) * kLn2d;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 128);
+  }
+}
+
+// Keys per CTA. head_dim 128 (the tensor-core kernel, two CTAs per SM): the
+// largest of 512, 256, 128 that divides the shard and still leaves about two
+// CTAs per SM, else 128 if it divides the shard. Otherwise (and for
+// head_dim 64, four CTAs per SM): the largest of 512, 256, 128, 64 that
+// leaves about four CTAs per SM; 64 if none does.
+int pick_part_len(int64_t shard, int64_t ctas_per_part, int head_dim) {
+  if (head_dim == 128) {
+    for (int L : {kDecMaxL, 256, 128})
+      if (shard % L == 0 && (shard / L) * ctas_per_part >= 152 * 2) return L;
+    if (shard % 128 == 0) return 128;
+  }
   for (int L : {kDecMaxL, 256, 128})
-    if (shard % L == 0 && (shard / L) * ctas_per_part >= want) return L;
+    if (shard % L == 0 && (shard / L) * ctas_per_part >= 152 * 4) return L;
   return kDecTile;
+}
+
+// Device status word of the tensor-core decode kernel (its bounded waits
+// record a timeout there), one per device, looked up once with the device
+// current.
+__device__ int32_t g_decode_status[4];
+std::mutex g_status_mu;
+std::unordered_map<int, int32_t*> g_status_addr;
+
+cp_attn_status decode_status_address(int32_t** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(CP_ATTN_ERR_CUDA, "decode: no current CUDA device");
+  }
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  auto it = g_status_addr.find(dev);
+  if (it != g_status_addr.end()) {
+    *out = it->second;
+    return CP_ATTN_OK;
+  }
+  void* ptr = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&ptr, g_decode_status);
+  if (err != cudaSuccess || ptr == nullptr) {
+    cudaGetLastError();
+    return fail(CP_ATTN_ERR_CUDA, std::string("decode: status word lookup failed: ") +
+                                      cudaGetErrorString(err));
+  }
+  g_status_addr[dev] = static_cast<int32_t*>(ptr);
+  *out = static_cast<int32_t*>(ptr);
+  return CP_ATTN_OK;
+}
+
+cp_attn_status launch_tc(const void* k, const void* v, const DecTcParams& p, int parts,
+                         cudaStream_t s) {
+  CUtensorMap tk, tv;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.kv_len;
+  cp_attn_status st = encode_bf16_rows_map(&tk, k, rows, p.Hkv, 128);
+  if (st != CP_ATTN_OK) return st;
+  if ((st = encode_bf16_rows_map(&tv, v, rows, p.Hkv, 128)) != CP_ATTN_OK) return st;
+  const size_t smem = DecTcSmem::kBytes;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+    if (err != cudaSuccess)
+      return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc attr: ") + cudaGetErrorString(err));
+    attr = true;
+  }
+  decode_tc_kernel<<<dim3(parts, p.Hkv, p.B), kTcThreads, smem, s>>>(tk, tv, p);
+  const cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc: ") + cudaGetErrorString(err));
+  count_launch();
+  return CP_ATTN_OK;
 }
 
 cp_attn_status validate(const cp_attn_decode_desc* d) {
@@ -309,7 +670,8 @@ cp_attn_status validate(const cp_attn_decode_desc* d) {
 
 int64_t n_parts(const cp_attn_decode_desc* d) {
   const int64_t shard = d->kv_len / d->cp;
-  const int L = pick_part_len(shard, static_cast<int64_t>(d->cp) * d->n_kv_heads * d->batch);
+  const int L = pick_part_len(shard, static_cast<int64_t>(d->cp) * d->n_kv_heads * d->batch,
+                             d->head_dim);
   return d->kv_len / L;
 }
 
@@ -389,7 +751,23 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
   if (parts > 0x7fffffff) return cpa::fail(CP_ATTN_ERR_SHAPE, "decode: too many key runs");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int np = static_cast<int>(parts);
-  if (desc->head_dim == 128) {
+  if (desc->head_dim == 128 && p.L % 128 == 0 &&
+      static_cast<int64_t>(desc->batch) * desc->kv_len <= 0x7fffffff) {
+    cpa::DecTcParams tp;
+    tp.q = p.q;
+    tp.o_part = p.o_part;
+    tp.lse_part = p.lse_part;
+    tp.B = p.B;
+    tp.Hq = p.Hq;
+    tp.Hkv = p.Hkv;
+    tp.G = p.G;
+    tp.kv_len = p.kv_len;
+    tp.L = p.L;
+    tp.scale_log2 = p.scale_log2;
+    tp.wait_limit_ns = 1000000000ull;
+    if ((st = cpa::decode_status_address(&tp.status)) != CP_ATTN_OK) return st;
+    st = cpa::launch_tc(k, v, tp, np, s);
+  } else if (desc->head_dim == 128) {
     st = G <= 4 ? cpa::launch<128, 1>(p, np, s) : G <= 8 ? cpa::launch<128, 2>(p, np, s)
                                                           : cpa::launch<128, 4>(p, np, s);
   } else {
@@ -401,6 +779,30 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
   return cpa::launch_merge_lse(np, desc->batch, desc->n_q_heads, desc->head_dim, o_part,
                                rows * desc->head_dim, lse_part, rows,
                                static_cast<__nv_bfloat16*>(o), nullptr, lse, s);
+}
+
+cp_attn_status cp_attn_decode_sync_status(void* stream) {
+  cpa::clear_error();
+  int32_t* status = nullptr;
+  cp_attn_status st = cpa::decode_status_address(&status);
+  if (st != CP_ATTN_OK) return st;
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess)
+    return cpa::fail(CP_ATTN_ERR_CUDA, std::string("decode_sync_status: ") + cudaGetErrorString(err));
+  int32_t h[4] = {0, 0, 0, 0};
+  err = cudaMemcpy(h, status, sizeof(h), cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess && h[0] != 0) err = cudaMemset(status, 0, sizeof(h));
+  if (err != cudaSuccess)
+    return cpa::fail(CP_ATTN_ERR_CUDA, std::string("decode_sync_status: ") + cudaGetErrorString(err));
+  if (h[0] != 0)
+    return cpa::fail(static_cast<cp_attn_status>(h[0]),
+                     "decode: device-side error in block " + std::to_string(h[1]) +
+                         " at wait site 0x" + [&] {
+                           char b[16];
+                           std::snprintf(b, sizeof(b), "%x", h[2]);
+                           return std::string(b);
+                         }());
+  return CP_ATTN_OK;
 }
 
 }  // extern "C"

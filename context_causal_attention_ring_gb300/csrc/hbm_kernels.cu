@@ -87,6 +87,76 @@ __global__ void __launch_bounds__(256) merge_lse_kernel(
   if (lane == 0) lse_out[lse_idx] = (M == -INFINITY) ? -INFINITY : L * kLn2;
 }
 
+// The same merge for few (row, head) pairs and many parts (a decode row
+// merges every rank's and every run's partial): one CTA of 8 warps per (row,
+// head). Every warp computes the global L = M + log2 sum_i 2^(LSE_i - M)
+// (lanes split the parts), then sums w_i O_i over parts w, w + 8, ... for
+// its float4 chunk of d (d <= 128); warp 0 adds the 8 sums. The CTA reads
+// all parts before it writes, so o_out_f32 may alias part 0.
+__global__ void __launch_bounds__(256) merge_lse_wide_kernel(
+    int n_parts, int64_t rows, int heads, int d, const float* __restrict__ o_parts,
+    int64_t part_stride, const float* __restrict__ lse_parts, int64_t lse_part_stride,
+    __nv_bfloat16* __restrict__ o_out, float* __restrict__ o_out_f32,
+    float* __restrict__ lse_out) {
+  __shared__ float4 s_acc[8][32];
+  const int64_t pair = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = pair / heads;
+  const int h = static_cast<int>(pair % heads);
+  const int64_t lse_idx = static_cast<int64_t>(h) * rows + row;
+  float M = -INFINITY;
+  for (int i = lane; i < n_parts; i += 32)
+    M = fmaxf(M, __ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = -INFINITY;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t o_off = (row * heads + h) * static_cast<int64_t>(d);
+  const bool has = lane < (d >> 2);
+  if (M != -INFINITY) {
+    float S = 0.f;
+    for (int i = lane; i < n_parts; i += 32)
+      S += ptx::ex2(__ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    L = M + ptx::lg2(S);
+    for (int i = warp; i < n_parts; i += 8) {
+      const float w = ptx::ex2(__ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e - L);
+      if (w == 0.f || !has) continue;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(o_parts + i * part_stride + o_off) +
+                             lane);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+  }
+  s_acc[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = s_acc[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      const float4 u = s_acc[w][lane];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    if (has) {
+      if (o_out_f32) reinterpret_cast<float4*>(o_out_f32 + o_off)[lane] = t;
+      if (o_out) {
+        uint2 pk;
+        pk.x = ptx::pack_bf16(t.x, t.y);
+        pk.y = ptx::pack_bf16(t.z, t.w);
+        reinterpret_cast<uint2*>(o_out + o_off)[lane] = pk;
+      }
+    }
+    if (lane == 0) lse_out[lse_idx] = (M == -INFINITY) ? -INFINITY : L * kLn2;
+  }
+}
+
 // out[dst] = in[src] for 16-byte vectors; row_map[i] = natural row of
 // rank-major row i. to_natural: out[row_map[i]] = in[i]; else
 // out[i] = in[row_map[i]].
@@ -251,6 +321,13 @@ cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
                                 cudaStream_t s) {
   const int64_t warps = rows * heads;
   if (warps == 0) return CP_ATTN_OK;
+  // few (row, head) pairs with many parts: eight warps per pair
+  if (d <= 128 && n_parts >= 16 && warps * 8 <= 152 * 64) {
+    merge_lse_wide_kernel<<<static_cast<unsigned>(warps), 256, 0, s>>>(
+        n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
+        o_out_f32, lse_out);
+    return check_launch("merge_lse");
+  }
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (d <= 128)
     merge_lse_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, s>>>(

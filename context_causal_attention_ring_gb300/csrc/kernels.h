@@ -110,6 +110,10 @@ cp_attn_status launch_bwd_preprocess(int64_t rows, int heads, int d, const __nv_
 
 cp_attn_status launch_zero_f32(float* p, int64_t n, cudaStream_t s);
 
+// [rows, heads, d] bf16 tensor map, 64 x 1 x 128 boxes, 128-byte swizzle (api.cu).
+cp_attn_status encode_bf16_rows_map(CUtensorMap* m, const void* base, int64_t rows, int heads,
+                                    int d);
+
 cp_attn_status launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 // n = element count, a multiple of 8

@@ -419,7 +419,10 @@ cp_attn_status cp_attn_head_a2a(int64_t rows, int heads, int64_t head_bytes, int
  * [batch, Hq, d]; lse: fp32 [Hq, batch] (natural log, scale applied).
  * workspace: cp_attn_decode_workspace_size bytes (fp32 partials), 16-byte
  * aligned like every pointer. Supported: head_dim 64 or 128, at most 16 query
- * heads per KV head, kv_len a multiple of 64*cp. */
+ * heads per KV head, kv_len a multiple of 64*cp. With head_dim 128 and key
+ * runs that are multiples of 128 the partials come from the tensor cores
+ * (S^T = K Q^T and O^T = V^T P^T with the query heads as N = 16, P in bf16);
+ * otherwise from the CUDA cores in fp32. */
 typedef struct cp_attn_decode_desc {
   int batch;           /* sequences, one new row each */
   int cp;              /* ring size R: ranks sharing each sequence's keys */
@@ -433,6 +436,10 @@ cp_attn_status cp_attn_decode_workspace_size(const cp_attn_decode_desc* desc, si
 cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, const void* k,
                               const void* v, void* o, float* lse, void* workspace,
                               size_t workspace_bytes, void* stream);
+/* Synchronise `stream`, then read and clear the decode kernels' device status
+ * word (one per device: the tensor-core decode records a timed-out pipeline
+ * wait there, CP_ATTN_ERR_TIMEOUT). Returns CP_ATTN_OK or that error. */
+cp_attn_status cp_attn_decode_sync_status(void* stream);
 
 /* Synchronise `stream`, then read and clear the plan's device status word.
  * Returns CP_ATTN_OK or the first device-side error (ERR_TIMEOUT). */

@@ -3,8 +3,10 @@ the K4 merge; Pass Q for decode, "Context Parallelism for Scalable
 Million-Token Inference") against the fp64 oracle, through the C ABI. Covers
 one to sixteen query heads per KV head (including group sizes that are not a
 multiple of four), both head dimensions, several ring sizes and a 405B-shaped
-row over 131072 keys. Tolerances: O (bf16) 1e-2 plus half a bf16 ulp, LSE
-1e-3."""
+row over 131072 keys. With head_dim 128 and key runs of 128, 256 or 512 the
+tensor-core kernel (K9) computes the partials; head_dim 64 and 64-key runs
+use the CUDA-core kernel (K8). Tolerances: O (bf16) 1e-2 plus half a bf16
+ulp, LSE 1e-3."""
 import numpy as np
 import pytest
 
@@ -28,7 +30,7 @@ def _check(B, T, Hq, Hkv, d, R, seed, qk_scale=1.0):
     ws = torch.empty(cpa.decode_workspace_size(B, R, T, Hq, Hkv, d), dtype=torch.uint8,
                      device="cuda")
     cpa.decode(qd, kd, vd, o, lse, ws, R)
-    torch.cuda.synchronize()
+    cpa.decode_sync_status()
     O_r, L_r = oracle.decode(bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v), R)
     tag = f"decode B={B} T={T} {Hq}/{Hkv} d={d} R={R}"
     assert_close_bf16(bf16_to_f64(o), O_r, 1e-2, tag + " O")
@@ -41,6 +43,9 @@ def _check(B, T, Hq, Hkv, d, R, seed, qk_scale=1.0):
     (3, 512, 4, 4, 64, 2),        # one head per group, d = 64
     (2, 768, 12, 2, 128, 3),      # 6 heads per group, odd ring
     (1, 64, 2, 1, 64, 1),         # a single 64-key run
+    (16, 2048, 32, 8, 128, 8),    # many sequences: 256-key runs
+    (2, 8192, 64, 4, 128, 4),     # 16 heads per group, 128-key runs of a 2048-key shard
+    (3, 1536, 12, 1, 128, 2),     # 12 heads per group, 128-key runs of a 768-key shard
 ])
 def test_decode_small(B, T, Hq, Hkv, d, R):
     _check(B, T, Hq, Hkv, d, R, seed=B * 100 + R)

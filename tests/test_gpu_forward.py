@@ -154,9 +154,13 @@ def test_pass_kv_equals_pass_q_on_device():
     assert np.abs(outs[0][1] - outs[1][1]).max() <= 1e-3
 
 
-def test_merge_kernel_against_oracle():
+@pytest.mark.parametrize("n,rows,H,d", [
+    (5, 300, 3, 128),    # one warp per (row, head)
+    (40, 30, 3, 128),    # many parts, few pairs: eight warps per pair
+    (24, 16, 4, 64),     # the same with head_dim 64
+])
+def test_merge_kernel_against_oracle(n, rows, H, d):
     rng = np.random.default_rng(5)
-    n, rows, H, d = 5, 300, 3, 128
     o = rng.standard_normal((n, rows, H, d)).astype(np.float32)
     lse = (rng.standard_normal((n, H, rows)) * 3).astype(np.float32)
     lse[1, :, ::7] = -np.inf
