@@ -488,6 +488,11 @@ cp_attn_status step_bwd_impl(cp_attn_plan_t p, int step, const void* half_ops, c
   bp.dv = dv_acc;
   bp.status = p->d_status;
   bp.wait_limit_ns = kWaitLimitNs;
+  // Measured on GB300: letting a chained step's main loop run beside the
+  // previous step's tail gains ~2 % with up to 8 query heads per KV head and
+  // loses up to 17 % with 16 (the 405B-shaped and packed 128/8-head layers),
+  // so larger groups wait before the loop and only the launch overlaps.
+  bp.dep_wait_early = (p->Hq / p->Hkv > 8) ? 1 : 0;
   const int n_items = p->bwd_off[step + 1] - p->bwd_off[step];
   if (n_items == 0) return CP_ATTN_OK;
   *launched = true;

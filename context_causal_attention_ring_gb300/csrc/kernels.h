@@ -52,6 +52,9 @@ struct BwdParams {
   float* dv;
   int32_t* status;
   uint64_t wait_limit_ns;
+  // chained launch: wait for the previous step before the main loop instead
+  // of before the dK / dV read-modify-write
+  int dep_wait_early;
 };
 
 // chained: launch with programmatic stream serialization, so that the grid

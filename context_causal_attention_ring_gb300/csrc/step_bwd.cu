@@ -490,6 +490,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   const uint32_t tmem = *s_tmem;
   // the next ring step may start on SMs this grid leaves idle
   if (threadIdx.x == 0) ptx::grid_dep_launch();
+  // chained after a previous step: with large GQA groups only the launch
+  // overlaps its tail (see the host side)
+  if (p.dep_wait_early) ptx::grid_dep_wait();
   const uint32_t tDV = tmem + 256;
   const uint32_t tDK = tmem + 384;
 
