@@ -267,6 +267,50 @@ def run_ours(args, w):
         step()
     plan.sync_status(stream)
 
+    graphs = None
+    launches_per_step = 0
+    if args.graph:
+        # the three phases captured once each; the timed region replays them
+        graphs = []
+        n0 = cpa.launch_count()
+        cap = torch.cuda.Stream()  # capture needs a stream other than the default one
+
+        def fwd_part():
+            for t in range(R):
+                plan.step_fwd(t, q, k, v, o_acc, lse, cpa.ACCUMULATE,
+                              o if t == R - 1 else None, cap)
+
+        def pre_part():
+            plan.bwd_preprocess(q, k, v, o, do, delta, half_ops, dq, dk, dv, o_f32=o_acc,
+                                stream=cap)
+
+        def bwd_part():
+            for t in range(R):
+                plan.step_bwd(t, half_ops, lse, delta, dq, dk, dv, cap)
+
+        cap.wait_stream(stream)
+        for part in (fwd_part, pre_part, bwd_part):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                part()
+            graphs.append(g)
+        stream.wait_stream(cap)
+        launches_per_step = cpa.launch_count() - n0
+        for _ in range(args.warmup):
+            for g in graphs:
+                g.replay()
+        torch.cuda.synchronize()
+        plan.sync_status(stream)
+
+        def step(ev=None):  # noqa: F811 -- the replaying version
+            with torch.cuda.stream(stream):
+                for i, g in enumerate(graphs):
+                    if ev is not None:
+                        ev[i].record(stream)
+                    g.replay()
+                if ev is not None:
+                    ev[3].record(stream)
+
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
               for _ in range(args.steps)]
     sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
@@ -278,7 +322,7 @@ def run_ours(args, w):
     for i in range(args.steps):
         step(events[i])
     torch.cuda.synchronize()
-    n_launches = cpa.launch_count() - n_launch0
+    n_launches = cpa.launch_count() - n_launch0 + launches_per_step * args.steps
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -333,6 +377,7 @@ def run_ours(args, w):
                        "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d,
                        "layout": w.layout, "variant": "pass_kv", "parallelism": f"replicas{ws}",
                        "l2": l2_note,
+                       "launch": "cuda_graph replay" if args.graph else "stream",
                        "flops_per_step": fwd_flops + bwd_flops},
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
             "fwd_ms": statistics.median(fwd_ms), "bwd_ms": statistics.median(bwd_ms),
@@ -744,6 +789,8 @@ def main():
                     help="time Pass KV against Pass Q at several KV-cache hit rates")
     ap.add_argument("--usp-sweep", action="store_true",
                     help="time the layer as zigzag ring, USP and pure Ulysses arrangements")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of the step captured as CUDA graphs (launch-bound shapes)")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) forward against bf16 on the 405B-shaped prefill")
     ap.add_argument("--fp8-workload", default="prefill_405b_full", choices=sorted(WORKLOADS),
