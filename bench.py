@@ -38,9 +38,9 @@ METRIC = "causal attn TFLOPS fwd/bwd (unmasked FLOPs) and % of GB300 dense BF16 
 # only while the kernel source is the one that was profiled.
 PROFILED_TRAFFIC = {
     "step_bwd": ("context_causal_attention_ring_gb300/csrc/step_bwd.cu",
-                 "bb08c296ea737c1e0859b8dc93e1670e4c445e2eacc8f2e67a1ec2c7300cc727", 3.100231e9),
+                 "a662b08e9cd0ec616e01d1bf47a75b9b02a3a44f8c008dc149a884986215c990", 3.102382e9),
     "step_fwd": ("context_causal_attention_ring_gb300/csrc/step_fwd.cu",
-                 "9f265fea77a8e823b62a3ac07383f5921ac0a1824df8c31409ef5ab60ea3c0b9", 1.295524e9),
+                 "ac5c1f474e66330e520fa5f8d3118fa8562c79b8da5ba0c7020367774e078c03", 1.295558e9),
 }
 
 
