@@ -27,7 +27,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_per_tensor", "dequantize",
-           "pv_rounding_bound"]
+           "pv_rounding_bound", "quantize_rows"]
 
 E4M3_MAX = 448.0
 _BIAS = 7
@@ -153,3 +153,16 @@ def pv_rounding_bound(q, k, v, qpos, kpos, cu_seqlens=None, scale=None, *, windo
                 (sub_abs / L)[:, None] * (sub.astype(np.float64) @ vh_[kh])
             B[r0:r1, h, :] = np.where(has[:, None], b, 0.0)
     return B
+
+
+def quantize_rows(x):
+    """(codes, scales): E4M3 quantization of each row of x (the last axis)
+    with its own scale, the per-tensor rule applied row by row (the decode
+    quantizes each head's query row this way)."""
+    x = np.asarray(x, dtype=np.float64)
+    flat = x.reshape(-1, x.shape[-1])
+    codes = np.empty(flat.shape, dtype=np.uint8)
+    scales = np.empty(flat.shape[0], dtype=np.float32)
+    for i in range(flat.shape[0]):
+        codes[i], scales[i], _ = quantize_per_tensor(flat[i])
+    return codes.reshape(x.shape), scales.reshape(x.shape[:-1])

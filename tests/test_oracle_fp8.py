@@ -163,3 +163,19 @@ def test_pv_rounding_bound_is_reached_by_the_worst_rounding(spread):
     B = f8.pv_rounding_bound(q, k, v, pos, pos, scale=1.0 / np.sqrt(d))[:, 0, :]
     W = _worst_case_change(q[:, 0], k[:, 0], v[:, 0], 1.0 / np.sqrt(d))
     np.testing.assert_allclose(B, W, rtol=1e-9, atol=1e-15)
+
+
+def test_quantize_rows_scales_each_row_on_its_own():
+    """Rows of very different ranges: each row's largest magnitude maps to
+    +-448 with that row's scale, and each row is within its own half-step
+    bound."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((6, 128)) * np.array([1e-3, 1, 30, 0.2, 5e2, 7])[:, None]
+    x = x.astype(np.float32).astype(np.float64)
+    codes, scales = f8.quantize_rows(x)
+    for i in range(6):
+        amax = np.abs(x[i]).max()
+        assert scales[i] == np.float32(amax) / np.float32(448.0)
+        assert abs(f8.e4m3_decode(codes[i, np.argmax(np.abs(x[i]))])) == 448.0
+        err = np.abs(f8.dequantize(codes[i], scales[i]) - x[i])
+        assert np.all(err <= 2.0 ** -4 * np.abs(x[i]) * 1.0001 + 2.0 ** -10 * float(scales[i]) * 1.0001)
