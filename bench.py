@@ -545,11 +545,14 @@ def run_usp_sweep(args):
 
 
 def run_decode_bench(args):
-    """One-row decode over the emulated ring (cp_attn_decode: K8 partials and
-    the K4 merge) on two shapes: a 405B-shaped row (128 / 8 heads) over 131072
-    keys on 8 ranks, and a batch of 16 sequences with 8B-shaped heads (32 / 8)
-    over 32768 keys each. Both read more K/V than the L2 holds. The roofline
-    is HBM: algorithmic bytes = K + V + q + o (+ the LSE), once."""
+    """One-row decode over the emulated ring (cp_attn_decode: the partials over
+    runs of keys and the K4 merge) on two shapes: a 405B-shaped row (128 / 8
+    heads) over 131072 keys on 8 ranks, and a batch of 16 sequences with
+    8B-shaped heads (32 / 8) over 32768 keys each; each with a bf16 KV cache
+    and with an E4M3 one (cp_attn_decode_fp8, K and V quantized per tensor
+    before the timed calls). Both read more K/V than the L2 holds. The
+    roofline is HBM: algorithmic bytes = K + V (at their element size) + q + o
+    (+ the LSE), once."""
     import torch
     import context_causal_attention_ring_gb300 as cpa
     from workloads import make_decode_inputs
@@ -557,6 +560,31 @@ def run_decode_bench(args):
     torch.cuda.set_device(0)
     peaks, peak_kind = _peaks()
     rows = []
+
+    def time_calls(call):
+        for _ in range(max(3, args.warmup)):
+            call()
+        n = max(20, args.steps)
+        ev = [(torch.cuda.Event(True), torch.cuda.Event(True)) for _ in range(n)]
+        n0 = cpa.launch_count()
+        for e0, e1 in ev:
+            e0.record()
+            call()
+            e1.record()
+        torch.cuda.synchronize()
+        cpa.decode_sync_status()
+        return (statistics.median(e0.elapsed_time(e1) for e0, e1 in ev),
+                (cpa.launch_count() - n0) // n)
+
+    def quantize(x, n_rows, heads, d, transpose):
+        amax = torch.zeros(4, dtype=torch.float32, device="cuda")
+        scale = torch.zeros(4, dtype=torch.float32, device="cuda")
+        cpa.fp8_absmax(x, n_rows * heads * d, amax)
+        out = torch.empty((heads, d, n_rows) if transpose else (n_rows, heads, d),
+                          dtype=torch.uint8, device="cuda")
+        cpa.fp8_quantize(x, n_rows, heads, d, amax, out, scale, transpose=transpose)
+        return out, scale
+
     for name, B, T, Hq, Hkv, d, R in (("405b_row_131072", 1, 131072, 128, 8, 128, 8),
                                       ("8b_batch16_32768", 16, 32768, 32, 8, 128, 8)):
         q, k, v = make_decode_inputs(B, T, Hq, Hkv, d, seed=3)
@@ -568,26 +596,20 @@ def run_decode_bench(args):
         lse = torch.empty((Hq, B), dtype=torch.float32, device="cuda")
         ws = torch.empty(cpa.decode_workspace_size(B, R, T, Hq, Hkv, d), dtype=torch.uint8,
                          device="cuda")
-        for _ in range(max(3, args.warmup)):
-            cpa.decode(qd, kd, vd, o, lse, ws, R)
-        n = max(20, args.steps)
-        ev = [(torch.cuda.Event(True), torch.cuda.Event(True)) for _ in range(n)]
-        n0 = cpa.launch_count()
-        for e0, e1 in ev:
-            e0.record()
-            cpa.decode(qd, kd, vd, o, lse, ws, R)
-            e1.record()
-        torch.cuda.synchronize()
-        launches = (cpa.launch_count() - n0) // n
-        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
-        kv_bytes = 2 * B * T * Hkv * d * 2
-        algo = kv_bytes + 2 * B * Hq * d * 2 + Hq * B * 4
-        gbs = algo / (ms * 1e-3) / 1e9
-        rows.append({"workload": name, "batch": B, "kv_len": T, "n_q_heads": Hq,
-                     "n_kv_heads": Hkv, "head_dim": d, "cp": R, "ms": ms,
-                     "algorithmic_bytes": algo, "achieved_gbs": gbs,
-                     "frac_of_hbm": gbs / peaks["hbm_gbs"], "launches_per_call": launches})
-        del qd, kd, vd, o, lse, ws
+        k8, sk = quantize(kd.view(B * T, Hkv, d), B * T, Hkv, d, False)
+        vt8, sv = quantize(vd.view(B * T, Hkv, d), B * T, Hkv, d, True)
+        scales = torch.stack([sk[0], sv[0]])
+        for kv_dtype, elt, call in (
+                ("bf16", 2, lambda: cpa.decode(qd, kd, vd, o, lse, ws, R)),
+                ("e4m3", 1, lambda: cpa.decode_fp8(qd, k8, vt8, scales, o, lse, ws, R))):
+            ms, launches = time_calls(call)
+            algo = 2 * B * T * Hkv * d * elt + 2 * B * Hq * d * 2 + Hq * B * 4
+            gbs = algo / (ms * 1e-3) / 1e9
+            rows.append({"workload": name, "kv_dtype": kv_dtype, "batch": B, "kv_len": T,
+                         "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d, "cp": R, "ms": ms,
+                         "algorithmic_bytes": algo, "achieved_gbs": gbs,
+                         "frac_of_hbm": gbs / peaks["hbm_gbs"], "launches_per_call": launches})
+        del qd, kd, vd, o, lse, ws, k8, vt8
         torch.cuda.empty_cache()
     print(json.dumps({"metric": "decode_hbm_bandwidth", "unit": "GB/s",
                       "peak": peaks["hbm_gbs"], "peak_kind": f"hbm_gbs ({peak_kind})",

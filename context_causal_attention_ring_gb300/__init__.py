@@ -6,7 +6,7 @@ there is no CPU fallback.
 """
 from ._abi import (  # noqa: F401
     ACCUMULATE, CpAttnError, GATHER_HEADS, LAYOUT_CONTIGUOUS, LAYOUT_USP, LAYOUT_ZIGZAG,
-    OP_BACKWARD, SPLIT_HEADS, decode, decode_sync_status, decode_workspace_size, fp8_absmax, fp8_quantize, head_a2a,
+    OP_BACKWARD, SPLIT_HEADS, decode, decode_fp8, decode_sync_status, decode_workspace_size, fp8_absmax, fp8_quantize, head_a2a,
     OP_FORWARD, PASS_KV, PASS_Q, VARIANT_AUTO, Plan, TENSOR_KV, TENSOR_Q, TO_NATURAL,
     TO_RANK_MAJOR, WRITE_PARTIAL, exported_symbols, launch_count, lib_path,
     load, merge_lse, select_variant, status_string,

@@ -82,6 +82,7 @@ _SIG = {
     "cp_attn_plan_destroy": (None, [_P]),
     "cp_attn_plan_set_chaining": (_I, [_P, _I]),
     "cp_attn_decode_sync_status": (_I, [_P]),
+    "cp_attn_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_fp8_absmax": (_I, [_P, _I64, _P, _P]),
     "cp_attn_fp8_quantize": (_I, [_P, _I64, _I, _I, _P, _I, _P, _P, _P]),
     "cp_attn_step_fwd_fp8": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
@@ -206,6 +207,20 @@ def decode(q, k, v, o, lse, workspace, cp: int, softmax_scale: float = 0.0, stre
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().cp_attn_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                  _ptr(lse), _ptr(workspace), int(nbytes), _stream(stream)))
+
+
+def decode_fp8(q, k8, vt8, kv_scales, o, lse, workspace, cp: int, softmax_scale: float = 0.0,
+               stream=None):
+    """cp_attn_decode_fp8: q bf16 [B, Hq, 128]; k8 E4M3 [B*T, Hkv, 128]; vt8 E4M3
+    [Hkv, 128, B*T]; kv_scales device [2] (K, V descale factors)."""
+    B, Hq, d = q.shape
+    Hkv = k8.shape[1]
+    T = k8.shape[0] // B
+    desc = _decode_desc(B, cp, T, Hq, Hkv, d, softmax_scale)
+    _check(load().cp_attn_decode_fp8(ctypes.byref(desc), _ptr(q), _ptr(k8), _ptr(vt8),
+                                     _ptr(kv_scales), _ptr(o), _ptr(lse), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
 
 
 def decode_sync_status(stream=None):

@@ -204,6 +204,13 @@ cp_attn_status encode_bf16_rows_map(CUtensorMap* m, const void* base, int64_t ro
   return tmap_bf16(m, base, rows, heads, d);
 }
 
+// One-byte [rows, heads, d] map (128-byte boxes), or the transposed
+// [heads, d, rows] one (128 x d boxes), for kernels outside this file.
+cp_attn_status encode_u8_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int d,
+                             bool transposed) {
+  return tmap_u8(m, base, rows, heads, d, transposed);
+}
+
 }  // namespace cpa
 
 using namespace cpa;

@@ -304,23 +304,30 @@ constexpr int kTcN = 16;                    // MMA N: the query heads, padded
 constexpr int kTcMaxTiles = kDecMaxL / 128;
 
 enum : int {
-  TB_FULL = 0,    // [2] tile of the slot landed
-  TB_EMPTY = 2,   // [2] slot read by its MMAs
-  TB_S = 4,       // all scores of the run in TMEM
-  TB_P = 5,       // 128 arrivals: P in shared memory
-  TB_O = 6,       // O^T complete
-  TB_RED = 7,     // 128 arrivals per phase: the warps' partial maxima, then sums
-  TB_COUNT = 8
+  TB_FULL = 0,    // [4] tile of the slot landed
+  TB_EMPTY = 4,   // [4] slot read by its MMAs
+  TB_S = 8,       // all scores of the run in TMEM
+  TB_P = 9,       // 128 arrivals: P in shared memory
+  TB_O = 10,      // O^T complete
+  TB_RED = 11,    // 128 arrivals per phase: the warps' partial maxima, then sums
+  TB_COUNT = 12
 };
 
+// F8: E4M3 K rows and V^T tiles (one byte per element, 16 KB per tile, a
+// four-slot ring), the query rows and P in E4M3; else bf16 (32 KB tiles, two
+// slots).
+template <bool F8>
 struct DecTcSmem {
-  static constexpr int kTile = 128 * 128 * 2;               // a K or V tile
-  static constexpr int kRing = 0;                           // [2]
-  static constexpr int kQ = kRing + 2 * kTile;              // [16][128] bf16: 2 blocks of 2 KB
-  static constexpr int kP = kQ + kTcN * 128 * 2;            // [16][512] bf16: 8 blocks of 2 KB
-  static constexpr int kRed = kP + kTcN * kDecMaxL * 2;     // [max | sum][4 warps][16] f32
-  static constexpr int kBar = kRed + 2 * 4 * kTcN * 4;
-  static constexpr int kMisc = kBar + TB_COUNT * 8;
+  static constexpr int kElt = F8 ? 1 : 2;
+  static constexpr int kSlots = F8 ? 4 : 2;
+  static constexpr int kTile = 128 * 128 * kElt;            // a K or V tile
+  static constexpr int kRing = 0;                           // [kSlots]
+  static constexpr int kQ = kRing + kSlots * kTile;         // [16][128] query rows
+  static constexpr int kP = kQ + kTcN * 128 * kElt;         // [16][512] P
+  static constexpr int kRed = kP + kTcN * kDecMaxL * kElt;  // [max | sum][4 warps][16] f32
+  static constexpr int kQs = kRed + 2 * 4 * kTcN * 4;       // [16] f32 query scales (F8)
+  static constexpr int kBar = kQs + kTcN * 4;
+  static constexpr int kMisc = kBar + (TB_COUNT + 4) * 8;
   static constexpr int kBytes = kMisc + 16;
 };
 
@@ -334,7 +341,16 @@ struct DecTcParams {
   float scale_log2;
   int32_t* status;         // [4] device status word
   uint64_t wait_limit_ns;
+  const float* kv_scales;  // F8: device [2] descale factors of K and V
 };
+
+// Byte offset of element (row, col) of a K-major 8-bit operand with 16 rows:
+// 128-column blocks of 16 x 128 bytes (2 KB), 16-byte units XOR-swizzled by
+// row.
+__device__ __forceinline__ uint32_t kmaj16_off8(int row, int col) {
+  const int chunk = ((col & 127) >> 4) ^ (row & 7);
+  return static_cast<uint32_t>((col >> 7) * 2048 + row * 128 + (chunk << 4) + (col & 15));
+}
 
 // Byte offset of element (row, col) of a K-major bf16 operand with 16 rows:
 // 64-column blocks of 16 x 128 bytes (2 KB), 16-byte units XOR-swizzled by
@@ -344,10 +360,16 @@ __device__ __forceinline__ uint32_t kmaj16_off(int row, int col) {
   return static_cast<uint32_t>((col >> 6) * 2048 + row * 128 + (chunk << 4) + ((col & 7) << 1));
 }
 
+// F8: tm_k maps E4M3 K [B*kv_len][Hkv][128] (128-byte boxes), tm_v maps V^T
+// E4M3 [Hkv][128][B*kv_len]; each head's query row is quantized here with its
+// own scale, S^T and O^T are kind::f8f6f4 with K = 32, and P goes to shared
+// memory as E4M3 scaled by 2^8 (P <= 1 against the run's exact maximum).
+template <bool F8>
 __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const DecTcParams p) {
-  using S = DecTcSmem;
+  using S = DecTcSmem<F8>;
+  constexpr int NSL = S::kSlots;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
   if (sbase & 1023u) {
@@ -389,15 +411,38 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
     ptx::tmem_relinquish();
   }
   if (warp < 4) {
-    // the group's query rows as the K-major B operand of S^T; rows past G zero
-    for (int c = threadIdx.x; c < kTcN * 16; c += 128) {
-      const int h = c >> 4;
-      const int d0 = (c & 15) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (h < G)
-        v = __ldg(reinterpret_cast<const uint4*>(
-            p.q + (static_cast<int64_t>(b) * p.Hq + kh * G + h) * 128 + d0));
-      *reinterpret_cast<uint4*>(smem + S::kQ + kmaj16_off(h, d0)) = v;
+    if constexpr (F8) {
+      // each head's query row to E4M3 with its own scale (amax / 448); warp w
+      // takes rows w, w + 4, ...: lane l holds d = 4l .. 4l + 3
+      float* qs = reinterpret_cast<float*>(smem + S::kQs);
+      for (int h = warp; h < kTcN; h += 4) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (h < G) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(
+              p.q + (static_cast<int64_t>(b) * p.Hq + kh * G + h) * 128 + 4 * lane));
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+          const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+          x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
+        }
+        float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float inv = m > 0.f ? 448.f / m : 1.f;
+        if (lane == 0) qs[h] = m > 0.f ? m / 448.f : 1.f;
+        const uint32_t q4 = ptx::pack_e4m3x4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv);
+        *reinterpret_cast<uint32_t*>(smem + S::kQ + kmaj16_off8(h, 4 * lane)) = q4;
+      }
+    } else {
+      // the group's query rows as the K-major B operand of S^T; rows past G zero
+      for (int c = threadIdx.x; c < kTcN * 16; c += 128) {
+        const int h = c >> 4;
+        const int d0 = (c & 15) * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (h < G)
+          v = __ldg(reinterpret_cast<const uint4*>(
+              p.q + (static_cast<int64_t>(b) * p.Hq + kh * G + h) * 128 + d0));
+        *reinterpret_cast<uint4*>(smem + S::kQ + kmaj16_off(h, d0)) = v;
+      }
     }
     ptx::fence_proxy_async_smem();
   }
@@ -413,23 +458,28 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
     ptx::prefetch_tmap(&tm_v);
     int issued = 0;
     for (int i = 0; i < 2 * nt; ++i) {
-      const int slot = i & 1;
-      if (i >= 2 && !ptx::mbar_wait(bar(TB_EMPTY + slot), ((i >> 1) - 1) & 1, s_abort,
-                                    p.wait_limit_ns)) {
+      const int slot = i % NSL;
+      if (i >= NSL && !ptx::mbar_wait(bar(TB_EMPTY + slot), ((i / NSL) - 1) & 1, s_abort,
+                                      p.wait_limit_ns)) {
         ptx::record_timeout(p.status, s_abort, 0x9100 + i);
         break;
       }
-      const CUtensorMap* tm = i < nt ? &tm_k : &tm_v;
+      const bool is_k = i < nt;
       const int row = row0 + (i % nt) * 128;
       ptx::mbar_arrive_expect_tx(bar(TB_FULL + slot), S::kTile);
-      for (int blk = 0; blk < 2; ++blk)
-        ptx::tma_load_3d(sRing + slot * S::kTile + blk * 16384, tm, bar(TB_FULL + slot), blk * 64,
-                         kh, row);
+      if (F8 && !is_k) {
+        // V^T box: 128 keys (bytes) x 128 d rows of head kh
+        ptx::tma_load_3d(sRing + slot * S::kTile, &tm_v, bar(TB_FULL + slot), row, 0, kh);
+      } else {
+        for (int blk = 0; blk < (F8 ? 1 : 2); ++blk)
+          ptx::tma_load_3d(sRing + slot * S::kTile + blk * 16384, is_k ? &tm_k : &tm_v,
+                           bar(TB_FULL + slot), blk * 64, kh, row);
+      }
       issued = i + 1;
     }
     // every issued copy must land before the CTA may exit
-    for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-      ptx::mbar_wait(bar(TB_FULL + (i & 1)), (i >> 1) & 1, &never, p.wait_limit_ns);
+    for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
+      ptx::mbar_wait(bar(TB_FULL + (i % NSL)), (i / NSL) & 1, &never, p.wait_limit_ns);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t leader = ptx::elect_one();
@@ -438,22 +488,34 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
       if (!w_ok && leader) ptx::record_timeout(p.status, s_abort, where);
       return __all_sync(0xffffffffu, w_ok);
     };
-    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, kTcN, 0, 0);  // K-major A and B
-    constexpr uint32_t idesc_o = ptx::idesc_bf16(128, kTcN, 1, 0);  // A (V^T) MN-major
+    // bf16: K-major A and B for S^T, MN-major A (V) for O^T. E4M3 (format 0
+    // of kind::f8f6f4): K-major everywhere (V arrives as V^T)
+    constexpr uint32_t idesc_s = F8 ? ptx::idesc_f16kind(128, kTcN, 0, 0, 0u)
+                                    : ptx::idesc_bf16(128, kTcN, 0, 0);
+    constexpr uint32_t idesc_o = F8 ? ptx::idesc_f16kind(128, kTcN, 0, 0, 0u)
+                                    : ptx::idesc_bf16(128, kTcN, 1, 0);
     const uint64_t dQ = ptx::sdesc_sw128(sQ, 16, 1024);
     const uint64_t dP = ptx::sdesc_sw128(sP, 16, 1024);
     bool ok = true;
     for (int t = 0; ok && t < nt; ++t) {
-      const int slot = t & 1;
-      if (!wait_w(bar(TB_FULL + slot), (t >> 1) & 1, 0x9200 + t)) { ok = false; break; }
+      const int slot = t % NSL;
+      if (!wait_w(bar(TB_FULL + slot), (t / NSL) & 1, 0x9200 + t)) { ok = false; break; }
       ptx::tc_fence_after();
-      // K tile [128 keys][128 d] in two 64-column blocks of 16 KB
       const uint64_t dK = ptx::sdesc_sw128(sRing + slot * S::kTile, 16, 1024);
+      if constexpr (F8) {
+        // K tile [128 keys][128 d bytes]: one swizzle atom, 32 d per MMA
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        ptx::mma_ss_w(tmem + kTcN * t, ptx::sdesc_add(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
-                      ptx::sdesc_add(dQ, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s,
-                      kk > 0 ? 1u : 0u, leader);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_ss_f8_w(tmem + kTcN * t, ptx::sdesc_add(dK, kk * 32),
+                           ptx::sdesc_add(dQ, kk * 32), idesc_s, kk > 0 ? 1u : 0u, leader);
+      } else {
+        // K tile [128 keys][128 d] in two 64-column blocks of 16 KB
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_ss_w(tmem + kTcN * t, ptx::sdesc_add(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
+                        ptx::sdesc_add(dQ, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s,
+                        kk > 0 ? 1u : 0u, leader);
+      }
       ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
     }
     ptx::mma_commit_w(bar(TB_S), leader);
@@ -461,17 +523,29 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
     if (ok) ptx::tc_fence_after();
     for (int t = 0; ok && t < nt; ++t) {
       const int i = nt + t;
-      const int slot = i & 1;
-      if (!wait_w(bar(TB_FULL + slot), (i >> 1) & 1, 0x9400 + t)) { ok = false; break; }
+      const int slot = i % NSL;
+      if (!wait_w(bar(TB_FULL + slot), (i / NSL) & 1, 0x9400 + t)) { ok = false; break; }
       ptx::tc_fence_after();
-      // V tile as the MN-major A of O^T (M = d: d 64..127 at +16 KB; K = keys,
-      // 16 keys = 2 KB per step); P as the K-major B, 64 keys per 2 KB block
-      const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16384, 1024);
+      if constexpr (F8) {
+        // V^T tile [128 d][128 keys bytes] as the K-major A; P as the K-major
+        // B, 128 keys per 2 KB block, 32 keys per MMA
+        const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        ptx::mma_ss_w(tmem + 64, ptx::sdesc_add(dV, kk * 2048),
-                      ptx::sdesc_add(dP, (2 * t + (kk >> 2)) * 2048 + (kk & 3) * 32), idesc_o,
-                      (t > 0 || kk > 0) ? 1u : 0u, leader);
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_ss_f8_w(tmem + 64, ptx::sdesc_add(dV, kk * 32),
+                           ptx::sdesc_add(dP, t * 2048 + kk * 32), idesc_o,
+                           (t > 0 || kk > 0) ? 1u : 0u, leader);
+      } else {
+        // V tile as the MN-major A of O^T (M = d: d 64..127 at +16 KB; K =
+        // keys, 16 keys = 2 KB per step); P as the K-major B, 64 keys per 2 KB
+        // block
+        const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_ss_w(tmem + 64, ptx::sdesc_add(dV, kk * 2048),
+                        ptx::sdesc_add(dP, (2 * t + (kk >> 2)) * 2048 + (kk & 3) * 32), idesc_o,
+                        (t > 0 || kk > 0) ? 1u : 0u, leader);
+      }
       ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
     }
     ptx::mma_commit_w(bar(TB_O), leader);
@@ -487,13 +561,24 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
     float M[kTcN], l[kTcN];
     if (__all_sync(0xffffffffu, ok)) {
       ptx::tc_fence_after();
+      // base-2 score factor per head (E4M3: times the query row's and K's
+      // descale factors)
+      float sf[kTcN];
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) sf[h] = p.scale_log2;
+      if constexpr (F8) {
+        const float* qs = reinterpret_cast<const float*>(smem + S::kQs);
+        const float sk = __ldg(p.kv_scales);
+#pragma unroll
+        for (int h = 0; h < kTcN; ++h) sf[h] *= qs[h] * sk;
+      }
 #pragma unroll
       for (int i = 0; i < kTcMaxTiles; ++i) {
         if (i < nt) {
           uint32_t r[16];
           ptx::tmem_ld16(tmem + lane_base + kTcN * i, r);
 #pragma unroll
-          for (int h = 0; h < kTcN; ++h) x[i][h] = __uint_as_float(r[h]) * p.scale_log2;
+          for (int h = 0; h < kTcN; ++h) x[i][h] = __uint_as_float(r[h]) * sf[h];
         } else {
 #pragma unroll
           for (int h = 0; h < kTcN; ++h) x[i][h] = -INFINITY;
@@ -529,8 +614,14 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
           if (i < nt) {
             const float e = ptx::ex2(x[i][h] - M[h]);
             sum += e;
-            *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h, i * 128 + t)) =
-                __float2bfloat16_rn(e);
+            if constexpr (F8) {
+              // 2^8 P <= 256: probabilities down to 2^-14 stay normal
+              smem[S::kP + kmaj16_off8(h, i * 128 + t)] =
+                  static_cast<uint8_t>(ptx::pack_e4m3x4(e * 256.f, 0.f, 0.f, 0.f) & 0xFFu);
+            } else {
+              *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h, i * 128 + t)) =
+                  __float2bfloat16_rn(e);
+            }
           }
         }
 #pragma unroll
@@ -559,10 +650,12 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
       uint32_t r[16];
       ptx::tmem_ld16(tmem + lane_base + 64, r);
       const int64_t obase = (static_cast<int64_t>(part) * p.B + b) * p.Hq + kh * G;
+      // E4M3: O^T carries 2^8 of P and V's descale factor
+      const float oscale = F8 ? __ldg(p.kv_scales + 1) * (1.f / 256.f) : 1.f;
 #pragma unroll
       for (int h = 0; h < kTcN; ++h) {
         if (h < G) {
-          p.o_part[(obase + h) * 128 + t] = __uint_as_float(r[h]) / l[h];
+          p.o_part[(obase + h) * 128 + t] = __uint_as_float(r[h]) * oscale / l[h];
           if (t == h)
             p.lse_part[(static_cast<int64_t>(part) * p.Hq + kh * G + h) * p.B + b] =
                 (M[h] + ptx::lg2(l[h])) * kLn2d;
@@ -627,24 +720,29 @@ cp_attn_status decode_status_address(int32_t** out) {
   return CP_ATTN_OK;
 }
 
+// F8: k is E4M3 [B*kv_len][Hkv][128], v the E4M3 V^T [Hkv][128][B*kv_len].
+template <bool F8>
 cp_attn_status launch_tc(const void* k, const void* v, const DecTcParams& p, int parts,
                          cudaStream_t s) {
   CUtensorMap tk, tv;
   const int64_t rows = static_cast<int64_t>(p.B) * p.kv_len;
-  cp_attn_status st = encode_bf16_rows_map(&tk, k, rows, p.Hkv, 128);
+  cp_attn_status st = F8 ? encode_u8_map(&tk, k, rows, p.Hkv, 128, false)
+                         : encode_bf16_rows_map(&tk, k, rows, p.Hkv, 128);
   if (st != CP_ATTN_OK) return st;
-  if ((st = encode_bf16_rows_map(&tv, v, rows, p.Hkv, 128)) != CP_ATTN_OK) return st;
-  const size_t smem = DecTcSmem::kBytes;
+  if ((st = F8 ? encode_u8_map(&tv, v, rows, p.Hkv, 128, true)
+               : encode_bf16_rows_map(&tv, v, rows, p.Hkv, 128)) != CP_ATTN_OK)
+    return st;
+  const size_t smem = DecTcSmem<F8>::kBytes;
   static bool attr = false;
   if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel,
+    const cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<F8>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
     if (err != cudaSuccess)
       return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc attr: ") + cudaGetErrorString(err));
     attr = true;
   }
-  decode_tc_kernel<<<dim3(parts, p.Hkv, p.B), kTcThreads, smem, s>>>(tk, tv, p);
+  decode_tc_kernel<F8><<<dim3(parts, p.Hkv, p.B), kTcThreads, smem, s>>>(tk, tv, p);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc: ") + cudaGetErrorString(err));
   count_launch();
@@ -766,7 +864,8 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
     tp.scale_log2 = p.scale_log2;
     tp.wait_limit_ns = 1000000000ull;
     if ((st = cpa::decode_status_address(&tp.status)) != CP_ATTN_OK) return st;
-    st = cpa::launch_tc(k, v, tp, np, s);
+    tp.kv_scales = nullptr;
+    st = cpa::launch_tc<false>(k, v, tp, np, s);
   } else if (desc->head_dim == 128) {
     st = G <= 4 ? cpa::launch<128, 1>(p, np, s) : G <= 8 ? cpa::launch<128, 2>(p, np, s)
                                                           : cpa::launch<128, 4>(p, np, s);
@@ -778,6 +877,56 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
   // Pass Q's merge over every rank's (and run's) partial
   return cpa::launch_merge_lse(np, desc->batch, desc->n_q_heads, desc->head_dim, o_part,
                                rows * desc->head_dim, lse_part, rows,
+                               static_cast<__nv_bfloat16*>(o), nullptr, lse, s);
+}
+
+cp_attn_status cp_attn_decode_fp8(const cp_attn_decode_desc* desc, const void* q, const void* k8,
+                                  const void* vt8, const float* kv_scales, void* o, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  cpa::clear_error();
+  size_t need = 0;
+  cp_attn_status st = cp_attn_decode_workspace_size(desc, &need);
+  if (st != CP_ATTN_OK) return st;
+  if (desc->head_dim != 128)
+    return cpa::fail(CP_ATTN_ERR_UNSUPPORTED, "decode_fp8: head_dim must be 128");
+  if (!q || !k8 || !vt8 || !kv_scales || !o || !lse || !workspace)
+    return cpa::fail(CP_ATTN_ERR_INVALID_ARG, "decode_fp8: null pointer");
+  for (const void* ptr : {q, k8, vt8, static_cast<const void*>(kv_scales),
+                          static_cast<const void*>(o), static_cast<const void*>(lse),
+                          static_cast<const void*>(workspace)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16)
+      return cpa::fail(CP_ATTN_ERR_INVALID_ARG, "decode_fp8: pointers must be 16-byte aligned");
+  if (workspace_bytes < need) return cpa::fail(CP_ATTN_ERR_SHAPE, "decode_fp8: workspace too small");
+  const int64_t parts = cpa::n_parts(desc);
+  const int L = static_cast<int>(desc->kv_len / parts);
+  if (L % 128 || static_cast<int64_t>(desc->batch) * desc->kv_len > 0x7fffffff)
+    return cpa::fail(CP_ATTN_ERR_SHAPE,
+                     "decode_fp8: kv_len / cp must be a multiple of 128 and batch * kv_len < 2^31");
+  const int G = desc->n_q_heads / desc->n_kv_heads;
+  const int64_t rows = static_cast<int64_t>(desc->batch) * desc->n_q_heads;
+  const size_t o_bytes = static_cast<size_t>(parts * rows * desc->head_dim) * 4;
+  cpa::DecTcParams tp;
+  tp.q = static_cast<const __nv_bfloat16*>(q);
+  tp.o_part = static_cast<float*>(workspace);
+  tp.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+  tp.B = desc->batch;
+  tp.Hq = desc->n_q_heads;
+  tp.Hkv = desc->n_kv_heads;
+  tp.G = G;
+  tp.kv_len = desc->kv_len;
+  tp.L = L;
+  const float scale = desc->softmax_scale > 0.f
+                          ? desc->softmax_scale
+                          : static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->head_dim)));
+  tp.scale_log2 = scale * cpa::kLog2ed;
+  tp.wait_limit_ns = 1000000000ull;
+  tp.kv_scales = kv_scales;
+  if ((st = cpa::decode_status_address(&tp.status)) != CP_ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int np = static_cast<int>(parts);
+  if ((st = cpa::launch_tc<true>(k8, vt8, tp, np, s)) != CP_ATTN_OK) return st;
+  return cpa::launch_merge_lse(np, desc->batch, desc->n_q_heads, desc->head_dim, tp.o_part,
+                               rows * desc->head_dim, tp.lse_part, rows,
                                static_cast<__nv_bfloat16*>(o), nullptr, lse, s);
 }
 

@@ -116,6 +116,10 @@ cp_attn_status launch_zero_f32(float* p, int64_t n, cudaStream_t s);
 // [rows, heads, d] bf16 tensor map, 64 x 1 x 128 boxes, 128-byte swizzle (api.cu).
 cp_attn_status encode_bf16_rows_map(CUtensorMap* m, const void* base, int64_t rows, int heads,
                                     int d);
+// One-byte tensor map: [rows, heads, d] with d x 1 x 128 boxes, or transposed
+// [heads, d, rows] with 128 x d x 1 boxes; 128-byte swizzle (api.cu).
+cp_attn_status encode_u8_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int d,
+                             bool transposed);
 
 cp_attn_status launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);
 

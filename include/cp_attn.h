@@ -441,6 +441,23 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
  * wait there, CP_ATTN_ERR_TIMEOUT). Returns CP_ATTN_OK or that error. */
 cp_attn_status cp_attn_decode_sync_status(void* stream);
 
+/* cp_attn_decode over an E4M3 KV cache (the pages' FP8-quantized model,
+ * "Experimental Setup & Results"), head_dim 128, on the tensor cores.
+ * q: bf16 [batch][n_q_heads][128]; each head's row is quantized to E4M3 in the
+ *   kernel with its own scale (max|row| / 448, the per-tensor rule of
+ *   cp_attn_fp8_quantize applied per row).
+ * k8: E4M3 [batch * kv_len][n_kv_heads][128] and vt8: E4M3 V^T
+ *   [n_kv_heads][128][batch * kv_len] (cp_attn_fp8_quantize of K with
+ *   transpose 0 and of V with transpose 1, rows = batch * kv_len);
+ *   kv_scales: device [2] floats, their descale factors (K, V).
+ * P is rounded to E4M3 (after scaling by 2^8) for P V; sums, LSE and
+ * accumulation stay fp32. Outputs, workspace and errors as cp_attn_decode;
+ * also ERR_UNSUPPORTED for head_dim != 128 and ERR_SHAPE unless kv_len / cp is
+ * a multiple of 128 and batch * kv_len < 2^31. */
+cp_attn_status cp_attn_decode_fp8(const cp_attn_decode_desc* desc, const void* q, const void* k8,
+                                  const void* vt8, const float* kv_scales, void* o, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the plan's device status word.
  * Returns CP_ATTN_OK or the first device-side error (ERR_TIMEOUT). */
 cp_attn_status cp_attn_sync_status(cp_attn_plan_t plan, void* stream);
