@@ -96,7 +96,7 @@ __device__ __forceinline__ void stage_tile(uint32_t tile, const __nv_bfloat16* s
 template <int D, int HPG>  // HPG: query heads per thread-key in the score phase (1, 2, 4)
 __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecParams p) {
   using S = DecSmem<D>;
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   float* q_s = reinterpret_cast<float*>(smem + S::kQ);
   float* s_s = reinterpret_cast<float*>(smem + S::kS);
   float* o_s = reinterpret_cast<float*>(smem + S::kO);
@@ -290,16 +290,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecPa
 // N = 16 side of two products per 128-key tile, both accumulated in TMEM:
 //   S^T  = K Q^T    (M = 128 keys, N = 16 heads, K = d)
 //   O^T += V^T P^T  (M = d, N = 16 heads, K = keys)
-// The K tiles and then the V tiles of the run stream through a two-slot TMA
-// ring. The whole run's scores fit in TMEM (16 columns per tile), so the
-// softmax is one pass between the two products: per head, the maximum and
-// the sum over the run, reduced across the four softmax warps through shared
-// memory. P goes to shared memory in bf16 as the B operand of O^T. Query rows
-// past G are zero and their columns are ignored.
-// Warps: 0-3 softmax and epilogue (thread = key of a tile, then column of d),
-// 4 TMA producer, 5 TMEM owner and MMA issuer. About 85 KB of shared memory,
-// so two CTAs share an SM.
-constexpr int kTcThreads = 192;
+// The K tiles and then the V tiles of the run stream through a TMA ring (two
+// 32 KB slots for bf16, four 16 KB slots for E4M3); the producer starts the
+// first slots' loads before the block's setup barrier. The whole run's scores
+// fit in TMEM (16 columns per tile), so the softmax is one pass between the
+// two products: per head, the maximum and the sum over the run, reduced
+// across the four warps that hold its keys through shared memory. P goes to
+// shared memory as the B operand of O^T. Query rows past G are zero; only the
+// group's heads, rounded up to 4, 8 or 16, go through the softmax.
+// Warps: SW softmax and epilogue warps (4, or 8 for 16 heads: warp w holds
+// keys / columns of d 32 (w mod 4) .. +31 and a quarter or half of the
+// heads), then the TMA producer and the TMEM owner and MMA issuer. 77 KB
+// (E4M3) or 87 KB (bf16) of shared memory: two CTAs share an SM, three for
+// E4M3 when the group has at most four heads.
 constexpr int kTcN = 16;                    // MMA N: the query heads, padded
 constexpr int kTcMaxTiles = kDecMaxL / 128;
 
@@ -360,16 +363,48 @@ __device__ __forceinline__ uint32_t kmaj16_off(int row, int col) {
   return static_cast<uint32_t>((col >> 6) * 2048 + row * 128 + (chunk << 4) + ((col & 7) << 1));
 }
 
+// Tile i of a run of nt K tiles and then nt V tiles (rows row0 + 128 (i mod
+// nt) of KV head kh) into ring slot i mod kSlots, completing on that slot's
+// full barrier.
+template <bool F8>
+__device__ __forceinline__ void dec_issue_tile(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                               uint32_t ring, uint32_t bar0, int i, int nt,
+                                               int row0, int kh) {
+  using S = DecTcSmem<F8>;
+  const int slot = i % S::kSlots;
+  const uint32_t full = bar0 + 8u * static_cast<uint32_t>(TB_FULL + slot);
+  const int row = row0 + (i % nt) * 128;
+  ptx::mbar_arrive_expect_tx(full, S::kTile);
+  if (F8 && i >= nt) {
+    // V^T box: 128 keys (bytes) x 128 d rows of head kh
+    ptx::tma_load_3d(ring + slot * S::kTile, tm_v, full, row, 0, kh);
+  } else {
+#pragma unroll
+    for (int blk = 0; blk < (F8 ? 1 : 2); ++blk)
+      ptx::tma_load_3d(ring + slot * S::kTile + blk * 16384, i < nt ? tm_k : tm_v, full, blk * 64,
+                       kh, row);
+  }
+}
+
 // F8: tm_k maps E4M3 K [B*kv_len][Hkv][128] (128-byte boxes), tm_v maps V^T
 // E4M3 [Hkv][128][B*kv_len]; each head's query row is quantized here with its
 // own scale, S^T and O^T are kind::f8f6f4 with K = 32, and P goes to shared
 // memory as E4M3 scaled by 2^8 (P <= 1 against the run's exact maximum).
-template <bool F8>
-__global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
+// Softmax warps of the tensor-core decode: eight (two groups of four, eight
+// heads each) when all 16 columns of N are heads, else four.
+constexpr int dec_softmax_warps(int nh) { return nh == 16 ? 8 : 4; }
+
+// NH: the group's query heads rounded up to 4, 8 or 16 (a compile-time
+// count, so that the per-head softmax chains interleave without branches);
+// columns past NH are padding of N and are never read.
+template <bool F8, int NH>
+__global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const DecTcParams p) {
   using S = DecTcSmem<F8>;
   constexpr int NSL = S::kSlots;
+  constexpr int SW = dec_softmax_warps(NH);  // softmax warps; then the producer, the MMA warp
+  constexpr int HPW = NH * 4 / SW;           // heads per softmax warp
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
   if (sbase & 1023u) {
@@ -400,30 +435,48 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
   const int row0 = static_cast<int>(static_cast<int64_t>(b) * p.kv_len +
                                     static_cast<int64_t>(part) * p.L);
 
-  if (threadIdx.x == 0) {
+  const int n_first = 2 * nt < NSL ? 2 * nt : NSL;  // tiles that need no free slot
+  if (warp == SW && lane == 0) {
+    // the producer sets up the barriers itself and starts the first ring of
+    // loads at once, so that they overlap the query rows and the TMEM
+    // allocation; nobody else touches a barrier before the block barrier
     for (int i = 0; i < TB_COUNT; ++i)
-      ptx::mbar_init(bar(i), (i == TB_P || i == TB_RED) ? 128u : 1u);
+      ptx::mbar_init(bar(i), (i == TB_P || i == TB_RED) ? 32u * SW : 1u);
     *s_abort = 0;
     ptx::fence_barrier_init();
+    for (int i = 0; i < n_first; ++i) dec_issue_tile<F8>(&tm_k, &tm_v, sRing, bar0, i, nt, row0, kh);
   }
-  if (warp == 5) {
+  if (warp == SW + 1) {
     ptx::tmem_alloc(ptx::smem_u32(s_tmem), 128);
     ptx::tmem_relinquish();
   }
-  if (warp < 4) {
+  // E4M3 descale factors of K and V, loaded before they are needed
+  float kv_sk = 1.f, kv_sv = 1.f;
+  if (F8 && warp < SW) {
+    kv_sk = __ldg(p.kv_scales);
+    kv_sv = __ldg(p.kv_scales + 1);
+  }
+  if (warp < SW) {
     if constexpr (F8) {
       // each head's query row to E4M3 with its own scale (amax / 448); warp w
-      // takes rows w, w + 4, ...: lane l holds d = 4l .. 4l + 3
+      // takes rows w, w + SW, ...: lane l holds d = 4l .. 4l + 3
       float* qs = reinterpret_cast<float*>(smem + S::kQs);
-      for (int h = warp; h < kTcN; h += 4) {
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (h < G) {
-          const uint2 u = __ldg(reinterpret_cast<const uint2*>(
+      // all of the warp's rows' loads first, so that their latencies overlap
+      uint2 u[kTcN / SW];
+#pragma unroll
+      for (int j = 0; j < kTcN / SW; ++j) {
+        const int h = warp + SW * j;
+        u[j] = make_uint2(0u, 0u);
+        if (h < G)
+          u[j] = __ldg(reinterpret_cast<const uint2*>(
               p.q + (static_cast<int64_t>(b) * p.Hq + kh * G + h) * 128 + 4 * lane));
-          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-          const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-          x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
-        }
+      }
+#pragma unroll
+      for (int j = 0; j < kTcN / SW; ++j) {
+        const int h = warp + SW * j;
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j].x));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j].y));
+        const float x[4] = {a.x, a.y, c.x, c.y};
         float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -434,14 +487,20 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
       }
     } else {
       // the group's query rows as the K-major B operand of S^T; rows past G zero
-      for (int c = threadIdx.x; c < kTcN * 16; c += 128) {
+      uint4 v[kTcN * 16 / (32 * SW)];
+#pragma unroll
+      for (int j = 0; j < kTcN * 16 / (32 * SW); ++j) {
+        const int c = threadIdx.x + 32 * SW * j;
         const int h = c >> 4;
-        const int d0 = (c & 15) * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
         if (h < G)
-          v = __ldg(reinterpret_cast<const uint4*>(
-              p.q + (static_cast<int64_t>(b) * p.Hq + kh * G + h) * 128 + d0));
-        *reinterpret_cast<uint4*>(smem + S::kQ + kmaj16_off(h, d0)) = v;
+          v[j] = __ldg(reinterpret_cast<const uint4*>(
+              p.q + (static_cast<int64_t>(b) * p.Hq + kh * G + h) * 128 + (c & 15) * 8));
+      }
+#pragma unroll
+      for (int j = 0; j < kTcN * 16 / (32 * SW); ++j) {
+        const int c = threadIdx.x + 32 * SW * j;
+        *reinterpret_cast<uint4*>(smem + S::kQ + kmaj16_off(c >> 4, (c & 15) * 8)) = v[j];
       }
     }
     ptx::fence_proxy_async_smem();
@@ -452,35 +511,23 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
   const uint32_t tmem = *s_tmem;
   const volatile int never = 0;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == SW && lane == 0) {
     // ------------------------------------------------------------ producer
-    ptx::prefetch_tmap(&tm_k);
-    ptx::prefetch_tmap(&tm_v);
-    int issued = 0;
-    for (int i = 0; i < 2 * nt; ++i) {
+    // tiles [0, n_first) were issued before the block barrier
+    int issued = n_first;
+    for (int i = n_first; i < 2 * nt; ++i) {
       const int slot = i % NSL;
-      if (i >= NSL && !ptx::mbar_wait(bar(TB_EMPTY + slot), ((i / NSL) - 1) & 1, s_abort,
-                                      p.wait_limit_ns)) {
+      if (!ptx::mbar_wait(bar(TB_EMPTY + slot), ((i / NSL) - 1) & 1, s_abort, p.wait_limit_ns)) {
         ptx::record_timeout(p.status, s_abort, 0x9100 + i);
         break;
       }
-      const bool is_k = i < nt;
-      const int row = row0 + (i % nt) * 128;
-      ptx::mbar_arrive_expect_tx(bar(TB_FULL + slot), S::kTile);
-      if (F8 && !is_k) {
-        // V^T box: 128 keys (bytes) x 128 d rows of head kh
-        ptx::tma_load_3d(sRing + slot * S::kTile, &tm_v, bar(TB_FULL + slot), row, 0, kh);
-      } else {
-        for (int blk = 0; blk < (F8 ? 1 : 2); ++blk)
-          ptx::tma_load_3d(sRing + slot * S::kTile + blk * 16384, is_k ? &tm_k : &tm_v,
-                           bar(TB_FULL + slot), blk * 64, kh, row);
-      }
+      dec_issue_tile<F8>(&tm_k, &tm_v, sRing, bar0, i, nt, row0, kh);
       issued = i + 1;
     }
     // every issued copy must land before the CTA may exit
     for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
       ptx::mbar_wait(bar(TB_FULL + (i % NSL)), (i / NSL) & 1, &never, p.wait_limit_ns);
-  } else if (warp == 5) {
+  } else if (warp == SW + 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t leader = ptx::elect_one();
     auto wait_w = [&](uint32_t b_, uint32_t parity, int where) -> bool {
@@ -551,42 +598,48 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
     ptx::mma_commit_w(bar(TB_O), leader);
     ptx::mbar_wait(bar(TB_O), 0, &never, p.wait_limit_ns);
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < SW) {
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x;  // key of each tile, then column of d
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // warp w: TMEM lanes 32 (w mod 4) .. +31 (key of each tile, then column
+    // of d) and heads [h0, h0 + HPW)
+    const int t = threadIdx.x & 127;
+    const int qw = warp & 3;
+    const int h0 = (warp >> 2) * HPW;
+    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
     bool ok = ptx::mbar_wait(bar(TB_S), 0, s_abort, p.wait_limit_ns);
     if (!ok) ptx::record_timeout(p.status, s_abort, 0x9500);
-    float x[kTcMaxTiles][kTcN];
-    float M[kTcN], l[kTcN];
+    float x[kTcMaxTiles][HPW];
+    float M[HPW], l[HPW];
     if (__all_sync(0xffffffffu, ok)) {
       ptx::tc_fence_after();
       // base-2 score factor per head (E4M3: times the query row's and K's
       // descale factors)
-      float sf[kTcN];
+      float sf[HPW];
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) sf[h] = p.scale_log2;
+      for (int h = 0; h < HPW; ++h) sf[h] = p.scale_log2;
       if constexpr (F8) {
         const float* qs = reinterpret_cast<const float*>(smem + S::kQs);
-        const float sk = __ldg(p.kv_scales);
 #pragma unroll
-        for (int h = 0; h < kTcN; ++h) sf[h] *= qs[h] * sk;
+        for (int h = 0; h < HPW; ++h) sf[h] *= qs[h0 + h] * kv_sk;
       }
 #pragma unroll
       for (int i = 0; i < kTcMaxTiles; ++i) {
         if (i < nt) {
-          uint32_t r[16];
-          ptx::tmem_ld16(tmem + lane_base + kTcN * i, r);
+          uint32_t r[HPW];
+          ptx::tmem_ld_n<HPW>(tmem + lane_base + kTcN * i + h0, r);
 #pragma unroll
-          for (int h = 0; h < kTcN; ++h) x[i][h] = __uint_as_float(r[h]) * sf[h];
+          for (int h = 0; h < HPW; ++h) x[i][h] = __uint_as_float(r[h]) * sf[h];
         } else {
 #pragma unroll
-          for (int h = 0; h < kTcN; ++h) x[i][h] = -INFINITY;
+          for (int h = 0; h < HPW; ++h) x[i][h] = -INFINITY;
         }
       }
-      // per head: maximum over the thread's keys, the warp, then the 4 warps
+      // per head: maximum over the thread's keys, the warp, then the four
+      // warps of the head's group. Columns past NH are skipped here and
+      // below: their P is left as it is and only feeds O^T columns that are
+      // never read.
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) {
+      for (int h = 0; h < HPW; ++h) {
         float m = x[0][h];
 #pragma unroll
         for (int i = 1; i < kTcMaxTiles; ++i) m = fmaxf(m, x[i][h]);
@@ -595,19 +648,21 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
         M[h] = m;
       }
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h)
-        if (lane == h) red[warp * kTcN + h] = M[h];
+      for (int h = 0; h < HPW; ++h)
+        if (lane == h) red[qw * kTcN + h0 + h] = M[h];
       ptx::mbar_arrive(bar(TB_RED));
       ok = ptx::mbar_wait(bar(TB_RED), 0, s_abort, p.wait_limit_ns);
       if (!ok) ptx::record_timeout(p.status, s_abort, 0x9600);
     }
     if (__all_sync(0xffffffffu, ok)) {
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h)
-        M[h] = fmaxf(fmaxf(red[h], red[kTcN + h]), fmaxf(red[2 * kTcN + h], red[3 * kTcN + h]));
-      // P = 2^(x - M) (bf16 into shared memory) and the per-head sums
+      for (int h = 0; h < HPW; ++h) {
+        const int hh = h0 + h;
+        M[h] = fmaxf(fmaxf(red[hh], red[kTcN + hh]), fmaxf(red[2 * kTcN + hh], red[3 * kTcN + hh]));
+      }
+      // P = 2^(x - M) (bf16 or E4M3 into shared memory) and the per-head sums
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) {
+      for (int h = 0; h < HPW; ++h) {
         float sum = 0.f;
 #pragma unroll
         for (int i = 0; i < kTcMaxTiles; ++i) {
@@ -616,10 +671,10 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
             sum += e;
             if constexpr (F8) {
               // 2^8 P <= 256: probabilities down to 2^-14 stay normal
-              smem[S::kP + kmaj16_off8(h, i * 128 + t)] =
+              smem[S::kP + kmaj16_off8(h0 + h, i * 128 + t)] =
                   static_cast<uint8_t>(ptx::pack_e4m3x4(e * 256.f, 0.f, 0.f, 0.f) & 0xFFu);
             } else {
-              *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h, i * 128 + t)) =
+              *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h0 + h, i * 128 + t)) =
                   __float2bfloat16_rn(e);
             }
           }
@@ -629,8 +684,8 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
         l[h] = sum;
       }
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h)
-        if (lane == h) red[4 * kTcN + warp * kTcN + h] = l[h];
+      for (int h = 0; h < HPW; ++h)
+        if (lane == h) red[4 * kTcN + qw * kTcN + h0 + h] = l[h];
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(bar(TB_P));
       ptx::mbar_arrive(bar(TB_RED));
@@ -640,24 +695,32 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
     if (__all_sync(0xffffffffu, ok)) {
       const float* rs = red + 4 * kTcN;
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) l[h] = (rs[h] + rs[kTcN + h]) + (rs[2 * kTcN + h] + rs[3 * kTcN + h]);
+      for (int h = 0; h < HPW; ++h) {
+        const int hh = h0 + h;
+        l[h] = (rs[hh] + rs[kTcN + hh]) + (rs[2 * kTcN + hh] + rs[3 * kTcN + hh]);
+      }
       ok = ptx::mbar_wait(bar(TB_O), 0, s_abort, p.wait_limit_ns);
       if (!ok) ptx::record_timeout(p.status, s_abort, 0x9800);
     }
     if (__all_sync(0xffffffffu, ok)) {
       ptx::tc_fence_after();
       // O^T: TMEM lane = column t of d, column h = query head
-      uint32_t r[16];
-      ptx::tmem_ld16(tmem + lane_base + 64, r);
+      uint32_t r[HPW];
+      ptx::tmem_ld_n<HPW>(tmem + lane_base + 64 + h0, r);
       const int64_t obase = (static_cast<int64_t>(part) * p.B + b) * p.Hq + kh * G;
-      // E4M3: O^T carries 2^8 of P and V's descale factor
-      const float oscale = F8 ? __ldg(p.kv_scales + 1) * (1.f / 256.f) : 1.f;
+      // E4M3: O^T carries 2^8 of P and V's descale factor. One correctly
+      // rounded reciprocal per head (the padded heads' sums are finite too)
+      const float oscale = F8 ? kv_sv * (1.f / 256.f) : 1.f;
+      float inv_l[HPW];
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) {
-        if (h < G) {
-          p.o_part[(obase + h) * 128 + t] = __uint_as_float(r[h]) * oscale / l[h];
-          if (t == h)
-            p.lse_part[(static_cast<int64_t>(part) * p.Hq + kh * G + h) * p.B + b] =
+      for (int h = 0; h < HPW; ++h) inv_l[h] = __frcp_rn(l[h]) * oscale;
+#pragma unroll
+      for (int h = 0; h < HPW; ++h) {
+        const int hh = h0 + h;
+        if (hh < G) {
+          p.o_part[(obase + hh) * 128 + t] = __uint_as_float(r[h]) * inv_l[h];
+          if (t == hh)
+            p.lse_part[(static_cast<int64_t>(part) * p.Hq + kh * G + hh) * p.B + b] =
                 (M[h] + ptx::lg2(l[h])) * kLn2d;
         }
       }
@@ -666,7 +729,7 @@ __global__ void __launch_bounds__(kTcThreads) decode_tc_kernel(
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == SW + 1) {
     __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 128);
@@ -733,16 +796,19 @@ cp_attn_status launch_tc(const void* k, const void* v, const DecTcParams& p, int
                : encode_bf16_rows_map(&tv, v, rows, p.Hkv, 128)) != CP_ATTN_OK)
     return st;
   const size_t smem = DecTcSmem<F8>::kBytes;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<F8>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int nh = p.G <= 4 ? 4 : p.G <= 8 ? 8 : 16;
+  auto kernel = nh == 4 ? decode_tc_kernel<F8, 4>
+                : nh == 8 ? decode_tc_kernel<F8, 8> : decode_tc_kernel<F8, 16>;
+  static bool attr[3] = {false, false, false};
+  const int ai = nh == 4 ? 0 : nh == 8 ? 1 : 2;
+  if (!attr[ai]) {
+    const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
     if (err != cudaSuccess)
       return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc attr: ") + cudaGetErrorString(err));
-    attr = true;
+    attr[ai] = true;
   }
-  decode_tc_kernel<F8><<<dim3(parts, p.Hkv, p.B), kTcThreads, smem, s>>>(tk, tv, p);
+  kernel<<<dim3(parts, p.Hkv, p.B), 32 * (dec_softmax_warps(nh) + 2), smem, s>>>(tk, tv, p);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc: ") + cudaGetErrorString(err));
   count_launch();

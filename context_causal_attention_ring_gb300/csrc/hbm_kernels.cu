@@ -88,48 +88,83 @@ __global__ void __launch_bounds__(256) merge_lse_kernel(
 }
 
 // The same merge for few (row, head) pairs and many parts (a decode row
-// merges every rank's and every run's partial): one CTA of 8 warps per (row,
-// head). Every warp computes the global L = M + log2 sum_i 2^(LSE_i - M)
-// (lanes split the parts), then sums w_i O_i over parts w, w + 8, ... for
-// its float4 chunk of d (d <= 128); warp 0 adds the 8 sums. The CTA reads
-// all parts before it writes, so o_out_f32 may alias part 0.
-__global__ void __launch_bounds__(256) merge_lse_wide_kernel(
+// merges every rank's and every run's partial): one block of 8 warps per
+// (row, head). The block first turns every part's LSE into its weight
+// 2^(LSE_i - L), L = M + log2 sum_i 2^(LSE_i - M), in shared memory (one
+// parallel pass for M, one for the sum); then each warp streams its share of
+// the parts' rows (float4 chunks of d <= 128), eight loads in flight, and
+// warp 0 adds the eight sums. A part whose weight is 0 (no visible key) is
+// never read into the sum. The block reads all parts before it writes, so
+// o_out_f32 may alias part 0.
+constexpr int kWideWarps = 8;
+constexpr int kWideMaxParts = 4096;
+constexpr int kWideUnroll = 8;
+
+__global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
     int n_parts, int64_t rows, int heads, int d, const float* __restrict__ o_parts,
     int64_t part_stride, const float* __restrict__ lse_parts, int64_t lse_part_stride,
     __nv_bfloat16* __restrict__ o_out, float* __restrict__ o_out_f32,
     float* __restrict__ lse_out) {
-  __shared__ float4 s_acc[8][32];
+  __shared__ float s_w[kWideMaxParts];
+  __shared__ float s_red[2][kWideWarps];
+  __shared__ float4 s_acc[kWideWarps][32];
   const int64_t pair = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t row = pair / heads;
   const int h = static_cast<int>(pair % heads);
   const int64_t lse_idx = static_cast<int64_t>(h) * rows + row;
+  // the parts' LSEs (base 2) and their maximum
   float M = -INFINITY;
-  for (int i = lane; i < n_parts; i += 32)
-    M = fmaxf(M, __ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e);
+  for (int i = threadIdx.x; i < n_parts; i += 32 * kWideWarps) {
+    const float v = __ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e;
+    s_w[i] = v;
+    M = fmaxf(M, v);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[0][warp] = M;
+  __syncthreads();
+  M = s_red[0][0];
+#pragma unroll
+  for (int w = 1; w < kWideWarps; ++w) M = fmaxf(M, s_red[0][w]);
   float L = -INFINITY;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t o_off = (row * heads + h) * static_cast<int64_t>(d);
   const bool has = lane < (d >> 2);
-  if (M != -INFINITY) {
+  if (M != -INFINITY) {  // uniform across the block
     float S = 0.f;
-    for (int i = lane; i < n_parts; i += 32)
-      S += ptx::ex2(__ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e - M);
+    for (int i = threadIdx.x; i < n_parts; i += 32 * kWideWarps) S += ptx::ex2(s_w[i] - M);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    if (lane == 0) s_red[1][warp] = S;
+    __syncthreads();
+    S = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWideWarps; ++w) S += s_red[1][w];
     L = M + ptx::lg2(S);
-    for (int i = warp; i < n_parts; i += 8) {
-      const float w = ptx::ex2(__ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e - L);
-      if (w == 0.f || !has) continue;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(o_parts + i * part_stride + o_off) +
-                             lane);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+    // each thread rewrites only the entries it read, so no barrier is needed
+    // between the reads above and these writes
+    for (int i = threadIdx.x; i < n_parts; i += 32 * kWideWarps) s_w[i] = ptx::ex2(s_w[i] - L);
+    __syncthreads();
+    for (int i0 = warp; i0 < n_parts; i0 += kWideWarps * kWideUnroll) {
+      float w[kWideUnroll];
+      float4 v[kWideUnroll];
+#pragma unroll
+      for (int u = 0; u < kWideUnroll; ++u) {
+        const int i = i0 + u * kWideWarps;
+        w[u] = i < n_parts ? s_w[i] : 0.f;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (w[u] != 0.f && has)
+          v[u] = __ldg(reinterpret_cast<const float4*>(o_parts + i * part_stride + o_off) + lane);
+      }
+#pragma unroll
+      for (int u = 0; u < kWideUnroll; ++u) {
+        acc.x = fmaf(w[u], v[u].x, acc.x);
+        acc.y = fmaf(w[u], v[u].y, acc.y);
+        acc.z = fmaf(w[u], v[u].z, acc.z);
+        acc.w = fmaf(w[u], v[u].w, acc.w);
+      }
     }
   }
   s_acc[warp][lane] = acc;
@@ -137,7 +172,7 @@ __global__ void __launch_bounds__(256) merge_lse_wide_kernel(
   if (warp == 0) {
     float4 t = s_acc[0][lane];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) {
+    for (int w = 1; w < kWideWarps; ++w) {
       const float4 u = s_acc[w][lane];
       t.x += u.x;
       t.y += u.y;
@@ -322,8 +357,8 @@ cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
   const int64_t warps = rows * heads;
   if (warps == 0) return CP_ATTN_OK;
   // few (row, head) pairs with many parts: eight warps per pair
-  if (d <= 128 && n_parts >= 16 && warps * 8 <= 152 * 64) {
-    merge_lse_wide_kernel<<<static_cast<unsigned>(warps), 256, 0, s>>>(
+  if (d <= 128 && n_parts >= 16 && n_parts <= kWideMaxParts && warps * kWideWarps <= 152 * 64) {
+    merge_lse_wide_kernel<<<static_cast<unsigned>(warps), 32 * kWideWarps, 0, s>>>(
         n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
         o_out_f32, lse_out);
     return check_launch("merge_lse");
