@@ -88,18 +88,19 @@ __global__ void __launch_bounds__(256) merge_lse_kernel(
 }
 
 // The same merge for few (row, head) pairs and many parts (a decode row
-// merges every rank's and every run's partial): one block of 8 warps per
+// merges every rank's and every run's partial): one block of 16 warps per
 // (row, head). The block first turns every part's LSE into its weight
 // 2^(LSE_i - L), L = M + log2 sum_i 2^(LSE_i - M), in shared memory (one
 // parallel pass for M, one for the sum); then each warp streams its share of
-// the parts' rows (float4 chunks of d <= 128), eight loads in flight, and
-// warp 0 adds the eight sums. A part whose weight is 0 (no visible key) is
+// the parts' rows (float4 chunks of d <= 128), up to sixteen loads in
+// flight, and warp 0 adds the sixteen sums. A part whose weight is 0 (no visible key) is
 // never read into the sum. The block reads all parts before it writes, so
 // o_out_f32 may alias part 0.
-constexpr int kWideWarps = 8;
+constexpr int kWideWarps = 16;
 constexpr int kWideMaxParts = 4096;
-constexpr int kWideUnroll = 8;
 
+// U: loads in flight per lane, about the parts per warp (4, 8 or 16).
+template <int U>
 __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
     int n_parts, int64_t rows, int heads, int d, const float* __restrict__ o_parts,
     int64_t part_stride, const float* __restrict__ lse_parts, int64_t lse_part_stride,
@@ -147,23 +148,29 @@ __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
     // between the reads above and these writes
     for (int i = threadIdx.x; i < n_parts; i += 32 * kWideWarps) s_w[i] = ptx::ex2(s_w[i] - L);
     __syncthreads();
-    for (int i0 = warp; i0 < n_parts; i0 += kWideWarps * kWideUnroll) {
-      float w[kWideUnroll];
-      float4 v[kWideUnroll];
+    // The loads are unconditional so that all of them are in flight at once:
+    // a part past the end reads the last part and a lane past d/4 reads
+    // chunk 0 (both in bounds); their weight is 0 or their sum is not
+    // stored. A zero weight adds 0 * 0, so rows that were never written
+    // cannot reach the sum.
+    const int l4 = has ? lane : 0;
+    for (int i0 = warp; i0 < n_parts; i0 += kWideWarps * U) {
+      float w[U];
+      float4 v[U];
 #pragma unroll
-      for (int u = 0; u < kWideUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int i = i0 + u * kWideWarps;
+        const int ic = i < n_parts ? i : n_parts - 1;
         w[u] = i < n_parts ? s_w[i] : 0.f;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (w[u] != 0.f && has)
-          v[u] = __ldg(reinterpret_cast<const float4*>(o_parts + i * part_stride + o_off) + lane);
+        v[u] = __ldg(reinterpret_cast<const float4*>(o_parts + ic * part_stride + o_off) + l4);
       }
 #pragma unroll
-      for (int u = 0; u < kWideUnroll; ++u) {
-        acc.x = fmaf(w[u], v[u].x, acc.x);
-        acc.y = fmaf(w[u], v[u].y, acc.y);
-        acc.z = fmaf(w[u], v[u].z, acc.z);
-        acc.w = fmaf(w[u], v[u].w, acc.w);
+      for (int u = 0; u < U; ++u) {
+        const bool use = w[u] != 0.f;
+        acc.x = fmaf(w[u], use ? v[u].x : 0.f, acc.x);
+        acc.y = fmaf(w[u], use ? v[u].y : 0.f, acc.y);
+        acc.z = fmaf(w[u], use ? v[u].z : 0.f, acc.z);
+        acc.w = fmaf(w[u], use ? v[u].w : 0.f, acc.w);
       }
     }
   }
@@ -356,9 +363,13 @@ cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
                                 cudaStream_t s) {
   const int64_t warps = rows * heads;
   if (warps == 0) return CP_ATTN_OK;
-  // few (row, head) pairs with many parts: eight warps per pair
+  // few (row, head) pairs with many parts: a block of warps per pair
   if (d <= 128 && n_parts >= 16 && n_parts <= kWideMaxParts && warps * kWideWarps <= 152 * 64) {
-    merge_lse_wide_kernel<<<static_cast<unsigned>(warps), 32 * kWideWarps, 0, s>>>(
+    const int per_warp = (n_parts + kWideWarps - 1) / kWideWarps;
+    auto kernel = per_warp <= 4   ? merge_lse_wide_kernel<4>
+                  : per_warp <= 8 ? merge_lse_wide_kernel<8>
+                                  : merge_lse_wide_kernel<16>;
+    kernel<<<static_cast<unsigned>(warps), 32 * kWideWarps, 0, s>>>(
         n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
         o_out_f32, lse_out);
     return check_launch("merge_lse");
