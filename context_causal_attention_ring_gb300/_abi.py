@@ -29,6 +29,8 @@ TO_RANK_MAJOR, TO_NATURAL = 0, 1
 
 LAYOUTS = {"contiguous": LAYOUT_CONTIGUOUS, "zigzag": LAYOUT_ZIGZAG, "usp": LAYOUT_USP}
 VARIANTS = {"pass_kv": PASS_KV, "pass_q": PASS_Q, "auto": VARIANT_AUTO}
+F32, BF16 = 0, 1
+DTYPES = {"f32": F32, "bf16": BF16}
 VARIANT_NAMES = {PASS_KV: "pass_kv", PASS_Q: "pass_q"}
 
 
@@ -53,6 +55,8 @@ class _PlanDesc(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("window", ctypes.c_int64),
         ("a2a", ctypes.c_int),
+        ("partial_dtype", ctypes.c_int),
+        ("grad_dtype", ctypes.c_int),
     ]
 
 
@@ -98,6 +102,7 @@ _SIG = {
     "cp_attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_merge_lse": (_I, [_I, _I64, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
+    "cp_attn_merge_lse_ex": (_I, [_I, _I64, _I, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "cp_attn_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_forward_noalloc_capacity": (ctypes.c_size_t, []),
@@ -247,7 +252,8 @@ class Plan:
     def __init__(self, seq_len: int, cp: int, n_q_heads: int, n_kv_heads: int,
                  head_dim: int, layout: str = "zigzag", variant: str = "pass_kv",
                  cu_seqlens=None, kv_prefix_len: int = 0,
-                 softmax_scale: float = 0.0, window: int = 0, a2a: int = 1):
+                 softmax_scale: float = 0.0, window: int = 0, a2a: int = 1,
+                 partial_dtype: str = "f32", grad_dtype: str = "f32"):
         lib = load()
         self._keep = None
         desc = _PlanDesc()
@@ -267,6 +273,8 @@ class Plan:
         desc.softmax_scale = float(softmax_scale)
         desc.window = int(window)
         desc.a2a = int(a2a)
+        desc.partial_dtype = DTYPES[partial_dtype] if isinstance(partial_dtype, str) else int(partial_dtype)
+        desc.grad_dtype = DTYPES[grad_dtype] if isinstance(grad_dtype, str) else int(grad_dtype)
         h = _P()
         _check(lib.cp_attn_plan_ex(ctypes.byref(h), ctypes.byref(desc)))
         self.handle = h
@@ -280,6 +288,8 @@ class Plan:
         # the ring ordering in use ("auto" resolved by the library)
         self.variant = VARIANT_NAMES[var]
         self.kv_prefix_len = int(kv_prefix_len)
+        self.partial_dtype = desc.partial_dtype
+        self.grad_dtype = desc.grad_dtype
 
     def close(self):
         if getattr(self, "handle", None):
@@ -402,11 +412,21 @@ def fp8_quantize(x, rows, heads, head_dim, amax, out, scale=None, transpose=Fals
 
 
 def merge_lse(n_parts, rows, heads, head_dim, o_parts, part_stride, lse_parts,
-              lse_part_stride, o_out=None, o_out_f32=None, lse_out=None, stream=None):
-    _check(load().cp_attn_merge_lse(n_parts, rows, heads, head_dim, _ptr(o_parts),
-                                    int(part_stride), _ptr(lse_parts), int(lse_part_stride),
-                                    _ptr(o_out), _ptr(o_out_f32), _ptr(lse_out),
-                                    _stream(stream)))
+              lse_part_stride, o_out=None, o_out_f32=None, lse_out=None, stream=None,
+              parts_dtype="f32"):
+    """cp_attn_merge_lse (fp32 parts) or cp_attn_merge_lse_ex (parts_dtype
+    "bf16"); part_stride in elements."""
+    dt = DTYPES[parts_dtype] if isinstance(parts_dtype, str) else int(parts_dtype)
+    if dt == F32:
+        _check(load().cp_attn_merge_lse(n_parts, rows, heads, head_dim, _ptr(o_parts),
+                                        int(part_stride), _ptr(lse_parts), int(lse_part_stride),
+                                        _ptr(o_out), _ptr(o_out_f32), _ptr(lse_out),
+                                        _stream(stream)))
+    else:
+        _check(load().cp_attn_merge_lse_ex(n_parts, rows, heads, head_dim, dt, _ptr(o_parts),
+                                           int(part_stride), _ptr(lse_parts),
+                                           int(lse_part_stride), _ptr(o_out), _ptr(o_out_f32),
+                                           _ptr(lse_out), _stream(stream)))
 
 
 def launch_count() -> int:

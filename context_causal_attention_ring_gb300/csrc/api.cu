@@ -343,16 +343,51 @@ cp_attn_status cp_attn_plan_visible_pairs(cp_attn_plan_t p, int step, int64_t* o
   return CP_ATTN_OK;
 }
 
+namespace {
+
+// Pass-Q forward workspace: R O partial slots (fp32 or bf16), then R fp32
+// LSE slots.
+struct PassQLayout {
+  int64_t o_slot, l_slot;  // elements per slot
+  size_t lse_off, total;   // bytes
+};
+PassQLayout pass_q_layout(cp_attn_plan_t p) {
+  PassQLayout L;
+  L.o_slot = p->T_q * p->Hq * p->d;
+  L.l_slot = p->T_q * p->Hq;
+  const size_t elt = p->part_bf16 ? 2 : 4;
+  L.lse_off = round256(static_cast<size_t>(L.o_slot) * p->R * elt);
+  L.total = L.lse_off + round256(static_cast<size_t>(L.l_slot) * p->R * sizeof(float));
+  return L;
+}
+
+// Backward workspace: delta, the fp16 operand copies, then (bf16 gradients)
+// the fp32 accumulators of dq, dk, dv.
+struct BwdLayout {
+  size_t half_ops, dq, dk, dv, total;  // byte offsets, size
+};
+BwdLayout bwd_layout(cp_attn_plan_t p) {
+  BwdLayout L;
+  L.half_ops = round256(static_cast<size_t>(p->T_q) * p->Hq * sizeof(float));
+  L.dq = L.half_ops + half_ops_layout(p).total;
+  const size_t nq = static_cast<size_t>(p->T_q) * p->Hq * p->d * sizeof(float);
+  const size_t nk = static_cast<size_t>(p->T_kv) * p->Hkv * p->d * sizeof(float);
+  L.dk = L.dq + (p->grad_bf16 ? round256(nq) : 0);
+  L.dv = L.dk + (p->grad_bf16 ? round256(nk) : 0);
+  L.total = L.dv + (p->grad_bf16 ? round256(nk) : 0);
+  return L;
+}
+
+}  // namespace
+
 cp_attn_status cp_attn_workspace_size(cp_attn_plan_t p, cp_attn_op op, size_t* bytes) {
   clear_error();
   if (!p || !bytes) return fail(CP_ATTN_ERR_INVALID_ARG, "workspace_size: bad arguments");
   const size_t o = static_cast<size_t>(p->T_q) * p->Hq * p->d * sizeof(float);
-  const size_t l = static_cast<size_t>(p->T_q) * p->Hq * sizeof(float);
-  auto round = round256;
   if (op == CP_ATTN_OP_FORWARD) {
-    *bytes = p->variant == CP_ATTN_PASS_KV ? round(o) : round(o * p->R) + round(l * p->R);
+    *bytes = p->variant == CP_ATTN_PASS_KV ? round256(o) : pass_q_layout(p).total;
   } else if (op == CP_ATTN_OP_BACKWARD) {
-    *bytes = round(l) + half_ops_layout(p).total;
+    *bytes = bwd_layout(p).total;
   } else {
     return fail(CP_ATTN_ERR_INVALID_ARG, "workspace_size: bad op");
   }
@@ -374,7 +409,7 @@ namespace {
 // scales != NULL selects the E4M3 kernel: q, k E4M3 [T][H][128], v then
 // holds V^T E4M3 [Hkv][128][T_kv], scales the device descale factors.
 cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const void* k,
-                             const void* v, float* o_part, float* lse_part,
+                             const void* v, void* o_part, float* lse_part,
                              cp_attn_merge_mode mode, void* o_final, void* stream, bool chained,
                              bool* launched, const float* scales = nullptr) {
   *launched = false;
@@ -421,7 +456,8 @@ cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const vo
   fp.scale_log2 = p->scale * 1.44269504088896340736f;
   fp.mode = mode;
   fp.first = (mode == CP_ATTN_ACCUMULATE && step == 0) ? 1 : 0;
-  fp.o_part = o_part;
+  fp.part_bf16 = (mode == CP_ATTN_WRITE_PARTIAL && p->part_bf16) ? 1 : 0;
+  fp.o_part = static_cast<float*>(o_part);
   fp.lse_part = lse_part;
   fp.o_final = mode == CP_ATTN_ACCUMULATE ? static_cast<__nv_bfloat16*>(o_final) : nullptr;
   fp.scales = scales;
@@ -511,7 +547,7 @@ cp_attn_status step_bwd_impl(cp_attn_plan_t p, int step, const void* half_ops, c
 }  // namespace
 
 cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const void* k,
-                                const void* v, float* o_part, float* lse_part,
+                                const void* v, void* o_part, float* lse_part,
                                 cp_attn_merge_mode mode, void* o_final, void* stream) {
   clear_error();
   bool launched = false;
@@ -537,7 +573,7 @@ cp_attn_status cp_attn_plan_set_chaining(cp_attn_plan_t p, int enable) {
 }
 
 cp_attn_status cp_attn_step_fwd_fp8(cp_attn_plan_t p, int step, const void* q8, const void* k8,
-                                    const void* vt8, const float* scales, float* o_part,
+                                    const void* vt8, const float* scales, void* o_part,
                                     float* lse_part, cp_attn_merge_mode mode, void* o_final,
                                     void* stream) {
   clear_error();
@@ -609,21 +645,41 @@ cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* q, const voi
   return CP_ATTN_OK;
 }
 
-cp_attn_status cp_attn_merge_lse(int n_parts, int64_t rows, int heads, int head_dim,
-                                 const float* o_parts, int64_t part_stride,
-                                 const float* lse_parts, int64_t lse_part_stride, void* o_out,
-                                 float* o_out_f32, float* lse_out, void* stream) {
+cp_attn_status cp_attn_merge_lse_ex(int n_parts, int64_t rows, int heads, int head_dim,
+                                    cp_attn_dtype parts_dtype, const void* o_parts,
+                                    int64_t part_stride, const float* lse_parts,
+                                    int64_t lse_part_stride, void* o_out, float* o_out_f32,
+                                    float* lse_out, void* stream) {
   clear_error();
   if (n_parts < 1 || rows < 0 || heads < 1 || head_dim < 4 || head_dim % 4 || head_dim > 256)
     return fail(CP_ATTN_ERR_SHAPE, "merge_lse: bad sizes");
+  if (parts_dtype != CP_ATTN_F32 && parts_dtype != CP_ATTN_BF16)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "merge_lse: parts_dtype must be F32 or BF16");
   if (!o_parts || !lse_parts || !lse_out)
     return fail(CP_ATTN_ERR_INVALID_ARG, "merge_lse: null pointer");
   if (!aligned16(o_parts) || (part_stride % 4) || (o_out && (reinterpret_cast<uintptr_t>(o_out) & 7)) ||
       (o_out_f32 && !aligned16(o_out_f32)))
     return fail(CP_ATTN_ERR_INVALID_ARG, "merge_lse: misaligned pointer or stride");
+  const bool bf16 = parts_dtype == CP_ATTN_BF16;
+  if (bf16 && o_out_f32) {
+    // the fp32 output may not overlap the bf16 parts (they are read by other blocks)
+    const char* a = static_cast<const char*>(o_parts);
+    const char* b = reinterpret_cast<const char*>(o_out_f32);
+    const int64_t span = ((n_parts - 1) * part_stride + rows * heads * head_dim) * 2;
+    if (b < a + span && a < b + rows * heads * head_dim * 4)
+      return fail(CP_ATTN_ERR_INVALID_ARG, "merge_lse: o_out_f32 overlaps bf16 parts");
+  }
   return launch_merge_lse(n_parts, rows, heads, head_dim, o_parts, part_stride, lse_parts,
                           lse_part_stride, static_cast<__nv_bfloat16*>(o_out), o_out_f32, lse_out,
-                          static_cast<cudaStream_t>(stream));
+                          static_cast<cudaStream_t>(stream), bf16);
+}
+
+cp_attn_status cp_attn_merge_lse(int n_parts, int64_t rows, int heads, int head_dim,
+                                 const float* o_parts, int64_t part_stride,
+                                 const float* lse_parts, int64_t lse_part_stride, void* o_out,
+                                 float* o_out_f32, float* lse_out, void* stream) {
+  return cp_attn_merge_lse_ex(n_parts, rows, heads, head_dim, CP_ATTN_F32, o_parts, part_stride,
+                              lse_parts, lse_part_stride, o_out, o_out_f32, lse_out, stream);
 }
 
 cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, const void* v,
@@ -656,10 +712,8 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, c
   // Pass Q: KV stays, Q moves. Each step writes its partials to the slot of
   // the kv owner (the permutation back to order); the n-way merge per q owner
   // stands for the all-to-all plus merge.
-  const int64_t o_slot = p->T_q * p->Hq * p->d;
-  const int64_t l_slot = p->T_q * p->Hq;
-  const size_t o_bytes = (static_cast<size_t>(o_slot) * p->R * sizeof(float) + 255) & ~static_cast<size_t>(255);
-  float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  const PassQLayout L = pass_q_layout(p);
+  float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.lse_off);
   bool prev = false;
   for (int t = 0; t < p->R; ++t) {
     bool launched = false;
@@ -669,9 +723,11 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t p, const void* q, const void* k, c
     prev = prev || launched;
   }
   // The merge also leaves the fp32 result in slot 0 (each (row, head) is read
-  // completely by one warp before that warp writes it).
-  return cp_attn_merge_lse(p->R, p->T_q, p->Hq, p->d, ws, o_slot, ws_lse, l_slot, o, ws, lse,
-                           stream);
+  // completely by one warp before that warp writes it); bf16 slots are too
+  // small for it.
+  return cp_attn_merge_lse_ex(p->R, p->T_q, p->Hq, p->d, p->part_bf16 ? CP_ATTN_BF16 : CP_ATTN_F32,
+                              ws, L.o_slot, ws_lse, L.l_slot, o, p->part_bf16 ? nullptr : ws, lse,
+                              stream);
 }
 
 cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t p, const void* q8, const void* k8,
@@ -700,10 +756,8 @@ cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t p, const void* q8, const void*
     }
     return CP_ATTN_OK;
   }
-  const int64_t o_slot = p->T_q * p->Hq * p->d;
-  const int64_t l_slot = p->T_q * p->Hq;
-  const size_t o_bytes = (static_cast<size_t>(o_slot) * p->R * sizeof(float) + 255) & ~static_cast<size_t>(255);
-  float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  const PassQLayout L = pass_q_layout(p);
+  float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.lse_off);
   for (int t = 0; t < p->R; ++t) {
     bool launched = false;
     st = step_fwd_impl(p, t, q8, k8, vt8, ws, ws_lse, CP_ATTN_WRITE_PARTIAL, nullptr, stream,
@@ -711,13 +765,14 @@ cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t p, const void* q8, const void*
     if (st != CP_ATTN_OK) return st;
     prev = prev || launched;
   }
-  return cp_attn_merge_lse(p->R, p->T_q, p->Hq, p->d, ws, o_slot, ws_lse, l_slot, o, ws, lse,
-                           stream);
+  return cp_attn_merge_lse_ex(p->R, p->T_q, p->Hq, p->d, p->part_bf16 ? CP_ATTN_BF16 : CP_ATTN_F32,
+                              ws, L.o_slot, ws_lse, L.l_slot, o, p->part_bf16 ? nullptr : ws, lse,
+                              stream);
 }
 
 cp_attn_status cp_attn_backward(cp_attn_plan_t p, const void* q, const void* k, const void* v,
                                 const void* o, const float* o_f32, const float* lse,
-                                const void* dout, float* dq, float* dk, float* dv,
+                                const void* dout, void* dq, void* dk, void* dv,
                                 void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   cp_attn_status st = check_device_plan(p);
@@ -728,21 +783,35 @@ cp_attn_status cp_attn_backward(cp_attn_plan_t p, const void* q, const void* k, 
     return fail(CP_ATTN_ERR_INVALID_ARG, "backward: workspace smaller than cp_attn_workspace_size");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(CP_ATTN_ERR_INVALID_ARG, "backward: workspace must be 256-byte aligned");
-  float* delta = static_cast<float*>(workspace);
-  void* half_ops = static_cast<char*>(workspace) +
-                   round256(static_cast<size_t>(p->T_q) * p->Hq * sizeof(float));
-  if ((st = cp_attn_bwd_preprocess(p, q, k, v, o, o_f32, dout, delta, half_ops, dq, dk, dv,
-                                   stream)) !=
-      CP_ATTN_OK)
+  if (!dq || !dk || !dv) return fail(CP_ATTN_ERR_INVALID_ARG, "backward: null gradient");
+  if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "backward: gradients must be 16-byte aligned");
+  const BwdLayout L = bwd_layout(p);
+  char* wb = static_cast<char*>(workspace);
+  float* delta = reinterpret_cast<float*>(wb);
+  void* half_ops = wb + L.half_ops;
+  // bf16 gradients: the fp32 sums live in the workspace until the finalize
+  float* dq_acc = p->grad_bf16 ? reinterpret_cast<float*>(wb + L.dq) : static_cast<float*>(dq);
+  float* dk_acc = p->grad_bf16 ? reinterpret_cast<float*>(wb + L.dk) : static_cast<float*>(dk);
+  float* dv_acc = p->grad_bf16 ? reinterpret_cast<float*>(wb + L.dv) : static_cast<float*>(dv);
+  if ((st = cp_attn_bwd_preprocess(p, q, k, v, o, o_f32, dout, delta, half_ops, dq_acc, dk_acc,
+                                   dv_acc, stream)) != CP_ATTN_OK)
     return st;
   bool prev = false;
   for (int t = 0; t < p->R; ++t) {
     bool launched = false;
-    st = step_bwd_impl(p, t, half_ops, lse, delta, dq, dk, dv, stream, prev, &launched);
+    st = step_bwd_impl(p, t, half_ops, lse, delta, dq_acc, dk_acc, dv_acc, stream, prev,
+                       &launched);
     if (st != CP_ATTN_OK) return st;
     prev = prev || launched;
   }
-  return CP_ATTN_OK;
+  if (!p->grad_bf16) return CP_ATTN_OK;
+  // K6: the summed gradients rounded to bf16
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t nq = p->T_q * p->Hq * p->d, nk = p->T_kv * p->Hkv * p->d;
+  if ((st = launch_f32_to_bf16(dq_acc, dq, nq, s)) != CP_ATTN_OK) return st;
+  if ((st = launch_f32_to_bf16(dk_acc, dk, nk, s)) != CP_ATTN_OK) return st;
+  return launch_f32_to_bf16(dv_acc, dv, nk, s);
 }
 
 cp_attn_status cp_attn_layout_apply(cp_attn_plan_t p, cp_attn_tensor_kind kind,

@@ -21,10 +21,22 @@ namespace {
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// Four consecutive elements of an O part (fp32 or bf16) as fp32.
+__device__ __forceinline__ float4 load4(const float* __restrict__ base, int64_t off) {
+  return __ldg(reinterpret_cast<const float4*>(base + off));
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* __restrict__ base, int64_t off) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(base + off));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // One warp per (row, head). Lane l handles float4 chunks l, l+32, ...
-template <int CHUNKS>  // float4 chunks per lane (d/4/32 rounded up)
+// TP: element type of the O parts (float or __nv_bfloat16).
+template <int CHUNKS, typename TP>  // float4 chunks per lane (d/4/32 rounded up)
 __global__ void __launch_bounds__(256) merge_lse_kernel(
-    int n_parts, int64_t rows, int heads, int d, const float* __restrict__ o_parts,
+    int n_parts, int64_t rows, int heads, int d, const TP* __restrict__ o_parts,
     int64_t part_stride, const float* __restrict__ lse_parts, int64_t lse_part_stride,
     __nv_bfloat16* __restrict__ o_out, float* __restrict__ o_out_f32,
     float* __restrict__ lse_out) {
@@ -56,12 +68,11 @@ __global__ void __launch_bounds__(256) merge_lse_kernel(
     for (int i = 0; i < n_parts; ++i) {
       const float w = ptx::ex2(__ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e - L);
       if (w == 0.f) continue;  // empty part (LSE = -inf) or negligible
-      const float4* src = reinterpret_cast<const float4*>(o_parts + i * part_stride + o_off);
 #pragma unroll
       for (int c = 0; c < CHUNKS; ++c) {
         const int j = lane + 32 * c;
         if (j < n4) {
-          const float4 v = __ldg(src + j);
+          const float4 v = load4(o_parts, i * part_stride + o_off + 4 * j);
           acc[c].x = fmaf(w, v.x, acc[c].x);
           acc[c].y = fmaf(w, v.y, acc[c].y);
           acc[c].z = fmaf(w, v.z, acc[c].z);
@@ -99,10 +110,11 @@ __global__ void __launch_bounds__(256) merge_lse_kernel(
 constexpr int kWideWarps = 16;
 constexpr int kWideMaxParts = 4096;
 
-// U: loads in flight per lane, about the parts per warp (4, 8 or 16).
-template <int U>
+// U: loads in flight per lane, about the parts per warp (4, 8 or 16); TP:
+// element type of the O parts.
+template <int U, typename TP>
 __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
-    int n_parts, int64_t rows, int heads, int d, const float* __restrict__ o_parts,
+    int n_parts, int64_t rows, int heads, int d, const TP* __restrict__ o_parts,
     int64_t part_stride, const float* __restrict__ lse_parts, int64_t lse_part_stride,
     __nv_bfloat16* __restrict__ o_out, float* __restrict__ o_out_f32,
     float* __restrict__ lse_out) {
@@ -162,7 +174,7 @@ __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
         const int i = i0 + u * kWideWarps;
         const int ic = i < n_parts ? i : n_parts - 1;
         w[u] = i < n_parts ? s_w[i] : 0.f;
-        v[u] = __ldg(reinterpret_cast<const float4*>(o_parts + ic * part_stride + o_off) + l4);
+        v[u] = load4(o_parts, ic * part_stride + o_off + 4 * l4);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -312,6 +324,20 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
   if (bad) atomicCAS(status, 0, static_cast<int>(CP_ATTN_ERR_RANGE));
 }
 
+// K6 finalize of bf16 gradients: 8 fp32 values per thread -> bf16, rounded
+// to nearest even (grid-stride; 32 bytes read, 16 written per thread and
+// iteration).
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4* __restrict__ in,
+                                                          uint4* __restrict__ out, int64_t n8) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(in + 2 * i);
+    const float4 b = __ldg(in + 2 * i + 1);
+    out[i] = make_uint4(ptx::pack_bf16(a.x, a.y), ptx::pack_bf16(a.z, a.w),
+                        ptx::pack_bf16(b.x, b.y), ptx::pack_bf16(b.z, b.w));
+  }
+}
+
 // One CTA waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up after limit_ns and records the timeout like every kernel wait.
 __global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
@@ -351,24 +377,34 @@ cp_attn_status launch_bf16_to_f16(const void* in, void* out, int64_t n, int32_t*
   return check_launch("bf16_to_f16");
 }
 
+cp_attn_status launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t s) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return CP_ATTN_OK;
+  f32_to_bf16_kernel<<<grid_for(n8, 256, 152 * 16), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+  return check_launch("f32_to_bf16");
+}
+
 cp_attn_status launch_selftest_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s) {
   selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
   return check_launch("selftest_wait");
 }
 
-cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
-                                const float* o_parts, int64_t part_stride,
-                                const float* lse_parts, int64_t lse_part_stride,
-                                __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
-                                cudaStream_t s) {
+namespace {
+
+template <typename TP>
+cp_attn_status merge_lse_typed(int n_parts, int64_t rows, int heads, int d, const TP* o_parts,
+                               int64_t part_stride, const float* lse_parts,
+                               int64_t lse_part_stride, __nv_bfloat16* o_out, float* o_out_f32,
+                               float* lse_out, cudaStream_t s) {
   const int64_t warps = rows * heads;
   if (warps == 0) return CP_ATTN_OK;
   // few (row, head) pairs with many parts: a block of warps per pair
   if (d <= 128 && n_parts >= 16 && n_parts <= kWideMaxParts && warps * kWideWarps <= 152 * 64) {
     const int per_warp = (n_parts + kWideWarps - 1) / kWideWarps;
-    auto kernel = per_warp <= 4   ? merge_lse_wide_kernel<4>
-                  : per_warp <= 8 ? merge_lse_wide_kernel<8>
-                                  : merge_lse_wide_kernel<16>;
+    auto kernel = per_warp <= 4   ? merge_lse_wide_kernel<4, TP>
+                  : per_warp <= 8 ? merge_lse_wide_kernel<8, TP>
+                                  : merge_lse_wide_kernel<16, TP>;
     kernel<<<static_cast<unsigned>(warps), 32 * kWideWarps, 0, s>>>(
         n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
         o_out_f32, lse_out);
@@ -376,14 +412,28 @@ cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
   }
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (d <= 128)
-    merge_lse_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+    merge_lse_kernel<1, TP><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
         o_out_f32, lse_out);
   else
-    merge_lse_kernel<2><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+    merge_lse_kernel<2, TP><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
         o_out_f32, lse_out);
   return check_launch("merge_lse");
+}
+
+}  // namespace
+
+cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
+                                const void* o_parts, int64_t part_stride,
+                                const float* lse_parts, int64_t lse_part_stride,
+                                __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
+                                cudaStream_t s, bool parts_bf16) {
+  if (parts_bf16)
+    return merge_lse_typed(n_parts, rows, heads, d, static_cast<const __nv_bfloat16*>(o_parts),
+                           part_stride, lse_parts, lse_part_stride, o_out, o_out_f32, lse_out, s);
+  return merge_lse_typed(n_parts, rows, heads, d, static_cast<const float*>(o_parts), part_stride,
+                         lse_parts, lse_part_stride, o_out, o_out_f32, lse_out, s);
 }
 
 cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t row_bytes,

@@ -71,6 +71,8 @@ struct cp_attn_plan_s {
   int32_t* d_row_kv = nullptr;  // rank-major row -> natural row (keys)
   // per-step calls of steps >= 1 launch chained to the kernel before them
   int chain_steps = 0;
+  int part_bf16 = 0;        // WRITE_PARTIAL O partials (and Pass-Q slots) in bf16
+  int grad_bf16 = 0;        // cp_attn_backward hands out bf16 gradients
 };
 
 namespace cpa {

@@ -25,6 +25,7 @@ struct FwdParams {
   float scale_log2;           // softmax scale * log2(e)
   int mode;                   // cp_attn_merge_mode
   int first;                  // ACCUMULATE: initialise the accumulators
+  int part_bf16;              // WRITE_PARTIAL: o_part holds bf16 partials
   float* o_part;
   float* lse_part;
   __nv_bfloat16* o_final;     // optional
@@ -93,11 +94,16 @@ size_t step_bwd_smem_bytes(int d);
 // Rows of the Q / dO tensor-map box the backward kernel for head_dim d uses.
 int step_bwd_q_box_rows(int d);
 
+// o_parts: fp32, or bf16 when parts_bf16 (part_stride in elements).
 cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
-                                const float* o_parts, int64_t part_stride,
+                                const void* o_parts, int64_t part_stride,
                                 const float* lse_parts, int64_t lse_part_stride,
                                 __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
-                                cudaStream_t s);
+                                cudaStream_t s, bool parts_bf16 = false);
+
+// K6: n fp32 values -> bf16 (round to nearest even); n a multiple of 8,
+// both pointers 16-byte aligned.
+cp_attn_status launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t s);
 
 // Sequence <-> head all-to-all (gather = 0: split heads, 1: gather them).
 cp_attn_status launch_head_a2a(int64_t rows, int heads, int64_t head_bytes, int a2a, int gather,

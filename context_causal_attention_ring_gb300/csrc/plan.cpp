@@ -123,6 +123,9 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
     return fail(CP_ATTN_ERR_SHAPE, "plan: total tokens must fit in int32 positions");
   if (!(desc->softmax_scale >= 0.f) || std::isinf(desc->softmax_scale))
     return fail(CP_ATTN_ERR_INVALID_ARG, "plan: softmax_scale must be finite and >= 0");
+  for (cp_attn_dtype t : {desc->partial_dtype, desc->grad_dtype})
+    if (t != CP_ATTN_F32 && t != CP_ATTN_BF16)
+      return fail(CP_ATTN_ERR_INVALID_ARG, "plan: partial_dtype and grad_dtype must be F32 or BF16");
 
   p->N = N;
   p->P = P;
@@ -132,6 +135,8 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
   p->d = desc->head_dim;
   p->layout = desc->layout;
   p->a2a = a2a;
+  p->part_bf16 = desc->partial_dtype == CP_ATTN_BF16 ? 1 : 0;
+  p->grad_bf16 = desc->grad_dtype == CP_ATTN_BF16 ? 1 : 0;
   p->variant = desc->variant == CP_ATTN_VARIANT_AUTO
                    ? select_variant_rule(N, P, desc->n_q_heads, desc->n_kv_heads)
                    : desc->variant;

@@ -320,8 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool merge = (p.mode == CP_ATTN_ACCUMULATE) && !p.first;
       float* o_dst = p.o_part;
       float* lse_dst = p.lse_part;
+      // WRITE_PARTIAL with bf16 partials: the slot holds bf16 elements
+      const bool part_bf16 = p.part_bf16 && p.mode == CP_ATTN_WRITE_PARTIAL;
+      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.o_part);
       if (p.mode == CP_ATTN_WRITE_PARTIAL) {
-        o_dst += static_cast<int64_t>(w.kv_owner) * p.T_q * p.Hq * D;
+        const int64_t slot = static_cast<int64_t>(w.kv_owner) * p.T_q * p.Hq * D;
+        o_dst += slot;
+        ob += slot;
         lse_dst += static_cast<int64_t>(w.kv_owner) * p.Hq * p.T_q;
       }
       if (merge) {
@@ -365,13 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.z = u.z * w_old + v.z * w_new;
             v.w = u.w * w_old + v.w * w_new;
           }
-          od[c * 8 + x4] = v;
-          if (p.o_final) {
-            uint2 pk;
-            pk.x = ptx::pack_bf16(v.x, v.y);
-            pk.y = ptx::pack_bf16(v.z, v.w);
-            *reinterpret_cast<uint2*>(p.o_final + row_off + c * 32 + x4 * 4) = pk;
-          }
+          uint2 pk;
+          pk.x = ptx::pack_bf16(v.x, v.y);
+          pk.y = ptx::pack_bf16(v.z, v.w);
+          if (part_bf16)
+            *reinterpret_cast<uint2*>(ob + row_off + c * 32 + x4 * 4) = pk;
+          else
+            od[c * 8 + x4] = v;
+          if (p.o_final) *reinterpret_cast<uint2*>(p.o_final + row_off + c * 32 + x4 * 4) = pk;
         }
       }
     }
@@ -817,8 +823,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const bool merge = (p.mode == CP_ATTN_ACCUMULATE) && !p.first;
       float* o_dst = p.o_part;
       float* lse_dst = p.lse_part;
+      // WRITE_PARTIAL with bf16 partials: the slot holds bf16 elements
+      const bool part_bf16 = p.part_bf16 && p.mode == CP_ATTN_WRITE_PARTIAL;
+      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.o_part);
       if (p.mode == CP_ATTN_WRITE_PARTIAL) {
-        o_dst += static_cast<int64_t>(w.kv_owner) * p.T_q * p.Hq * D;
+        const int64_t slot = static_cast<int64_t>(w.kv_owner) * p.T_q * p.Hq * D;
+        o_dst += slot;
+        ob += slot;
         lse_dst += static_cast<int64_t>(w.kv_owner) * p.Hq * p.T_q;
       }
       if (merge) {
@@ -897,13 +908,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
               v.w = fmaf(old[it].w, b_r[it], v.w);
             }
             const int64_t off = base_off + row * row_stride + c * 32;
-            if (!keep_old) *reinterpret_cast<float4*>(o_dst + off) = v;
-            if (p.o_final) {
-              uint2 pk;
-              pk.x = ptx::pack_bf16(v.x, v.y);
-              pk.y = ptx::pack_bf16(v.z, v.w);
-              *reinterpret_cast<uint2*>(p.o_final + off) = pk;
-            }
+            uint2 pk;
+            pk.x = ptx::pack_bf16(v.x, v.y);
+            pk.y = ptx::pack_bf16(v.z, v.w);
+            if (part_bf16)
+              *reinterpret_cast<uint2*>(ob + off) = pk;
+            else if (!keep_old)
+              *reinterpret_cast<float4*>(o_dst + off) = v;
+            if (p.o_final) *reinterpret_cast<uint2*>(p.o_final + off) = pk;
           }
           if (merge && c + 1 < D / 32) {
 #pragma unroll

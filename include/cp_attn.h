@@ -88,9 +88,10 @@ typedef enum cp_attn_variant {
 
 /* Epilogue of cp_attn_step_fwd.
  * WRITE_PARTIAL: the partial (O_t, LSE_t) of pair (q_owner, kv_owner) is
- *   written to slot kv_owner: o_part + kv_owner*T_q*Hq*d and
- *   lse_part + kv_owner*Hq*T_q, at the q_owner's rows. Rows that see no key
- *   in this step get O = 0, LSE = -inf. (Storing by kv_owner is the
+ *   written to slot kv_owner: element kv_owner*T_q*Hq*d of o_part (fp32, or
+ *   bf16 when the plan's partial_dtype is BF16) and lse_part +
+ *   kv_owner*Hq*T_q (fp32), at the q_owner's rows. Rows that see no key in
+ *   this step get O = 0, LSE = -inf. (Storing by kv_owner is the
  *   permutation back to order that Pass Q needs before its merge.)
  * ACCUMULATE: the running merge "as it goes" of the P2P ring. o_part is an
  *   fp32 accumulator [T_q, Hq, d] and lse_part an fp32 [Hq, T_q]
@@ -116,6 +117,12 @@ typedef enum cp_attn_direction {
 } cp_attn_direction;
 
 typedef struct cp_attn_plan_s* cp_attn_plan_t;
+
+/* Element type of the partial outputs and of the gradients a plan hands out. */
+typedef enum cp_attn_dtype {
+  CP_ATTN_F32 = 0,
+  CP_ATTN_BF16 = 1
+} cp_attn_dtype;
 
 /* Full description of a plan. Zero-initialise and set the fields. */
 typedef struct cp_attn_plan_desc {
@@ -148,6 +155,19 @@ typedef struct cp_attn_plan_desc {
   int a2a;                /* USP layout: all-to-all group size (devices per
                              ring rank), >= 1; ignored (treated as 1) by the
                              other layouts */
+  cp_attn_dtype partial_dtype; /* O partials written by WRITE_PARTIAL steps
+                             (cp_attn_step_fwd's o_part) and kept by
+                             cp_attn_forward for Pass Q: F32 (default) or
+                             BF16, which halves the R partial slots of a
+                             Pass-Q forward ("bf16 partials" for the
+                             memory of the 405B-shaped Pass-Q prefill). The
+                             LSE partials and the ACCUMULATE running output
+                             stay fp32. */
+  cp_attn_dtype grad_dtype; /* dq, dk, dv of cp_attn_backward: F32 (default)
+                             or BF16, accumulated in fp32 in the workspace
+                             and rounded to nearest even once at the end.
+                             The step-level cp_attn_step_bwd always adds to
+                             fp32 accumulators. */
 } cp_attn_plan_desc;
 
 /* Build a plan: per-rank positions (zigzag or contiguous), the per-step
@@ -202,9 +222,11 @@ cp_attn_status cp_attn_plan_block_mask(cp_attn_plan_t plan, uint8_t* out);
 cp_attn_status cp_attn_plan_visible_pairs(cp_attn_plan_t plan, int step, int64_t* out);
 
 /* Device workspace, in bytes, for cp_attn_forward (op FORWARD: the fp32
- * running output for Pass KV, or R fp32 partial slots for Pass Q) or
- * cp_attn_backward (op BACKWARD: the fp32 delta rows, then the fp16 operand
- * copies of cp_attn_half_ops_size). */
+ * running output for Pass KV, or R partial slots for Pass Q, fp32 or bf16 by
+ * the plan's partial_dtype, then R fp32 LSE slots) or cp_attn_backward (op
+ * BACKWARD: the fp32 delta rows, then the fp16 operand copies of
+ * cp_attn_half_ops_size, then, when the plan's grad_dtype is BF16, the fp32
+ * accumulators of dq, dk and dv). */
 cp_attn_status cp_attn_workspace_size(cp_attn_plan_t plan, cp_attn_op op, size_t* bytes);
 
 /* One forward ring step (kernel K1). For every pair (q_owner, kv_owner) of
@@ -217,7 +239,7 @@ cp_attn_status cp_attn_workspace_size(cp_attn_plan_t plan, cp_attn_op op, size_t
  * ERR_INVALID_ARG for null/misaligned pointers or a step outside [0, R). */
 cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
                                 const void* q, const void* k, const void* v,
-                                float* o_part, float* lse_part,
+                                void* o_part, float* lse_part,
                                 cp_attn_merge_mode mode, void* o_final,
                                 void* stream);
 
@@ -274,7 +296,7 @@ cp_attn_status cp_attn_fp8_quantize(const void* x, int64_t rows, int heads, int 
                                     void* stream);
 cp_attn_status cp_attn_step_fwd_fp8(cp_attn_plan_t plan, int step, const void* q8,
                                     const void* k8, const void* vt8, const float* scales,
-                                    float* o_part, float* lse_part, cp_attn_merge_mode mode,
+                                    void* o_part, float* lse_part, cp_attn_merge_mode mode,
                                     void* o_final, void* stream);
 cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t plan, const void* q8, const void* k8,
                                    const void* vt8, const float* scales, void* o, float* lse,
@@ -328,13 +350,23 @@ cp_attn_status cp_attn_merge_lse(int n_parts, int64_t rows, int heads, int head_
                                  const float* lse_parts, int64_t lse_part_stride,
                                  void* o_out, float* o_out_f32, float* lse_out,
                                  void* stream);
+/* cp_attn_merge_lse with the O parts in parts_dtype (F32 or BF16, e.g. the
+ * bf16 partials of a plan with partial_dtype BF16); part_stride counts
+ * elements. The sums are fp32 either way. With BF16 parts o_out_f32 must not
+ * alias them. ERR_INVALID_ARG for another dtype. */
+cp_attn_status cp_attn_merge_lse_ex(int n_parts, int64_t rows, int heads, int head_dim,
+                                    cp_attn_dtype parts_dtype, const void* o_parts,
+                                    int64_t part_stride, const float* lse_parts,
+                                    int64_t lse_part_stride, void* o_out, float* o_out_f32,
+                                    float* lse_out, void* stream);
 
 /* Whole forward pass over the emulated ring: R step launches in step
  * order, then (Pass Q) the n-way merge over kv_owner slots. o: bf16
  * [T_q,Hq,d]; lse: fp32 [Hq,T_q]. workspace: device buffer of at least
  * cp_attn_workspace_size(plan, FORWARD) bytes, 256-byte aligned. On return
  * the workspace starts with O in fp32 [T_q,Hq,d] (the unrounded result),
- * which cp_attn_backward can take as o_f32. */
+ * which cp_attn_backward can take as o_f32 -- except for Pass Q with bf16
+ * partials, whose slots are too small for it. */
 cp_attn_status cp_attn_forward(cp_attn_plan_t plan, const void* q, const void* k,
                                const void* v, void* o, float* lse,
                                void* workspace, size_t workspace_bytes,
@@ -364,13 +396,15 @@ size_t cp_attn_forward_noalloc_capacity(void);
 
 /* Whole backward pass: preprocess, then R backward steps in the plan's
  * ring order. o: bf16 [T_q,Hq,d]; o_f32: optional fp32 O used for delta
- * (see cp_attn_bwd_preprocess); dq: fp32 [T_q,Hq,d]; dk, dv: fp32
- * [T_kv,Hkv,d] (overwritten). workspace: at least
+ * (see cp_attn_bwd_preprocess); dq [T_q,Hq,d]; dk, dv [T_kv,Hkv,d]
+ * (overwritten), fp32 or, when the plan's grad_dtype is BF16, bf16: then
+ * the fp32 sums live in the workspace and a last kernel (K6) rounds them to
+ * nearest even into dq, dk, dv. workspace: at least
  * cp_attn_workspace_size(plan, BACKWARD) bytes, 256-byte aligned. */
 cp_attn_status cp_attn_backward(cp_attn_plan_t plan, const void* q, const void* k,
                                 const void* v, const void* o, const float* o_f32,
-                                const float* lse, const void* dout, float* dq, float* dk,
-                                float* dv, void* workspace, size_t workspace_bytes,
+                                const float* lse, const void* dout, void* dq, void* dk,
+                                void* dv, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
 /* Reorder a [tokens, row_bytes] tensor between natural token order and the

@@ -67,6 +67,7 @@ __all__ = [
     "partial_attention",
     "attention",
     "lse_merge",
+    "round_bf16",
     "ring_forward",
     "attention_backward",
     "ring_backward",
@@ -326,8 +327,28 @@ def _split(x, R):
     return [x[r * n:(r + 1) * n] for r in range(R)]
 
 
+def round_bf16(x):
+    """Nearest bf16 value of each float64, ties to the even significand: 8
+    significant bits over the fp32 exponent range; below 2^-126 the spacing
+    stays 2^-133 (subnormals); magnitudes at or above the overflow point
+    (2 - 2^-8) * 2^127 become infinite; NaN stays NaN. The storage rounding
+    of bf16 partial outputs (reading: a plan with bf16 partials stores each
+    ring step's O in this format before the merge)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    finite = np.isfinite(a)
+    a0 = np.where(finite, a, 0.0)
+    _, e = np.frexp(a0)                   # a = f * 2^e with f in [0.5, 1)
+    e = np.maximum(e, -125)               # subnormals keep the spacing of 2^-126
+    spacing = np.ldexp(1.0, e - 8)
+    r = np.rint(a0 / spacing) * spacing   # a / spacing is exact; rint: half to even
+    r = np.where(r >= 2.0 ** 128, np.inf, r)
+    r = np.where(finite, r, a)
+    return np.copysign(r, x)
+
+
 def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
-                 variant: str = "pass_kv", *, window: int = 0):
+                 variant: str = "pass_kv", *, window: int = 0, partial_dtype: str = "f32"):
     """Explicit ring over R virtual ranks; inputs in rank-major order.
 
     q: [R*n_q, Hq, d] (rank r's queries are rows r*n_q ...), k/v:
@@ -335,8 +356,12 @@ def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
     running result in step order. Pass Q stores the partial result of
     (q_owner, kv_owner) at the kv_owner's slot (the permutation back to
     order), hands each q_owner its R partials (the all-to-all), and merges
-    them in kv_owner order. Returns O [R*n_q, Hq, d], LSE [Hq, R*n_q].
+    them in kv_owner order; with partial_dtype "bf16" a slot holds its O
+    rounded to bf16 (round_bf16; the LSE stays exact). Returns
+    O [R*n_q, Hq, d], LSE [Hq, R*n_q].
     """
+    if partial_dtype not in ("f32", "bf16"):
+        raise ValueError("partial_dtype must be 'f32' or 'bf16'")
     R = len(q_pos)
     Q = _split(_as_f64(q), R)
     K = _split(_as_f64(k), R)
@@ -356,9 +381,9 @@ def ring_forward(q, k, v, q_pos, kv_pos, cu_seqlens=None, scale=None,
         for t in range(R):
             for r in range(R):
                 qo, ko = sched[t][r]
-                slots[qo][ko] = partial_attention(Q[qo], K[ko], V[ko],
-                                                  q_pos[qo], kv_pos[ko],
-                                                  cu_seqlens, scale, window=window)
+                o_t, l_t = partial_attention(Q[qo], K[ko], V[ko], q_pos[qo], kv_pos[ko],
+                                             cu_seqlens, scale, window=window)
+                slots[qo][ko] = (round_bf16(o_t) if partial_dtype == "bf16" else o_t, l_t)
         outs = [lse_merge(slots[qo]) for qo in range(R)]
     O = np.concatenate([o for o, _ in outs], axis=0)
     LSE = np.concatenate([l for _, l in outs], axis=1)

@@ -463,3 +463,61 @@ def test_ring_backward_steps_sum_to_whole():
     parts = [oracle.ring_backward(*args, steps=[t]) for t in range(R)]
     for i in range(3):
         np.testing.assert_allclose(sum(p[i] for p in parts), whole[i], atol=1e-13)
+
+
+# ---------------------------------------------------------------- bf16 storage rounding
+def test_round_bf16_hand_values():
+    """Values pinned by hand: representable values stay, ties go to the even
+    significand, subnormals keep the 2^-133 spacing, the overflow point and
+    above become infinite."""
+    r = oracle.round_bf16
+    keep = np.array([0.0, 1.0, 1.0 + 2.0 ** -7, -3.0, 2.0 ** -126, 2.0 ** -133,
+                     255.0 * 2.0 ** 120, -(2.0 - 2.0 ** -7) * 2.0 ** 127])
+    assert np.array_equal(r(keep), keep)
+    assert r(1.0 + 2.0 ** -8) == 1.0                       # tie, down to even
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6       # tie, up to even
+    assert r(-(1.0 + 2.0 ** -8)) == -1.0
+    assert r(1.0 + 2.0 ** -8 + 2.0 ** -30) == 1.0 + 2.0 ** -7  # above the tie
+    assert r(1.5 * 2.0 ** -133) == 2.0 ** -132            # subnormal tie to even
+    assert r(0.5 * 2.0 ** -133) == 0.0                     # half the smallest: to even (0)
+    assert r((2.0 - 2.0 ** -8) * 2.0 ** 127) == np.inf     # the overflow point
+    assert r((2.0 - 2.0 ** -8 - 2.0 ** -20) * 2.0 ** 127) == (2.0 - 2.0 ** -7) * 2.0 ** 127
+    assert np.isnan(r(np.nan)) and r(-np.inf) == -np.inf
+
+
+def test_round_bf16_matches_torch_conversion():
+    """On fp32 inputs over the whole exponent range the oracle's rounding is
+    the library's round-to-nearest-even fp32 -> bf16 conversion, bit for
+    bit."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(200000) * np.exp2(rng.uniform(-140, 126, 200000))).astype(np.float32)
+    # plus every tie of the first few binades
+    ties = (np.arange(1, 4096, dtype=np.float64) * 2.0 ** -16 + 1.0).astype(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(x.astype(np.float64))
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), x[~same][:5]
+
+
+def test_ring_forward_bf16_partials_pass_q():
+    """Pass Q with bf16 partial slots: each slot's O is rounded before the
+    merge, so O moves by at most half a bf16 ulp of the largest partial
+    (relative 2^-8 of it) and the LSE not at all; Pass KV ignores the
+    option."""
+    R, n, H, d = 4, 8, 2, 4
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((R * 2 * n, H, d))
+    k = rng.standard_normal((R * 2 * n, H, d))
+    v = rng.standard_normal((R * 2 * n, H, d))
+    qpos, kvpos = oracle.plan_positions(R * 2 * n, R, "zigzag")
+    O32, L32 = oracle.ring_forward(q, k, v, qpos, kvpos, variant="pass_q")
+    O16, L16 = oracle.ring_forward(q, k, v, qpos, kvpos, variant="pass_q", partial_dtype="bf16")
+    assert np.array_equal(L16, L32)
+    diff = np.abs(O16 - O32)
+    assert diff.max() > 0                                      # the rounding happened
+    assert (diff <= 2.0 ** -8 * np.abs(v).max() + 1e-15).all()
+    Ok, Lk = oracle.ring_forward(q, k, v, qpos, kvpos, variant="pass_kv", partial_dtype="bf16")
+    Ok32, _ = oracle.ring_forward(q, k, v, qpos, kvpos, variant="pass_kv")
+    assert np.array_equal(Ok, Ok32)

@@ -150,3 +150,49 @@ def test_step_chaining_flag_is_validated():
     lib = cpa.load()
     assert lib.cp_attn_plan_set_chaining(plan.handle, 2) == 1  # CP_ATTN_ERR_INVALID_ARG
     assert lib.cp_attn_plan_set_chaining(None, 1) == 1  # CP_ATTN_ERR_INVALID_ARG
+
+
+def _round256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_partial_and_grad_dtypes_set_the_workspace():
+    """bf16 Pass-Q partials halve the R partial slots (the LSE slots stay
+    fp32); bf16 gradients add the three fp32 accumulators to the backward
+    workspace. Host-only plans, sizes from the element counts."""
+    N, R, Hq, Hkv, d = 2048, 4, 8, 2, 128
+    base = cpa.Plan(N, R, Hq, Hkv, d, variant="pass_q")
+    half = cpa.Plan(N, R, Hq, Hkv, d, variant="pass_q", partial_dtype="bf16")
+    o_el, l_el = N * Hq * d, N * Hq
+    assert base.workspace_size(cpa.OP_FORWARD) == _round256(o_el * R * 4) + _round256(l_el * R * 4)
+    assert half.workspace_size(cpa.OP_FORWARD) == _round256(o_el * R * 2) + _round256(l_el * R * 4)
+    # Pass KV keeps its fp32 running output whatever the partial type
+    kv = cpa.Plan(N, R, Hq, Hkv, d, variant="pass_kv", partial_dtype="bf16")
+    assert kv.workspace_size(cpa.OP_FORWARD) == _round256(o_el * 4)
+    g32 = cpa.Plan(N, R, Hq, Hkv, d)
+    g16 = cpa.Plan(N, R, Hq, Hkv, d, grad_dtype="bf16")
+    k_el = N * Hkv * d
+    extra = _round256(o_el * 4) + 2 * _round256(k_el * 4)
+    assert g16.workspace_size(cpa.OP_BACKWARD) == g32.workspace_size(cpa.OP_BACKWARD) + extra
+    assert (half.partial_dtype, g16.grad_dtype, base.partial_dtype) == (cpa.BF16, cpa.BF16, cpa.F32)
+
+
+@pytest.mark.parametrize("field", ["partial_dtype", "grad_dtype"])
+def test_plan_rejects_unknown_dtype(field):
+    with pytest.raises(cpa.CpAttnError) as e:
+        cpa.Plan(1024, 4, 2, 1, 64, **{field: 2})
+    assert e.value.status == 1  # CP_ATTN_ERR_INVALID_ARG
+
+
+def test_merge_rejects_unknown_parts_dtype_and_overlap():
+    """Argument checks of cp_attn_merge_lse_ex that need no device: an
+    unknown dtype, and an fp32 output that overlaps bf16 parts (both fail
+    before any launch; the pointers are never dereferenced)."""
+    lib = cpa.load()
+    base = 1 << 20
+    # parts_dtype 7: ERR_INVALID_ARG
+    assert lib.cp_attn_merge_lse_ex(2, 4, 1, 64, 7, base, 256, base + 4096, 4, None, None,
+                                    base + 8192, None) == 1
+    # bf16 parts [base, base + 2*(256 + 256)*2) and an fp32 output starting inside them
+    assert lib.cp_attn_merge_lse_ex(2, 4, 1, 64, cpa.BF16, base, 256, base + 65536, 4, None,
+                                    base + 512, base + 131072, None) == 1
