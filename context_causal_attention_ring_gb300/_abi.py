@@ -57,6 +57,7 @@ class _PlanDesc(ctypes.Structure):
         ("a2a", ctypes.c_int),
         ("partial_dtype", ctypes.c_int),
         ("grad_dtype", ctypes.c_int),
+        ("batch", ctypes.c_int),
     ]
 
 
@@ -253,7 +254,7 @@ class Plan:
                  head_dim: int, layout: str = "zigzag", variant: str = "pass_kv",
                  cu_seqlens=None, kv_prefix_len: int = 0,
                  softmax_scale: float = 0.0, window: int = 0, a2a: int = 1,
-                 partial_dtype: str = "f32", grad_dtype: str = "f32"):
+                 partial_dtype: str = "f32", grad_dtype: str = "f32", batch: int = 1):
         lib = load()
         self._keep = None
         desc = _PlanDesc()
@@ -275,14 +276,15 @@ class Plan:
         desc.a2a = int(a2a)
         desc.partial_dtype = DTYPES[partial_dtype] if isinstance(partial_dtype, str) else int(partial_dtype)
         desc.grad_dtype = DTYPES[grad_dtype] if isinstance(grad_dtype, str) else int(grad_dtype)
+        desc.batch = int(batch)
         h = _P()
         _check(lib.cp_attn_plan_ex(ctypes.byref(h), ctypes.byref(desc)))
         self.handle = h
-        info = (_I64 * 15)()
-        _check(lib.cp_attn_plan_info(h, info, 15))
+        info = (_I64 * 16)()
+        _check(lib.cp_attn_plan_info(h, info, 16))
         (self.T_q, self.T_kv, self.n_q, self.n_kv, self.R, self.Hq, self.Hkv,
          self.d, self.n_qt, self.n_kt, self.n_docs, on_dev, var,
-         self.window, self.a2a) = [int(x) for x in info]
+         self.window, self.a2a, self.batch) = [int(x) for x in info]
         self.on_device = bool(on_dev)
         self.layout = layout
         # the ring ordering in use ("auto" resolved by the library)

@@ -168,7 +168,13 @@ cp_attn_status upload_plan(cp_attn_plan_s* p) {
     return CP_ATTN_OK;
   }
   std::vector<int32_t> row_q(p->q_pos.size()), row_kv(p->kv_pos.size());
-  for (size_t i = 0; i < row_q.size(); ++i) row_q[i] = static_cast<int32_t>(p->q_pos[i] - p->P);
+  // natural query row of position x: sequence b = x / (P + N), then its new
+  // token x - b (P + N) - P
+  const int64_t seq = p->P + p->N;
+  for (size_t i = 0; i < row_q.size(); ++i) {
+    const int64_t b = p->q_pos[i] / seq;
+    row_q[i] = static_cast<int32_t>(b * p->N + (p->q_pos[i] - b * seq - p->P));
+  }
   for (size_t i = 0; i < row_kv.size(); ++i) row_kv[i] = static_cast<int32_t>(p->kv_pos[i]);
   const int32_t zeros[kStatusWords] = {0, 0, 0, 0};
   cp_attn_status st;
@@ -287,11 +293,11 @@ cp_attn_status cp_attn_select_variant(int64_t n_new, int64_t n_cached, int n_q_h
 
 cp_attn_status cp_attn_plan_info(cp_attn_plan_t p, int64_t* info, int n) {
   clear_error();
-  if (!p || !info || n < 0 || n > 15) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_info: bad arguments");
-  const int64_t v[15] = {p->T_q, p->T_kv, p->n_q, p->n_kv, p->R, p->Hq, p->Hkv, p->d,
+  if (!p || !info || n < 0 || n > 16) return fail(CP_ATTN_ERR_INVALID_ARG, "plan_info: bad arguments");
+  const int64_t v[16] = {p->T_q, p->T_kv, p->n_q, p->n_kv, p->R, p->Hq, p->Hkv, p->d,
                          p->n_qt, p->n_kt, static_cast<int64_t>(p->cu.size()) - 1,
                          p->on_device ? 1 : 0, static_cast<int64_t>(p->variant), p->window,
-                         p->a2a};
+                         p->a2a, p->B};
   for (int i = 0; i < n; ++i) info[i] = v[i];
   return CP_ATTN_OK;
 }

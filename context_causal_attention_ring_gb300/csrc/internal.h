@@ -39,6 +39,7 @@ struct cp_attn_plan_s {
   // description
   int64_t N = 0;   // new tokens
   int64_t P = 0;   // cached prefix
+  int64_t B = 1;   // independent sequences (each P + N tokens)
   int R = 0, Hq = 0, Hkv = 0, d = 0;
   cp_attn_layout layout = CP_ATTN_LAYOUT_ZIGZAG;
   int a2a = 1;              // USP all-to-all group size

@@ -119,7 +119,9 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
     return fail(CP_ATTN_ERR_SHAPE,
                 "plan: seq_len and kv_prefix_len must be multiples of " +
                     std::to_string(unit) + " (every chunk a multiple of 128 tokens)");
-  if (N + P > (1LL << 31) - 1024)
+  if (desc->batch < 0) return fail(CP_ATTN_ERR_SHAPE, "plan: batch must be >= 0");
+  const int64_t B = desc->batch > 0 ? desc->batch : 1;
+  if (B * (N + P) > (1LL << 31) - 1024)
     return fail(CP_ATTN_ERR_SHAPE, "plan: total tokens must fit in int32 positions");
   if (!(desc->softmax_scale >= 0.f) || std::isinf(desc->softmax_scale))
     return fail(CP_ATTN_ERR_INVALID_ARG, "plan: softmax_scale must be finite and >= 0");
@@ -129,6 +131,7 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
 
   p->N = N;
   p->P = P;
+  p->B = B;
   p->R = R;
   p->Hq = desc->n_q_heads;
   p->Hkv = desc->n_kv_heads;
@@ -140,39 +143,46 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
   p->variant = desc->variant == CP_ATTN_VARIANT_AUTO
                    ? select_variant_rule(N, P, desc->n_q_heads, desc->n_kv_heads)
                    : desc->variant;
-  // a window as long as the whole sequence masks nothing
+  // a window as long as a whole sequence masks nothing
   p->window = desc->window >= N + P ? 0 : desc->window;
   p->scale = desc->softmax_scale > 0.f ? desc->softmax_scale
                                        : static_cast<float>(1.0 / std::sqrt(static_cast<double>(p->d)));
-  // documents
+  // documents; sequence b of the batch occupies positions [b L, (b + 1) L)
   p->cu.clear();
-  const int64_t total = N + P;
+  const int64_t L = N + P;
+  const int64_t total = B * L;
   if (desc->cu_seqlens) {
     if (desc->n_docs < 1) return fail(CP_ATTN_ERR_SHAPE, "plan: n_docs must be >= 1");
     for (int i = 0; i <= desc->n_docs; ++i) p->cu.push_back(desc->cu_seqlens[i]);
     if (p->cu.front() != 0 || p->cu.back() != total)
-      return fail(CP_ATTN_ERR_SHAPE, "plan: cu_seqlens must start at 0 and end at kv_prefix_len + seq_len");
+      return fail(CP_ATTN_ERR_SHAPE,
+                  "plan: cu_seqlens must start at 0 and end at batch * (kv_prefix_len + seq_len)");
     for (int i = 0; i < desc->n_docs; ++i)
       if (p->cu[i + 1] <= p->cu[i])
         return fail(CP_ATTN_ERR_SHAPE, "plan: cu_seqlens must be strictly increasing");
+    for (int64_t b = 1; b < B; ++b)
+      if (!std::binary_search(p->cu.begin(), p->cu.end(), static_cast<int32_t>(b * L)))
+        return fail(CP_ATTN_ERR_SHAPE, "plan: cu_seqlens must contain every sequence start");
   } else {
-    p->cu = {0, static_cast<int32_t>(total)};
+    for (int64_t b = 0; b <= B; ++b) p->cu.push_back(static_cast<int32_t>(b * L));
   }
 
-  // positions
-  p->n_q = N / R;
-  p->n_kv = (N + P) / R;
-  p->T_q = N;
-  p->T_kv = N + P;
+  // positions: per rank, its shard of sequence 0, then of sequence 1, ...
+  p->n_q = B * N / R;
+  p->n_kv = B * L / R;
+  p->T_q = B * N;
+  p->T_kv = B * L;
   p->n_qt = static_cast<int>(p->n_q / kTile);
   p->n_kt = static_cast<int>(p->n_kv / kTile);
   p->q_pos.clear();
   p->kv_pos.clear();
-  for (int r = 0; r < R; ++r) shard(N, R, p->layout, p->a2a, P, r, p->q_pos);
-  for (int r = 0; r < R; ++r) {
-    if (P > 0) shard(P, R, p->layout, p->a2a, 0, r, p->kv_pos);
-    shard(N, R, p->layout, p->a2a, P, r, p->kv_pos);
-  }
+  for (int r = 0; r < R; ++r)
+    for (int64_t b = 0; b < B; ++b) shard(N, R, p->layout, p->a2a, b * L + P, r, p->q_pos);
+  for (int r = 0; r < R; ++r)
+    for (int64_t b = 0; b < B; ++b) {
+      if (P > 0) shard(P, R, p->layout, p->a2a, b * L, r, p->kv_pos);
+      shard(N, R, p->layout, p->a2a, b * L + P, r, p->kv_pos);
+    }
   p->q_tile_pos.resize(static_cast<size_t>(R) * p->n_qt);
   p->kv_tile_pos.resize(static_cast<size_t>(R) * p->n_kt);
   for (size_t i = 0; i < p->q_tile_pos.size(); ++i) {

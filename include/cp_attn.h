@@ -168,6 +168,18 @@ typedef struct cp_attn_plan_desc {
                              and rounded to nearest even once at the end.
                              The step-level cp_attn_step_bwd always adds to
                              fp32 accumulators. */
+  int batch;              /* B >= 1 independent sequences of kv_prefix_len +
+                             seq_len tokens each (0 means 1). Each sequence is
+                             sharded over the ring as described for the
+                             layout; rank r holds its part of sequence 0, then
+                             of sequence 1, ... Natural order is sequence-
+                             major: q/dout [B*seq_len, Hq, d], k/v
+                             [B*(kv_prefix_len+seq_len), Hkv, d]. Positions
+                             live in one space where sequence b starts at
+                             b*(kv_prefix_len+seq_len); cu_seqlens, when
+                             given, covers all B*(kv_prefix_len+seq_len)
+                             positions and must contain every sequence
+                             start (NULL: one document per sequence). */
 } cp_attn_plan_desc;
 
 /* Build a plan: per-rank positions (zigzag or contiguous), the per-step
@@ -198,12 +210,12 @@ cp_attn_status cp_attn_select_variant(int64_t n_new, int64_t n_cached, int n_q_h
                                       int n_kv_heads, cp_attn_variant* out);
 void cp_attn_plan_destroy(cp_attn_plan_t plan);
 
-/* Sizes of a plan, written to info[0..n-1] (n <= 15):
+/* Sizes of a plan, written to info[0..n-1] (n <= 16):
  * 0 T_q (= R*n_q), 1 T_kv (= R*n_kv), 2 n_q (query rows per rank),
  * 3 n_kv (KV rows per rank), 4 R, 5 Hq, 6 Hkv, 7 d, 8 q tiles per rank,
  * 9 kv tiles per rank, 10 n_docs, 11 has device tables (0/1),
  * 12 ring ordering (cp_attn_variant, AUTO resolved), 13 window,
- * 14 a2a (1 unless USP). */
+ * 14 a2a (1 unless USP), 15 batch. */
 cp_attn_status cp_attn_plan_info(cp_attn_plan_t plan, int64_t* info, int n);
 
 /* Host queries (bit-exact plan artefacts; no device needed).

@@ -59,6 +59,7 @@ __all__ = [
     "rank_chunks",
     "shard_positions",
     "plan_positions",
+    "batch_cu_seqlens",
     "ring_schedule",
     "doc_index",
     "visible_mask",
@@ -128,22 +129,40 @@ def shard_positions(n_tokens: int, R: int, layout: str = "zigzag",
 
 
 def plan_positions(seq_len: int, R: int, layout: str = "zigzag",
-                   kv_prefix_len: int = 0, a2a: int = 1):
+                   kv_prefix_len: int = 0, a2a: int = 1, batch: int = 1):
     """Per-rank global positions of the query tokens and of the KV tokens.
 
     Full prefill: Q and KV are the same tokens. Partial prefill (a cached
     prefix of length P): the cache and the new tokens are each sharded the
     same way; rank r's KV is its cache shard followed by its new-token shard,
     and the new tokens (the queries) sit at positions P, P+1, ...
+    A batch of B independent sequences (reading: each one sharded on its
+    own, a rank holding its part of sequence 0, then of sequence 1, ...)
+    lives in one position space where sequence b starts at b*(P + seq_len);
+    its documents must separate the sequences (batch_cu_seqlens).
     """
     P = int(kv_prefix_len)
-    q_pos = shard_positions(seq_len, R, layout, offset=P, a2a=a2a)
-    if P == 0:
-        kv_pos = [p.copy() for p in q_pos]
-    else:
-        cache = shard_positions(P, R, layout, offset=0, a2a=a2a)
-        kv_pos = [np.concatenate([cache[r], q_pos[r]]) for r in range(R)]
+    L = P + int(seq_len)
+    q_pos = [[] for _ in range(R)]
+    kv_pos = [[] for _ in range(R)]
+    for b in range(int(batch)):
+        new = shard_positions(seq_len, R, layout, offset=b * L + P, a2a=a2a)
+        cache = shard_positions(P, R, layout, offset=b * L, a2a=a2a) if P else None
+        for r in range(R):
+            q_pos[r].append(new[r])
+            if cache is not None:
+                kv_pos[r].append(cache[r])
+            kv_pos[r].append(new[r])
+    q_pos = [np.concatenate(x) for x in q_pos]
+    kv_pos = [np.concatenate(x) for x in kv_pos]
     return q_pos, kv_pos
+
+
+def batch_cu_seqlens(seq_len: int, batch: int, kv_prefix_len: int = 0) -> np.ndarray:
+    """Document offsets of a batch: one document per sequence of
+    kv_prefix_len + seq_len positions."""
+    L = int(kv_prefix_len) + int(seq_len)
+    return np.arange(int(batch) + 1, dtype=np.int64) * L
 
 
 def ring_schedule(R: int, variant: str = "pass_kv"):

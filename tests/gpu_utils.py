@@ -75,9 +75,14 @@ class DeviceRun:
             self.dout = torch.empty_like(do)
             plan.layout_apply(cpa.TENSOR_Q, cpa.TO_RANK_MAJOR, do, self.dout)
         del q, k, v
-        # natural row of each rank-major row
+        # natural row of each rank-major row (sequence b of a batch holds
+        # positions [b L, (b + 1) L), L = prefix + new tokens)
         P = plan.kv_prefix_len
-        self.q_nat = np.concatenate([plan.positions(cpa.TENSOR_Q, r) for r in range(plan.R)]) - P
+        N = plan.T_q // plan.batch
+        L = plan.T_kv // plan.batch
+        qpos = np.concatenate([plan.positions(cpa.TENSOR_Q, r) for r in range(plan.R)])
+        b = qpos // L
+        self.q_nat = b * N + (qpos - b * L - P)
         self.kv_nat = np.concatenate([plan.positions(cpa.TENSOR_KV, r) for r in range(plan.R)])
 
     def forward(self):

@@ -64,9 +64,15 @@ CASES = [
      [lambda: pins.test_ring_equals_monolithic("pass_kv", "zigzag", False)]),
     ("lse_merge", "np.exp(lses - LSE_safe[None])", "np.exp(lses - M_safe[None])",
      [lambda: pins.test_ring_equals_monolithic("pass_q", "zigzag", False)]),
-    ("plan_positions", "np.concatenate([cache[r], q_pos[r]])",
-     "np.concatenate([q_pos[r], cache[r]])",
+    ("plan_positions", """            if cache is not None:
+                kv_pos[r].append(cache[r])
+            kv_pos[r].append(new[r])""",
+     """            kv_pos[r].append(new[r])
+            if cache is not None:
+                kv_pos[r].append(cache[r])""",
      [pins.test_partial_prefill_plan]),
+    ("plan_positions", "offset=b * L + P, a2a=a2a)", "offset=b * int(seq_len) + P, a2a=a2a)",
+     [pins.test_batch_positions_partition_and_balance]),
     ("_pair_backward", "ds = p * (dp - D[h, r0:r1][:, None])", "ds = p * dp",
      [lambda: pins.test_backward_finite_differences(None)]),
     ("_pair_backward", "dq[r0:r1, h, :] += scale * (ds @ kk)",

@@ -521,3 +521,27 @@ def test_ring_forward_bf16_partials_pass_q():
     Ok, Lk = oracle.ring_forward(q, k, v, qpos, kvpos, variant="pass_kv", partial_dtype="bf16")
     Ok32, _ = oracle.ring_forward(q, k, v, qpos, kvpos, variant="pass_kv")
     assert np.array_equal(Ok, Ok32)
+
+
+def test_batch_positions_partition_and_balance():
+    """A batch's positions: the ranks together hold every position of the B
+    sequences exactly once, each sequence's tokens are split evenly, and
+    within each sequence every rank sees the same number of causal pairs
+    (the zigzag balance of one sequence, sequence by sequence)."""
+    B, N, P, R = 3, 512, 512, 2
+    L = N + P
+    q_pos, kv_pos = oracle.plan_positions(N, R, "zigzag", kv_prefix_len=P, batch=B)
+    allkv = np.sort(np.concatenate(kv_pos))
+    assert np.array_equal(allkv, np.arange(B * L))
+    allq = np.sort(np.concatenate(q_pos))
+    assert np.array_equal(allq, np.concatenate([b * L + P + np.arange(N) for b in range(B)]))
+    cu = oracle.batch_cu_seqlens(N, B, P)
+    for b in range(B):
+        per_rank = []
+        for r in range(R):
+            mine = q_pos[r][(q_pos[r] >= b * L) & (q_pos[r] < (b + 1) * L)]
+            assert len(mine) == N // R
+            per_rank.append(oracle.count_visible(mine, allkv, cu))
+        assert len(set(per_rank)) == 1
+        # a query of sequence b sees exactly its own sequence's earlier tokens
+        assert sum(per_rank) == sum(P + j + 1 for j in range(N))

@@ -196,3 +196,49 @@ def test_merge_rejects_unknown_parts_dtype_and_overlap():
     # bf16 parts [base, base + 2*(256 + 256)*2) and an fp32 output starting inside them
     assert lib.cp_attn_merge_lse_ex(2, 4, 1, 64, cpa.BF16, base, 256, base + 65536, 4, None,
                                     base + 512, base + 131072, None) == 1
+
+
+@pytest.mark.parametrize("B,N,P,R,variant", [
+    (3, 1024, 0, 4, "pass_kv"),
+    (2, 512, 1536, 2, "pass_q"),
+    (4, 512, 0, 2, "pass_q"),
+])
+def test_batch_plan_bit_exact(B, N, P, R, variant):
+    """A batch of B sequences: positions (each sequence sharded on its own,
+    sequence-major within a rank), the one-document-per-sequence offsets and
+    the block classes bit-exact against the oracle's brute force; tiles of
+    different sequences are EMPTY; visible pairs are B times one sequence's."""
+    p = cpa.Plan(N, R, 2, 1, 64, variant=variant, kv_prefix_len=P, batch=B)
+    assert (p.batch, p.T_q, p.T_kv, p.n_docs) == (B, B * N, B * (N + P), B)
+    q_pos, kv_pos = oracle.plan_positions(N, R, "zigzag", kv_prefix_len=P, batch=B)
+    cu = oracle.batch_cu_seqlens(N, B, P)
+    for r in range(R):
+        assert np.array_equal(p.positions(cpa.TENSOR_Q, r), q_pos[r])
+        assert np.array_equal(p.positions(cpa.TENSOR_KV, r), kv_pos[r])
+    bm = p.block_mask()
+    assert np.array_equal(bm, oracle.block_mask(q_pos, kv_pos, cu))
+    one = cpa.Plan(N, R, 2, 1, 64, variant=variant, kv_prefix_len=P)
+    assert p.visible_pairs() == B * one.visible_pairs()
+    sched = oracle.ring_schedule(R, variant)
+    for t in range(R):
+        exp = sum(oracle.count_visible(q_pos[qo], kv_pos[ko], cu) for qo, ko in sched[t])
+        assert p.visible_pairs(t) == exp
+
+
+def test_batch_with_documents_and_bad_offsets():
+    """Documents inside a batch: cu_seqlens covers the whole batch and must
+    contain every sequence start."""
+    N, R, B = 1024, 2, 2
+    cu = np.array([0, 300, 1024, 1500, 2048], dtype=np.int32)
+    p = cpa.Plan(N, R, 2, 1, 64, cu_seqlens=cu, batch=B)
+    q_pos, kv_pos = oracle.plan_positions(N, R, "zigzag", batch=B)
+    assert np.array_equal(p.block_mask(), oracle.block_mask(q_pos, kv_pos, cu))
+    with pytest.raises(cpa.CpAttnError) as e:   # misses the start of sequence 1 (1024)
+        cpa.Plan(N, R, 2, 1, 64, cu_seqlens=[0, 300, 1500, 2048], batch=B)
+    assert e.value.status == 2
+    with pytest.raises(cpa.CpAttnError) as e:   # ends at one sequence's length
+        cpa.Plan(N, R, 2, 1, 64, cu_seqlens=[0, 1024], batch=B)
+    assert e.value.status == 2
+    with pytest.raises(cpa.CpAttnError) as e:
+        cpa.Plan(N, R, 2, 1, 64, batch=-1)
+    assert e.value.status == 2
