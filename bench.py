@@ -40,7 +40,7 @@ PROFILED_TRAFFIC = {
     "step_bwd": ("context_causal_attention_ring_gb300/csrc/step_bwd.cu",
                  "a662b08e9cd0ec616e01d1bf47a75b9b02a3a44f8c008dc149a884986215c990", 3.102382e9),
     "step_fwd": ("context_causal_attention_ring_gb300/csrc/step_fwd.cu",
-                 "ac5c1f474e66330e520fa5f8d3118fa8562c79b8da5ba0c7020367774e078c03", 1.295558e9),
+                 "f4fc50876e8994d130ae17e023bed0c52b0f413a83d691661fb2569d1bfa47a8", 1.295203e9),
 }
 
 

@@ -463,7 +463,10 @@ static_assert(FwdPairSmemT<true>::kAlloc <= 232448, "pair kernel shared memory")
 // running maximum moves when it grows by more than 2^4 (so P * 2^4 <= 2^8 =
 // 256 < 448, the largest E4M3 value), and the per-tensor descale
 // factors p.scales[0..2] (q, k, v) multiply the scores and the output.
-template <bool F8>
+// PB: WRITE_PARTIAL with bf16 partials (the slot holds bf16 elements at the
+// same element offsets); a separate instance, so that the fp32 epilogue keeps
+// its registers.
+template <bool F8, bool PB>
 __global__ void __launch_bounds__(kThreadsP, 1)
     step_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -823,13 +826,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const bool merge = (p.mode == CP_ATTN_ACCUMULATE) && !p.first;
       float* o_dst = p.o_part;
       float* lse_dst = p.lse_part;
-      // WRITE_PARTIAL with bf16 partials: the slot holds bf16 elements
-      const bool part_bf16 = p.part_bf16 && p.mode == CP_ATTN_WRITE_PARTIAL;
-      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.o_part);
+      __nv_bfloat16* ob = nullptr;  // PB: the bf16 slot
       if (p.mode == CP_ATTN_WRITE_PARTIAL) {
         const int64_t slot = static_cast<int64_t>(w.kv_owner) * p.T_q * p.Hq * D;
+        if constexpr (PB) ob = reinterpret_cast<__nv_bfloat16*>(p.o_part) + slot;
         o_dst += slot;
-        ob += slot;
         lse_dst += static_cast<int64_t>(w.kv_owner) * p.Hq * p.T_q;
       }
       if (merge) {
@@ -908,14 +909,20 @@ __global__ void __launch_bounds__(kThreadsP, 1)
               v.w = fmaf(old[it].w, b_r[it], v.w);
             }
             const int64_t off = base_off + row * row_stride + c * 32;
-            uint2 pk;
-            pk.x = ptx::pack_bf16(v.x, v.y);
-            pk.y = ptx::pack_bf16(v.z, v.w);
-            if (part_bf16)
+            if constexpr (PB) {
+              uint2 pk;
+              pk.x = ptx::pack_bf16(v.x, v.y);
+              pk.y = ptx::pack_bf16(v.z, v.w);
               *reinterpret_cast<uint2*>(ob + off) = pk;
-            else if (!keep_old)
-              *reinterpret_cast<float4*>(o_dst + off) = v;
-            if (p.o_final) *reinterpret_cast<uint2*>(p.o_final + off) = pk;
+            } else {
+              if (!keep_old) *reinterpret_cast<float4*>(o_dst + off) = v;
+              if (p.o_final) {
+                uint2 pk;
+                pk.x = ptx::pack_bf16(v.x, v.y);
+                pk.y = ptx::pack_bf16(v.z, v.w);
+                *reinterpret_cast<uint2*>(p.o_final + off) = pk;
+              }
+            }
           }
           if (merge && c + 1 < D / 32) {
 #pragma unroll
@@ -946,14 +953,16 @@ int step_fwd_heads_per_cta(int d) { return d == 128 ? 2 : 1; }
 cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, const FwdParams& p, bool chained) {
-  static bool attr_done[2] = {false, false};
+  static bool attr_done[3] = {false, false, false};
   cudaError_t err;
   if (d == 128) {
-    if (!attr_done[1]) {
-      err = cudaFuncSetAttribute(step_fwd_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool pb = p.part_bf16 != 0;
+    auto kernel = pb ? step_fwd_pair_kernel<false, true> : step_fwd_pair_kernel<false, false>;
+    if (!attr_done[pb ? 2 : 1]) {
+      err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
       if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd attr: ") + cudaGetErrorString(err));
-      attr_done[1] = true;
+      attr_done[pb ? 2 : 1] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -965,7 +974,7 @@ cp_attn_status launch_step_fwd(int d, dim3 grid, size_t smem, cudaStream_t s,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = chained ? 1 : 0;
-    err = cudaLaunchKernelEx(&cfg, step_fwd_pair_kernel<false>, tq, tk, tv, p);
+    err = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p);
     if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd launch: ") + cudaGetErrorString(err));
   } else {
     if (!attr_done[0]) {
@@ -987,13 +996,15 @@ size_t step_fwd_fp8_smem_bytes() { return FwdPairSmemT<true>::kAlloc; }
 cp_attn_status launch_step_fwd_fp8(dim3 grid, size_t smem, cudaStream_t s,
                                    const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tvt, const FwdParams& p, bool chained) {
-  static bool attr_done = false;
+  static bool attr_done[2] = {false, false};
   cudaError_t err;
-  if (!attr_done) {
-    err = cudaFuncSetAttribute(step_fwd_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool pb = p.part_bf16 != 0;
+  auto kernel = pb ? step_fwd_pair_kernel<true, true> : step_fwd_pair_kernel<true, false>;
+  if (!attr_done[pb ? 1 : 0]) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
     if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd_fp8 attr: ") + cudaGetErrorString(err));
-    attr_done = true;
+    attr_done[pb ? 1 : 0] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -1005,7 +1016,7 @@ cp_attn_status launch_step_fwd_fp8(dim3 grid, size_t smem, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = chained ? 1 : 0;
-  err = cudaLaunchKernelEx(&cfg, step_fwd_pair_kernel<true>, tq, tk, tvt, p);
+  err = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tvt, p);
   if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("step_fwd_fp8 launch: ") + cudaGetErrorString(err));
   count_launch();
   return CP_ATTN_OK;
