@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -143,16 +144,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_sample(w, budget_heads: int, inp=None):
+def cpu_oracle_sample(w, n_heads_sample: int, inp=None):
     """Time the fp64 oracle's forward and backward of one off-diagonal ring
-    pair (step 1, rank 1) over `budget_heads` query heads. Returns
+    pair (step 1, rank 1) over `n_heads_sample` query heads. Returns
     (TFLOPS, seconds, description)."""
     import oracle
     if inp is None:
         inp = make_inputs(w)
     q_pos, kv_pos = oracle.plan_positions(w.seq_len, w.cp, w.layout, w.kv_prefix_len)
     qo, ko = 1 % w.cp, 0
-    H = min(budget_heads, w.n_q_heads)
+    H = min(n_heads_sample, w.n_q_heads)
     G = w.group
     Hk = max(1, H // G)
     qrows = q_pos[qo] - w.kv_prefix_len
@@ -313,8 +314,9 @@ def run_ours(args, w):
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
               for _ in range(args.steps)]
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/cp_clocks.csv")
+    clocks_csv = (args.clocks_csv.replace("{rank}", str(rank)) if args.clocks_csv
+                  else os.path.join(tempfile.gettempdir(), f"cp_attn_clocks_rank{rank}.csv"))
+    sampler = ClockSampler(local, clocks_csv)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -817,6 +819,9 @@ def main():
                     help="time the FP8 (E4M3) forward against bf16 on the 405B-shaped prefill")
     ap.add_argument("--fp8-workload", default="prefill_405b_full", choices=sorted(WORKLOADS),
                     help="workload of --fp8")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="where the nvidia-smi clock samples of the timed region go "
+                         "('{rank}' is replaced by the rank); a temporary file by default")
     ap.add_argument("--decode", action="store_true",
                     help="time the one-row decode against the HBM roofline")
     args = ap.parse_args()

@@ -7,7 +7,7 @@ Source: [CP-Inference] "Context Parallelism for Scalable Million-Token
 Inference", "Experimental Setup & Results" (Model and Quantization): the
 Llama 3 405B model of the benchmarks is quantized to FP8 throughout, for
 memory and throughput. The pages name neither the FP8 format nor how the
-scales are chosen. Readings (each is listed in the design doc):
+scales are chosen. Readings:
 
 * The format is E4M3 as defined by the OCP 8-bit floating point
   specification: one sign bit, four exponent bits with bias 7, three

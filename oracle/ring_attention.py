@@ -22,7 +22,7 @@ Sources (page title, then section):
   vs. Tensor Parallelism (TP)" (grouped-query heads: few KV heads shared by
   many Q heads).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 * Rank r holds chunks r and 2R-1-r, in that order ("Load Balancing in CP"
   says rank 0 may take the first and last chunk).
 * Ring direction: at step t rank r holds the KV (Pass KV) or the Q (Pass Q)
