@@ -182,10 +182,15 @@ typedef struct cp_attn_plan_desc {
                              start (NULL: one document per sequence). */
 } cp_attn_plan_desc;
 
-/* Build a plan: per-rank positions (zigzag or contiguous), the per-step
- * (q_owner, kv_owner) schedule, the 128x128 block classes and the per-step
- * work lists, uploaded to the current CUDA device if there is one (a plan
- * made without a device serves the host-side queries only).
+/* Build a plan: per-rank positions (zigzag or contiguous; "Context
+ * Parallelism for Scalable Million-Token Inference", "Load Balancing in CP"),
+ * the per-step (q_owner, kv_owner) schedule (same page, "Ring Attention
+ * Algorithms"), the 128x128 block classes (fully masked blocks skipped,
+ * packed sequences without padding: "Announcing Long-Context Training on
+ * TPUs with MaxText Context Parallelism", "Built on a fast attention
+ * kernel") and the per-step work lists, uploaded to the current CUDA device
+ * if there is one (a plan made without a device serves the host-side
+ * queries only).
  * Chunk rule: zigzag needs N and P to be multiples of 256*R; USP multiples
  * of 256*R*a2a; contiguous multiples of 128*R. Returns ERR_SHAPE otherwise. On success *out
  * owns host and device tables until cp_attn_plan_destroy. */
@@ -218,7 +223,9 @@ void cp_attn_plan_destroy(cp_attn_plan_t plan);
  * 14 a2a (1 unless USP), 15 batch. */
 cp_attn_status cp_attn_plan_info(cp_attn_plan_t plan, int64_t* info, int n);
 
-/* Host queries (bit-exact plan artefacts; no device needed).
+/* Host queries (bit-exact plan artefacts; no device needed): the layout of
+ * "Load Balancing in CP" and the ring order of "Ring Attention Algorithms"
+ * ("Context Parallelism for Scalable Million-Token Inference").
  * positions: global positions of rank `rank`'s query (kind Q, n_q values) or
  *   KV (kind KV, n_kv values) tokens, in local order, into a host int32 array.
  * schedule: out[(t*R + r)*2 + {0,1}] = (q_owner, kv_owner) of rank r at
@@ -241,7 +248,10 @@ cp_attn_status cp_attn_plan_visible_pairs(cp_attn_plan_t plan, int step, int64_t
  * accumulators of dq, dk and dv). */
 cp_attn_status cp_attn_workspace_size(cp_attn_plan_t plan, cp_attn_op op, size_t* bytes);
 
-/* One forward ring step (kernel K1). For every pair (q_owner, kv_owner) of
+/* One forward ring step (kernel K1): the attention kernel called once per
+ * ring step on the local queries and the visiting KV chunk ("Announcing
+ * Long-Context Training on TPUs with MaxText Context Parallelism", "Built on
+ * a fast attention kernel"). For every pair (q_owner, kv_owner) of
  * step `step` and every query head: S = scale*Q K^T on the visible 128x128
  * tiles only (fully masked tiles are skipped, partial ones masked), online
  * softmax, O = P V, then the epilogue of `mode` (see cp_attn_merge_mode).
@@ -321,7 +331,8 @@ cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t plan, const void* q8, const vo
  * 8); every bf16 value of magnitude in [2^-14, 65504] converts exactly. */
 cp_attn_status cp_attn_half_ops_size(cp_attn_plan_t plan, size_t* bytes);
 
-/* Backward preprocess (kernel K3): delta[h][t] = sum_d dO[t,h,:]*O[t,h,:]
+/* Backward preprocess (kernel K3; the per-step backward of "Built on a fast
+ * attention kernel" needs the rows' delta): delta[h][t] = sum_d dO[t,h,:]*O[t,h,:]
  * in fp32, taking O from o_f32 (fp32 [T_q,Hq,d], e.g. the fp32 output that
  * cp_attn_forward leaves at the start of its workspace) when it is not NULL,
  * else from the bf16 o; fp16 copies of q, k, v, dout into `half_ops` (a
@@ -348,7 +359,10 @@ cp_attn_status cp_attn_step_bwd(cp_attn_plan_t plan, int step, const void* half_
                                 const float* lse, const float* delta, float* dq_acc,
                                 float* dk_acc, float* dv_acc, void* stream);
 
-/* LSE merge of n_parts partial results (kernel K4): for each (row, head),
+/* LSE merge of n_parts partial results (kernel K4; the merge "as it goes"
+ * of P2P in "Context Parallelism in MaxText", and Pass Q's merge after the
+ * all-to-all in "Ring Attention Algorithms" of "Context Parallelism for
+ * Scalable Million-Token Inference"): for each (row, head),
  * LSE = M + ln sum_i exp(LSE_i - M) with M = max_i LSE_i, and
  * O = sum_i exp(LSE_i - LSE) * O_i. Parts with LSE_i = -inf weigh 0; a row
  * whose parts are all -inf gets O = 0, LSE = -inf.
@@ -372,8 +386,9 @@ cp_attn_status cp_attn_merge_lse_ex(int n_parts, int64_t rows, int heads, int he
                                     int64_t lse_part_stride, void* o_out, float* o_out_f32,
                                     float* lse_out, void* stream);
 
-/* Whole forward pass over the emulated ring: R step launches in step
- * order, then (Pass Q) the n-way merge over kv_owner slots. o: bf16
+/* Whole forward pass over the emulated ring ("Ring Attention Algorithms":
+ * Pass KV and Pass Q): R step launches in step order, then (Pass Q) the
+ * n-way merge over kv_owner slots. o: bf16
  * [T_q,Hq,d]; lse: fp32 [Hq,T_q]. workspace: device buffer of at least
  * cp_attn_workspace_size(plan, FORWARD) bytes, 256-byte aligned. On return
  * the workspace starts with O in fp32 [T_q,Hq,d] (the unrounded result),
@@ -406,8 +421,9 @@ cp_attn_status cp_attn_forward_noalloc(cp_attn_plan_t plan, const void* q, const
                                        const void* v, void* o, float* lse, void* stream);
 size_t cp_attn_forward_noalloc_capacity(void);
 
-/* Whole backward pass: preprocess, then R backward steps in the plan's
- * ring order. o: bf16 [T_q,Hq,d]; o_f32: optional fp32 O used for delta
+/* Whole backward pass ("Built on a fast attention kernel": the kernel runs
+ * once per ring step in the backward pass too): preprocess, then R
+ * backward steps in the plan's ring order. o: bf16 [T_q,Hq,d]; o_f32: optional fp32 O used for delta
  * (see cp_attn_bwd_preprocess); dq [T_q,Hq,d]; dk, dv [T_kv,Hkv,d]
  * (overwritten), fp32 or, when the plan's grad_dtype is BF16, bf16: then
  * the fp32 sums live in the workspace and a last kernel (K6) rounds them to
@@ -420,7 +436,7 @@ cp_attn_status cp_attn_backward(cp_attn_plan_t plan, const void* q, const void* 
                                 void* stream);
 
 /* Reorder a [tokens, row_bytes] tensor between natural token order and the
- * plan's rank-major order (kernel K5), for the query-side (T_q rows) or the
+ * plan's rank-major order (kernel K5; the sharding of "Load Balancing in CP"), for the query-side (T_q rows) or the
  * key-side (T_kv rows) token set. row_bytes = heads*head_dim*element size,
  * a multiple of 16. `in` and `out` must not overlap. */
 cp_attn_status cp_attn_layout_apply(cp_attn_plan_t plan, cp_attn_tensor_kind kind,
