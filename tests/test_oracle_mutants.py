@@ -73,6 +73,14 @@ CASES = [
      [pins.test_partial_prefill_plan]),
     ("plan_positions", "offset=b * L + P, a2a=a2a)", "offset=b * int(seq_len) + P, a2a=a2a)",
      [pins.test_batch_positions_partition_and_balance]),
+    ("round_bf16", "np.rint(a0 / spacing)", "np.floor(a0 / spacing)",
+     [pins.test_round_bf16_hand_values, pins.test_round_bf16_matches_torch_conversion]),
+    ("round_bf16", "np.maximum(e, -125)", "np.maximum(e, -200)",
+     [pins.test_round_bf16_hand_values, pins.test_round_bf16_matches_torch_conversion]),
+    ("round_bf16", "np.ldexp(1.0, e - 8)", "np.ldexp(1.0, e - 7)",
+     [pins.test_round_bf16_hand_values, pins.test_round_bf16_matches_torch_conversion]),
+    ("ring_forward", 'round_bf16(o_t) if partial_dtype == "bf16" else o_t', "o_t",
+     [pins.test_ring_forward_bf16_partials_pass_q]),
     ("_pair_backward", "ds = p * (dp - D[h, r0:r1][:, None])", "ds = p * dp",
      [lambda: pins.test_backward_finite_differences(None)]),
     ("_pair_backward", "dq[r0:r1, h, :] += scale * (ds @ kk)",
