@@ -220,3 +220,26 @@ def test_fp8_prefill_405b_sampled(name):
         _check_o(run.base.take(o, rows), O_ref, B, f"{name} {variant} O")
         del run, o, lse
         torch.cuda.empty_cache()
+
+
+def test_fp8_pass_q_bf16_partials():
+    """The E4M3 forward with bf16 Pass-Q partials against the same forward with
+    fp32 partials, on the same device inputs: both compute the same fp32
+    partials, so the LSE is identical and O moves only by the bf16 rounding of
+    the partials (at most 2^-8 of the largest partial, itself at most max |V|)
+    plus the bf16 rounding of either output."""
+    w = Workload("fp8p16", 2048, 8, 2, 128, 4)
+    inp = make_inputs(w, with_dout=False)
+    outs = []
+    for pd in ("f32", "bf16"):
+        plan = cpa.Plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                        variant="pass_q", partial_dtype=pd)
+        run = Fp8Run(plan, inp)
+        o, lse, _ = run.forward()
+        outs.append((bf16_to_f64(o), f32_to_f64(lse), run))
+    (o32, l32, run), (o16, l16, _) = outs
+    assert np.array_equal(l16, l32)
+    _, _, vd = _oracle_inputs(inp)
+    lim = 2.0 ** -8 * np.abs(vd).max() + 2 * bf16_half_ulp(np.maximum(np.abs(o32), np.abs(o16)))
+    assert (np.abs(o16 - o32) <= lim).all()
+    assert np.abs(o16 - o32).max() > 0   # the bf16 slots were used
