@@ -466,7 +466,7 @@ cp_attn_status cp_attn_head_a2a(int64_t rows, int heads, int64_t head_bytes, int
                                 cp_attn_a2a_direction direction, const void* in, void* out,
                                 void* stream);
 
-/* One-row decode over the emulated ring (kernel K8, then the K4 merge):
+/* One-row decode over the emulated ring (kernel K9 or K8, then the K4 merge):
  * Pass Q for decode ("Context Parallelism for Scalable Million-Token
  * Inference": "Attention Compute Patterns in Multi-Turn Chat" -- decode is a
  * single-row attention of the new token over every earlier token -- and
