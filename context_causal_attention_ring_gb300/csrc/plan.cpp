@@ -218,22 +218,29 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
     return (a.hi - a.lo) > (b.hi - b.lo);
   };
   std::vector<int> cls(static_cast<size_t>(p->n_qt) * p->n_kt);
+  // A rank's rows are sequence-major: q tiles [b sq, (b + 1) sq) and kv tiles
+  // [b sk, (b + 1) sk) belong to sequence b, and tiles of different sequences
+  // are EMPTY, so only a sequence's own tiles are classified.
+  const int sq = static_cast<int>(p->n_qt / B), sk = static_cast<int>(p->n_kt / B);
   for (int t = 0; t < R; ++t) {
     std::vector<WorkItem> fwd, bwd;
     for (int r = 0; r < R; ++r) {
       const int qo = p->sched[(static_cast<size_t>(t) * R + r) * 2 + 0];
       const int ko = p->sched[(static_cast<size_t>(t) * R + r) * 2 + 1];
-      for (int i = 0; i < p->n_qt; ++i)
-        for (int j = 0; j < p->n_kt; ++j) {
+      for (int i = 0; i < p->n_qt; ++i) {
+        const int j0 = (i / sq) * sk;
+        for (int j = j0; j < j0 + sk; ++j) {
           const int c = tile_class(p, qo, i, ko, j);
           cls[static_cast<size_t>(i) * p->n_kt + j] = c;
           if (c == 2) p->step_pairs[t] += static_cast<int64_t>(kTile) * kTile;
           else if (c == 1) p->step_pairs[t] += tile_visible_pairs(p, qo, i, ko, j);
         }
-      // forward: per q tile, its run of non-empty kv tiles
+      }
+      // forward: per q tile, its run of non-empty kv tiles (of its sequence)
       for (int i = 0; i < p->n_qt; ++i) {
         int lo = -1, hi = -1, nfull = 0;
-        for (int j = 0; j < p->n_kt; ++j) {
+        const int j0 = (i / sq) * sk;
+        for (int j = j0; j < j0 + sk; ++j) {
           const int c = cls[static_cast<size_t>(i) * p->n_kt + j];
           if (c) {
             if (lo < 0) lo = j;
@@ -245,10 +252,11 @@ cp_attn_status build_plan(cp_attn_plan_s* p, const cp_attn_plan_desc* desc) {
         if (lo < 0) lo = hi = 0;
         fwd.push_back(WorkItem{qo, ko, i, lo, hi, nfull, 0, 0});
       }
-      // backward: per kv tile, its run of non-empty q tiles
+      // backward: per kv tile, its run of non-empty q tiles (of its sequence)
       for (int j = 0; j < p->n_kt; ++j) {
         int lo = -1, hi = -1, nfull = 0;
-        for (int i = 0; i < p->n_qt; ++i) {
+        const int i0 = (j / sk) * sq;
+        for (int i = i0; i < i0 + sq; ++i) {
           const int c = cls[static_cast<size_t>(i) * p->n_kt + j];
           if (c) {
             if (lo < 0) lo = i;
