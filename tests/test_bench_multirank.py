@@ -1,6 +1,7 @@
 """The N > 1 path of bench.py on CPU: two gloo ranks (replicas). Each rank
 times its own replica; the job's time is the maximum over ranks and its value
 the FLOPs of all ranks over that time. Only rank 0 runs the reference arm."""
+import json
 import os
 import subprocess
 import sys
@@ -63,3 +64,27 @@ def test_reference_arm_runs_on_rank_zero_only():
                        env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_prints_the_contract_line():
+    """Rank 0 of the reference arm (the oracle on the host cores) prints one
+    JSON line with the contract's keys: impl, metric and unit, the step
+    counts, a cpu_baseline describing the run and an e2e with no host-device
+    bytes."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_ring", "--steps", "1", "--warmup", "1"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stdout.strip().splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 1
+    for key in ("metric", "unit", "n_gpus", "ms_per_step", "higher_is_better", "dtype", "config"):
+        assert key in d, key
+    assert d["config"]["workload"] == "tiny_ring"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
