@@ -104,6 +104,7 @@ _SIG = {
     "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_merge_lse": (_I, [_I, _I64, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "cp_attn_merge_lse_ex": (_I, [_I, _I64, _I, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
+    "cp_attn_plan_work_list": (_I, [_P, _I, _I, _P, ctypes.POINTER(_I64)]),
     "cp_attn_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "cp_attn_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_forward_noalloc_capacity": (ctypes.c_size_t, []),
@@ -328,6 +329,18 @@ class Plan:
         out = _I64()
         _check(load().cp_attn_plan_visible_pairs(self.handle, step, ctypes.byref(out)))
         return int(out.value)
+
+    def work_list(self, step: int, backward: bool = False) -> np.ndarray:
+        """[n, 6] int32: q_owner, kv_owner, tile, lo, hi, n_full per item of
+        the step's forward (or backward) work list, in launch order."""
+        lib = load()
+        n = _I64()
+        _check(lib.cp_attn_plan_work_list(self.handle, step, 1 if backward else 0, None,
+                                          ctypes.byref(n)))
+        out = np.empty((int(n.value), 6), dtype=np.int32)
+        _check(lib.cp_attn_plan_work_list(self.handle, step, 1 if backward else 0,
+                                          out.ctypes.data, ctypes.byref(n)))
+        return out
 
     def workspace_size(self, op: int) -> int:
         out = ctypes.c_size_t()

@@ -302,6 +302,30 @@ cp_attn_status cp_attn_plan_info(cp_attn_plan_t p, int64_t* info, int n) {
   return CP_ATTN_OK;
 }
 
+cp_attn_status cp_attn_plan_work_list(cp_attn_plan_t p, int step, int backward, int32_t* out,
+                                      int64_t* n_items) {
+  clear_error();
+  if (!p || !n_items || step < 0 || step >= p->R || (backward != 0 && backward != 1))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "plan_work_list: bad arguments");
+  const std::vector<cpa::WorkItem>& items = backward ? p->bwd_items : p->fwd_items;
+  const std::vector<int>& off = backward ? p->bwd_off : p->fwd_off;
+  const int a = off[step], b = off[step + 1];
+  *n_items = b - a;
+  if (out) {
+    for (int i = a; i < b; ++i) {
+      const cpa::WorkItem& w = items[i];
+      int32_t* o = out + static_cast<int64_t>(i - a) * 6;
+      o[0] = w.q_owner;
+      o[1] = w.kv_owner;
+      o[2] = w.tile;
+      o[3] = w.lo;
+      o[4] = w.hi;
+      o[5] = w.n_full;
+    }
+  }
+  return CP_ATTN_OK;
+}
+
 cp_attn_status cp_attn_plan_positions(cp_attn_plan_t p, cp_attn_tensor_kind kind, int rank,
                                       int32_t* out) {
   clear_error();

@@ -240,6 +240,22 @@ cp_attn_status cp_attn_plan_schedule(cp_attn_plan_t plan, int32_t* out);
 cp_attn_status cp_attn_plan_block_mask(cp_attn_plan_t plan, uint8_t* out);
 cp_attn_status cp_attn_plan_visible_pairs(cp_attn_plan_t plan, int step, int64_t* out);
 
+/* The compacted work list that step `step` of the forward (backward = 0) or
+ * backward (backward = 1) kernel consumes (host query; block skipping of
+ * "Built on a fast attention kernel" in "Announcing Long-Context Training on
+ * TPUs with MaxText Context Parallelism"). Forward: one item per (q_owner,
+ * q tile) of the step's pairs, with the run [lo, hi) of its non-empty kv
+ * tiles of kv_owner (lo = hi = 0 when there is none). Backward: one item per
+ * (kv_owner, kv tile) with a non-empty run [lo, hi) of q tiles of q_owner.
+ * Items are generated pair by pair in rank order, tile by tile, then sorted
+ * by run length, longest first (stable), so the heaviest tiles start in the
+ * first wave. out (host, may be NULL to query the count) receives 6 int32 per
+ * item: q_owner, kv_owner, tile, lo, hi, n_full (the run's FULL tiles);
+ * *n_items the number of items. ERR_INVALID_ARG for a bad plan, step or
+ * pointer. */
+cp_attn_status cp_attn_plan_work_list(cp_attn_plan_t plan, int step, int backward, int32_t* out,
+                                      int64_t* n_items);
+
 /* Device workspace, in bytes, for cp_attn_forward (op FORWARD: the fp32
  * running output for Pass KV, or R partial slots for Pass Q, fp32 or bf16 by
  * the plan's partial_dtype, then R fp32 LSE slots) or cp_attn_backward (op

@@ -64,6 +64,7 @@ __all__ = [
     "doc_index",
     "visible_mask",
     "block_mask",
+    "work_list",
     "count_visible",
     "partial_attention",
     "attention",
@@ -238,6 +239,34 @@ def block_mask(q_pos, kv_pos, cu_seqlens=None, tile: int = TILE, *, window: int 
             allv = v4.all(axis=(1, 3))
             out[a, b] = np.where(allv, FULL, np.where(anyv, PARTIAL, EMPTY))
     return out
+
+
+def work_list(bm, sched, step: int, backward: bool = False) -> np.ndarray:
+    """The compacted work list of ring step ``step`` from the block classes
+    bm[q_owner][kv_owner][q tile][kv tile] ([MaxText] "Built on a fast
+    attention kernel": fully masked blocks are skipped). Reading: the step's
+    pairs are taken in rank order and their tiles in order; forward, one
+    item per query tile with the run [lo, hi) of its non-empty key tiles
+    (lo = hi = 0 when there is none); backward, one item per key tile that
+    has a non-empty run of query tiles. A run must be contiguous. The list is
+    then sorted by run length, longest first, equal lengths keeping their
+    order. Rows: q_owner, kv_owner, tile, lo, hi, number of FULL tiles."""
+    items = []
+    for qo, ko in sched[step]:
+        m = np.asarray(bm[qo][ko])
+        n_tiles = m.shape[1] if backward else m.shape[0]
+        for t in range(n_tiles):
+            line = m[:, t] if backward else m[t]
+            nz = np.nonzero(line)[0]
+            if len(nz) == 0:
+                if not backward:
+                    items.append((qo, ko, t, 0, 0, 0))
+                continue
+            lo, hi = int(nz[0]), int(nz[-1]) + 1
+            assert len(nz) == hi - lo, "non-contiguous run of visible tiles"
+            items.append((qo, ko, t, lo, hi, int((line[lo:hi] == FULL).sum())))
+    items.sort(key=lambda it: -(it[4] - it[3]))   # list.sort is stable
+    return np.array(items, dtype=np.int64).reshape(-1, 6)
 
 
 def count_visible(qpos, kpos, cu_seqlens=None, *, window: int = 0) -> int:

@@ -81,6 +81,11 @@ CASES = [
      [pins.test_round_bf16_hand_values, pins.test_round_bf16_matches_torch_conversion]),
     ("ring_forward", 'round_bf16(o_t) if partial_dtype == "bf16" else o_t', "o_t",
      [pins.test_ring_forward_bf16_partials_pass_q]),
+    ("work_list", "items.sort(key=lambda it: -(it[4] - it[3]))",
+     "items.sort(key=lambda it: it[4] - it[3])",
+     [pins.test_work_list_closed_forms]),
+    ("work_list", "lo, hi = int(nz[0]), int(nz[-1]) + 1", "lo, hi = int(nz[0]), int(nz[-1])",
+     [pins.test_work_list_closed_forms]),
     ("_pair_backward", "ds = p * (dp - D[h, r0:r1][:, None])", "ds = p * dp",
      [lambda: pins.test_backward_finite_differences(None)]),
     ("_pair_backward", "dq[r0:r1, h, :] += scale * (ds @ kk)",

@@ -545,3 +545,39 @@ def test_batch_positions_partition_and_balance():
         assert len(set(per_rank)) == 1
         # a query of sequence b sees exactly its own sequence's earlier tokens
         assert sum(per_rank) == sum(P + j + 1 for j in range(N))
+
+
+def test_work_list_closed_forms():
+    """The oracle's work lists on the zigzag ring against the closed forms of
+    the chunk plan: over the whole ring each rank's runs cover (2R-1) m^2 +
+    m (m + 1) non-empty tiles (m = tiles per half-chunk); every step after the
+    first has 2 m^2 FULL tiles per rank and the first 2 m^2 - m FULL plus 2 m
+    PARTIAL; run lengths never grow down a list; the backward lists cover the
+    same tiles as the forward ones."""
+    R, m = 4, 2
+    N = 2 * R * m * oracle.TILE
+    q_pos, kv_pos = oracle.plan_positions(N, R, "zigzag")
+    bm = oracle.block_mask(q_pos, kv_pos)
+    sched = oracle.ring_schedule(R, "pass_kv")
+    per_rank = np.zeros(R, dtype=np.int64)
+    for t in range(R):
+        fw = oracle.work_list(bm, sched, t)
+        bw = oracle.work_list(bm, sched, t, backward=True)
+        for lst in (fw, bw):
+            lengths = lst[:, 4] - lst[:, 3]
+            assert np.all(np.diff(lengths) <= 0)
+        assert (fw[:, 4] - fw[:, 3]).sum() == (bw[:, 4] - bw[:, 3]).sum()
+        assert fw[:, 5].sum() == bw[:, 5].sum()
+        for r in range(R):
+            mine = fw[fw[:, 0] == r]
+            assert len(mine) == 2 * m                       # every query tile once
+            per_rank[r] += (mine[:, 4] - mine[:, 3]).sum()
+            full = mine[:, 5].sum()
+            if t == 0:
+                # the later chunk against the earlier one (m^2 FULL) and two
+                # diagonal triangles (m (m - 1) / 2 FULL and m PARTIAL each)
+                assert full == 2 * m * m - m
+                assert (mine[:, 4] - mine[:, 3]).sum() - full == 2 * m
+            else:
+                assert full == 2 * m * m
+    assert np.all(per_rank == (2 * R - 1) * m * m + m * (m + 1))

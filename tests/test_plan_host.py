@@ -242,3 +242,35 @@ def test_batch_with_documents_and_bad_offsets():
     with pytest.raises(cpa.CpAttnError) as e:
         cpa.Plan(N, R, 2, 1, 64, batch=-1)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("kw", [
+    dict(N=1024, R=4, layout="zigzag", variant="pass_kv"),
+    dict(N=1024, R=4, layout="contiguous", variant="pass_q"),
+    dict(N=4096, R=4, cu=[0, 1, 130, 1000, 1023, 1024, 2500, 4096]),
+    dict(N=1024, R=2, P=3072, variant="pass_q"),
+    dict(N=2048, R=4, window=300),
+    dict(N=1024, R=2, B=3),
+    dict(N=2048, R=2, layout="usp", a2a=2),
+])
+def test_work_lists_bit_exact(kw):
+    """The work lists the step kernels consume, forward and backward, every
+    step: bit-exact against the oracle's list built from its brute-force
+    block classes (runs, FULL counts, longest-first order)."""
+    N, R = kw["N"], kw["R"]
+    layout, variant = kw.get("layout", "zigzag"), kw.get("variant", "pass_kv")
+    P, B, window, a2a = kw.get("P", 0), kw.get("B", 1), kw.get("window", 0), kw.get("a2a", 1)
+    cu = kw.get("cu")
+    cu_arr = None if cu is None else np.array(cu, dtype=np.int32)
+    p = cpa.Plan(N, R, 2, 1, 64, layout=layout, variant=variant, cu_seqlens=cu_arr,
+                 kv_prefix_len=P, window=window, a2a=a2a, batch=B)
+    q_pos, kv_pos = oracle.plan_positions(N, R, layout, kv_prefix_len=P, a2a=a2a, batch=B)
+    docs = oracle.batch_cu_seqlens(N, B, P) if (cu is None and B > 1) else cu
+    bm = oracle.block_mask(q_pos, kv_pos, docs, window=window)
+    assert np.array_equal(p.block_mask(), bm)
+    sched = oracle.ring_schedule(R, variant)
+    for t in range(R):
+        for bwd in (False, True):
+            got = p.work_list(t, bwd)
+            want = oracle.work_list(bm, sched, t, bwd)
+            assert np.array_equal(got, want), (t, bwd)
