@@ -274,3 +274,33 @@ def test_work_lists_bit_exact(kw):
             got = p.work_list(t, bwd)
             want = oracle.work_list(bm, sched, t, bwd)
             assert np.array_equal(got, want), (t, bwd)
+
+
+def test_decode_fp8_argument_checks_on_the_host():
+    """cp_attn_decode_fp8 refuses bad arguments before any device work: an
+    unsupported head_dim, null or misaligned pointers, a short workspace and
+    runs of keys that are not multiples of 128 (fake device addresses that
+    are never dereferenced)."""
+    import ctypes
+    from context_causal_attention_ring_gb300 import _abi
+    lib = cpa.load()
+    base = 1 << 32
+
+    def call(desc, ptrs=None, ws_bytes=None):
+        p = ptrs or [base + i * (1 << 24) for i in range(7)]
+        need = cpa.decode_workspace_size(desc.batch, desc.cp, desc.kv_len, desc.n_q_heads,
+                                         desc.n_kv_heads, desc.head_dim)
+        return lib.cp_attn_decode_fp8(ctypes.byref(desc), *p[:5], p[5], p[6],
+                                      need if ws_bytes is None else ws_bytes, None)
+
+    ok = _abi._decode_desc(2, 4, 4096, 8, 2, 128)
+    assert call(_abi._decode_desc(2, 4, 4096, 8, 2, 64)) == 3          # head_dim 64
+    ptrs = [base + i * (1 << 24) for i in range(7)]
+    for i in range(7):
+        bad = list(ptrs)
+        bad[i] = None
+        assert call(ok, bad) == 1, i                                    # a null pointer
+        bad[i] = ptrs[i] + 8
+        assert call(ok, bad) == 1, i                                    # misaligned
+    assert call(ok, ws_bytes=16) == 2                                   # workspace too small
+    assert call(_abi._decode_desc(1, 4, 256, 2, 1, 128)) == 2          # 64-key runs
