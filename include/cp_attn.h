@@ -21,8 +21,9 @@
  *    head_dim contiguous, in rank-major token order (see
  *    cp_attn_layout_apply). Base addresses must be 16-byte aligned.
  *  - LSE and delta are fp32 [heads, tokens] (natural log, softmax scale
- *    applied). Gradients and fp32 partial outputs are fp32
- *    [tokens, heads, head_dim].
+ *    applied). Gradients and partial outputs are [tokens, heads, head_dim],
+ *    fp32 unless the plan asks for bf16 (cp_attn_plan_desc.grad_dtype,
+ *    partial_dtype).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream). Compute calls are asynchronous on that stream; argument errors
  *    are detected on the host before anything is enqueued.
