@@ -101,7 +101,9 @@ _SIG = {
     "cp_attn_step_fwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _I, _P, _P]),
     "cp_attn_half_ops_size": (_I, [_P, ctypes.POINTER(ctypes.c_size_t)]),
     "cp_attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "cp_attn_step_bwd": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                              ctypes.c_size_t, _P]),
+    "cp_attn_step_bwd_half": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "cp_attn_merge_lse": (_I, [_I, _I64, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "cp_attn_merge_lse_ex": (_I, [_I, _I64, _I, _I, _I, _P, _I64, _P, _I64, _P, _P, _P, _P]),
     "cp_attn_plan_work_list": (_I, [_P, _I, _I, _P, ctypes.POINTER(_I64)]),
@@ -382,10 +384,19 @@ class Plan:
                                              _ptr(half_ops), _ptr(dq), _ptr(dk), _ptr(dv),
                                              _stream(stream)))
 
-    def step_bwd(self, step, half_ops, lse, delta, dq, dk, dv, stream=None):
-        _check(load().cp_attn_step_bwd(self.handle, step, _ptr(half_ops), _ptr(lse),
-                                       _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv),
-                                       _stream(stream)))
+    def step_bwd(self, step, q, k, v, dout, lse, delta, dq, dk, dv, workspace,
+                 workspace_bytes=None, stream=None):
+        if workspace_bytes is None:
+            workspace_bytes = workspace.numel() * workspace.element_size()
+        _check(load().cp_attn_step_bwd(self.handle, step, _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), _ptr(workspace),
+                                       int(workspace_bytes), _stream(stream)))
+
+    def step_bwd_half(self, step, half_ops, lse, delta, dq, dk, dv, stream=None):
+        _check(load().cp_attn_step_bwd_half(self.handle, step, _ptr(half_ops), _ptr(lse),
+                                            _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv),
+                                            _stream(stream)))
 
     def forward(self, q, k, v, o, lse, workspace, workspace_bytes=None, stream=None):
         if workspace_bytes is None:

@@ -585,13 +585,47 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t p, int step, const void* q, const
                        p && p->chain_steps && step > 0, &launched);
 }
 
-cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* half_ops,
-                                const float* lse, const float* delta, float* dq_acc,
-                                float* dk_acc, float* dv_acc, void* stream) {
+cp_attn_status cp_attn_step_bwd_half(cp_attn_plan_t p, int step, const void* half_ops,
+                                     const float* lse, const float* delta, float* dq_acc,
+                                     float* dk_acc, float* dv_acc, void* stream) {
   clear_error();
   bool launched = false;
   return step_bwd_impl(p, step, half_ops, lse, delta, dq_acc, dk_acc, dv_acc, stream,
                        p && p->chain_steps && step > 0, &launched);
+}
+
+cp_attn_status cp_attn_step_bwd(cp_attn_plan_t p, int step, const void* q, const void* k,
+                                const void* v, const void* dout, const float* lse,
+                                const float* delta, float* dq_acc, float* dk_acc,
+                                float* dv_acc, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  clear_error();
+  cp_attn_status st = check_device_plan(p);
+  if (st != CP_ATTN_OK) return st;
+  if (step < 0 || step >= p->R) return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: step out of range");
+  if (!q || !k || !v || !dout || !workspace)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout))
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: q, k, v, dout must be 16-byte aligned");
+  const HalfOps ho = half_ops_layout(p);
+  if (workspace_bytes < ho.total)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: workspace smaller than cp_attn_half_ops_size");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(CP_ATTN_ERR_INVALID_ARG, "step_bwd: workspace must be 256-byte aligned");
+  if (step == 0) {
+    // the ring's first step makes the fp16 operand copies every step reads
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* hb = static_cast<char*>(workspace);
+    const int64_t nq = p->T_q * p->Hq * p->d, nk = p->T_kv * p->Hkv * p->d;
+    if ((st = launch_bf16_to_f16(q, hb + ho.q, nq, p->d_status, s)) != CP_ATTN_OK) return st;
+    if ((st = launch_bf16_to_f16(k, hb + ho.k, nk, p->d_status, s)) != CP_ATTN_OK) return st;
+    if ((st = launch_bf16_to_f16(v, hb + ho.v, nk, p->d_status, s)) != CP_ATTN_OK) return st;
+    if ((st = launch_bf16_to_f16(dout, hb + ho.dout, nq, p->d_status, s)) != CP_ATTN_OK)
+      return st;
+  }
+  bool launched = false;
+  return step_bwd_impl(p, step, workspace, lse, delta, dq_acc, dk_acc, dv_acc, stream,
+                       p->chain_steps && step > 0, &launched);
 }
 
 cp_attn_status cp_attn_plan_set_chaining(cp_attn_plan_t p, int enable) {
@@ -650,9 +684,10 @@ cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* q, const voi
   clear_error();
   cp_attn_status st = check_device_plan(p);
   if (st != CP_ATTN_OK) return st;
-  if (!q || !k || !v || (!o && !o_f32) || !dout || !delta || !half_ops)
+  if ((half_ops && (!q || !k || !v)) || (!o && !o_f32) || !dout || !delta)
     return fail(CP_ATTN_ERR_INVALID_ARG, "bwd_preprocess: null pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (o && !aligned16(o)) ||
+  if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
+      (o && !aligned16(o)) ||
       (o_f32 && !aligned16(o_f32)) || !aligned16(dout) ||
       (reinterpret_cast<uintptr_t>(half_ops) & 255u) || (dq_acc && !aligned16(dq_acc)) ||
       (dk_acc && !aligned16(dk_acc)) || (dv_acc && !aligned16(dv_acc)))
@@ -665,10 +700,13 @@ cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t p, const void* q, const voi
   const HalfOps ho = half_ops_layout(p);
   char* hb = static_cast<char*>(half_ops);
   const int64_t nq = p->T_q * p->Hq * p->d, nk = p->T_kv * p->Hkv * p->d;
-  if ((st = launch_bf16_to_f16(q, hb + ho.q, nq, p->d_status, s)) != CP_ATTN_OK) return st;
-  if ((st = launch_bf16_to_f16(k, hb + ho.k, nk, p->d_status, s)) != CP_ATTN_OK) return st;
-  if ((st = launch_bf16_to_f16(v, hb + ho.v, nk, p->d_status, s)) != CP_ATTN_OK) return st;
-  if ((st = launch_bf16_to_f16(dout, hb + ho.dout, nq, p->d_status, s)) != CP_ATTN_OK) return st;
+  if (half_ops) {
+    if ((st = launch_bf16_to_f16(q, hb + ho.q, nq, p->d_status, s)) != CP_ATTN_OK) return st;
+    if ((st = launch_bf16_to_f16(k, hb + ho.k, nk, p->d_status, s)) != CP_ATTN_OK) return st;
+    if ((st = launch_bf16_to_f16(v, hb + ho.v, nk, p->d_status, s)) != CP_ATTN_OK) return st;
+    if ((st = launch_bf16_to_f16(dout, hb + ho.dout, nq, p->d_status, s)) != CP_ATTN_OK)
+      return st;
+  }
   if (dq_acc && (st = launch_zero_f32(dq_acc, nq, s)) != CP_ATTN_OK) return st;
   if (dk_acc && (st = launch_zero_f32(dk_acc, nk, s)) != CP_ATTN_OK) return st;
   if (dv_acc && (st = launch_zero_f32(dv_acc, nk, s)) != CP_ATTN_OK) return st;

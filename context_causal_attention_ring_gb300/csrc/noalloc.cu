@@ -8,46 +8,42 @@
 // fp32 workspace. This entry point takes that workspace from a fixed array in
 // the library's own device image instead.
 #include <cstring>
-#include <mutex>
 #include <string>
-#include <unordered_map>
 
 #include "kernels.h"
 
 namespace {
 
 // Fixed scratch for the forward workspace (the fp32 running output, or the
-// Pass-Q partial slots). Every device that loads the library holds these
-// bytes until the process exits.
+// Pass-Q partial slots). A device holds these bytes from the moment the
+// library's device image is loaded on it (its first kernel launch or symbol
+// lookup, under CUDA's lazy module loading) until the process exits.
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-std::unordered_map<int, void*> g_scratch_addr;  // device ordinal -> device address
-
-// Device address of the scratch array on the current device. In host code
+// Device address of the scratch array in the current context. In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device with that device current, then reused.
+// with the device current. The lookup runs on every call and allocates
+// nothing: an address kept from an earlier call could belong to a context
+// that has since been destroyed (cudaDeviceReset, or a host program that
+// makes its own context current on the same device).
 cp_attn_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return cpa::fail(CP_ATTN_ERR_CUDA, "forward_noalloc: no current CUDA device");
   }
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  auto it = g_scratch_addr.find(dev);
-  if (it != g_scratch_addr.end()) {
-    *out = it->second;
-    return CP_ATTN_OK;
-  }
   void* ptr = nullptr;
   const cudaError_t err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
   if (err != cudaSuccess || ptr == nullptr) {
     cudaGetLastError();
-    return cpa::fail(CP_ATTN_ERR_CUDA, std::string("forward_noalloc: cudaGetSymbolAddress failed: ") +
-                                           cudaGetErrorString(err));
+    // the library's device image (and with it the array) is loaded on the
+    // first call on each device; that load can run out of device memory
+    const cp_attn_status st =
+        err == cudaErrorMemoryAllocation ? CP_ATTN_ERR_OOM : CP_ATTN_ERR_CUDA;
+    return cpa::fail(st, std::string("forward_noalloc: cudaGetSymbolAddress failed on device ") +
+                             std::to_string(dev) + ": " + cudaGetErrorString(err));
   }
-  g_scratch_addr[dev] = ptr;
   *out = ptr;
   return CP_ATTN_OK;
 }

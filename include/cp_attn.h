@@ -283,7 +283,8 @@ cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
                                 void* stream);
 
 /* Chained ring steps (programmatic dependent launch). With enable = 1,
- * cp_attn_step_fwd and cp_attn_step_bwd launch every step >= 1 so that it
+ * cp_attn_step_fwd, cp_attn_step_bwd and cp_attn_step_bwd_half launch every
+ * step >= 1 so that it
  * may start on SMs left idle while the kernel before it on the stream drains;
  * the step waits for that kernel to finish before it reads or writes the
  * running output and LSE (forward, ACCUMULATE) or dK and dV (backward). Its
@@ -345,20 +346,27 @@ cp_attn_status cp_attn_forward_fp8(cp_attn_plan_t plan, const void* q8, const vo
  * fp16 copies of q, k, v and dout, in that order, each starting on a
  * 256-byte boundary. The backward MMAs run on fp16 operands so that the
  * probabilities P and dS they multiply keep 11 significant bits (bf16 keeps
- * 8); every bf16 value of magnitude in [2^-14, 65504] converts exactly. */
+ * 8). Domain of the copies: a bf16 value of magnitude in [2^-14, 65504]
+ * converts exactly; a smaller one becomes an fp16 subnormal, off by at most
+ * 2^-25 in absolute terms (values below 2^-25 become 0); a finite value
+ * above 65504 is reported as CP_ATTN_ERR_RANGE. The absolute error of the
+ * small values stays far below the gradients' 1e-2 tolerance (a score
+ * moves by at most scale * 2^-25 * sum|other operand|). */
 cp_attn_status cp_attn_half_ops_size(cp_attn_plan_t plan, size_t* bytes);
 
 /* Backward preprocess (kernel K3; the per-step backward of "Built on a fast
  * attention kernel" needs the rows' delta): delta[h][t] = sum_d dO[t,h,:]*O[t,h,:]
  * in fp32, taking O from o_f32 (fp32 [T_q,Hq,d], e.g. the fp32 output that
  * cp_attn_forward leaves at the start of its workspace) when it is not NULL,
- * else from the bf16 o; fp16 copies of q, k, v, dout into `half_ops` (a
- * device buffer of cp_attn_half_ops_size bytes, 256-byte aligned); zeroes the
- * fp32 gradient accumulators dq [T_q,Hq,d], dk and dv [T_kv,Hkv,d] (any of
- * the three may be NULL to skip). A finite input of magnitude above 65504
- * (not representable in fp16) sets CP_ATTN_ERR_RANGE in the plan's status
- * word. Using the fp32 O keeps the bf16 rounding of O out of delta (it
- * otherwise moves dQ and dK by up to ~6e-3 on N(0,1) inputs). */
+ * else from the bf16 o; zeroes the fp32 gradient accumulators dq
+ * [T_q,Hq,d], dk and dv [T_kv,Hkv,d] (any of the three may be NULL to skip);
+ * and, when half_ops is not NULL, makes the fp16 copies of q, k, v, dout
+ * that cp_attn_step_bwd_half reads (half_ops: a device buffer of
+ * cp_attn_half_ops_size bytes, 256-byte aligned; q, k, v may be NULL when
+ * half_ops is). A finite input of magnitude above 65504 (not representable
+ * in fp16) sets CP_ATTN_ERR_RANGE in the plan's status word. Using the fp32
+ * O keeps the bf16 rounding of O out of delta (it otherwise moves dQ and dK
+ * by up to ~6e-3 on N(0,1) inputs). */
 cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t plan, const void* q, const void* k,
                                       const void* v, const void* o, const float* o_f32,
                                       const void* dout, float* delta, void* half_ops,
@@ -368,13 +376,35 @@ cp_attn_status cp_attn_bwd_preprocess(cp_attn_plan_t plan, const void* q, const 
 /* One backward ring step (kernel K2), with the merged (global) lse and
  * delta: P = exp(scale*Q K^T - LSE) on visible pairs, dV += P^T dO,
  * dP = dO V^T, dS = P*(dP - delta), dQ += scale*dS K, dK += scale*dS^T Q
- * ("Built on a fast attention kernel": the ring calls the kernel once per
- * step in the backward pass too). dK and dV are summed over the query heads
- * of each KV head. half_ops: the buffer filled by cp_attn_bwd_preprocess.
- * All three accumulators are fp32 and are added to. */
-cp_attn_status cp_attn_step_bwd(cp_attn_plan_t plan, int step, const void* half_ops,
-                                const float* lse, const float* delta, float* dq_acc,
-                                float* dk_acc, float* dv_acc, void* stream);
+ * ("Built on a fast attention kernel" in "Announcing Long-Context Training
+ * on TPUs with MaxText Context Parallelism": the ring calls the kernel once
+ * per step in the backward pass too). dK and dV are summed over the query
+ * heads of each KV head.
+ * q, dout: bf16 [T_q, Hq, d]; k, v: bf16 [T_kv, Hkv, d] (rank-major, 16-byte
+ *   aligned); lse, delta: fp32 [Hq, T_q] (the merged forward LSE, and delta
+ *   from cp_attn_bwd_preprocess); dq_acc [T_q, Hq, d], dk_acc and dv_acc
+ *   [T_kv, Hkv, d]: fp32 accumulators that the step adds to (zero them
+ *   before step 0, e.g. with cp_attn_bwd_preprocess).
+ * workspace: device buffer of at least cp_attn_half_ops_size bytes,
+ *   256-byte aligned, owned by the caller and kept across the ring's steps.
+ *   The backward MMAs run on fp16 copies of the four inputs (see
+ *   cp_attn_half_ops_size): step 0 makes them there, from q, k, v, dout, and
+ *   steps 1..R-1 read the copies step 0 left. Run step 0 of a ring first, on
+ *   the same stream and workspace, as the ring order does; a later step
+ *   called without it reads whatever the workspace holds.
+ * ERR_INVALID_ARG for null or misaligned pointers, a small workspace or a
+ * step outside [0, R). */
+cp_attn_status cp_attn_step_bwd(cp_attn_plan_t plan, int step, const void* q, const void* k,
+                                const void* v, const void* dout, const float* lse,
+                                const float* delta, float* dq_acc, float* dk_acc,
+                                float* dv_acc, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* cp_attn_step_bwd on fp16 copies made beforehand by cp_attn_bwd_preprocess
+ * (half_ops), for callers that make the copies once for several rings. */
+cp_attn_status cp_attn_step_bwd_half(cp_attn_plan_t plan, int step, const void* half_ops,
+                                     const float* lse, const float* delta, float* dq_acc,
+                                     float* dk_acc, float* dv_acc, void* stream);
 
 /* LSE merge of n_parts partial results (kernel K4; the merge "as it goes"
  * of P2P in "Context Parallelism in MaxText", and Pass Q's merge after the
@@ -417,22 +447,31 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t plan, const void* q, const void* k
                                void* stream);
 
 /* Forward pass that allocates nothing (no counterpart on the pages; a
- * convenience of this library). For callers that cannot call cudaMalloc --
- * a plugin inside a host program that owns the whole device-memory pool and
- * gives plugins no allocator, or a serving path that must never enter the
- * allocator -- and so cannot pass the forward workspace. Same result as
- * cp_attn_forward; the workspace comes from a fixed device array inside the
- * library of cp_attn_forward_noalloc_capacity() bytes (32 MiB), which every
- * GPU that loads the library keeps until the process exits.
+ * convenience of this library). For callers that cannot call cudaMalloc on
+ * the compute path -- a plugin inside a host program that owns the whole
+ * device-memory pool and gives plugins no allocator, or a serving path that
+ * must never enter the allocator -- and so cannot pass the forward
+ * workspace. Same result as cp_attn_forward; the workspace comes from a
+ * fixed device array inside the library of cp_attn_forward_noalloc_capacity()
+ * bytes (32 MiB).
+ *  - The plan itself still allocates its small device tables once, when it
+ *    is created (cp_attn_plan / cp_attn_plan_ex); build plans before the
+ *    allocation-free phase.
+ *  - A device holds the array from the moment the library's device image is
+ *    loaded on it (under CUDA's lazy module loading: the first launch or
+ *    symbol lookup of the library on that device) until the process exits.
+ *    If that load runs out of device memory the call returns
+ *    CP_ATTN_ERR_OOM.
  *  - Plans whose forward workspace (cp_attn_workspace_size, FORWARD) exceeds
  *    the capacity are rejected with CP_ATTN_ERR_SHAPE before any launch.
- *  - The first call on each device looks up the array's device address with
- *    that device current (cudaGetSymbolAddress); make that first call before
- *    any stream capture.
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress, which allocates nothing); the first call on a
+ *    device also loads the library's device image there, so make that first
+ *    call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents
- *    (nothing in it needs to start at zero). Calls that overlap on the GPU
- *    (on different streams, or from different threads) race on it: order
- *    them on one stream.
+ *    (nothing in it needs to start at zero: every row is written before it
+ *    is read). Calls that overlap on the GPU (on different streams, or from
+ *    different threads) race on it: order them on one stream.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine. */
 cp_attn_status cp_attn_forward_noalloc(cp_attn_plan_t plan, const void* q, const void* k,
                                        const void* v, void* o, float* lse, void* stream);

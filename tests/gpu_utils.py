@@ -34,14 +34,36 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(ax)) - 8)
 
 
+# Flat max-abs errors of the bf16 outputs checked in this session, reported
+# at the end of the run: (what, max |got - want|, elements, elements above
+# the flat tolerance, largest |want| among those).
+FLAT_LOG = []
+
+
 def assert_close_bf16(got, want, tol=1e-2, what=""):
-    """bf16 outputs: |got - want| <= tol + half a bf16 ulp of want (the
-    rounding every bf16 result carries)."""
+    """bf16 outputs against the target's flat max-abs tol.
+
+    * Everywhere, |got - want| <= tol + half a bf16 ulp of want: the
+      rounding every stored bf16 result carries, which alone reaches 2^-7 for
+      |want| in [2, 4) and exceeds tol beyond 4.
+    * With the target's tol (1e-2), wherever |want| < 2 the flat bound
+      |got - want| <= tol must hold (there the storage rounding is at most
+      2^-8, less than half of tol).
+    With the target's tol, the flat maximum over all elements and how many
+    elements exceed tol are recorded for the session report.
+    """
     err = np.abs(got - want)
     lim = tol + bf16_half_ulp(want)
     bad = err > lim
     assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of tolerance; "
                            f"max err {err.max():.3e}, max err-lim {(err - lim).max():.3e}")
+    if tol >= 1e-2:
+        small = np.abs(want) < 2.0
+        flat = float(err[small].max()) if small.any() else 0.0
+        assert flat <= tol, f"{what}: flat max err {flat:.3e} > {tol} where |O| < 2"
+        over = err > tol
+        FLAT_LOG.append((what, float(err.max()), int(err.size), int(over.sum()),
+                         float(np.abs(want[over]).max()) if over.any() else 0.0))
     return float(err.max())
 
 

@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 
 import oracle
-from workloads import WORKLOADS, Workload, bf16_bits_to_f64, make_inputs, sample_rows
+from workloads import (WORKLOADS, Workload, bf16_bits_to_f32, bf16_bits_to_f64,
+                       f32_to_bf16_bits, make_inputs, sample_rows)
 from gpu_utils import DeviceRun, assert_close, cuda_ok, f32_to_f64
 
 pytestmark = [pytest.mark.gpu,
@@ -118,7 +119,7 @@ def test_single_step_shares():
         dk = torch.empty((plan.T_kv, plan.Hkv, plan.d), device="cuda")
         dv = torch.empty_like(dk)
         plan.bwd_preprocess(run.q, run.k, run.v, o_dev, run.dout, delta, half_ops, dq, dk, dv)
-        plan.step_bwd(t, half_ops, lse_dev, delta, dq, dk, dv)
+        plan.step_bwd_half(t, half_ops, lse_dev, delta, dq, dk, dv)
         plan.sync_status()
         r_dq, r_dk, r_dv = oracle.ring_backward(q[qn], k[kn], v[kn], do[qn], O_b, L[:, qn],
                                                 q_pos, kv_pos, steps=[t])
@@ -133,28 +134,95 @@ def test_single_step_shares():
         assert not msgs, f"step {t}: " + " | ".join(msgs)
 
 
-def test_llama3_8b_layer_backward_sampled():
-    """Full-size backward (bench launch configuration): dQ at sampled rows,
-    dK/dV at the last 128 key positions, and sum_k dK_k = 0 per KV head."""
+@pytest.mark.parametrize("d,chained", [(64, False), (128, False), (128, True)])
+def test_step_bwd_ring_of_bf16_steps(d, chained):
+    """cp_attn_step_bwd with bf16 q, k, v, dout and a workspace, called once
+    per ring step: step 0 makes the fp16 operand copies in the workspace
+    (filled with NaN patterns first), later steps reuse them; delta and the
+    zeroed accumulators come from cp_attn_bwd_preprocess without copies."""
+    w = Workload("stepbwd", 2048, 8, 2, d, 4, backward=True)
+    plan = _plan(w)
+    plan.set_chaining(chained)
+    run = DeviceRun(plan, make_inputs(w))
+    o, lse, fws = run.forward()
+    p = plan
+    delta = torch.empty((p.Hq, p.T_q), dtype=torch.float32, device="cuda")
+    dq = torch.full((p.T_q, p.Hq, p.d), float("nan"), device="cuda")
+    dk = torch.full((p.T_kv, p.Hkv, p.d), float("nan"), device="cuda")
+    dv = torch.full_like(dk, float("nan"))
+    plan.bwd_preprocess(None, None, None, o, run.dout, delta, None, dq, dk, dv, o_f32=fws)
+    ws = torch.full((p.half_ops_size(),), 0xFF, dtype=torch.uint8, device="cuda")
+    for t in range(p.R):
+        plan.step_bwd(t, run.q, run.k, run.v, run.dout, lse, delta, dq, dk, dv, ws)
+    plan.sync_status()
+    _, _, (dq_r, dk_r, dv_r) = _oracle_grads(run.inp, plan, None)
+    tag = f"step_bwd ring d={d} chained={chained}"
+    assert_close(run.to_natural_rows(f32_to_f64(dq)), dq_r, GRAD_TOL, tag + " dQ")
+    assert_close(run.to_natural_rows(f32_to_f64(dk), "kv"), dk_r, GRAD_TOL, tag + " dK")
+    assert_close(run.to_natural_rows(f32_to_f64(dv), "kv"), dv_r, GRAD_TOL, tag + " dV")
+
+
+def test_backward_inputs_in_fp16_subnormal_range():
+    """Every K element scaled by 2^-20 (exact in bf16): all of them lie below
+    2^-14, where the backward's fp16 copies are subnormal and keep an
+    absolute error of at most 2^-25. The gradients still meet the absolute
+    1e-2 target against the oracle on the exact bf16 inputs, and dQ (which
+    scales with K) matches, to 1e-2 of its size, the oracle on K rounded to
+    fp16 as the documented conversion does."""
+    w = Workload("small_k", 2048, 4, 2, 128, 4, backward=True)
+    inp = make_inputs(w)
+    k_small = bf16_bits_to_f32(inp.k) * np.float32(2.0 ** -20)
+    inp.k = f32_to_bf16_bits(k_small)
+    assert np.all(bf16_bits_to_f64(inp.k) == k_small.astype(np.float64))  # exact scaling
+    assert np.abs(k_small).max() < 2.0 ** -14
+    run = DeviceRun(_plan(w), inp)
+    _, _, dq, dk, dv, _ = _grads(run)
+    q, k, v, do = (bf16_bits_to_f64(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    pos = np.arange(w.seq_len)
+    O, L = oracle.attention(q, k, v, pos, pos)
+    dq_r, dk_r, dv_r = oracle.attention_backward(q, k, v, do, O, L, pos, pos)
+    DQ = run.to_natural_rows(f32_to_f64(dq))
+    assert_close(DQ, dq_r, GRAD_TOL, "small K: dQ")
+    assert_close(run.to_natural_rows(f32_to_f64(dk), "kv"), dk_r, GRAD_TOL, "small K: dK")
+    assert_close(run.to_natural_rows(f32_to_f64(dv), "kv"), dv_r, GRAD_TOL, "small K: dV")
+    # the documented conversion: K rounded to fp16 (subnormal spacing 2^-24)
+    k16 = k.astype(np.float16).astype(np.float64)
+    assert np.abs(k16 - k).max() <= 2.0 ** -25
+    dq_16, _, _ = oracle.attention_backward(q, k16, v, do, O, L, pos, pos)
+    scale_dq = np.abs(dq_16).max()
+    rel16 = np.abs(DQ - dq_16).max() / scale_dq
+    rel_exact = np.abs(DQ - dq_r).max() / np.abs(dq_r).max()
+    assert rel16 <= 1e-2, (rel16, rel_exact)
+
+
+def test_llama3_8b_layer_backward_full_head_group(oracle_pool):
+    """Full-size backward in the bench's launch configuration: the whole
+    forward and backward of KV head 0 and its four query heads (every row of
+    dQ, every key of dK and dV), dQ of all heads at 1024 seeded rows, and dK
+    and dV of all KV heads at the last 512 keys; the oracle runs on the host
+    cores in parallel."""
     w = WORKLOADS["llama3_8b_layer"]
     inp = make_inputs(w)
+    N, G = w.seq_len, w.group
+    spec = oracle_pool.problem(inp)
+    rows = sample_rows(N, 1024)
+    jobs = {"head0": oracle_pool.backward_head(spec, 0),
+            "dq": oracle_pool.dq_rows(spec, rows),
+            "dkdv": oracle_pool.dkdv_keys(spec, N - 512, N)}
     plan = _plan(w)
     run = DeviceRun(plan, inp)
     _, _, dq, dk, dv, _ = _grads(run)
     DQ = run.to_natural_rows(f32_to_f64(dq))
     DK = run.to_natural_rows(f32_to_f64(dk), "kv")
     DV = run.to_natural_rows(f32_to_f64(dv), "kv")
-    q, k, v, do = (bf16_bits_to_f64(x) for x in (inp.q, inp.k, inp.v, inp.dout))
-    pos = np.arange(w.seq_len)
-    rows = sample_rows(w.seq_len, 48)
-    assert_close(DQ[rows], oracle.sampled_dq(q, k, v, do, rows, pos, pos), GRAD_TOL,
-                 "sampled dQ")
-    krows = np.arange(w.seq_len - 128, w.seq_len)
-    dk_r, dv_r = oracle.sampled_dkdv(q, k, v, do, krows, pos, pos)
-    assert_close(DK[krows], dk_r, GRAD_TOL, "last-key dK")
-    assert_close(DV[krows], dv_r, GRAD_TOL, "last-key dV")
-    # dS rows sum to zero: sum over keys of dK vanishes (fp64 sum of fp32)
-    assert np.abs(DK.sum(axis=0)).max() < 0.5
+    _, _, dq0, dk0, dv0 = jobs["head0"].get()
+    assert_close(DQ[:, :G], dq0, GRAD_TOL, "head group 0 dQ (all rows)")
+    assert_close(DK[:, 0], dk0, GRAD_TOL, "KV head 0 dK (all keys)")
+    assert_close(DV[:, 0], dv0, GRAD_TOL, "KV head 0 dV (all keys)")
+    assert_close(DQ[rows], jobs["dq"].get(), GRAD_TOL, "1024 sampled rows dQ")
+    dk_r, dv_r = jobs["dkdv"].get()
+    assert_close(DK[N - 512:], dk_r, GRAD_TOL, "last-512-key dK")
+    assert_close(DV[N - 512:], dv_r, GRAD_TOL, "last-512-key dV")
     assert np.isfinite(DQ).all() and np.isfinite(DK).all() and np.isfinite(DV).all()
 
 

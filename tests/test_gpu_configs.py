@@ -1,17 +1,25 @@
 """GPU parity at the full sizes of the remaining workloads (packed documents,
-405B-shaped full and partial prefill with both ring orderings, and the
-million-token head group), in the launch configuration bench.py uses.
+405B-shaped full and partial prefill with both ring orderings and the
+automatic choice between them, and the million-token head group), in the
+launch configuration bench.py uses.
 
-The oracle cannot afford the full N^2 work at these sizes, so each case is
-checked on outputs it can compute one by one:
-* packed documents: documents are independent, so the three shortest
-  documents are recomputed by the oracle in full (forward and backward) and
-  compared row for row;
-* the others: seeded sampled query rows (exact full-prefix softmax per row),
-  dQ on sampled rows, dK/dV on the last 128 keys, plus properties that hold at
-  any size (Pass-KV = Pass-Q, finite results, sum_k dK_k = 0).
-Rows are gathered on the device so that the host never holds the full
-tensors in fp64.
+The oracle cannot afford every output at these sizes in one process, so it
+runs on the host cores through tests/oracle_pool.py (its own functions on
+slices of the rows, put back together) and checks:
+* packed documents: the whole forward and backward of KV head 0 and its
+  four query heads (every row and every key of every document, including
+  the long documents that span many ranks), O and LSE at 128 seeded rows of
+  every document for all heads, dQ at those rows, and dK/dV of all KV heads
+  at the last 512 keys of the longest document; the three shortest
+  documents are also recomputed whole, all heads;
+* 405B-shaped prefill: O and LSE at 1024 seeded rows, for Pass KV, Pass Q
+  and the plan that chooses between them (VARIANT_AUTO, "Ring Attention
+  Algorithms"), which must pick Pass KV for the full prefill and Pass Q for
+  4096 new tokens after a 126976-token cache;
+* million-token head group: O and LSE at 4096 seeded rows (all heads), dQ
+  at 256 seeded rows, dK and dV at the last 512 keys.
+Device rows are gathered on the device so that the host never holds the
+full tensors in fp64.
 """
 import numpy as np
 import pytest
@@ -47,103 +55,138 @@ def _backward(run, o, lse, o_f32):
     return dq, dk, dv
 
 
-def _dk_sum_by_range(run, dk, ranges):
-    """max |sum_k dK_k| over each natural key range, summed on the device in fp64."""
-    worst = 0.0
-    for a, b in ranges:
-        g = torch.from_numpy(np.asarray(run.take_index(np.arange(a, b), "kv"))).cuda()
-        s = torch.index_select(dk, 0, g).double().sum(dim=0)
-        worst = max(worst, float(s.abs().max()))
-    return worst
+def _doc_rows(cu, per_doc, seed=0):
+    """The first two and last two rows of every document plus seeded rows
+    inside it, per_doc in all (fewer for short documents)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for a, b in zip(cu[:-1], cu[1:]):
+        a, b = int(a), int(b)
+        ends = np.array([a, a + 1, b - 2, b - 1])
+        inner = rng.choice(np.arange(a, b), size=min(per_doc - 4, b - a), replace=False)
+        out.append(np.union1d(ends, inner))
+    return np.unique(np.concatenate(out))
 
 
-def test_packed_docs_forward_backward():
+def test_packed_docs_forward_backward(oracle_pool):
     w = WORKLOADS["packed_docs"]
     inp = make_inputs(w)
     cu = inp.cu_seqlens
+    lens = np.diff(cu)
+    spec = oracle_pool.problem(inp)
+    # the oracle works on the host cores while the device runs
+    rows = _doc_rows(cu, 128)
+    longest = int(np.argmax(lens))
+    ka, kb = int(cu[longest + 1]) - 512, int(cu[longest + 1])
+    jobs = {"head0": oracle_pool.backward_head(spec, 0),
+            "fwd": oracle_pool.forward_rows(spec, rows),
+            "dq": oracle_pool.dq_rows(spec, rows),
+            "dkdv": oracle_pool.dkdv_keys(spec, ka, kb)}
     plan = _plan(w, cu=cu)
     run = DeviceRun(plan, inp)
     o, lse, ws = run.forward()
     dq, dk, dv = _backward(run, o, lse, ws)  # fp32 O from the forward workspace
     del ws
-    lens = np.diff(cu)
+    N = w.seq_len
+    G = w.group
+    allr = np.arange(N)
+
+    # KV head 0 and its query heads, every row and key of every document
+    O0, L0, dq0, dk0, dv0 = jobs["head0"].get()
+    hs = slice(0, G)
+    # (heads sliced on the device before the rows are gathered)
+    assert_close_bf16(run.take(o[:, hs], allr), O0, 1e-2, "head group 0 O (all rows)")
+    assert_close(run.take(lse[hs], allr, axis=1), L0, 1e-3, "head group 0 LSE (all rows)")
+    assert_close(run.take(dq[:, hs], allr), dq0, GRAD_TOL, "head group 0 dQ (all rows)")
+    assert_close(run.take(dk[:, 0], allr, "kv"), dk0, GRAD_TOL, "KV head 0 dK (all keys)")
+    assert_close(run.take(dv[:, 0], allr, "kv"), dv0, GRAD_TOL, "KV head 0 dV (all keys)")
+
+    # all heads at rows of every document
+    Or, Lr = jobs["fwd"].get()
+    assert_close_bf16(run.take(o, rows), Or, 1e-2, "rows of every document O")
+    assert_close(run.take(lse, rows, axis=1), Lr, 1e-3, "rows of every document LSE")
+    assert_close(run.take(dq, rows), jobs["dq"].get(), GRAD_TOL, "rows of every document dQ")
+    dk_r, dv_r = jobs["dkdv"].get()
+    krows = np.arange(ka, kb)
+    assert_close(run.take(dk, krows, "kv"), dk_r, GRAD_TOL, "longest document last-512 dK")
+    assert_close(run.take(dv, krows, "kv"), dv_r, GRAD_TOL, "longest document last-512 dV")
+
+    # the three shortest documents whole, all heads
     for doc in np.argsort(lens)[:3]:
         a, b = int(cu[doc]), int(cu[doc + 1])
-        rows = np.arange(a, b)
+        r = np.arange(a, b)
         q, k, v, do = (bf16_bits_to_f64(x[a:b]) for x in (inp.q, inp.k, inp.v, inp.dout))
         pos = np.arange(b - a)
-        Or, Lr = oracle.attention(q, k, v, pos, pos)
-        dq_r, dk_r, dv_r = oracle.attention_backward(q, k, v, do, Or, Lr, pos, pos)
+        Od, Ld = oracle.attention(q, k, v, pos, pos)
+        dq_d, dk_d, dv_d = oracle.attention_backward(q, k, v, do, Od, Ld, pos, pos)
         tag = f"document {doc} [{a},{b})"
-        assert_close_bf16(run.take(o, rows), Or, 1e-2, tag + " O")
-        assert_close(run.take(lse, rows, axis=1), Lr, 1e-3, tag + " LSE")
-        assert_close(run.take(dq, rows), dq_r, GRAD_TOL, tag + " dQ")
-        assert_close(run.take(dk, rows, "kv"), dk_r, GRAD_TOL, tag + " dK")
-        assert_close(run.take(dv, rows, "kv"), dv_r, GRAD_TOL, tag + " dV")
-    # whole-size property: per document, sum_k dK_k = 0
-    assert _dk_sum_by_range(run, dk, zip(cu[:-1], cu[1:])) < 0.5
+        assert_close_bf16(run.take(o, r), Od, 1e-2, tag + " O")
+        assert_close(run.take(lse, r, axis=1), Ld, 1e-3, tag + " LSE")
+        assert_close(run.take(dq, r), dq_d, GRAD_TOL, tag + " dQ")
+        assert_close(run.take(dk, r, "kv"), dk_d, GRAD_TOL, tag + " dK")
+        assert_close(run.take(dv, r, "kv"), dv_d, GRAD_TOL, tag + " dV")
     for t in (o, lse, dq, dk, dv):
         assert bool(torch.isfinite(t.float()).all())
 
 
-@pytest.mark.parametrize("name", ["prefill_405b_full", "prefill_405b_partial"])
-def test_prefill_405b_both_orderings(name):
+@pytest.mark.parametrize("name,auto_choice", [("prefill_405b_full", "pass_kv"),
+                                              ("prefill_405b_partial", "pass_q")])
+def test_prefill_405b_both_orderings(oracle_pool, name, auto_choice):
     w = WORKLOADS[name]
     inp = make_inputs(w, with_dout=False)
-    P, N = w.kv_prefix_len, w.seq_len
-    rows = sample_rows(N, 32)
-    k, v = bf16_bits_to_f64(inp.k), bf16_bits_to_f64(inp.v)
-    # only the sampled query rows are widened to fp64
-    Or, Lr = oracle.sampled_forward(bf16_bits_to_f64(inp.q[rows]), k, v,
-                                    np.arange(len(rows)), P + rows, np.arange(P + N))
-    del k, v
+    N = w.seq_len
+    rows = sample_rows(N, 1024)
+    job = oracle_pool.forward_rows(oracle_pool.problem(inp, w.kv_prefix_len), rows)
     results = {}
-    for variant in ("pass_kv", "pass_q"):
+    Or = Lr = None
+    for variant in ("pass_kv", "pass_q", "auto"):
         plan = _plan(w, variant)
+        if variant == "auto":
+            # the selector of "Ring Attention Algorithms": full prefill keeps
+            # Q still (Pass KV); a high cache-hit rate moves Q (Pass Q)
+            assert plan.variant == auto_choice
         run = DeviceRun(plan, inp)
         o, lse, ws = run.forward()
         del ws
+        if Or is None:
+            Or, Lr = job.get()
         assert_close_bf16(run.take(o, rows), Or, 1e-2, f"{name} {variant} sampled O")
         assert_close(run.take(lse, rows, axis=1), Lr, 1e-3, f"{name} {variant} sampled LSE")
-        # both plans share the same rank-major order, so outputs compare directly
+        # all plans share the same rank-major order, so outputs compare directly
         results[variant] = (o, lse)
         del run
     (o1, l1), (o2, l2) = results["pass_kv"], results["pass_q"]
     # the two orderings merge the same partial results in different orders
     assert float((o1.float() - o2.float()).abs().max()) <= 2e-2
     assert float((l1 - l2).abs().max()) <= 1e-3
+    oa, la = results["auto"]
+    ob, lb = results[auto_choice]
+    assert torch.equal(oa, ob) and torch.equal(la, lb)  # same kernels, same order
 
 
-def test_million_token_group_forward_backward():
+def test_million_token_group_forward_backward(oracle_pool):
     w = WORKLOADS["million_token_group"]
     inp = make_inputs(w)
+    N = w.seq_len
+    spec = oracle_pool.problem(inp)
+    rows = sample_rows(N, 4096)
+    rows_dq = sample_rows(N, 256, seed=1)
+    jobs = {"fwd": oracle_pool.forward_rows(spec, rows),
+            "dq": oracle_pool.dq_rows(spec, rows_dq),
+            "dkdv": oracle_pool.dkdv_keys(spec, N - 512, N)}
     plan = _plan(w)
     run = DeviceRun(plan, inp)
     o, lse, ws = run.forward()
     dq, dk, dv = _backward(run, o, lse, ws)  # fp32 O from the forward workspace
     del ws
-    N = w.seq_len
-    pos = np.arange(N)
-    k, v = bf16_bits_to_f64(inp.k), bf16_bits_to_f64(inp.v)
-
-    def rows_of(x, r):  # widen only the needed query rows to fp64
-        return bf16_bits_to_f64(x[r])
-
-    rows = sample_rows(N, 40)
-    sub = np.arange(len(rows))
-    Or, Lr = oracle.sampled_forward(rows_of(inp.q, rows), k, v, sub, rows, pos)
-    assert_close_bf16(run.take(o, rows), Or, 1e-2, "sampled O")
-    assert_close(run.take(lse, rows, axis=1), Lr, 1e-3, "sampled LSE")
-    rows_dq = sample_rows(N, 12)
-    dq_r = oracle.sampled_dq(rows_of(inp.q, rows_dq), k, v, rows_of(inp.dout, rows_dq),
-                             np.arange(len(rows_dq)), rows_dq, pos)
-    assert_close(run.take(dq, rows_dq), dq_r, GRAD_TOL, "sampled dQ")
-    # the last 128 keys are seen only by the last 128 queries
-    krows = np.arange(N - 128, N)
-    dk_r, dv_r = oracle.sampled_dkdv(rows_of(inp.q, krows), k, v, rows_of(inp.dout, krows),
-                                     krows, krows, pos)
-    assert_close(run.take(dk, krows, "kv"), dk_r, GRAD_TOL, "last-key dK")
-    assert_close(run.take(dv, krows, "kv"), dv_r, GRAD_TOL, "last-key dV")
-    assert float(dk.double().sum(dim=0).abs().max()) < 2.0
+    Or, Lr = jobs["fwd"].get()
+    assert_close_bf16(run.take(o, rows), Or, 1e-2, "4096 sampled rows O")
+    assert_close(run.take(lse, rows, axis=1), Lr, 1e-3, "4096 sampled rows LSE")
+    assert_close(run.take(dq, rows_dq), jobs["dq"].get(), GRAD_TOL, "256 sampled rows dQ")
+    # the last 512 keys are seen only by the last 512 queries
+    dk_r, dv_r = jobs["dkdv"].get()
+    krows = np.arange(N - 512, N)
+    assert_close(run.take(dk, krows, "kv"), dk_r, GRAD_TOL, "last-512-key dK")
+    assert_close(run.take(dv, krows, "kv"), dv_r, GRAD_TOL, "last-512-key dV")
     for t in (o, lse, dq, dk, dv):
         assert bool(torch.isfinite(t.float()).all())

@@ -204,27 +204,26 @@ def test_layout_permute_bit_exact(layout):
                           qx.view(torch.int16).cpu().numpy()[qperm])
 
 
-def test_llama3_8b_layer_forward_sampled():
+def test_llama3_8b_layer_forward_sampled(oracle_pool):
     """Full-size 32768-token forward in the bench's launch configuration,
-    checked on seeded sampled rows (all heads) by the oracle's full-prefix
-    softmax, plus properties that hold at any size."""
+    checked on 1024 seeded sampled rows (all heads) by the oracle's
+    full-prefix softmax (evaluated on the host cores in parallel), plus
+    properties that hold at any size."""
     w = WORKLOADS["llama3_8b_layer"]
     inp = make_inputs(w, with_dout=False)
+    rows = sample_rows(w.seq_len, 1024)
+    job = oracle_pool.forward_rows(oracle_pool.problem(inp), rows)
     plan = _plan(w)
     run = DeviceRun(plan, inp)
     o, lse, _ = run.forward()
     O = run.to_natural_rows(bf16_to_f64(o))
     L = run.to_natural_rows(f32_to_f64(lse), axis=1)
-    rows = sample_rows(w.seq_len, 128)
-    q = bf16_bits_to_f64(inp.q)
-    k = bf16_bits_to_f64(inp.k)
-    v = bf16_bits_to_f64(inp.v)
-    pos = np.arange(w.seq_len)
-    Or, Lr = oracle.sampled_forward(q, k, v, rows, pos, pos)
-    assert_close_bf16(O[rows], Or, 1e-2, "sampled O")
-    assert_close(L[:, rows], Lr, 1e-3, "sampled LSE")
+    Or, Lr = job.get()
+    assert_close_bf16(O[rows], Or, 1e-2, "1024 sampled rows O")
+    assert_close(L[:, rows], Lr, 1e-3, "1024 sampled rows LSE")
     # row 0 sees only itself
-    assert np.abs(O[0] - v[0, np.arange(w.n_q_heads) // w.group]).max() == 0.0
+    v0 = bf16_bits_to_f64(inp.v[0])
+    assert np.abs(O[0] - v0[np.arange(w.n_q_heads) // w.group]).max() == 0.0
     assert np.isfinite(L).all()
 
 

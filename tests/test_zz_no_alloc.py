@@ -1,19 +1,22 @@
 """The allocation-free forward entry point (cp_attn_forward_noalloc).
 
-It serves callers that cannot call cudaMalloc (for example a plugin in a host
-program that owns all device memory and gives it no allocator): they pass
-only inputs and outputs, and the forward workspace comes from a fixed device
-array inside the library. These checks call it through the C ABI, twice in a
-row on each plan, and compare with cp_attn_forward given a caller-allocated
-workspace, at the tolerances of the other forward tests. This file runs last
-so that a failure here never hides the other tests.
-"""
-import ctypes
+It serves callers that cannot call cudaMalloc on the compute path (for
+example a plugin in a host program that owns all device memory and gives it
+no allocator): they pass only inputs and outputs, and the forward workspace
+comes from a fixed device array inside the library. These checks call it
+through the C ABI and compare with cp_attn_forward given a caller-allocated
+workspace and with the oracle, at the tolerances of the other forward tests.
 
+Before the checked calls, another call with other inputs and the other ring
+ordering runs through the same array, so a forward that read leftover
+contents of the array instead of writing them first would be caught. This
+file runs last so that a failure here never hides the other tests.
+"""
 import numpy as np
 import pytest
 
-from workloads import Workload, make_inputs
+import oracle
+from workloads import Workload, bf16_bits_to_f64, make_inputs
 from gpu_utils import DeviceRun, assert_close, assert_close_bf16, bf16_to_f64, cuda_ok, f32_to_f64
 
 pytestmark = [pytest.mark.gpu,
@@ -26,10 +29,23 @@ if cuda_ok():
 
 def _noalloc(plan, run, o, lse):
     lib = cpa.load()
-    st = lib.cp_attn_forward_noalloc(plan.handle, run.q.data_ptr(), run.k.data_ptr(),
-                                     run.v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                     torch.cuda.current_stream().cuda_stream)
-    return st
+    return lib.cp_attn_forward_noalloc(plan.handle, run.q.data_ptr(), run.k.data_ptr(),
+                                       run.v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       torch.cuda.current_stream().cuda_stream)
+
+
+def _other_call(variant, shape):
+    """A forward through the array with other seeded inputs and the other
+    ring ordering, leaving its contents in the array."""
+    N, Hq, Hkv, d, R = shape
+    other = "pass_q" if variant == "pass_kv" else "pass_kv"
+    w = Workload("noalloc_other", N, Hq, Hkv, d, R, seed=7)
+    plan = cpa.Plan(N, R, Hq, Hkv, d, variant=other)
+    run = DeviceRun(plan, make_inputs(w))
+    o = torch.empty_like(run.q)
+    lse = torch.empty((Hq, plan.T_q), dtype=torch.float32, device="cuda")
+    assert _noalloc(plan, run, o, lse) == 0, cpa.load().cp_attn_last_error()
+    plan.sync_status()
 
 
 @pytest.mark.parametrize("variant,shape", [
@@ -39,22 +55,36 @@ def _noalloc(plan, run, o, lse):
 def test_forward_noalloc_matches_forward(variant, shape):
     N, Hq, Hkv, d, R = shape
     w = Workload("noalloc", N, Hq, Hkv, d, R)
+    inp = make_inputs(w)
     plan = cpa.Plan(N, R, Hq, Hkv, d, variant=variant)
-    run = DeviceRun(plan, make_inputs(w))
+    run = DeviceRun(plan, inp)
     assert plan.workspace_size(cpa.OP_FORWARD) <= cpa.load().cp_attn_forward_noalloc_capacity()
     o_ref, lse_ref, _ = run.forward()
     O_ref, L_ref = bf16_to_f64(o_ref), f32_to_f64(lse_ref)
-    free_after = []
+    # the oracle on the same bf16 inputs, in the plan's rank-major row order
+    pos = np.arange(N)
+    O_or, L_or = oracle.attention(*(bf16_bits_to_f64(x) for x in (inp.q, inp.k, inp.v)),
+                                  pos, pos)
+    qidx = run.take_index(pos)
+    torch.cuda.synchronize()
+    free = [torch.cuda.mem_get_info()[0]]
+    _other_call(variant, shape)
     for call in range(2):
         o = torch.full_like(o_ref, float("nan"))
         lse = torch.full_like(lse_ref, float("nan"))
         assert _noalloc(plan, run, o, lse) == 0, cpa.load().cp_attn_last_error()
         plan.sync_status()
-        assert_close_bf16(bf16_to_f64(o), O_ref, 1e-2, f"call {call} O")
-        assert_close(f32_to_f64(lse), L_ref, 1e-3, f"call {call} LSE")
-        free_after.append(torch.cuda.mem_get_info()[0])
-    # no device memory was taken by the second call
-    assert free_after[1] == free_after[0]
+        got_o, got_l = bf16_to_f64(o), f32_to_f64(lse)
+        assert_close_bf16(got_o, O_ref, 1e-2, f"call {call} O vs cp_attn_forward")
+        assert_close(got_l, L_ref, 1e-3, f"call {call} LSE vs cp_attn_forward")
+        assert_close_bf16(got_o[qidx], O_or, 1e-2, f"call {call} O vs oracle")
+        assert_close(got_l[:, qidx], L_or, 1e-3, f"call {call} LSE vs oracle")
+        del o, lse
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
+    # device memory does not grow across the checked calls (the array is part
+    # of the library's device image, loaded before the first reading here)
+    assert free[2] == free[1], free
 
 
 def test_forward_noalloc_rejects_plans_beyond_capacity():
