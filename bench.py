@@ -95,6 +95,32 @@ def whole_job_tflops(n_ranks: int, flops_per_rank_step: float, ms_per_step: floa
     return n_ranks * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
+def roofline_record(kernel, achieved, flops_per_launch, peaks, peak_kind, clocks):
+    """Roofline of a tensor-bound kernel timed in a sub-second loop.
+
+    frac is against the measured burst bf16 peak (a GEMM timed alone, the
+    regime of this loop). Two secondary figures: the peak scaled to the SM
+    clock seen during the timed region (peak x median MHz / max MHz), and
+    the sustained peak (a seconds-long GEMM loop under the power cap)."""
+    peak = peaks["bf16_tflops"]
+    rec = {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak,
+           "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+           "peak_kind": f"bf16_tflops burst ({peak_kind}): the kernel is timed in a "
+                        "sub-second loop, the regime of the burst measurement",
+           "flops_per_launch": flops_per_launch}
+    sust = peaks.get("bf16_tflops_sustained")
+    if sust:
+        rec["peak_sustained"] = sust
+        rec["frac_sustained"] = achieved / sust
+    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        scale = clocks["sm_mhz"] / clocks["sm_max_mhz"]
+        rec["clock_normalised"] = {
+            "sm_mhz_median": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+            "peak_at_clock": peak * scale, "frac": achieved / (peak * scale),
+            "basis": "burst peak x (median SM MHz in the timed region / max SM MHz)"}
+    return rec
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -205,6 +231,124 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def time_config(w, steps: int, warmup: int, dev):
+    """Forward and backward ring passes of another workload (per-step calls,
+    chained, fp32 accumulators), timed with CUDA events on the launching
+    stream: median fwd, bwd and whole-pass times and TFLOPS (unmasked FLOPs)."""
+    import torch
+    import context_causal_attention_ring_gb300 as cpa
+
+    stream = torch.cuda.current_stream()
+    inp = make_inputs(w, with_dout=True)
+    plan = cpa.Plan(w.seq_len, w.cp, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                    layout=w.layout, variant="pass_kv", cu_seqlens=inp.cu_seqlens,
+                    kv_prefix_len=w.kv_prefix_len)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    nat = [dev_bf16(x) for x in (inp.q, inp.k, inp.v, inp.dout)]
+    del inp
+    q, k, v, do = (torch.empty_like(x) for x in nat)
+    for kind, x, y in zip((cpa.TENSOR_Q, cpa.TENSOR_KV, cpa.TENSOR_KV, cpa.TENSOR_Q), nat,
+                          (q, k, v, do)):
+        plan.layout_apply(kind, cpa.TO_RANK_MAJOR, x, y)
+    del nat
+    R, Hq, Hkv, d = plan.R, plan.Hq, plan.Hkv, plan.d
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, plan.T_q), dtype=torch.float32, device=dev)
+    o_acc = torch.empty((plan.T_q, Hq, d), dtype=torch.float32, device=dev)
+    delta = torch.empty((Hq, plan.T_q), dtype=torch.float32, device=dev)
+    half_ops = torch.empty(plan.half_ops_size(), dtype=torch.uint8, device=dev)
+    dq = torch.empty((plan.T_q, Hq, d), dtype=torch.float32, device=dev)
+    dk = torch.empty((plan.T_kv, Hkv, d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    plan.set_chaining(True)
+    fwd_flops = 4.0 * d * Hq * plan.visible_pairs()
+
+    def one(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for t in range(R):
+            plan.step_fwd(t, q, k, v, o_acc, lse, cpa.ACCUMULATE, o if t == R - 1 else None,
+                          stream)
+        if ev is not None:
+            ev[1].record(stream)
+        plan.bwd_preprocess(q, k, v, o, do, delta, half_ops, dq, dk, dv, o_f32=o_acc,
+                            stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        for t in range(R):
+            plan.step_bwd_half(t, half_ops, lse, delta, dq, dk, dv, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in evs:
+        one(e)
+    torch.cuda.synchronize()
+    plan.sync_status(stream)
+    fwd = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd = statistics.median(e[2].elapsed_time(e[3]) for e in evs)
+    whole = statistics.median(e[0].elapsed_time(e[3]) for e in evs)
+    out = {"workload": w.name, "seq_len": w.seq_len, "cp": w.cp, "n_q_heads": Hq,
+           "n_kv_heads": Hkv, "head_dim": d, "steps": steps, "warmup": warmup,
+           "fwd_ms": fwd, "bwd_ms": bwd, "step_ms": whole,
+           "fwd_tflops": fwd_flops / (fwd * 1e-3) / 1e12,
+           "bwd_tflops": 2.5 * fwd_flops / (bwd * 1e-3) / 1e12,
+           "step_tflops": 3.5 * fwd_flops / (whole * 1e-3) / 1e12}
+    del q, k, v, do, o, lse, o_acc, delta, half_ops, dq, dk, dv, plan
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_oracle_plan_runs():
+    """The oracle as planned for the CPU baseline: the whole tiny ring
+    (forward ring with its merge, and the ring backward) and a sampled
+    million-token forward (a few seeded rows, exact full-prefix softmax each;
+    labelled sampled, not extrapolated)."""
+    import oracle
+    from workloads import sample_rows
+    runs = []
+    w = WORKLOADS["tiny_ring"]
+    inp = make_inputs(w, with_dout=True)
+    q_pos, kv_pos = oracle.plan_positions(w.seq_len, w.cp, w.layout)
+    qperm, kperm = np.concatenate(q_pos), np.concatenate(kv_pos)
+    q, k, v, do = (bf16_bits_to_f64(x) for x in (inp.q, inp.k, inp.v, inp.dout))
+    pairs = oracle.count_visible(np.arange(w.seq_len), np.arange(w.seq_len))
+    t0 = time.perf_counter()
+    O, L = oracle.ring_forward(q[qperm], k[kperm], v[kperm], q_pos, kv_pos)
+    oracle.ring_backward(q[qperm], k[kperm], v[kperm], do[qperm], O, L, q_pos, kv_pos)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.head_dim * w.n_q_heads * pairs * 3.5
+    runs.append({"workload": w.name, "kind": "full", "what": "ring forward + ring backward",
+                 "seconds": dt, "us": dt * 1e6, "gflops": flops / dt / 1e9})
+    w = WORKLOADS["million_token_group"]
+    N = w.seq_len
+    rows = sample_rows(N, 30)
+    # the sample's operands are drawn directly with the workload's recipe
+    # (N(0,1), Q and K x 0.5, bf16) from their own seeded stream: the
+    # oracle's time does not depend on the values, and drawing the whole
+    # workload first would dominate the bench
+    from workloads import draw_bf16
+    rng = np.random.default_rng(w.seed)
+    qr = bf16_bits_to_f64(draw_bf16(rng, (len(rows), w.n_q_heads, w.head_dim), w.qk_scale))
+    k = bf16_bits_to_f64(draw_bf16(rng, (N, w.n_kv_heads, w.head_dim), w.qk_scale))
+    v = bf16_bits_to_f64(draw_bf16(rng, (N, w.n_kv_heads, w.head_dim)))
+    t0 = time.perf_counter()
+    oracle.sampled_forward(qr, k, v, np.arange(len(rows)), rows, np.arange(N))
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.head_dim * w.n_q_heads * float(np.sum(rows + 1))
+    runs.append({"workload": w.name, "kind": "sampled",
+                 "what": f"forward O and LSE at {len(rows)} seeded rows of the 1M-token "
+                         "sequence, all heads, operands drawn for the sample",
+                 "rows": int(len(rows)), "seconds": dt, "gflops": flops / dt / 1e9})
+    return runs
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -255,12 +399,14 @@ def run_ours(args, w):
                           o if t == R - 1 else None, stream)
         if ev is not None:
             ev[1].record(stream)
+        # delta, zeroed accumulators and the fp16 operand copies, so that the
+        # backward phase times the K2 launches alone
         plan.bwd_preprocess(q, k, v, o, do, delta, half_ops, dq, dk, dv, o_f32=o_acc,
                             stream=stream)
         if ev is not None:
             ev[2].record(stream)
         for t in range(R):
-            plan.step_bwd(t, half_ops, lse, delta, dq, dk, dv, stream)
+            plan.step_bwd_half(t, half_ops, lse, delta, dq, dk, dv, stream)
         if ev is not None:
             ev[3].record(stream)
 
@@ -287,7 +433,7 @@ def run_ours(args, w):
 
         def bwd_part():
             for t in range(R):
-                plan.step_bwd(t, half_ops, lse, delta, dq, dk, dv, cap)
+                plan.step_bwd_half(t, half_ops, lse, delta, dq, dk, dv, cap)
 
         cap.wait_stream(stream)
         for part in (fwd_part, pre_part, bwd_part):
@@ -345,17 +491,14 @@ def run_ours(args, w):
     bwd_tflops = bwd_flops / (statistics.median(bwd_ms) * 1e-3) / 1e12
 
     peaks, peak_kind = _peaks()
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     # dominant kernel: the one with more device time per step
     if sum(bwd_ms) >= sum(fwd_ms):
         dom, dom_flops, dom_ms = "step_bwd", bwd_flops, sum(bwd_ms) / args.steps
     else:
         dom, dom_flops, dom_ms = "step_fwd", fwd_flops, sum(fwd_ms) / args.steps
     achieved = (dom_flops / R) / (dom_ms / R * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": _profiled_traffic(dom),
-                "peak_kind": f"bf16_tflops_sustained ({peak_kind}): timed inside a long loop",
-                "flops_per_launch": dom_flops / R}
+    roofline = roofline_record(dom, achieved, dom_flops / R, peaks, peak_kind, clocks)
+    roofline["traffic"] = _profiled_traffic(dom)
 
     # end to end through the public whole-op calls with host buffers
     e2e = None
@@ -368,6 +511,19 @@ def run_ours(args, w):
         val, dt, desc = cpu_oracle_sample(w, heads, inp)
         cpu = {"value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": desc, "seconds": dt}
+        if not args.no_configs:
+            cpu["plan_runs"] = cpu_oracle_plan_runs()
+
+    # the other workloads' figures (not the headline): the tiny ring in
+    # microseconds and the packed documents in TFLOPS
+    configs = None
+    if rank == 0 and ws == 1 and not args.no_configs:
+        del inp
+        configs = [time_config(WORKLOADS[name], n, 3, dev)
+                   for name, n in (("tiny_ring", 20), ("packed_docs", 5))]
+        configs[0]["fwd_us"] = configs[0]["fwd_ms"] * 1e3
+        configs[0]["bwd_us"] = configs[0]["bwd_ms"] * 1e3
+        configs[0]["step_us"] = configs[0]["step_ms"] * 1e3
 
     if rank == 0:
         line = {
@@ -387,6 +543,7 @@ def run_ours(args, w):
             "pct_of_peak_burst": 100.0 * value / ws / peaks["bf16_tflops"],
             "gpu_launches": n_launches,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -789,11 +946,29 @@ def run_e2e(args, plan, inp, dev, stream, flops, ws):
     torch.cuda.synchronize()
     plan.sync_status(stream)
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    # latency of one call with host buffers, nothing overlapped: copy-in,
+    # compute and copy-out of a single step with the device otherwise idle
+    lat = []
+    for i in range(3):
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        h2d_stream.wait_event(s0)
+        step(i)
+        stream.wait_stream(d2h_stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        lat.append(s0.elapsed_time(s1))
+    lat_ms = max_over_ranks(statistics.median(lat), dev)
     return {"value": whole_job_tflops(ws, flops, ms), "unit": UNIT, "ms_per_step": ms,
+            "latency_ms_unpipelined": lat_ms,
+            "value_unpipelined": whole_job_tflops(ws, flops, lat_ms),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "path": "pinned host -> device, layout to rank-major, cp_attn_forward, "
                     "cp_attn_backward, layout to natural, device -> pinned host; "
-                    "copies on their own streams, pipelined over two buffer sets"}
+                    "copies on their own streams, pipelined over two buffer sets; "
+                    "latency_ms_unpipelined: one step alone, copies not overlapped"}
 
 
 def main():
@@ -805,6 +980,8 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_layer", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' figures (tiny ring, packed documents)")
     ap.add_argument("--q-heads", type=int, default=0,
                     help="profiling aid: override the workload's query heads")
     ap.add_argument("--kv-heads", type=int, default=0,
