@@ -425,8 +425,9 @@ enum : int {
   PB_KE = PB_V + kVStagesMax,    // [kKStagesMax] K stage free
   PB_VE = PB_KE + kKStagesMax,   // [kVStagesMax] V stage free
   PB_S = PB_VE + kVStagesMax,    // [2] S of head slot ready
-  PB_P = PB_S + 2,               // [2] P of head slot written (128 arrivals)
-  PB_O = PB_P + 2,               // [2] final O of head slot ready
+  PB_P = PB_S + 2,               // [2 heads][2 halves] P of keys 0-63 / 64-127
+                                 // written (128 arrivals)
+  PB_O = PB_P + 4,               // [2] final O of head slot ready
   PB_DRAIN = PB_O + 2,
   PB_COUNT = PB_DRAIN + 1
 };
@@ -514,7 +515,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < PB_COUNT; ++i)
-      ptx::mbar_init(bar(i), (i == PB_P || i == PB_P + 1) ? 128u : 1u);
+      ptx::mbar_init(bar(i), (i >= PB_P && i < PB_P + 4) ? 128u : 1u);
     *s_abort = 0;
     ptx::fence_barrier_init();
   }
@@ -606,27 +607,41 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       ptx::mma_commit_w(bar(PB_S + hs), leader);
     };
-    auto issue_o = [&](int j, int hs) {
+    // O += P V over keys [64 half, 64 half + 64) of tile j
+    auto issue_o = [&](int j, int hs, int half) {
       if constexpr (F8) {
         // B = V^T [d][keys] K-major (one swizzle atom); A = P, four E4M3 per
         // column in the head's S columns: 32 keys = 8 columns per MMA
         const uint64_t dv = ptx::sdesc_sw128(sV + (j % VS) * L::kTile, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int kk = 2 * half + k2;
           ptx::mma_ts_f8_w(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
                            ptx::sdesc_add(dv, kk * 32), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
                            leader);
+        }
       } else {
         // B = V [keys][d] MN-major: 8-key groups at 1 KB, d 64..127 at +16 KB
         const uint64_t dv = ptx::sdesc_sw128(sV + (j % VS) * L::kTile, 16384, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int k4 = 0; k4 < 4; ++k4) {
           // A = P (bf16 pairs in the head's S columns), 16 keys = 8 columns
+          const int kk = 4 * half + k4;
           ptx::mma_ts_w(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
                         ptx::sdesc_add(dv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
                         leader);
         }
       }
+    };
+    // both halves of O += P V for head slot hs, each once its half of P is
+    // written (the first half starts while the second is computed)
+    auto issue_o_halves = [&](int jp, int hs, int where) -> bool {
+      issue_o(jp, hs, 0);
+      const uint32_t b[1] = {bar(PB_P + 2 * hs + 1)};
+      const uint32_t ph[1] = {static_cast<uint32_t>(jp & 1)};
+      if (!wait_set(b, ph, where)) return false;
+      issue_o(jp, hs, 1);
+      return true;
     };
     bool ok;
     {
@@ -652,14 +667,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                                      : static_cast<uint32_t>((jp / VS) & 1)};
         if (!wait_set(b, ph, 0x3300 + j)) { ok = false; break; }
       }
-      issue_o(jp, 0);
+      if (!issue_o_halves(jp, 0, 0x3400 + j)) { ok = false; break; }
       if (more) issue_s(j, 0);
       else ptx::mma_commit_w(bar(PB_O + 0), leader);
       if (nh == 2) {
-        const uint32_t b[1] = {bar(PB_P + 1)};
+        const uint32_t b[1] = {bar(PB_P + 2)};
         const uint32_t ph[1] = {static_cast<uint32_t>(jp & 1)};
         if (!wait_set(b, ph, 0x3500 + j)) { ok = false; break; }
-        issue_o(jp, 1);
+        if (!issue_o_halves(jp, 1, 0x3900 + j)) { ok = false; break; }
       }
       ptx::mma_commit_w(bar(PB_VE + jp % VS), leader);
       if (nh == 2) {
@@ -749,6 +764,26 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const float2 nb2 = make_float2(kPExp - base, kPExp - base);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
+      // P of keys 0-63 is handed to the MMA warp before that of keys
+      // 64-127. A moved maximum first rescales the running O, which the
+      // first half's P V accumulates into (S(j) complete implies O += P V of
+      // tile j-1 complete); the rescale runs after the first half's
+      // exponentials, when half of the scores are no longer held.
+      auto hand_over = [&](int half) {
+        if (half == 0 && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            ptx::tmem_ld32(tO + lane_base + c * 32, o);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] *= alpha;
+            ptx::tmem_st32(tO + lane_base + c * 32, o);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(PB_P + 2 * hs + half));
+      };
       if constexpr (F8) {
         // four keys per column: 64 keys = 16 columns per chunk
 #pragma unroll
@@ -767,6 +802,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             pk[x] = ptx::pack_e4m3x4(e0.x, e0.y, e1.x, e1.y);
           }
           ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
+          hand_over(c);
         }
       } else {
         // P = 2^(s * scale_log2 - base), two columns per instruction, packed
@@ -785,25 +821,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             pk[x] = ptx::pack_bf16(e.x, e.y);
           }
           ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
+          if (c & 1) hand_over(c >> 1);
         }
       }
       const float2 acc01 = ptx::add2(acc[0], acc[1]);
       const float2 acc23 = ptx::add2(acc[2], acc[3]);
       const float2 accs = ptx::add2(acc01, acc23);
       l += accs.x + accs.y;
-      ptx::tmem_wait_st();
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          ptx::tmem_ld32(tO + lane_base + c * 32, o);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] *= alpha;
-          ptx::tmem_st32(tO + lane_base + c * 32, o);
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(PB_P + hs));
     }
     if (ok && n_tiles > 0) {
       if (!ptx::mbar_wait(bar(PB_O + hs), 0, s_abort, p.wait_limit_ns)) {
