@@ -189,16 +189,25 @@ cp_attn_status upload_plan(cp_attn_plan_s* p) {
     free_plan_device(p);
     return st;
   }
+  const size_t v16_bytes = static_cast<size_t>(p->T_kv) * p->Hkv * p->d * 2;
+  if (cudaMalloc(&p->d_v16, v16_bytes > 0 ? v16_bytes : 16) != cudaSuccess) {
+    cudaGetLastError();
+    p->d_v16 = nullptr;
+    free_plan_device(p);
+    return fail(CP_ATTN_ERR_OOM, "plan: cannot allocate the fp16 copy of V (" +
+                                     std::to_string(v16_bytes) + " bytes)");
+  }
   p->on_device = true;
   return CP_ATTN_OK;
 }
 
 void free_plan_device(cp_attn_plan_s* p) {
-  void* ptrs[] = {p->d_q_tile_pos, p->d_kv_tile_pos, p->d_cu,    p->d_fwd,
-                  p->d_bwd,        p->d_status,      p->d_row_q, p->d_row_kv};
+  void* ptrs[] = {p->d_q_tile_pos, p->d_kv_tile_pos, p->d_cu,    p->d_fwd,  p->d_bwd,
+                  p->d_status,      p->d_row_q,       p->d_row_kv, p->d_v16};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   p->d_q_tile_pos = p->d_kv_tile_pos = p->d_cu = p->d_status = p->d_row_q = p->d_row_kv = nullptr;
+  p->d_v16 = nullptr;
   p->d_fwd = p->d_bwd = nullptr;
   p->on_device = false;
 }
@@ -464,9 +473,17 @@ cp_attn_status step_fwd_impl(cp_attn_plan_t p, int step, const void* q, const vo
     if ((st = tmap_u8(&tk, k, p->T_kv, p->Hkv, p->d, false)) != CP_ATTN_OK) return st;
     if ((st = tmap_u8(&tv, v, p->T_kv, p->Hkv, p->d, true)) != CP_ATTN_OK) return st;
   } else {
+    // the ring's first step copies V to fp16 for the P V products of every
+    // step (P then keeps 11 significant bits)
+    if (step == 0 &&
+        (st = launch_bf16_to_f16(v, p->d_v16, p->T_kv * p->Hkv * p->d, p->d_status,
+                                 static_cast<cudaStream_t>(stream))) != CP_ATTN_OK)
+      return st;
     if ((st = tmap_bf16(&tq, q, p->T_q, p->Hq, p->d)) != CP_ATTN_OK) return st;
     if ((st = tmap_bf16(&tk, k, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
-    if ((st = tmap_bf16(&tv, v, p->T_kv, p->Hkv, p->d)) != CP_ATTN_OK) return st;
+    if ((st = tmap_3d(&tv, p->d_v16, p->T_kv, p->Hkv, p->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) !=
+        CP_ATTN_OK)
+      return st;
   }
   FwdParams fp;
   std::memset(&fp, 0, sizeof(fp));

@@ -70,6 +70,9 @@ struct cp_attn_plan_s {
   int32_t* d_status = nullptr;
   int32_t* d_row_q = nullptr;   // rank-major row -> natural row (queries)
   int32_t* d_row_kv = nullptr;  // rank-major row -> natural row (keys)
+  // fp16 copy of V [T_kv][Hkv][d], made by step 0 of every bf16 forward ring:
+  // the P V products of the step kernels run on fp16 operands
+  void* d_v16 = nullptr;
   // per-step calls of steps >= 1 launch chained to the kernel before them
   int chain_steps = 0;
   int part_bf16 = 0;        // WRITE_PARTIAL O partials (and Pass-Q slots) in bf16

@@ -21,6 +21,11 @@
 // is only raised (and O rescaled in TMEM) when a tile's max exceeds it by
 // more than 8, so exponentials stay below 2^8 -- the result is the same
 // softmax; only the reference point of the exponentials moves.
+//
+// S = Q K^T runs on the bf16 inputs (the products are exact in fp32). O += P V
+// runs on fp16 operands: P rounded to fp16 keeps 11 significant bits against
+// bf16's 8, and V comes from the fp16 copy that step 0 of the ring makes
+// (exact for every bf16 value of magnitude in [2^-14, 65504]).
 #include <cmath>
 
 #include "kernels.h"
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, w_ok);
     };
     constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0, 0);
-    constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 0, 1);
+    constexpr uint32_t idesc_o = ptx::idesc_fp16(128, D, 0, 1);  // P and V fp16
     bool ok = wait_w(bar(BAR_Q), 0, 0x200);
     auto issue_pv = [&](int i) -> bool {
       if (!wait_w(bar(BAR_P), i & 1, 0x300 + i)) {
@@ -289,13 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P (bf16) -> shared memory, swizzled K-major
+      // P (fp16) -> shared memory, swizzled K-major
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
         const float* x = s + ch * 8;
-        ptx::st_shared_v4(sP + sw128_offset(r, ch), ptx::pack_bf16(x[0], x[1]),
-                          ptx::pack_bf16(x[2], x[3]), ptx::pack_bf16(x[4], x[5]),
-                          ptx::pack_bf16(x[6], x[7]));
+        ptx::st_shared_v4(sP + sw128_offset(r, ch), ptx::pack_f16(x[0], x[1]),
+                          ptx::pack_f16(x[2], x[3]), ptx::pack_f16(x[4], x[5]),
+                          ptx::pack_f16(x[6], x[7]));
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -400,8 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (so both see exactly the same K/V tiles and the same mask). Softmax
 // warpgroup A works on S_A(j) while the tensor core runs O_B += P_B V(j-1) and
 // S_B(j), and the other way round, so exponentials and MMAs overlap. P is
-// written back into its own S columns of TMEM as bf16 pairs and feeds
-// O += P V as the A operand read from tensor memory (no shared-memory copy).
+// written back into its own S columns of TMEM as fp16 pairs (E4M3 quads in
+// the F8 instance) and feeds O += P V as the A operand read from tensor
+// memory (no shared-memory copy); V is the fp16 copy of the ring.
 // K and V stream through separate rings with their own producer warps: a K
 // stage is released once both heads' S MMAs have read it, a V stage once both
 // O MMAs have, so the next tiles are requested well before they are needed.
@@ -578,11 +584,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // The whole warp runs the loop so that descriptors stay warp-uniform;
     // one elected lane issues each tcgen05 instruction.
     const uint32_t leader = ptx::elect_one();
-    // kind::f8f6f4 format code 0 is E4M3; kind::f16 code 1 is bf16
+    // kind::f8f6f4 format code 0 is E4M3; kind::f16: S on bf16 Q and K, O on
+    // fp16 P and V
     constexpr uint32_t idesc_s = F8 ? ptx::idesc_f16kind(128, 128, 0, 0, 0u)
                                     : ptx::idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idesc_o = F8 ? ptx::idesc_f16kind(128, D, 0, 0, 0u)
-                                    : ptx::idesc_bf16(128, D, 0, 1);
+                                    : ptx::idesc_fp16(128, D, 0, 1);
     const uint64_t dQ0 = ptx::sdesc_sw128(sQ, 16, 1024);
     auto wait_set = [&](const auto& bars, const auto& par, int where) -> bool {
       return ptx::wait_phases(bars, par, s_abort, p.wait_limit_ns, p.status, where);
@@ -625,7 +632,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const uint64_t dv = ptx::sdesc_sw128(sV + (j % VS) * L::kTile, 16384, 1024);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          // A = P (bf16 pairs in the head's S columns), 16 keys = 8 columns
+          // A = P (fp16 pairs in the head's S columns), 16 keys = 8 columns
           const int kk = 4 * half + k4;
           ptx::mma_ts_w(tmem + 256 + 128 * hs, tmem + 128 * hs + kk * 8,
                         ptx::sdesc_add(dv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u,
@@ -806,7 +813,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
       } else {
         // P = 2^(s * scale_log2 - base), two columns per instruction, packed
-        // to bf16 pairs and stored into this head's S columns [0, 64) chunk
+        // to fp16 pairs and stored into this head's S columns [0, 64) chunk
         // by chunk
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             e.x = ptx::ex2(e.x);
             e.y = ptx::ex2(e.y);
             acc[x & 3] = ptx::add2(acc[x & 3], e);
-            pk[x] = ptx::pack_bf16(e.x, e.y);
+            pk[x] = ptx::pack_f16(e.x, e.y);
           }
           ptx::tmem_st16_nw(tS + lane_base + c * 16, pk);
           if (c & 1) hand_over(c >> 1);

@@ -16,7 +16,7 @@
  * Conventions (all entry points):
  *  - Tensors are caller-owned DEVICE memory unless stated otherwise. The
  *    library never allocates on a compute call; plans allocate their own
- *    small device tables at creation time.
+ *    device tables (and a buffer for an fp16 copy of V) at creation time.
  *  - Q, K, V, O, dO are bf16, row-major [tokens, heads, head_dim] with
  *    head_dim contiguous, in rank-major token order (see
  *    cp_attn_layout_apply). Base addresses must be 16-byte aligned.
@@ -191,7 +191,9 @@ typedef struct cp_attn_plan_desc {
  * TPUs with MaxText Context Parallelism", "Built on a fast attention
  * kernel") and the per-step work lists, uploaded to the current CUDA device
  * if there is one (a plan made without a device serves the host-side
- * queries only).
+ * queries only). On the device the plan also holds a buffer for an fp16 copy
+ * of V (T_kv * Hkv * head_dim * 2 bytes; see cp_attn_step_fwd); ERR_OOM if
+ * it cannot be allocated.
  * Chunk rule: zigzag needs N and P to be multiples of 256*R; USP multiples
  * of 256*R*a2a; contiguous multiples of 128*R. Returns ERR_SHAPE otherwise. On success *out
  * owns host and device tables until cp_attn_plan_destroy. */
@@ -275,6 +277,15 @@ cp_attn_status cp_attn_workspace_size(cp_attn_plan_t plan, cp_attn_op op, size_t
  * q: [T_q, Hq, d] bf16; k, v: [T_kv, Hkv, d] bf16.
  * o_final: optional bf16 [T_q, Hq, d]; when non-NULL in ACCUMULATE mode the
  *   merged result is also written there in bf16 (use on the last step).
+ * Precision: S = Q K^T runs on the bf16 inputs; O += P V runs on fp16
+ * operands, so P keeps 11 significant bits (bf16 keeps 8). Step 0 copies v
+ * to fp16 into the plan's buffer and every step of the ring reads that copy:
+ * run step 0 of a ring first, with the v of the ring, as the ring order
+ * does (a later step called without it reads whatever the buffer holds), and
+ * do not run two forward rings of one plan at the same time. Every bf16 value
+ * of magnitude in [2^-14, 65504] converts exactly; smaller ones become fp16
+ * subnormals (off by at most 2^-25); a finite value above 65504 sets
+ * CP_ATTN_ERR_RANGE in the plan's status word.
  * ERR_INVALID_ARG for null/misaligned pointers or a step outside [0, R). */
 cp_attn_status cp_attn_step_fwd(cp_attn_plan_t plan, int step,
                                 const void* q, const void* k, const void* v,
@@ -434,8 +445,9 @@ cp_attn_status cp_attn_merge_lse_ex(int n_parts, int64_t rows, int heads, int he
                                     float* lse_out, void* stream);
 
 /* Whole forward pass over the emulated ring ("Ring Attention Algorithms":
- * Pass KV and Pass Q): R step launches in step order, then (Pass Q) the
- * n-way merge over kv_owner slots. o: bf16
+ * Pass KV and Pass Q): R step launches in step order (the first also makes
+ * the fp16 copy of v, see cp_attn_step_fwd), then (Pass Q) the n-way merge
+ * over kv_owner slots. o: bf16
  * [T_q,Hq,d]; lse: fp32 [Hq,T_q]. workspace: device buffer of at least
  * cp_attn_workspace_size(plan, FORWARD) bytes, 256-byte aligned. On return
  * the workspace starts with O in fp32 [T_q,Hq,d] (the unrounded result),
@@ -454,9 +466,9 @@ cp_attn_status cp_attn_forward(cp_attn_plan_t plan, const void* q, const void* k
  * workspace. Same result as cp_attn_forward; the workspace comes from a
  * fixed device array inside the library of cp_attn_forward_noalloc_capacity()
  * bytes (32 MiB).
- *  - The plan itself still allocates its small device tables once, when it
- *    is created (cp_attn_plan / cp_attn_plan_ex); build plans before the
- *    allocation-free phase.
+ *  - The plan itself still allocates its device tables and its fp16 copy
+ *    buffer for V once, when it is created (cp_attn_plan / cp_attn_plan_ex);
+ *    build plans before the allocation-free phase.
  *  - A device holds the array from the moment the library's device image is
  *    loaded on it (under CUDA's lazy module loading: the first launch or
  *    symbol lookup of the library on that device) until the process exits.

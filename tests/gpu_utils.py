@@ -40,15 +40,18 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
 FLAT_LOG = []
 
 
-def assert_close_bf16(got, want, tol=1e-2, what=""):
+def assert_close_bf16(got, want, tol=1e-2, what="", flat_below=4.0):
     """bf16 outputs against the target's flat max-abs tol.
 
     * Everywhere, |got - want| <= tol + half a bf16 ulp of want: the
       rounding every stored bf16 result carries, which alone reaches 2^-7 for
       |want| in [2, 4) and exceeds tol beyond 4.
-    * With the target's tol (1e-2), wherever |want| < 2 the flat bound
-      |got - want| <= tol must hold (there the storage rounding is at most
-      2^-8, less than half of tol).
+    * With the target's tol (1e-2), wherever |want| < flat_below the flat
+      bound |got - want| <= tol must hold. Below 4 the storage rounding is at
+      most 2^-7 = 0.0078, which leaves room for the kernel's own error (P
+      kept to 11 significant bits for P V). Results that were rounded to bf16
+      once before (bf16 partials, whose roundings can land on neighbouring
+      bf16 values on the two sides) pass flat_below=2.
     With the target's tol, the flat maximum over all elements and how many
     elements exceed tol are recorded for the session report.
     """
@@ -58,9 +61,10 @@ def assert_close_bf16(got, want, tol=1e-2, what=""):
     assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of tolerance; "
                            f"max err {err.max():.3e}, max err-lim {(err - lim).max():.3e}")
     if tol >= 1e-2:
-        small = np.abs(want) < 2.0
+        small = np.abs(want) < flat_below
         flat = float(err[small].max()) if small.any() else 0.0
-        assert flat <= tol, f"{what}: flat max err {flat:.3e} > {tol} where |O| < 2"
+        assert flat <= tol, (f"{what}: flat max err {flat:.3e} > {tol} where "
+                             f"|O| < {flat_below}")
         over = err > tol
         FLAT_LOG.append((what, float(err.max()), int(err.size), int(over.sum()),
                          float(np.abs(want[over]).max()) if over.any() else 0.0))

@@ -63,7 +63,8 @@ def test_pass_q_forward_bf16_partials(N, Hq, Hkv, d, R, docs):
     O_ref, L_ref = oracle.ring_forward(q, k, v, qpos, kvpos, cu, variant="pass_q",
                                        partial_dtype="bf16")
     what = f"bf16 partials N={N} {Hq}/{Hkv} d={d} docs={docs}"
-    assert_close_bf16(bf16_to_f64(o), O_ref, 1e-2, what + " O")
+    # the partials were rounded to bf16 before the merge (on both sides)
+    assert_close_bf16(bf16_to_f64(o), O_ref, 1e-2, what + " O", flat_below=2.0)
     assert_close(f32_to_f64(lse), L_ref, 1e-3, what + " LSE")
 
 

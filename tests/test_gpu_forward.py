@@ -227,6 +227,27 @@ def test_llama3_8b_layer_forward_sampled(oracle_pool):
     assert np.isfinite(L).all()
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp16_range_of_v_is_reported(d):
+    """O += P V runs on an fp16 copy of V made by step 0 of the ring: a finite
+    V value above 65504 (not representable in fp16) is reported as
+    CP_ATTN_ERR_RANGE, and the next forward with valid inputs is clean."""
+    w = Workload("rangef", 1024, 2, 1, d, 4)
+    plan = _plan(w)
+    run = DeviceRun(plan, make_inputs(w))
+    v_big = run.v.clone()
+    v_big[5, 0, 3] = 1.0e5
+    o = torch.empty_like(run.q)
+    lse = torch.empty((plan.Hq, plan.T_q), dtype=torch.float32, device="cuda")
+    ws = torch.empty(plan.workspace_size(cpa.OP_FORWARD), dtype=torch.uint8, device="cuda")
+    plan.forward(run.q, run.k, v_big, o, lse, ws)
+    with pytest.raises(cpa.CpAttnError) as e:
+        plan.sync_status()
+    assert e.value.status == 7
+    plan.forward(run.q, run.k, run.v, o, lse, ws)
+    plan.sync_status()
+
+
 def test_device_wait_timeout_is_reported():
     """A kernel wait that nothing completes gives up after its time limit and
     reports CP_ATTN_ERR_TIMEOUT through the plan's status word; the context
