@@ -25,9 +25,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 #include <string>
-#include <unordered_map>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -753,23 +751,17 @@ int pick_part_len(int64_t shard, int64_t ctas_per_part, int head_dim) {
 }
 
 // Device status word of the tensor-core decode kernel (its bounded waits
-// record a timeout there), one per device, looked up once with the device
-// current.
+// record a timeout there), one per device. Its device address is looked up in
+// the current context on every call (the lookup allocates nothing): an address
+// kept from an earlier call could belong to a context that has since been
+// destroyed.
 __device__ int32_t g_decode_status[4];
-std::mutex g_status_mu;
-std::unordered_map<int, int32_t*> g_status_addr;
 
 cp_attn_status decode_status_address(int32_t** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return fail(CP_ATTN_ERR_CUDA, "decode: no current CUDA device");
-  }
-  std::lock_guard<std::mutex> lock(g_status_mu);
-  auto it = g_status_addr.find(dev);
-  if (it != g_status_addr.end()) {
-    *out = it->second;
-    return CP_ATTN_OK;
   }
   void* ptr = nullptr;
   const cudaError_t err = cudaGetSymbolAddress(&ptr, g_decode_status);
@@ -778,7 +770,6 @@ cp_attn_status decode_status_address(int32_t** out) {
     return fail(CP_ATTN_ERR_CUDA, std::string("decode: status word lookup failed: ") +
                                       cudaGetErrorString(err));
   }
-  g_status_addr[dev] = static_cast<int32_t*>(ptr);
   *out = static_cast<int32_t*>(ptr);
   return CP_ATTN_OK;
 }
