@@ -41,7 +41,7 @@ PROFILED_TRAFFIC = {
     "step_bwd": ("context_causal_attention_ring_gb300/csrc/step_bwd.cu",
                  "a662b08e9cd0ec616e01d1bf47a75b9b02a3a44f8c008dc149a884986215c990", 3.102382e9),
     "step_fwd": ("context_causal_attention_ring_gb300/csrc/step_fwd.cu",
-                 "f012c898a89dee21c13986f716b39bdcac5fcd8bd33ea1c36b7d03b1921116a6", 1.292705e9),
+                 "03b628acb6c1b91979d4fd63e73eb892fc399c09de174a82b5d742f1cb4af938", 1.293140e9),
 }
 
 
