@@ -134,14 +134,18 @@ def test_single_step_shares():
         assert not msgs, f"step {t}: " + " | ".join(msgs)
 
 
-@pytest.mark.parametrize("d,chained", [(64, False), (128, False), (128, True)])
-def test_step_bwd_ring_of_bf16_steps(d, chained):
+@pytest.mark.parametrize("d,chained,variant,docs", [(64, False, "pass_kv", False),
+                                             (128, False, "pass_kv", False),
+                                             (128, True, "pass_kv", False),
+                                             (128, True, "pass_q", True)])
+def test_step_bwd_ring_of_bf16_steps(d, chained, variant, docs):
     """cp_attn_step_bwd with bf16 q, k, v, dout and a workspace, called once
     per ring step: step 0 makes the fp16 operand copies in the workspace
     (filled with NaN patterns first), later steps reuse them; delta and the
     zeroed accumulators come from cp_attn_bwd_preprocess without copies."""
     w = Workload("stepbwd", 2048, 8, 2, d, 4, backward=True)
-    plan = _plan(w)
+    cu = np.array([0, 1, 130, 1000, 1023, 1024, 1500, 2048], dtype=np.int32) if docs else None
+    plan = _plan(w, variant, cu=cu)
     plan.set_chaining(chained)
     run = DeviceRun(plan, make_inputs(w))
     o, lse, fws = run.forward()
@@ -155,8 +159,8 @@ def test_step_bwd_ring_of_bf16_steps(d, chained):
     for t in range(p.R):
         plan.step_bwd(t, run.q, run.k, run.v, run.dout, lse, delta, dq, dk, dv, ws)
     plan.sync_status()
-    _, _, (dq_r, dk_r, dv_r) = _oracle_grads(run.inp, plan, None)
-    tag = f"step_bwd ring d={d} chained={chained}"
+    _, _, (dq_r, dk_r, dv_r) = _oracle_grads(run.inp, plan, cu)
+    tag = f"step_bwd ring d={d} chained={chained} {variant} docs={docs}"
     assert_close(run.to_natural_rows(f32_to_f64(dq)), dq_r, GRAD_TOL, tag + " dQ")
     assert_close(run.to_natural_rows(f32_to_f64(dk), "kv"), dk_r, GRAD_TOL, tag + " dK")
     assert_close(run.to_natural_rows(f32_to_f64(dv), "kv"), dv_r, GRAD_TOL, tag + " dV")
