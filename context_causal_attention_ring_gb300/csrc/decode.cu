@@ -22,6 +22,7 @@
 //      warps' sums meet in shared memory;
 //   4. O_h / l_h and LSE_h = ln l_h + max to the partial slots.
 // The partials then go through the LSE merge (K4).
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -101,6 +102,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecPa
   float* st_max = reinterpret_cast<float*>(smem + S::kStat);
   float* st_sum = st_max + kDecMaxG;
   const uint32_t kv_s = ptx::smem_u32(smem + S::kKV);
+  // the merge that follows waits for this grid to complete (see decode_tc_kernel)
+  if (threadIdx.x == 0) ptx::grid_dep_launch();
 
   const int part = blockIdx.x;
   const int kh = blockIdx.y;
@@ -284,43 +287,65 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const DecPa
 }
 
 // K9: the same partial attention on the tensor cores (head_dim 128, runs of
-// 128, 256 or 512 keys). The G <= 16 query heads of a KV head form the
-// N = 16 side of two products per 128-key tile, both accumulated in TMEM:
+// 128, 256 or 512 keys: an item is one run of one KV head of one sequence).
+// The G <= 16 query heads of a KV head form the N = 16 side of two products
+// per 128-key tile, both accumulated in TMEM:
 //   S^T  = K Q^T    (M = 128 keys, N = 16 heads, K = d)
 //   O^T += V^T P^T  (M = d, N = 16 heads, K = keys)
-// The K tiles and then the V tiles of the run stream through a TMA ring (two
-// 32 KB slots for bf16, four 16 KB slots for E4M3); the producer starts the
-// first slots' loads before the block's setup barrier. The whole run's scores
-// fit in TMEM (16 columns per tile), so the softmax is one pass between the
-// two products: per head, the maximum and the sum over the run, reduced
-// across the four warps that hold its keys through shared memory. P goes to
-// shared memory as the B operand of O^T. Query rows past G are zero; only the
-// group's heads, rounded up to 4, 8 or 16, go through the softmax.
+// The grid is persistent (as many CTAs as the SMs hold, a multiple of Hkv);
+// each CTA keeps one KV head and takes that head's items one after another
+// from a work counter. The K tiles and then the V tiles of its items stream
+// through a TMA ring (two 32 KB slots for bf16, four 16 KB slots for E4M3,
+// six at 16 heads), so the next item's tiles load while the current one is
+// in its softmax; the producer starts the first slots' loads before the
+// block's setup barrier. An item's scores fit in TMEM (16 columns per tile),
+// so the softmax is one pass between the two products: per head, the maximum
+// and the sum over the run, reduced across the four warps that hold its keys
+// through shared memory. P goes to shared memory as the B operand of O^T.
+// The CTA merges the partial results of its consecutive items of one
+// sequence in TMEM and writes one partial per such run. Query rows past G
+// are zero; only the group's heads, rounded up to 4, 8 or 16, go through the
+// softmax.
 // Warps: SW softmax and epilogue warps (4, or 8 for 16 heads: warp w holds
 // keys / columns of d 32 (w mod 4) .. +31 and a quarter or half of the
-// heads), then the TMA producer and the TMEM owner and MMA issuer. 77 KB
-// (E4M3) or 87 KB (bf16) of shared memory: two CTAs share an SM, three for
-// E4M3 when the group has at most four heads.
+// heads), then the TMA producer and the TMEM owner and MMA issuer. About
+// 75 KB (E4M3), 107 KB (E4M3, 16 heads) or 87 KB (bf16) of shared memory:
+// two CTAs share an SM, three for E4M3 when the group has at most eight
+// heads.
 constexpr int kTcN = 16;                    // MMA N: the query heads, padded
 constexpr int kTcMaxTiles = kDecMaxL / 128;
 
-enum : int {
-  TB_FULL = 0,    // [4] tile of the slot landed
-  TB_EMPTY = 4,   // [4] slot read by its MMAs
-  TB_S = 8,       // all scores of the run in TMEM
-  TB_P = 9,       // 128 arrivals: P in shared memory
-  TB_O = 10,      // O^T complete
-  TB_RED = 11,    // 128 arrivals per phase: the warps' partial maxima, then sums
-  TB_COUNT = 12
-};
+constexpr int kDecMaxSlots = 6;  // ring slots, at most (see dec_slots)
 
-// F8: E4M3 K rows and V^T tiles (one byte per element, 16 KB per tile, a
-// four-slot ring), the query rows and P in E4M3; else bf16 (32 KB tiles, two
-// slots).
-template <bool F8>
+enum : int {
+  TB_FULL = 0,                      // [kDecMaxSlots] tile of the slot landed
+  TB_EMPTY = kDecMaxSlots,          // [kDecMaxSlots] slot read by its MMAs
+  TB_S = 2 * kDecMaxSlots,          // all scores of the run in TMEM
+  TB_P = 2 * kDecMaxSlots + 1,      // softmax-warp arrivals: P in shared memory
+  TB_O = 2 * kDecMaxSlots + 2,      // O^T complete
+  TB_RED = 2 * kDecMaxSlots + 3,    // softmax-warp arrivals per phase: partial maxima, then sums
+  TB_Q = 2 * kDecMaxSlots + 4,      // softmax-warp arrivals: the next group's query rows written
+  TB_DONE = 2 * kDecMaxSlots + 5,   // every MMA of the CTA complete
+  TB_OST = 2 * kDecMaxSlots + 6,    // softmax-warp arrivals: a run's O staged for its store
+  TB_SFREE = 2 * kDecMaxSlots + 7,  // the staging buffer's last store has read it (once)
+  TB_ITEM = 2 * kDecMaxSlots + 8,   // [kDecItemRing] the producer published an item
+  TB_COUNT = 2 * kDecMaxSlots + 8 + 8
+};
+constexpr int kDecItemRing = 8;  // items published ahead of their consumers, at most
+
+// Ring slots of the tensor-core decode: bf16 tiles (32 KB) two; E4M3 tiles
+// (16 KB) four, six at 16 heads (two CTAs per SM either way), so that the
+// next item's first K tiles load while the current item's V tiles wait for
+// P.
+constexpr int dec_slots(bool f8, int nh) { return f8 ? (nh == 16 ? 6 : 4) : 2; }
+
+// F8: E4M3 K rows and V^T tiles (one byte per element, 16 KB per tile), the
+// query rows and P in E4M3; else bf16 (32 KB tiles).
+template <bool F8, int SLOTS = dec_slots(F8, 4)>
 struct DecTcSmem {
   static constexpr int kElt = F8 ? 1 : 2;
-  static constexpr int kSlots = F8 ? 4 : 2;
+  static constexpr int kSlots = SLOTS;
+  static_assert(SLOTS <= kDecMaxSlots, "one full and one empty barrier per slot");
   static constexpr int kTile = 128 * 128 * kElt;            // a K or V tile
   static constexpr int kRing = 0;                           // [kSlots]
   static constexpr int kQ = kRing + kSlots * kTile;         // [16][128] query rows
@@ -328,9 +353,12 @@ struct DecTcSmem {
   static constexpr int kRed = kP + kTcN * kDecMaxL * kElt;  // [max | sum][4 warps][16] f32
   static constexpr int kQs = kRed + 2 * 4 * kTcN * 4;       // [16] f32 query scales (F8)
   static constexpr int kBar = kQs + kTcN * 4;
-  static constexpr int kMisc = kBar + (TB_COUNT + 4) * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kMisc = kBar + (TB_COUNT + 4) * 8;  // TMEM address, abort flag
+  static constexpr int kItem = kMisc + 16;                   // [kDecItemRing] int item ring
+  static constexpr int kBytes = kItem + kDecItemRing * 4;
 };
+// three E4M3 CTAs of the four-slot ring share an SM (1 KB reserved per CTA)
+static_assert(3 * (DecTcSmem<true, 4>::kBytes + 1024) <= 233472, "three CTAs per SM");
 
 struct DecTcParams {
   const __nv_bfloat16* q;  // [B][Hq][128]
@@ -339,6 +367,8 @@ struct DecTcParams {
   int B, Hq, Hkv, G;
   int64_t kv_len;
   int L;                   // keys per part: 128, 256 or 512
+  int parts;               // parts per sequence: kv_len / L
+  int* counters;           // [Hkv] work counters, zero at launch
   float scale_log2;
   int32_t* status;         // [4] device status word
   uint64_t wait_limit_ns;
@@ -362,14 +392,13 @@ __device__ __forceinline__ uint32_t kmaj16_off(int row, int col) {
 }
 
 // Tile i of a run of nt K tiles and then nt V tiles (rows row0 + 128 (i mod
-// nt) of KV head kh) into ring slot i mod kSlots, completing on that slot's
-// full barrier.
+// nt) of KV head kh) into ring slot `slot`, completing on that slot's full
+// barrier.
 template <bool F8>
 __device__ __forceinline__ void dec_issue_tile(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                               uint32_t ring, uint32_t bar0, int i, int nt,
-                                               int row0, int kh) {
+                                               uint32_t ring, uint32_t bar0, int slot, int i,
+                                               int nt, int row0, int kh) {
   using S = DecTcSmem<F8>;
-  const int slot = i % S::kSlots;
   const uint32_t full = bar0 + 8u * static_cast<uint32_t>(TB_FULL + slot);
   const int row = row0 + (i % nt) * 128;
   ptx::mbar_arrive_expect_tx(full, S::kTile);
@@ -391,15 +420,19 @@ __device__ __forceinline__ void dec_issue_tile(const CUtensorMap* tm_k, const CU
 // Softmax warps of the tensor-core decode: eight (two groups of four, eight
 // heads each) when all 16 columns of N are heads, else four.
 constexpr int dec_softmax_warps(int nh) { return nh == 16 ? 8 : 4; }
+// CTAs per SM the kernel is compiled for: three fit in shared memory; with
+// eight softmax warps the registers allow two.
+constexpr int dec_min_ctas(int nh) { return nh == 16 ? 2 : 3; }
 
 // NH: the group's query heads rounded up to 4, 8 or 16 (a compile-time
 // count, so that the per-head softmax chains interleave without branches);
 // columns past NH are padding of N and are never read.
 template <bool F8, int NH>
-__global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc_kernel(
+__global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas(NH))
+    decode_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const DecTcParams p) {
-  using S = DecTcSmem<F8>;
+  using S = DecTcSmem<F8, dec_slots(F8, NH)>;
   constexpr int NSL = S::kSlots;
   constexpr int SW = dec_softmax_warps(NH);  // softmax warps; then the producer, the MMA warp
   constexpr int HPW = NH * 4 / SW;           // heads per softmax warp
@@ -414,6 +447,9 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
     }
     return;
   }
+  // the merge that follows may be scheduled once every CTA has started; it
+  // waits for this grid to complete before it reads the partials
+  if (threadIdx.x == 0) ptx::grid_dep_launch();
   const uint32_t sRing = sbase + S::kRing;
   const uint32_t sQ = sbase + S::kQ;
   const uint32_t sP = sbase + S::kP;
@@ -423,26 +459,62 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::kMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::kMisc + 4);
 
-  const int part = blockIdx.x;
-  const int kh = blockIdx.y;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.G;
   const int nt = p.L / 128;
-  const int row0 = static_cast<int>(static_cast<int64_t>(b) * p.kv_len +
-                                    static_cast<int64_t>(part) * p.L);
+  // The items are (sequence b, part, KV head kh), numbered kh fastest. The
+  // grid is a multiple of Hkv and CTA c keeps KV head kh = c mod Hkv: its
+  // first item is the (c / Hkv)-th (b, part) of that head and each further
+  // one is taken from the head's work counter as the CTA gets to it, so CTAs
+  // that run faster take more items. A CTA's items thus come in increasing
+  // (b, part) order: its query rows change only with the sequence, and the
+  // heads advance together, so the CTAs running at one time read every KV
+  // head of the same rows (adjacent in memory). The producer publishes each
+  // item (its number, or -1 once there are none) in a ring of kDecItemRing
+  // entries with one barrier each; the other warps read it there. Fewer than
+  // 2^31 items: batch * kv_len < 2^31 and Hkv <= 128.
+  int* s_item = reinterpret_cast<int*>(smem + S::kItem);
+  struct Item {
+    int part, kh, b, row0;
+  };
+  auto item_of = [&](int i) {
+    Item r;
+    r.kh = i % p.Hkv;
+    const int bp = i / p.Hkv;
+    r.b = bp / p.parts;
+    r.part = bp - r.b * p.parts;
+    r.row0 = static_cast<int>(static_cast<int64_t>(r.b) * p.kv_len +
+                              static_cast<int64_t>(r.part) * p.L);
+    return r;
+  };
+  // the producer's j-th item (j > 0 takes a counter ticket), or -1
+  auto take_item = [&](int j) -> int {
+    const int kh = static_cast<int>(blockIdx.x) % p.Hkv;
+    const int per_head = static_cast<int>(gridDim.x) / p.Hkv;
+    const int bp = j == 0 ? static_cast<int>(blockIdx.x) / p.Hkv
+                          : per_head + atomicAdd(p.counters + kh, 1);
+    return bp < p.B * p.parts ? bp * p.Hkv + kh : -1;
+  };
+  const int item0 = take_item(0);  // no ticket: every thread knows it
+  const Item first = item_of(item0 < 0 ? 0 : item0);
 
-  const int n_first = 2 * nt < NSL ? 2 * nt : NSL;  // tiles that need no free slot
+  // tiles of the first item that need no free slot; tile i of the CTA's
+  // item j is the (j * 2 nt + i)-th tile through the ring
+  const int n_first = item0 >= 0 ? (2 * nt < NSL ? 2 * nt : NSL) : 0;
   if (warp == SW && lane == 0) {
-    // the producer sets up the barriers itself and starts the first ring of
-    // loads at once, so that they overlap the query rows and the TMEM
-    // allocation; nobody else touches a barrier before the block barrier
+    // the producer sets up the barriers itself, publishes the first item and
+    // starts the first ring of loads at once, so that they overlap the query
+    // rows and the TMEM allocation; nobody else touches a barrier before the
+    // block barrier
     for (int i = 0; i < TB_COUNT; ++i)
-      ptx::mbar_init(bar(i), (i == TB_P || i == TB_RED) ? 32u * SW : 1u);
+      ptx::mbar_init(bar(i), (i == TB_P || i == TB_RED || i == TB_Q || i == TB_OST) ? 32u * SW : 1u);
     *s_abort = 0;
     ptx::fence_barrier_init();
-    for (int i = 0; i < n_first; ++i) dec_issue_tile<F8>(&tm_k, &tm_v, sRing, bar0, i, nt, row0, kh);
+    s_item[0] = item0;
+    ptx::mbar_arrive(bar(TB_ITEM));
+    for (int i = 0; i < n_first; ++i)
+      dec_issue_tile<F8>(&tm_k, &tm_v, sRing, bar0, i, i, nt, first.row0, first.kh);
   }
   if (warp == SW + 1) {
     ptx::tmem_alloc(ptx::smem_u32(s_tmem), 128);
@@ -454,7 +526,9 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
     kv_sk = __ldg(p.kv_scales);
     kv_sv = __ldg(p.kv_scales + 1);
   }
-  if (warp < SW) {
+  // the query rows of group (b, kh) as the B operand of S^T, written by the
+  // softmax warps
+  auto write_q = [&](int b, int kh) {
     if constexpr (F8) {
       // each head's query row to E4M3 with its own scale (amax / 448); warp w
       // takes rows w, w + SW, ...: lane l holds d = 4l .. 4l + 3
@@ -484,7 +558,7 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
         *reinterpret_cast<uint32_t*>(smem + S::kQ + kmaj16_off8(h, 4 * lane)) = q4;
       }
     } else {
-      // the group's query rows as the K-major B operand of S^T; rows past G zero
+      // K-major rows; rows past G zero
       uint4 v[kTcN * 16 / (32 * SW)];
 #pragma unroll
       for (int j = 0; j < kTcN * 16 / (32 * SW); ++j) {
@@ -502,29 +576,53 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
       }
     }
     ptx::fence_proxy_async_smem();
-  }
+  };
+  if (warp < SW && item0 >= 0) write_q(first.b, first.kh);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  volatile int* v_item = s_item;
   const volatile int never = 0;
 
   if (warp == SW && lane == 0) {
     // ------------------------------------------------------------ producer
-    // tiles [0, n_first) were issued before the block barrier
-    int issued = n_first;
-    for (int i = n_first; i < 2 * nt; ++i) {
-      const int slot = i % NSL;
-      if (!ptx::mbar_wait(bar(TB_EMPTY + slot), ((i / NSL) - 1) & 1, s_abort, p.wait_limit_ns)) {
-        ptx::record_timeout(p.status, s_abort, 0x9100 + i);
-        break;
+    int issued = n_first;  // ring tiles issued so far
+    bool ok = true;
+    int idx = item0;
+    for (int j = 0; ok && idx >= 0; ++j) {
+      const Item c = item_of(idx);
+      // the next item is taken once this one's first tile is on its way, so
+      // that the counter's round trip overlaps the waits for free slots
+      int next = -1;
+      bool taken = false;
+      for (int i = j == 0 ? n_first : 0; i < 2 * nt; ++i) {
+        const int g = j * 2 * nt + i;
+        const int slot = g % NSL;
+        if (g >= NSL &&
+            !ptx::mbar_wait(bar(TB_EMPTY + slot), ((g / NSL) - 1) & 1, s_abort, p.wait_limit_ns)) {
+          ptx::record_timeout(p.status, s_abort, 0x9100 + i);
+          ok = false;
+          break;
+        }
+        dec_issue_tile<F8>(&tm_k, &tm_v, sRing, bar0, slot, i, nt, c.row0, c.kh);
+        issued = g + 1;
+        if (!taken) {
+          next = take_item(j + 1);
+          taken = true;
+        }
       }
-      dec_issue_tile<F8>(&tm_k, &tm_v, sRing, bar0, i, nt, row0, kh);
-      issued = i + 1;
+      if (!ok) break;
+      if (!taken) next = take_item(j + 1);
+      // publish item j + 1 (its entry's previous reader, item j + 1 - 8, is
+      // done: the producer runs at most a ring of tiles ahead of the MMAs)
+      v_item[(j + 1) % kDecItemRing] = next;
+      ptx::mbar_arrive(bar(TB_ITEM + (j + 1) % kDecItemRing));
+      idx = next;
     }
     // every issued copy must land before the CTA may exit
-    for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
-      ptx::mbar_wait(bar(TB_FULL + (i % NSL)), (i / NSL) & 1, &never, p.wait_limit_ns);
+    for (int g = issued > NSL ? issued - NSL : 0; g < issued; ++g)
+      ptx::mbar_wait(bar(TB_FULL + (g % NSL)), (g / NSL) & 1, &never, p.wait_limit_ns);
   } else if (warp == SW + 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t leader = ptx::elect_one();
@@ -542,59 +640,86 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
     const uint64_t dQ = ptx::sdesc_sw128(sQ, 16, 1024);
     const uint64_t dP = ptx::sdesc_sw128(sP, 16, 1024);
     bool ok = true;
-    for (int t = 0; ok && t < nt; ++t) {
-      const int slot = t % NSL;
-      if (!wait_w(bar(TB_FULL + slot), (t / NSL) & 1, 0x9200 + t)) { ok = false; break; }
-      ptx::tc_fence_after();
-      const uint64_t dK = ptx::sdesc_sw128(sRing + slot * S::kTile, 16, 1024);
-      if constexpr (F8) {
-        // K tile [128 keys][128 d bytes]: one swizzle atom, 32 d per MMA
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_ss_f8_w(tmem + kTcN * t, ptx::sdesc_add(dK, kk * 32),
-                           ptx::sdesc_add(dQ, kk * 32), idesc_s, kk > 0 ? 1u : 0u, leader);
-      } else {
-        // K tile [128 keys][128 d] in two 64-column blocks of 16 KB
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_ss_w(tmem + kTcN * t, ptx::sdesc_add(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
-                        ptx::sdesc_add(dQ, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s,
-                        kk > 0 ? 1u : 0u, leader);
+    int n_q = 0;  // query-row rewrites waited for
+    Item prev = first;
+    for (int j = 0; ok; ++j) {
+      int idx = item0;
+      if (j > 0) {
+        if (!wait_w(bar(TB_ITEM + j % kDecItemRing), (j / kDecItemRing) & 1, 0x9C00)) {
+          ok = false;
+          break;
+        }
+        idx = v_item[j % kDecItemRing];
       }
-      ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
-    }
-    ptx::mma_commit_w(bar(TB_S), leader);
-    if (ok) ok = wait_w(bar(TB_P), 0, 0x9300);
-    if (ok) ptx::tc_fence_after();
-    for (int t = 0; ok && t < nt; ++t) {
-      const int i = nt + t;
-      const int slot = i % NSL;
-      if (!wait_w(bar(TB_FULL + slot), (i / NSL) & 1, 0x9400 + t)) { ok = false; break; }
-      ptx::tc_fence_after();
-      if constexpr (F8) {
-        // V^T tile [128 d][128 keys bytes] as the K-major A; P as the K-major
-        // B, 128 keys per 2 KB block, 32 keys per MMA
-        const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_ss_f8_w(tmem + 64, ptx::sdesc_add(dV, kk * 32),
-                           ptx::sdesc_add(dP, t * 2048 + kk * 32), idesc_o,
-                           (t > 0 || kk > 0) ? 1u : 0u, leader);
-      } else {
-        // V tile as the MN-major A of O^T (M = d: d 64..127 at +16 KB; K =
-        // keys, 16 keys = 2 KB per step); P as the K-major B, 64 keys per 2 KB
-        // block
-        const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16384, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_ss_w(tmem + 64, ptx::sdesc_add(dV, kk * 2048),
-                        ptx::sdesc_add(dP, (2 * t + (kk >> 2)) * 2048 + (kk & 3) * 32), idesc_o,
-                        (t > 0 || kk > 0) ? 1u : 0u, leader);
+      if (idx < 0) break;
+      const Item c = item_of(idx);
+      const bool new_q = c.b != prev.b || c.kh != prev.kh;
+      prev = c;
+      if (new_q) {
+        // the softmax warps wrote the new group's query rows
+        if (!wait_w(bar(TB_Q), n_q & 1, 0x9A00)) { ok = false; break; }
+        ++n_q;
+        ptx::tc_fence_after();
       }
-      ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int g = j * 2 * nt + t;
+        const int slot = g % NSL;
+        if (!wait_w(bar(TB_FULL + slot), (g / NSL) & 1, 0x9200 + t)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint64_t dK = ptx::sdesc_sw128(sRing + slot * S::kTile, 16, 1024);
+        if constexpr (F8) {
+          // K tile [128 keys][128 d bytes]: one swizzle atom, 32 d per MMA
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_ss_f8_w(tmem + kTcN * t, ptx::sdesc_add(dK, kk * 32),
+                             ptx::sdesc_add(dQ, kk * 32), idesc_s, kk > 0 ? 1u : 0u, leader);
+        } else {
+          // K tile [128 keys][128 d] in two 64-column blocks of 16 KB
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            ptx::mma_ss_w(tmem + kTcN * t, ptx::sdesc_add(dK, (kk >> 2) * 16384 + (kk & 3) * 32),
+                          ptx::sdesc_add(dQ, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s,
+                          kk > 0 ? 1u : 0u, leader);
+        }
+        ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
+      }
+      if (!ok) break;
+      ptx::mma_commit_w(bar(TB_S), leader);
+      if (!wait_w(bar(TB_P), j & 1, 0x9300)) { ok = false; break; }
+      ptx::tc_fence_after();
+      for (int t = 0; ok && t < nt; ++t) {
+        const int g = j * 2 * nt + nt + t;
+        const int slot = g % NSL;
+        if (!wait_w(bar(TB_FULL + slot), (g / NSL) & 1, 0x9400 + t)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if constexpr (F8) {
+          // V^T tile [128 d][128 keys bytes] as the K-major A; P as the
+          // K-major B, 128 keys per 2 KB block, 32 keys per MMA
+          const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_ss_f8_w(tmem + 64, ptx::sdesc_add(dV, kk * 32),
+                             ptx::sdesc_add(dP, t * 2048 + kk * 32), idesc_o,
+                             (t > 0 || kk > 0) ? 1u : 0u, leader);
+        } else {
+          // V tile as the MN-major A of O^T (M = d: d 64..127 at +16 KB; K =
+          // keys, 16 keys = 2 KB per step); P as the K-major B, 64 keys per
+          // 2 KB block
+          const uint64_t dV = ptx::sdesc_sw128(sRing + slot * S::kTile, 16384, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            ptx::mma_ss_w(tmem + 64, ptx::sdesc_add(dV, kk * 2048),
+                          ptx::sdesc_add(dP, (2 * t + (kk >> 2)) * 2048 + (kk & 3) * 32),
+                          idesc_o, (t > 0 || kk > 0) ? 1u : 0u, leader);
+        }
+        ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
+      }
+      if (!ok) break;
+      ptx::mma_commit_w(bar(TB_O), leader);
     }
-    ptx::mma_commit_w(bar(TB_O), leader);
-    ptx::mbar_wait(bar(TB_O), 0, &never, p.wait_limit_ns);
+    // every MMA issued above must complete before the TMEM is released
+    ptx::mma_commit_w(bar(TB_DONE), leader);
+    ptx::mbar_wait(bar(TB_DONE), 0, &never, p.wait_limit_ns);
     __syncwarp();
   } else if (warp < SW) {
     // ------------------------------------------------------------ softmax
@@ -604,125 +729,237 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
     const int qw = warp & 3;
     const int h0 = (warp >> 2) * HPW;
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
-    bool ok = ptx::mbar_wait(bar(TB_S), 0, s_abort, p.wait_limit_ns);
-    if (!ok) ptx::record_timeout(p.status, s_abort, 0x9500);
-    float x[kTcMaxTiles][HPW];
-    float M[HPW], l[HPW];
-    if (__all_sync(0xffffffffu, ok)) {
-      ptx::tc_fence_after();
-      // base-2 score factor per head (E4M3: times the query row's and K's
-      // descale factors)
-      float sf[HPW];
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) sf[h] = p.scale_log2;
-      if constexpr (F8) {
-        const float* qs = reinterpret_cast<const float*>(smem + S::kQs);
-#pragma unroll
-        for (int h = 0; h < HPW; ++h) sf[h] *= qs[h0 + h] * kv_sk;
-      }
-#pragma unroll
-      for (int i = 0; i < kTcMaxTiles; ++i) {
-        if (i < nt) {
-          uint32_t r[HPW];
-          ptx::tmem_ld_n<HPW>(tmem + lane_base + kTcN * i + h0, r);
-#pragma unroll
-          for (int h = 0; h < HPW; ++h) x[i][h] = __uint_as_float(r[h]) * sf[h];
-        } else {
-#pragma unroll
-          for (int h = 0; h < HPW; ++h) x[i][h] = -INFINITY;
-        }
-      }
-      // per head: maximum over the thread's keys, the warp, then the four
-      // warps of the head's group. Columns past NH are skipped here and
-      // below: their P is left as it is and only feeds O^T columns that are
-      // never read.
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) {
-        float m = x[0][h];
-#pragma unroll
-        for (int i = 1; i < kTcMaxTiles; ++i) m = fmaxf(m, x[i][h]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        M[h] = m;
-      }
-#pragma unroll
-      for (int h = 0; h < HPW; ++h)
-        if (lane == h) red[qw * kTcN + h0 + h] = M[h];
-      ptx::mbar_arrive(bar(TB_RED));
-      ok = ptx::mbar_wait(bar(TB_RED), 0, s_abort, p.wait_limit_ns);
-      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9600);
-    }
-    if (__all_sync(0xffffffffu, ok)) {
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) {
-        const int hh = h0 + h;
-        M[h] = fmaxf(fmaxf(red[hh], red[kTcN + hh]), fmaxf(red[2 * kTcN + hh], red[3 * kTcN + hh]));
-      }
-      // P = 2^(x - M) (bf16 or E4M3 into shared memory) and the per-head sums
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) {
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < kTcMaxTiles; ++i) {
-          if (i < nt) {
-            const float e = ptx::ex2(x[i][h] - M[h]);
-            sum += e;
-            if constexpr (F8) {
-              // 2^8 P <= 256: probabilities down to 2^-14 stay normal
-              smem[S::kP + kmaj16_off8(h0 + h, i * 128 + t)] =
-                  static_cast<uint8_t>(ptx::pack_e4m3x4(e * 256.f, 0.f, 0.f, 0.f) & 0xFFu);
-            } else {
-              *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h0 + h, i * 128 + t)) =
-                  __float2bfloat16_rn(e);
-            }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        l[h] = sum;
-      }
-#pragma unroll
-      for (int h = 0; h < HPW; ++h)
-        if (lane == h) red[4 * kTcN + qw * kTcN + h0 + h] = l[h];
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(bar(TB_P));
-      ptx::mbar_arrive(bar(TB_RED));
-      ok = ptx::mbar_wait(bar(TB_RED), 1, s_abort, p.wait_limit_ns);
-      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9700);
-    }
-    if (__all_sync(0xffffffffu, ok)) {
-      const float* rs = red + 4 * kTcN;
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) {
-        const int hh = h0 + h;
-        l[h] = (rs[hh] + rs[kTcN + hh]) + (rs[2 * kTcN + hh] + rs[3 * kTcN + hh]);
-      }
-      ok = ptx::mbar_wait(bar(TB_O), 0, s_abort, p.wait_limit_ns);
-      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9800);
-    }
-    if (__all_sync(0xffffffffu, ok)) {
-      ptx::tc_fence_after();
-      // O^T: TMEM lane = column t of d, column h = query head
-      uint32_t r[HPW];
-      ptx::tmem_ld_n<HPW>(tmem + lane_base + 64 + h0, r);
-      const int64_t obase = (static_cast<int64_t>(part) * p.B + b) * p.Hq + kh * G;
-      // E4M3: O^T carries 2^8 of P and V's descale factor. One correctly
-      // rounded reciprocal per head (the padded heads' sums are finite too)
-      const float oscale = F8 ? kv_sv * (1.f / 256.f) : 1.f;
-      float inv_l[HPW];
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) inv_l[h] = __frcp_rn(l[h]) * oscale;
+    // base-2 score factor per head (E4M3: times the query row's and K's
+    // descale factors)
+    const float* qs = reinterpret_cast<const float*>(smem + S::kQs);
+    // E4M3: O^T carries 2^8 of P and V's descale factor
+    const float oscale = F8 ? kv_sv * (1.f / 256.f) : 1.f;
+    // The CTA merges its consecutive items of one sequence as it goes (the
+    // log-sum-exp merge, "Ring Attention Algorithms"): the run's maximum m
+    // and sum l per head, and O = sum of 2^(M_item - m) O_item, live in TMEM
+    // columns kRunM, kRunL and kRunO (one copy per lane). A run leaves as
+    // one partial in the slot of its first part; its other parts' slots get
+    // LSE = -inf (weight 0 in the merge that follows). The O rows of the
+    // group's G heads are contiguous in o_part: they are staged [head][d] in
+    // the P buffer (the item's O^T products have read P) and leave in one
+    // bulk store.
+    constexpr uint32_t kRunO = 80, kRunM = 96, kRunL = 112;
+    int run_b = -1, run_part = 0, n_flush = 0;
+    auto flush = [&](int kh) -> bool {
+      uint32_t o[HPW], m[HPW], l_[HPW];
+      ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunO + h0, o);
+      ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunM + h0, m);
+      ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunL + h0, l_);
+      float* stage = reinterpret_cast<float*>(smem + S::kP);
 #pragma unroll
       for (int h = 0; h < HPW; ++h) {
         const int hh = h0 + h;
         if (hh < G) {
-          p.o_part[(obase + hh) * 128 + t] = __uint_as_float(r[h]) * inv_l[h];
+          const float lh = __uint_as_float(l_[h]);
+          stage[hh * 128 + t] = __uint_as_float(o[h]) * __frcp_rn(lh);
           if (t == hh)
-            p.lse_part[(static_cast<int64_t>(part) * p.Hq + kh * G + hh) * p.B + b] =
-                (M[h] + ptx::lg2(l[h])) * kLn2d;
+            p.lse_part[(static_cast<int64_t>(run_part) * p.Hq + kh * G + hh) * p.B + run_b] =
+                (__uint_as_float(m[h]) + ptx::lg2(lh)) * kLn2d;
         }
       }
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(bar(TB_OST));
+      bool f_ok = true;
+      if (threadIdx.x == 0) {
+        f_ok = ptx::mbar_wait(bar(TB_OST), n_flush & 1, s_abort, p.wait_limit_ns);
+        if (f_ok) {
+          const int64_t obase = (static_cast<int64_t>(run_part) * p.B + run_b) * p.Hq + kh * G;
+          ptx::bulk_store(p.o_part + obase * 128, sP, static_cast<uint32_t>(G) * 512u);
+          ptx::bulk_commit();
+        } else {
+          ptx::record_timeout(p.status, s_abort, 0x9E00);
+        }
+      }
+      ++n_flush;
+      return f_ok;
+    };
+    bool ok = true;
+    int n_q = 0;
+    Item prev = first;
+    for (int j = 0; ok; ++j) {
+      int idx = item0;
+      if (j > 0) {
+        ok = ptx::mbar_wait(bar(TB_ITEM + j % kDecItemRing), (j / kDecItemRing) & 1, s_abort,
+                            p.wait_limit_ns);
+        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9D00);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        idx = v_item[j % kDecItemRing];
+      }
+      if (idx < 0) break;
+      const Item c = item_of(idx);
+      const bool new_q = c.b != prev.b || c.kh != prev.kh;
+      prev = c;
+      if (new_q) {
+        // the previous item's S^T products are complete (its softmax waited
+        // for them), so the query rows may be rewritten
+        write_q(c.b, c.kh);
+        ptx::mbar_arrive(bar(TB_Q));
+        // all softmax warps' rows (and E4M3 scales) written
+        ok = ptx::mbar_wait(bar(TB_Q), n_q & 1, s_abort, p.wait_limit_ns);
+        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9B00);
+        ++n_q;
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      ok = ptx::mbar_wait(bar(TB_S), j & 1, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9500);
+      float x[kTcMaxTiles][HPW];
+      float M[HPW], l[HPW];
+      if (__all_sync(0xffffffffu, ok)) {
+        ptx::tc_fence_after();
+        float sf[HPW];
+#pragma unroll
+        for (int h = 0; h < HPW; ++h) sf[h] = p.scale_log2;
+        if constexpr (F8) {
+#pragma unroll
+          for (int h = 0; h < HPW; ++h) sf[h] *= qs[h0 + h] * kv_sk;
+        }
+#pragma unroll
+        for (int i = 0; i < kTcMaxTiles; ++i) {
+          if (i < nt) {
+            uint32_t r[HPW];
+            ptx::tmem_ld_n<HPW>(tmem + lane_base + kTcN * i + h0, r);
+#pragma unroll
+            for (int h = 0; h < HPW; ++h) x[i][h] = __uint_as_float(r[h]) * sf[h];
+          } else {
+#pragma unroll
+            for (int h = 0; h < HPW; ++h) x[i][h] = -INFINITY;
+          }
+        }
+        // per head: maximum over the thread's keys, the warp, then the four
+        // warps of the head's group. Columns past NH are skipped here and
+        // below: their P is left as it is and only feeds O^T columns that
+        // are never read.
+#pragma unroll
+        for (int h = 0; h < HPW; ++h) {
+          float m = x[0][h];
+#pragma unroll
+          for (int i = 1; i < kTcMaxTiles; ++i) m = fmaxf(m, x[i][h]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          M[h] = m;
+        }
+#pragma unroll
+        for (int h = 0; h < HPW; ++h)
+          if (lane == h) red[qw * kTcN + h0 + h] = M[h];
+        // P is written after this phase, over the previous item's O staging:
+        // its store must have read it
+        if (threadIdx.x == 0) ptx::bulk_wait_read();
+        ptx::mbar_arrive(bar(TB_RED));
+        ok = ptx::mbar_wait(bar(TB_RED), 0, s_abort, p.wait_limit_ns);
+        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9600);
+      }
+      if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+        for (int h = 0; h < HPW; ++h) {
+          const int hh = h0 + h;
+          M[h] = fmaxf(fmaxf(red[hh], red[kTcN + hh]), fmaxf(red[2 * kTcN + hh], red[3 * kTcN + hh]));
+        }
+        // P = 2^(x - M) (bf16 or E4M3 into shared memory) and the per-head sums
+#pragma unroll
+        for (int h = 0; h < HPW; ++h) {
+          float sum = 0.f;
+#pragma unroll
+          for (int i = 0; i < kTcMaxTiles; ++i) {
+            if (i < nt) {
+              const float e = ptx::ex2(x[i][h] - M[h]);
+              sum += e;
+              if constexpr (F8) {
+                // 2^8 P <= 256: probabilities down to 2^-14 stay normal
+                smem[S::kP + kmaj16_off8(h0 + h, i * 128 + t)] =
+                    static_cast<uint8_t>(ptx::pack_e4m3x4(e * 256.f, 0.f, 0.f, 0.f) & 0xFFu);
+              } else {
+                *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h0 + h, i * 128 + t)) =
+                    __float2bfloat16_rn(e);
+              }
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          l[h] = sum;
+        }
+#pragma unroll
+        for (int h = 0; h < HPW; ++h)
+          if (lane == h) red[4 * kTcN + qw * kTcN + h0 + h] = l[h];
+        ptx::fence_proxy_async_smem();
+        // this warp's reads of S^T (and of the previous item's O^T) are done
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(TB_P));
+        ptx::mbar_arrive(bar(TB_RED));
+        ok = ptx::mbar_wait(bar(TB_RED), 1, s_abort, p.wait_limit_ns);
+        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9700);
+      }
+      if (__all_sync(0xffffffffu, ok)) {
+        const float* rs = red + 4 * kTcN;
+#pragma unroll
+        for (int h = 0; h < HPW; ++h) {
+          const int hh = h0 + h;
+          l[h] = (rs[hh] + rs[kTcN + hh]) + (rs[2 * kTcN + hh] + rs[3 * kTcN + hh]);
+        }
+        ok = ptx::mbar_wait(bar(TB_O), j & 1, s_abort, p.wait_limit_ns);
+        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9800);
+      }
+      if (__all_sync(0xffffffffu, ok)) {
+        ptx::tc_fence_after();
+        // O^T: TMEM lane = column t of d, column h = query head
+        uint32_t r[HPW];
+        ptx::tmem_ld_n<HPW>(tmem + lane_base + 64 + h0, r);
+        uint32_t ro[HPW], rm[HPW], rl[HPW];
+        if (c.b != run_b) {
+          // a new run: the previous one leaves, this item starts the next
+          if (run_b >= 0) ok = flush(c.kh);
+          run_b = c.b;
+          run_part = c.part;
+#pragma unroll
+          for (int h = 0; h < HPW; ++h) {
+            ro[h] = __float_as_uint(__uint_as_float(r[h]) * oscale);
+            rm[h] = __float_as_uint(M[h]);
+            rl[h] = __float_as_uint(l[h]);
+          }
+        } else {
+          ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunO + h0, ro);
+          ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunM + h0, rm);
+          ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunL + h0, rl);
+#pragma unroll
+          for (int h = 0; h < HPW; ++h) {
+            const float mr = __uint_as_float(rm[h]);
+            const float mn = fmaxf(mr, M[h]);
+            const float a = ptx::ex2(mr - mn);
+            const float bb = ptx::ex2(M[h] - mn);
+            ro[h] = __float_as_uint(a * __uint_as_float(ro[h]) + bb * oscale * __uint_as_float(r[h]));
+            rl[h] = __float_as_uint(a * __uint_as_float(rl[h]) + bb * l[h]);
+            rm[h] = __float_as_uint(mn);
+            // this part's slot carries no partial of its own
+            const int hh = h0 + h;
+            if (hh < G && t == hh)
+              p.lse_part[(static_cast<int64_t>(c.part) * p.Hq + c.kh * G + hh) * p.B + c.b] =
+                  -INFINITY;
+          }
+        }
+        ptx::tmem_st_n<HPW>(tmem + lane_base + kRunO + h0, ro);
+        ptx::tmem_st_n<HPW>(tmem + lane_base + kRunM + h0, rm);
+        ptx::tmem_st_n<HPW>(tmem + lane_base + kRunL + h0, rl);
+      }
+      ok = __all_sync(0xffffffffu, ok);
     }
+    // The last run leaves. Its staging may follow another run's in the same
+    // item (no P was written in between, so nothing has waited for that
+    // store to read the buffer): thread 0 waits for it and lets the others
+    // go on.
+    if (ok && run_b >= 0) {
+      if (threadIdx.x == 0) {
+        ptx::bulk_wait_read();
+        ptx::mbar_arrive(bar(TB_SFREE));
+      }
+      ok = ptx::mbar_wait(bar(TB_SFREE), 0, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9F10);
+      if (__all_sync(0xffffffffu, ok)) flush(prev.kh);
+    }
+    if (threadIdx.x == 0) ptx::bulk_wait_all();
   }
 
   ptx::tc_fence_before();
@@ -732,6 +969,66 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), 2) decode_tc
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 128);
   }
+}
+
+// Raises a kernel's dynamic shared-memory limit in the current context. A
+// function attribute belongs to the context, so it is set on every call (a
+// cheap driver call) rather than remembered.
+cp_attn_status set_smem_limit(const void* fn, size_t bytes, const char* what) {
+  const cudaError_t err =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return fail(CP_ATTN_ERR_CUDA, std::string(what) + " attr: " + cudaGetErrorString(err));
+  }
+  return CP_ATTN_OK;
+}
+
+// CTAs of kernel `fn` (one of kResidentSlots instances, `slot`) that the
+// current device holds at once, from the kernel's registers, its shared
+// memory and its threads against the SM's limits. It depends only on the
+// device and the kernel, so it is kept per (device, slot).
+constexpr int kResidentSlots = 6;
+constexpr int kResidentDevices = 64;
+cp_attn_status resident_ctas(const void* fn, int slot, int threads, size_t smem, int* out) {
+  static std::atomic<int> cache[kResidentDevices][kResidentSlots];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && dev >= 0 && dev < kResidentDevices) {
+    const int v = cache[dev][slot].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *out = v;
+      return CP_ATTN_OK;
+    }
+  }
+  int sms = 0, regs_sm = 0, smem_sm = 0, smem_rsv = 0, thr_sm = 0, blk_sm = 0;
+  cudaFuncAttributes fa{};
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(CP_ATTN_ERR_CUDA, std::string("decode occupancy: ") + cudaGetErrorString(e));
+  }
+  // registers are given out per warp in units of 256
+  const int warp_regs = ((fa.numRegs * 32 + 255) / 256) * 256;
+  const int by_regs = regs_sm / (warp_regs * ((threads + 31) / 32));
+  const int by_smem =
+      smem_sm / static_cast<int>(smem + fa.sharedSizeBytes + static_cast<size_t>(smem_rsv));
+  int per_sm = by_regs < by_smem ? by_regs : by_smem;
+  if (thr_sm / threads < per_sm) per_sm = thr_sm / threads;
+  if (blk_sm < per_sm) per_sm = blk_sm;
+  if (sms * per_sm <= 0) return fail(CP_ATTN_ERR_CUDA, "decode occupancy: no CTA fits on an SM");
+  *out = sms * per_sm;
+  if (dev >= 0 && dev < kResidentDevices) cache[dev][slot].store(*out, std::memory_order_relaxed);
+  return CP_ATTN_OK;
 }
 
 // Keys per CTA. head_dim 128 (the tensor-core kernel, two CTAs per SM): the
@@ -786,24 +1083,67 @@ cp_attn_status launch_tc(const void* k, const void* v, const DecTcParams& p, int
   if ((st = F8 ? encode_u8_map(&tv, v, rows, p.Hkv, 128, true)
                : encode_bf16_rows_map(&tv, v, rows, p.Hkv, 128)) != CP_ATTN_OK)
     return st;
-  const size_t smem = DecTcSmem<F8>::kBytes;
   const int nh = p.G <= 4 ? 4 : p.G <= 8 ? 8 : 16;
+  const size_t smem = nh == 16 ? DecTcSmem<F8, dec_slots(F8, 16)>::kBytes
+                               : DecTcSmem<F8, dec_slots(F8, 4)>::kBytes;
   auto kernel = nh == 4 ? decode_tc_kernel<F8, 4>
                 : nh == 8 ? decode_tc_kernel<F8, 8> : decode_tc_kernel<F8, 16>;
-  static bool attr[3] = {false, false, false};
   const int ai = nh == 4 ? 0 : nh == 8 ? 1 : 2;
-  if (!attr[ai]) {
-    const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-    if (err != cudaSuccess)
-      return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc attr: ") + cudaGetErrorString(err));
-    attr[ai] = true;
+  const int threads = 32 * (dec_softmax_warps(nh) + 2);
+  int resident = 0;
+  cp_attn_status st2 = set_smem_limit(reinterpret_cast<const void*>(kernel), smem, "decode_tc");
+  if (st2 == CP_ATTN_OK) {
+    // all of the unified L1 / shared memory as shared memory, so that the
+    // occupancy below counts the CTAs that really fit
+    const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc carveout: ") + cudaGetErrorString(e));
+    }
+    st2 = resident_ctas(reinterpret_cast<const void*>(kernel), F8 * 3 + ai, threads, smem, &resident);
   }
-  kernel<<<dim3(parts, p.Hkv, p.B), 32 * (dec_softmax_warps(nh) + 2), smem, s>>>(tk, tv, p);
+  if (st2 != CP_ATTN_OK) return st2;
+  // A persistent grid: as many CTAs as fit on the device at once. When that
+  // is at least Hkv, a multiple of Hkv whose CTAs take their items from the
+  // per-KV-head work counters (zeroed here, on the stream); otherwise the
+  // items are dealt round robin.
+  DecTcParams q = p;
+  q.parts = parts;
+  const int64_t items = static_cast<int64_t>(p.B) * p.Hkv * parts;
+  int64_t grid_n = resident >= p.Hkv ? resident - resident % p.Hkv : resident;
+  if (grid_n > items) grid_n = items;
+  if (grid_n % p.Hkv != 0) q.counters = nullptr;
+  if (q.counters) {
+    const cudaError_t e = cudaMemsetAsync(q.counters, 0, sizeof(int) * p.Hkv, s);
+    if (e != cudaSuccess)
+      return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc counters: ") + cudaGetErrorString(e));
+  }
+  const unsigned grid = static_cast<unsigned>(grid_n);
+  kernel<<<grid, threads, smem, s>>>(tk, tv, q);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc: ") + cudaGetErrorString(err));
   count_launch();
   return CP_ATTN_OK;
+}
+
+// Workspace of a decode call: the fp32 partial outputs [parts][B][Hq][d], the
+// partial LSEs [parts][Hq][B] and the tensor-core kernel's work counters
+// [Hkv], each at a 256-byte offset.
+struct DecodeLayout {
+  size_t lse_off, ctr_off, total;
+};
+int64_t n_parts(const cp_attn_decode_desc* d);
+DecodeLayout decode_layout(const cp_attn_decode_desc* d) {
+  const int64_t parts = n_parts(d);
+  const int64_t rows = static_cast<int64_t>(d->batch) * d->n_q_heads;
+  auto up = [](size_t x) { return ((x + 255) / 256) * 256; };
+  DecodeLayout l;
+  l.lse_off = up(static_cast<size_t>(parts * rows * d->head_dim) * 4);
+  l.ctr_off = up(l.lse_off + static_cast<size_t>(parts * rows) * 4);
+  l.total = l.ctr_off + static_cast<size_t>(d->n_kv_heads) * 4;
+  return l;
 }
 
 cp_attn_status validate(const cp_attn_decode_desc* d) {
@@ -833,15 +1173,9 @@ int64_t n_parts(const cp_attn_decode_desc* d) {
 template <int D, int HPG>
 cp_attn_status launch(const DecParams& p, int parts, cudaStream_t s) {
   const size_t smem = DecSmem<D>::kBytes;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<D, HPG>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-    if (err != cudaSuccess)
-      return fail(CP_ATTN_ERR_CUDA, std::string("decode attr: ") + cudaGetErrorString(err));
-    attr = true;
-  }
+  const cp_attn_status st =
+      set_smem_limit(reinterpret_cast<const void*>(decode_partial_kernel<D, HPG>), smem, "decode");
+  if (st != CP_ATTN_OK) return st;
   decode_partial_kernel<D, HPG><<<dim3(parts, p.Hkv, p.B), kDecThreads, smem, s>>>(p);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("decode: ") + cudaGetErrorString(err));
@@ -859,10 +1193,7 @@ cp_attn_status cp_attn_decode_workspace_size(const cp_attn_decode_desc* desc, si
   cp_attn_status st = cpa::validate(desc);
   if (st != CP_ATTN_OK) return st;
   if (!bytes) return cpa::fail(CP_ATTN_ERR_INVALID_ARG, "decode_workspace_size: null out");
-  const int64_t parts = cpa::n_parts(desc);
-  const int64_t rows = static_cast<int64_t>(desc->batch) * desc->n_q_heads;
-  const size_t o_bytes = static_cast<size_t>(parts * rows * desc->head_dim) * 4;
-  *bytes = ((o_bytes + 255) / 256) * 256 + static_cast<size_t>(parts * rows) * 4;
+  *bytes = cpa::decode_layout(desc).total;
   return CP_ATTN_OK;
 }
 
@@ -884,9 +1215,9 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
   const int64_t parts = cpa::n_parts(desc);
   const int G = desc->n_q_heads / desc->n_kv_heads;
   const int64_t rows = static_cast<int64_t>(desc->batch) * desc->n_q_heads;
-  const size_t o_bytes = static_cast<size_t>(parts * rows * desc->head_dim) * 4;
+  const cpa::DecodeLayout lay = cpa::decode_layout(desc);
   float* o_part = static_cast<float*>(workspace);
-  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lay.lse_off);
   cpa::DecParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
@@ -922,6 +1253,7 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
     tp.wait_limit_ns = 1000000000ull;
     if ((st = cpa::decode_status_address(&tp.status)) != CP_ATTN_OK) return st;
     tp.kv_scales = nullptr;
+    tp.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + lay.ctr_off);
     st = cpa::launch_tc<false>(k, v, tp, np, s);
   } else if (desc->head_dim == 128) {
     st = G <= 4 ? cpa::launch<128, 1>(p, np, s) : G <= 8 ? cpa::launch<128, 2>(p, np, s)
@@ -934,7 +1266,8 @@ cp_attn_status cp_attn_decode(const cp_attn_decode_desc* desc, const void* q, co
   // Pass Q's merge over every rank's (and run's) partial
   return cpa::launch_merge_lse(np, desc->batch, desc->n_q_heads, desc->head_dim, o_part,
                                rows * desc->head_dim, lse_part, rows,
-                               static_cast<__nv_bfloat16*>(o), nullptr, lse, s);
+                               static_cast<__nv_bfloat16*>(o), nullptr, lse, s, false,
+                               /*pdl=*/true);
 }
 
 cp_attn_status cp_attn_decode_fp8(const cp_attn_decode_desc* desc, const void* q, const void* k8,
@@ -961,11 +1294,12 @@ cp_attn_status cp_attn_decode_fp8(const cp_attn_decode_desc* desc, const void* q
                      "decode_fp8: kv_len / cp must be a multiple of 128 and batch * kv_len < 2^31");
   const int G = desc->n_q_heads / desc->n_kv_heads;
   const int64_t rows = static_cast<int64_t>(desc->batch) * desc->n_q_heads;
-  const size_t o_bytes = static_cast<size_t>(parts * rows * desc->head_dim) * 4;
+  const cpa::DecodeLayout lay = cpa::decode_layout(desc);
   cpa::DecTcParams tp;
   tp.q = static_cast<const __nv_bfloat16*>(q);
   tp.o_part = static_cast<float*>(workspace);
-  tp.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+  tp.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lay.lse_off);
+  tp.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + lay.ctr_off);
   tp.B = desc->batch;
   tp.Hq = desc->n_q_heads;
   tp.Hkv = desc->n_kv_heads;
@@ -984,7 +1318,8 @@ cp_attn_status cp_attn_decode_fp8(const cp_attn_decode_desc* desc, const void* q
   if ((st = cpa::launch_tc<true>(k8, vt8, tp, np, s)) != CP_ATTN_OK) return st;
   return cpa::launch_merge_lse(np, desc->batch, desc->n_q_heads, desc->head_dim, tp.o_part,
                                rows * desc->head_dim, tp.lse_part, rows,
-                               static_cast<__nv_bfloat16*>(o), nullptr, lse, s);
+                               static_cast<__nv_bfloat16*>(o), nullptr, lse, s, false,
+                               /*pdl=*/true);
 }
 
 cp_attn_status cp_attn_decode_sync_status(void* stream) {

@@ -103,15 +103,16 @@ __global__ void __launch_bounds__(256) merge_lse_kernel(
 // (row, head). The block first turns every part's LSE into its weight
 // 2^(LSE_i - L), L = M + log2 sum_i 2^(LSE_i - M), in shared memory (one
 // parallel pass for M, one for the sum); then each warp streams its share of
-// the parts' rows (float4 chunks of d <= 128), up to sixteen loads in
-// flight, and warp 0 adds the sixteen sums. A part whose weight is 0 (no visible key) is
-// never read into the sum. The block reads all parts before it writes, so
-// o_out_f32 may alias part 0.
+// the parts' rows (a float4 of d <= 128 per lane), up to sixteen loads in
+// flight, and warp 0 adds the sixteen sums. A part whose weight is 0 (no
+// visible key, or LSE = -inf) is neither loaded nor added. The block reads
+// all parts before it writes, so o_out_f32 may alias part 0.
 constexpr int kWideWarps = 16;
 constexpr int kWideMaxParts = 4096;
 
-// U: loads in flight per lane, about the parts per warp (4, 8 or 16); TP:
-// element type of the O parts.
+// U: loads in flight per lane (4, 8 or 16); TP: element type of the O parts.
+// The kernel waits on the previous kernel of the stream (programmatic
+// dependent launch) before it reads anything.
 template <int U, typename TP>
 __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
     int n_parts, int64_t rows, int heads, int d, const TP* __restrict__ o_parts,
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
   __shared__ float s_w[kWideMaxParts];
   __shared__ float s_red[2][kWideWarps];
   __shared__ float4 s_acc[kWideWarps][32];
+  ptx::grid_dep_wait();
   const int64_t pair = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -130,9 +132,9 @@ __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
   // the parts' LSEs (base 2) and their maximum
   float M = -INFINITY;
   for (int i = threadIdx.x; i < n_parts; i += 32 * kWideWarps) {
-    const float v = __ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e;
-    s_w[i] = v;
-    M = fmaxf(M, v);
+    const float x = __ldg(lse_parts + i * lse_part_stride + lse_idx) * kLog2e;
+    s_w[i] = x;
+    M = fmaxf(M, x);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -160,11 +162,9 @@ __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
     // between the reads above and these writes
     for (int i = threadIdx.x; i < n_parts; i += 32 * kWideWarps) s_w[i] = ptx::ex2(s_w[i] - L);
     __syncthreads();
-    // The loads are unconditional so that all of them are in flight at once:
-    // a part past the end reads the last part and a lane past d/4 reads
-    // chunk 0 (both in bounds); their weight is 0 or their sum is not
-    // stored. A zero weight adds 0 * 0, so rows that were never written
-    // cannot reach the sum.
+    // A warp's loads depend only on the weights (the same for its 32 lanes),
+    // so a weight-0 part costs no load; a lane past d/4 reads chunk 0 (in
+    // bounds) and its sum is not stored.
     const int l4 = has ? lane : 0;
     for (int i0 = warp; i0 < n_parts; i0 += kWideWarps * U) {
       float w[U];
@@ -172,17 +172,16 @@ __global__ void __launch_bounds__(32 * kWideWarps) merge_lse_wide_kernel(
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u * kWideWarps;
-        const int ic = i < n_parts ? i : n_parts - 1;
         w[u] = i < n_parts ? s_w[i] : 0.f;
-        v[u] = load4(o_parts, ic * part_stride + o_off + 4 * l4);
+        v[u] = w[u] != 0.f ? load4(o_parts, i * part_stride + o_off + 4 * l4)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const bool use = w[u] != 0.f;
-        acc.x = fmaf(w[u], use ? v[u].x : 0.f, acc.x);
-        acc.y = fmaf(w[u], use ? v[u].y : 0.f, acc.y);
-        acc.z = fmaf(w[u], use ? v[u].z : 0.f, acc.z);
-        acc.w = fmaf(w[u], use ? v[u].w : 0.f, acc.w);
+        acc.x = fmaf(w[u], v[u].x, acc.x);
+        acc.y = fmaf(w[u], v[u].y, acc.y);
+        acc.z = fmaf(w[u], v[u].z, acc.z);
+        acc.w = fmaf(w[u], v[u].w, acc.w);
       }
     }
   }
@@ -396,7 +395,7 @@ template <typename TP>
 cp_attn_status merge_lse_typed(int n_parts, int64_t rows, int heads, int d, const TP* o_parts,
                                int64_t part_stride, const float* lse_parts,
                                int64_t lse_part_stride, __nv_bfloat16* o_out, float* o_out_f32,
-                               float* lse_out, cudaStream_t s) {
+                               float* lse_out, cudaStream_t s, bool pdl) {
   const int64_t warps = rows * heads;
   if (warps == 0) return CP_ATTN_OK;
   // few (row, head) pairs with many parts: a block of warps per pair
@@ -405,9 +404,19 @@ cp_attn_status merge_lse_typed(int n_parts, int64_t rows, int heads, int d, cons
     auto kernel = per_warp <= 4   ? merge_lse_wide_kernel<4, TP>
                   : per_warp <= 8 ? merge_lse_wide_kernel<8, TP>
                                   : merge_lse_wide_kernel<16, TP>;
-    kernel<<<static_cast<unsigned>(warps), 32 * kWideWarps, 0, s>>>(
-        n_parts, rows, heads, d, o_parts, part_stride, lse_parts, lse_part_stride, o_out,
-        o_out_f32, lse_out);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(warps));
+    cfg.blockDim = dim3(32 * kWideWarps);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, n_parts, rows, heads, d, o_parts,
+                                               part_stride, lse_parts, lse_part_stride, o_out,
+                                               o_out_f32, lse_out);
+    if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("merge_lse: ") + cudaGetErrorString(err));
     return check_launch("merge_lse");
   }
   const int64_t blocks = (warps * 32 + 255) / 256;
@@ -428,12 +437,13 @@ cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
                                 const void* o_parts, int64_t part_stride,
                                 const float* lse_parts, int64_t lse_part_stride,
                                 __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
-                                cudaStream_t s, bool parts_bf16) {
+                                cudaStream_t s, bool parts_bf16, bool pdl) {
   if (parts_bf16)
     return merge_lse_typed(n_parts, rows, heads, d, static_cast<const __nv_bfloat16*>(o_parts),
-                           part_stride, lse_parts, lse_part_stride, o_out, o_out_f32, lse_out, s);
+                           part_stride, lse_parts, lse_part_stride, o_out, o_out_f32, lse_out, s,
+                           pdl);
   return merge_lse_typed(n_parts, rows, heads, d, static_cast<const float*>(o_parts), part_stride,
-                         lse_parts, lse_part_stride, o_out, o_out_f32, lse_out, s);
+                         lse_parts, lse_part_stride, o_out, o_out_f32, lse_out, s, pdl);
 }
 
 cp_attn_status launch_permute_rows(const int32_t* row_map, int64_t rows, int64_t row_bytes,

@@ -94,12 +94,15 @@ size_t step_bwd_smem_bytes(int d);
 // Rows of the Q / dO tensor-map box the backward kernel for head_dim d uses.
 int step_bwd_q_box_rows(int d);
 
-// o_parts: fp32, or bf16 when parts_bf16 (part_stride in elements).
+// o_parts: fp32, or bf16 when parts_bf16 (part_stride in elements). pdl:
+// the merge of few (row, head) pairs over many parts is launched as a
+// programmatic dependent of the previous kernel on s, and waits for it before
+// it reads anything.
 cp_attn_status launch_merge_lse(int n_parts, int64_t rows, int heads, int d,
                                 const void* o_parts, int64_t part_stride,
                                 const float* lse_parts, int64_t lse_part_stride,
                                 __nv_bfloat16* o_out, float* o_out_f32, float* lse_out,
-                                cudaStream_t s, bool parts_bf16 = false);
+                                cudaStream_t s, bool parts_bf16 = false, bool pdl = false);
 
 // K6: n fp32 values -> bf16 (round to nearest even); n a multiple of 8,
 // both pointers 16-byte aligned.

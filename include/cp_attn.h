@@ -547,8 +547,10 @@ cp_attn_status cp_attn_head_a2a(int64_t rows, int heads, int64_t head_bytes, int
  * the GPU, and the merge combines every run's partial.
  * q: bf16 [batch, Hq, d]; k, v: bf16 [batch, kv_len, Hkv, d]; o: bf16
  * [batch, Hq, d]; lse: fp32 [Hq, batch] (natural log, scale applied).
- * workspace: cp_attn_decode_workspace_size bytes (fp32 partials), 16-byte
- * aligned like every pointer. Supported: head_dim 64 or 128, at most 16 query
+ * workspace: cp_attn_decode_workspace_size bytes (fp32 partials and, for the
+ * tensor-core path, one work counter per KV head that the call zeroes on
+ * `stream` first), 16-byte aligned like every pointer; calls that run at the
+ * same time need workspaces of their own. Supported: head_dim 64 or 128, at most 16 query
  * heads per KV head, kv_len a multiple of 64*cp. With head_dim 128 and key
  * runs that are multiples of 128 the partials come from the tensor cores
  * (S^T = K Q^T and O^T = V^T P^T with the query heads as N = 16, P in bf16);
