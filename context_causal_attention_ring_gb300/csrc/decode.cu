@@ -417,6 +417,35 @@ __device__ __forceinline__ void dec_issue_tile(const CUtensorMap* tm_k, const CU
 // E4M3 [Hkv][128][B*kv_len]; each head's query row is quantized here with its
 // own scale, S^T and O^T are kind::f8f6f4 with K = 32, and P goes to shared
 // memory as E4M3 scaled by 2^8 (P <= 1 against the run's exact maximum).
+// The warp-wide reduction (max or sum) of each of a lane's N values (N = 4 or
+// 8, one per head), by halving: at each of the first log2 N steps a lane
+// keeps half of its values, sends the other half to its partner and combines
+// the halves it holds, so that the last steps work on a single value. It
+// costs N - 1 + 5 - log2 N shuffles instead of 5 N. Lane l returns the
+// reduction of value l >> (5 - log2 N).
+template <int N, bool MAX>
+__device__ __forceinline__ float warp_reduce_heads(const float (&v)[N], int lane) {
+  static_assert(N == 4 || N == 8, "four or eight values per lane");
+  auto op = [](float a, float b) { return MAX ? fmaxf(a, b) : a + b; };
+  float w[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) w[k] = v[k];
+#pragma unroll
+  for (int n = N, off = 16; n > 1; n >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float keep = upper ? w[k + n / 2] : w[k];
+      const float send = upper ? w[k] : w[k + n / 2];
+      w[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+  constexpr int kDone = N == 8 ? 3 : 2;  // offsets 16 .. 32 >> kDone used above
+#pragma unroll
+  for (int off = 16 >> kDone; off > 0; off >>= 1) w[0] = op(w[0], __shfl_xor_sync(0xffffffffu, w[0], off));
+  return w[0];
+}
+
 // Softmax warps of the tensor-core decode: eight (two groups of four, eight
 // heads each) when all 16 columns of N are heads, else four.
 constexpr int dec_softmax_warps(int nh) { return nh == 16 ? 8 : 4; }
@@ -729,6 +758,7 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
     const int qw = warp & 3;
     const int h0 = (warp >> 2) * HPW;
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+    constexpr int kHeadShift = HPW == 8 ? 2 : 3;  // warp_reduce_heads: lane l ends with head l >> kHeadShift
     // base-2 score factor per head (E4M3: times the query row's and K's
     // descale factors)
     const float* qs = reinterpret_cast<const float*>(smem + S::kQs);
@@ -839,13 +869,12 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
           float m = x[0][h];
 #pragma unroll
           for (int i = 1; i < kTcMaxTiles; ++i) m = fmaxf(m, x[i][h]);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
           M[h] = m;
         }
-#pragma unroll
-        for (int h = 0; h < HPW; ++h)
-          if (lane == h) red[qw * kTcN + h0 + h] = M[h];
+        {
+          const float m = warp_reduce_heads<HPW, true>(M, lane);
+          if ((lane & ((1 << kHeadShift) - 1)) == 0) red[qw * kTcN + h0 + (lane >> kHeadShift)] = m;
+        }
         // P is written after this phase, over the previous item's O staging:
         // its store must have read it
         if (threadIdx.x == 0) ptx::bulk_wait_read();
@@ -878,13 +907,13 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
               }
             }
           }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
           l[h] = sum;
         }
-#pragma unroll
-        for (int h = 0; h < HPW; ++h)
-          if (lane == h) red[4 * kTcN + qw * kTcN + h0 + h] = l[h];
+        {
+          const float sm = warp_reduce_heads<HPW, false>(l, lane);
+          if ((lane & ((1 << kHeadShift) - 1)) == 0)
+            red[4 * kTcN + qw * kTcN + h0 + (lane >> kHeadShift)] = sm;
+        }
         ptx::fence_proxy_async_smem();
         // this warp's reads of S^T (and of the previous item's O^T) are done
         ptx::tc_fence_before();
