@@ -721,6 +721,12 @@ def run_decode_bench(args):
     rows = []
 
     def time_calls(call):
+        """(GPU ms per call, host-inclusive median ms per call, launches per
+        call). The GPU time is that of n back-to-back calls enqueued behind a
+        ~20 ms device sleep, so that the host's enqueue time never leaves the
+        stream idle; the second figure brackets each call with its own events
+        as it is enqueued, and so also holds the host's per-call overhead
+        whenever that is longer than the call."""
         for _ in range(max(3, args.warmup)):
             call()
         n = max(20, args.steps)
@@ -731,9 +737,17 @@ def run_decode_bench(args):
             call()
             e1.record()
         torch.cuda.synchronize()
+        host_ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        launches = (cpa.launch_count() - n0) // n
+        a, b = torch.cuda.Event(True), torch.cuda.Event(True)
+        torch.cuda._sleep(40_000_000)
+        a.record()
+        for _ in range(n):
+            call()
+        b.record()
+        torch.cuda.synchronize()
         cpa.decode_sync_status()
-        return (statistics.median(e0.elapsed_time(e1) for e0, e1 in ev),
-                (cpa.launch_count() - n0) // n)
+        return a.elapsed_time(b) / n, host_ms, launches
 
     def quantize(x, n_rows, heads, d, transpose):
         amax = torch.zeros(4, dtype=torch.float32, device="cuda")
@@ -761,17 +775,20 @@ def run_decode_bench(args):
         for kv_dtype, elt, call in (
                 ("bf16", 2, lambda: cpa.decode(qd, kd, vd, o, lse, ws, R)),
                 ("e4m3", 1, lambda: cpa.decode_fp8(qd, k8, vt8, scales, o, lse, ws, R))):
-            ms, launches = time_calls(call)
+            ms, host_ms, launches = time_calls(call)
             algo = 2 * B * T * Hkv * d * elt + 2 * B * Hq * d * 2 + Hq * B * 4
             gbs = algo / (ms * 1e-3) / 1e9
             rows.append({"workload": name, "kv_dtype": kv_dtype, "batch": B, "kv_len": T,
                          "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d, "cp": R, "ms": ms,
+                         "ms_per_call_host": host_ms,
                          "algorithmic_bytes": algo, "achieved_gbs": gbs,
                          "frac_of_hbm": gbs / peaks["hbm_gbs"], "launches_per_call": launches})
         del qd, kd, vd, o, lse, ws, k8, vt8
         torch.cuda.empty_cache()
     print(json.dumps({"metric": "decode_hbm_bandwidth", "unit": "GB/s",
                       "peak": peaks["hbm_gbs"], "peak_kind": f"hbm_gbs ({peak_kind})",
+                      "timing": "ms: GPU time per call, back-to-back calls on a stream kept busy; "
+                                "ms_per_call_host: median of calls bracketed one by one",
                       "rows": rows}), flush=True)
 
 
