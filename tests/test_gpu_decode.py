@@ -5,7 +5,10 @@ one to sixteen query heads per KV head (including group sizes that are not a
 multiple of four), both head dimensions, several ring sizes and a 405B-shaped
 row over 131072 keys. With head_dim 128 and key runs of 128, 256 or 512 the
 tensor-core kernel (K9) computes the partials; head_dim 64 and 64-key runs
-use the CUDA-core kernel (K8). Tolerances: O (bf16) 1e-2 plus half a bf16
+use the CUDA-core kernel (K8). K9 is a persistent grid whose CTAs each keep
+one KV head and take its runs from a work counter, merging consecutive runs
+of one sequence: the cases with several sequences and more runs than CTAs
+cover runs that cross sequences. Tolerances: O (bf16) 1e-2 plus half a bf16
 ulp, LSE 1e-3."""
 import numpy as np
 import pytest
@@ -46,6 +49,8 @@ def _check(B, T, Hq, Hkv, d, R, seed, qk_scale=1.0):
     (16, 2048, 32, 8, 128, 8),    # many sequences: 256-key runs
     (2, 8192, 64, 4, 128, 4),     # 16 heads per group, 128-key runs of a 2048-key shard
     (3, 1536, 12, 1, 128, 2),     # 12 heads per group, 128-key runs of a 768-key shard
+    (2, 1536, 48, 3, 128, 2),     # 16 heads per group, 3 KV heads (the grid is a multiple of 3)
+    (4, 16384, 32, 2, 128, 2),    # 16 heads per group, a CTA's runs cross sequences
 ])
 def test_decode_small(B, T, Hq, Hkv, d, R):
     _check(B, T, Hq, Hkv, d, R, seed=B * 100 + R)
