@@ -1134,17 +1134,19 @@ cp_attn_status launch_tc(const void* k, const void* v, const DecTcParams& p, int
     st2 = resident_ctas(reinterpret_cast<const void*>(kernel), F8 * 3 + ai, threads, smem, &resident);
   }
   if (st2 != CP_ATTN_OK) return st2;
-  // A persistent grid: as many CTAs as fit on the device at once. When that
-  // is at least Hkv, a multiple of Hkv whose CTAs take their items from the
-  // per-KV-head work counters (zeroed here, on the stream); otherwise the
-  // items are dealt round robin.
+  // A persistent grid: as many CTAs as fit on the device at once, rounded
+  // down to a multiple of Hkv (at least Hkv: with more KV heads than resident
+  // CTAs the rest wait for a slot), and no more than there are items. Its
+  // CTAs take their items from the per-KV-head work counters, zeroed here on
+  // the stream. items = B * parts * Hkv is a multiple of Hkv too.
+  if (p.counters == nullptr) return fail(CP_ATTN_ERR_INVALID_ARG, "decode_tc: no work counters");
   DecTcParams q = p;
   q.parts = parts;
   const int64_t items = static_cast<int64_t>(p.B) * p.Hkv * parts;
-  int64_t grid_n = resident >= p.Hkv ? resident - resident % p.Hkv : resident;
+  int64_t grid_n = resident - resident % p.Hkv;
+  if (grid_n < p.Hkv) grid_n = p.Hkv;
   if (grid_n > items) grid_n = items;
-  if (grid_n % p.Hkv != 0) q.counters = nullptr;
-  if (q.counters) {
+  {
     const cudaError_t e = cudaMemsetAsync(q.counters, 0, sizeof(int) * p.Hkv, s);
     if (e != cudaSuccess)
       return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc counters: ") + cudaGetErrorString(e));
