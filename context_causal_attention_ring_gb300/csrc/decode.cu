@@ -671,6 +671,7 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
     bool ok = true;
     int n_q = 0;  // query-row rewrites waited for
     Item prev = first;
+    int run_b = -1;  // the sequence of the run the O^T accumulator holds
     for (int j = 0; ok; ++j) {
       int idx = item0;
       if (j > 0) {
@@ -684,6 +685,10 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
       const Item c = item_of(idx);
       const bool new_q = c.b != prev.b || c.kh != prev.kh;
       prev = c;
+      // a new run starts the O^T accumulator afresh (the softmax warps read
+      // the previous run out before they hand over this item's P)
+      const uint32_t acc0 = c.b != run_b ? 0u : 1u;
+      run_b = c.b;
       if (new_q) {
         // the softmax warps wrote the new group's query rows
         if (!wait_w(bar(TB_Q), n_q & 1, 0x9A00)) { ok = false; break; }
@@ -729,7 +734,7 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
           for (int kk = 0; kk < 4; ++kk)
             ptx::mma_ss_f8_w(tmem + 64, ptx::sdesc_add(dV, kk * 32),
                              ptx::sdesc_add(dP, t * 2048 + kk * 32), idesc_o,
-                             (t > 0 || kk > 0) ? 1u : 0u, leader);
+                             (t > 0 || kk > 0) ? 1u : acc0, leader);
         } else {
           // V tile as the MN-major A of O^T (M = d: d 64..127 at +16 KB; K =
           // keys, 16 keys = 2 KB per step); P as the K-major B, 64 keys per
@@ -739,7 +744,7 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
           for (int kk = 0; kk < 8; ++kk)
             ptx::mma_ss_w(tmem + 64, ptx::sdesc_add(dV, kk * 2048),
                           ptx::sdesc_add(dP, (2 * t + (kk >> 2)) * 2048 + (kk & 3) * 32),
-                          idesc_o, (t > 0 || kk > 0) ? 1u : 0u, leader);
+                          idesc_o, (t > 0 || kk > 0) ? 1u : acc0, leader);
         }
         ptx::mma_commit_w(bar(TB_EMPTY + slot), leader);
       }
@@ -764,20 +769,23 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
     const float* qs = reinterpret_cast<const float*>(smem + S::kQs);
     // E4M3: O^T carries 2^8 of P and V's descale factor
     const float oscale = F8 ? kv_sv * (1.f / 256.f) : 1.f;
-    // The CTA merges its consecutive items of one sequence as it goes (the
-    // log-sum-exp merge, "Ring Attention Algorithms"): the run's maximum m
-    // and sum l per head, and O = sum of 2^(M_item - m) O_item, live in TMEM
-    // columns kRunM, kRunL and kRunO (one copy per lane). A run leaves as
-    // one partial in the slot of its first part; its other parts' slots get
-    // LSE = -inf (weight 0 in the merge that follows). The O rows of the
-    // group's G heads are contiguous in o_part: they are staged [head][d] in
-    // the P buffer (the item's O^T products have read P) and leave in one
-    // bulk store.
-    constexpr uint32_t kRunO = 80, kRunM = 96, kRunL = 112;
+    // The CTA merges its consecutive items of one sequence (a run) as it
+    // goes, in the online form of the log-sum-exp merge ("Ring Attention
+    // Algorithms"): the run's maximum m and sum l per head live in TMEM
+    // columns kRunM and kRunL (one copy per lane), its O in the O^T
+    // accumulator, which the items' O^T = V^T P^T products keep adding into.
+    // P is taken against m, raised to an item's maximum when that is larger
+    // (O and l are then scaled by 2^(m_old - m_new) before the item's O^T
+    // products), so P <= 1 as within an item. A run leaves as one partial in
+    // the slot of its first part; its other parts' slots get LSE = -inf
+    // (weight 0 in the merge that follows). The O rows of the group's G
+    // heads are contiguous in o_part: they are staged [head][d] in the P
+    // buffer (the last O^T products have read P) and leave in one bulk store.
+    constexpr uint32_t kRunM = 96, kRunL = 112;
     int run_b = -1, run_part = 0, n_flush = 0;
     auto flush = [&](int kh) -> bool {
       uint32_t o[HPW], m[HPW], l_[HPW];
-      ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunO + h0, o);
+      ptx::tmem_ld_n<HPW>(tmem + lane_base + 64 + h0, o);
       ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunM + h0, m);
       ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunL + h0, l_);
       float* stage = reinterpret_cast<float*>(smem + S::kP);
@@ -786,7 +794,7 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
         const int hh = h0 + h;
         if (hh < G) {
           const float lh = __uint_as_float(l_[h]);
-          stage[hh * 128 + t] = __uint_as_float(o[h]) * __frcp_rn(lh);
+          stage[hh * 128 + t] = __uint_as_float(o[h]) * (__frcp_rn(lh) * oscale);
           if (t == hh)
             p.lse_part[(static_cast<int64_t>(run_part) * p.Hq + kh * G + hh) * p.B + run_b] =
                 (__uint_as_float(m[h]) + ptx::lg2(lh)) * kLn2d;
@@ -810,6 +818,7 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
     };
     bool ok = true;
     int n_q = 0;
+    int last_j = -1;  // the last item this CTA's softmax warps finished
     Item prev = first;
     for (int j = 0; ok; ++j) {
       int idx = item0;
@@ -835,12 +844,21 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
         ++n_q;
         if (!__all_sync(0xffffffffu, ok)) break;
       }
+      // S^T of this item complete implies the previous item's O^T products
+      // complete (issued before it)
       ok = ptx::mbar_wait(bar(TB_S), j & 1, s_abort, p.wait_limit_ns);
       if (!ok) ptx::record_timeout(p.status, s_abort, 0x9500);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const bool run_start = c.b != run_b;
+      if (run_start && run_b >= 0) {
+        // the previous run leaves before this item's O^T products start anew
+        ok = flush(c.kh);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
       float x[kTcMaxTiles][HPW];
       float M[HPW], l[HPW];
-      if (__all_sync(0xffffffffu, ok)) {
-        ptx::tc_fence_after();
+      {
         float sf[HPW];
 #pragma unroll
         for (int h = 0; h < HPW; ++h) sf[h] = p.scale_log2;
@@ -871,109 +889,117 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
           for (int i = 1; i < kTcMaxTiles; ++i) m = fmaxf(m, x[i][h]);
           M[h] = m;
         }
-        {
-          const float m = warp_reduce_heads<HPW, true>(M, lane);
-          if ((lane & ((1 << kHeadShift) - 1)) == 0) red[qw * kTcN + h0 + (lane >> kHeadShift)] = m;
-        }
-        // P is written after this phase, over the previous item's O staging:
-        // its store must have read it
-        if (threadIdx.x == 0) ptx::bulk_wait_read();
-        ptx::mbar_arrive(bar(TB_RED));
-        ok = ptx::mbar_wait(bar(TB_RED), 0, s_abort, p.wait_limit_ns);
-        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9600);
+        const float m = warp_reduce_heads<HPW, true>(M, lane);
+        if ((lane & ((1 << kHeadShift) - 1)) == 0) red[qw * kTcN + h0 + (lane >> kHeadShift)] = m;
       }
-      if (__all_sync(0xffffffffu, ok)) {
+      // P is written after this phase, over the previous run's O staging:
+      // its store must have read it
+      if (threadIdx.x == 0) ptx::bulk_wait_read();
+      ptx::mbar_arrive(bar(TB_RED));
+      ok = ptx::mbar_wait(bar(TB_RED), 0, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9600);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // the run's reference maximum per head: the item's at a run's start,
+      // else raised to it (O and l scaled down) when it is larger
+      uint32_t rm[HPW], rl[HPW];
+      if (run_start) {
 #pragma unroll
         for (int h = 0; h < HPW; ++h) {
           const int hh = h0 + h;
-          M[h] = fmaxf(fmaxf(red[hh], red[kTcN + hh]), fmaxf(red[2 * kTcN + hh], red[3 * kTcN + hh]));
+          rm[h] = __float_as_uint(
+              fmaxf(fmaxf(red[hh], red[kTcN + hh]), fmaxf(red[2 * kTcN + hh], red[3 * kTcN + hh])));
+          rl[h] = __float_as_uint(0.f);
         }
-        // P = 2^(x - M) (bf16 or E4M3 into shared memory) and the per-head sums
+      } else {
+        ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunM + h0, rm);
+        ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunL + h0, rl);
+        float fac[HPW];
+        bool moved = false;
 #pragma unroll
         for (int h = 0; h < HPW; ++h) {
-          float sum = 0.f;
+          const int hh = h0 + h;
+          const float mi =
+              fmaxf(fmaxf(red[hh], red[kTcN + hh]), fmaxf(red[2 * kTcN + hh], red[3 * kTcN + hh]));
+          const float mr = __uint_as_float(rm[h]);
+          fac[h] = 1.f;
+          if (mi > mr) {
+            fac[h] = ptx::ex2(mr - mi);
+            rm[h] = __float_as_uint(mi);
+            rl[h] = __float_as_uint(__uint_as_float(rl[h]) * fac[h]);
+            moved = true;
+          }
+        }
+        if (__any_sync(0xffffffffu, moved)) {
+          // O^T: TMEM lane = column t of d, column h = query head
+          uint32_t o[HPW];
+          ptx::tmem_ld_n<HPW>(tmem + lane_base + 64 + h0, o);
 #pragma unroll
-          for (int i = 0; i < kTcMaxTiles; ++i) {
-            if (i < nt) {
-              const float e = ptx::ex2(x[i][h] - M[h]);
-              sum += e;
-              if constexpr (F8) {
-                // 2^8 P <= 256: probabilities down to 2^-14 stay normal
-                smem[S::kP + kmaj16_off8(h0 + h, i * 128 + t)] =
-                    static_cast<uint8_t>(ptx::pack_e4m3x4(e * 256.f, 0.f, 0.f, 0.f) & 0xFFu);
-              } else {
-                *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h0 + h, i * 128 + t)) =
-                    __float2bfloat16_rn(e);
-              }
+          for (int h = 0; h < HPW; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * fac[h]);
+          ptx::tmem_st_n<HPW>(tmem + lane_base + 64 + h0, o);
+        }
+      }
+      // P = 2^(x - m) (bf16 or E4M3 into shared memory) and the per-head sums
+#pragma unroll
+      for (int h = 0; h < HPW; ++h) {
+        const float mr = __uint_as_float(rm[h]);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kTcMaxTiles; ++i) {
+          if (i < nt) {
+            const float e = ptx::ex2(x[i][h] - mr);
+            sum += e;
+            if constexpr (F8) {
+              // 2^8 P <= 256: probabilities down to 2^-14 stay normal
+              smem[S::kP + kmaj16_off8(h0 + h, i * 128 + t)] =
+                  static_cast<uint8_t>(ptx::pack_e4m3x4(e * 256.f, 0.f, 0.f, 0.f) & 0xFFu);
+            } else {
+              *reinterpret_cast<__nv_bfloat16*>(smem + S::kP + kmaj16_off(h0 + h, i * 128 + t)) =
+                  __float2bfloat16_rn(e);
             }
           }
-          l[h] = sum;
         }
-        {
-          const float sm = warp_reduce_heads<HPW, false>(l, lane);
-          if ((lane & ((1 << kHeadShift) - 1)) == 0)
-            red[4 * kTcN + qw * kTcN + h0 + (lane >> kHeadShift)] = sm;
-        }
-        ptx::fence_proxy_async_smem();
-        // this warp's reads of S^T (and of the previous item's O^T) are done
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(TB_P));
-        ptx::mbar_arrive(bar(TB_RED));
-        ok = ptx::mbar_wait(bar(TB_RED), 1, s_abort, p.wait_limit_ns);
-        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9700);
+        l[h] = sum;
       }
-      if (__all_sync(0xffffffffu, ok)) {
+      {
+        const float sm = warp_reduce_heads<HPW, false>(l, lane);
+        if ((lane & ((1 << kHeadShift) - 1)) == 0)
+          red[4 * kTcN + qw * kTcN + h0 + (lane >> kHeadShift)] = sm;
+      }
+      ptx::fence_proxy_async_smem();
+      // this warp's reads of S^T and its scaling of O^T are done
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(TB_P));
+      ptx::mbar_arrive(bar(TB_RED));
+      ok = ptx::mbar_wait(bar(TB_RED), 1, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9700);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      {
         const float* rs = red + 4 * kTcN;
 #pragma unroll
         for (int h = 0; h < HPW; ++h) {
           const int hh = h0 + h;
-          l[h] = (rs[hh] + rs[kTcN + hh]) + (rs[2 * kTcN + hh] + rs[3 * kTcN + hh]);
+          rl[h] = __float_as_uint(__uint_as_float(rl[h]) +
+                                  ((rs[hh] + rs[kTcN + hh]) + (rs[2 * kTcN + hh] + rs[3 * kTcN + hh])));
+          // a part inside a run carries no partial of its own
+          if (!run_start && hh < G && t == hh)
+            p.lse_part[(static_cast<int64_t>(c.part) * p.Hq + c.kh * G + hh) * p.B + c.b] =
+                -INFINITY;
         }
-        ok = ptx::mbar_wait(bar(TB_O), j & 1, s_abort, p.wait_limit_ns);
-        if (!ok) ptx::record_timeout(p.status, s_abort, 0x9800);
       }
-      if (__all_sync(0xffffffffu, ok)) {
-        ptx::tc_fence_after();
-        // O^T: TMEM lane = column t of d, column h = query head
-        uint32_t r[HPW];
-        ptx::tmem_ld_n<HPW>(tmem + lane_base + 64 + h0, r);
-        uint32_t ro[HPW], rm[HPW], rl[HPW];
-        if (c.b != run_b) {
-          // a new run: the previous one leaves, this item starts the next
-          if (run_b >= 0) ok = flush(c.kh);
-          run_b = c.b;
-          run_part = c.part;
-#pragma unroll
-          for (int h = 0; h < HPW; ++h) {
-            ro[h] = __float_as_uint(__uint_as_float(r[h]) * oscale);
-            rm[h] = __float_as_uint(M[h]);
-            rl[h] = __float_as_uint(l[h]);
-          }
-        } else {
-          ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunO + h0, ro);
-          ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunM + h0, rm);
-          ptx::tmem_ld_n<HPW>(tmem + lane_base + kRunL + h0, rl);
-#pragma unroll
-          for (int h = 0; h < HPW; ++h) {
-            const float mr = __uint_as_float(rm[h]);
-            const float mn = fmaxf(mr, M[h]);
-            const float a = ptx::ex2(mr - mn);
-            const float bb = ptx::ex2(M[h] - mn);
-            ro[h] = __float_as_uint(a * __uint_as_float(ro[h]) + bb * oscale * __uint_as_float(r[h]));
-            rl[h] = __float_as_uint(a * __uint_as_float(rl[h]) + bb * l[h]);
-            rm[h] = __float_as_uint(mn);
-            // this part's slot carries no partial of its own
-            const int hh = h0 + h;
-            if (hh < G && t == hh)
-              p.lse_part[(static_cast<int64_t>(c.part) * p.Hq + c.kh * G + hh) * p.B + c.b] =
-                  -INFINITY;
-          }
-        }
-        ptx::tmem_st_n<HPW>(tmem + lane_base + kRunO + h0, ro);
-        ptx::tmem_st_n<HPW>(tmem + lane_base + kRunM + h0, rm);
-        ptx::tmem_st_n<HPW>(tmem + lane_base + kRunL + h0, rl);
+      ptx::tmem_st_n<HPW>(tmem + lane_base + kRunM + h0, rm);
+      ptx::tmem_st_n<HPW>(tmem + lane_base + kRunL + h0, rl);
+      if (run_start) {
+        run_b = c.b;
+        run_part = c.part;
       }
+      last_j = j;
+    }
+    // the last item's O^T products complete before the last run leaves
+    if (ok && last_j >= 0) {
+      ok = ptx::mbar_wait(bar(TB_O), last_j & 1, s_abort, p.wait_limit_ns);
+      if (!ok) ptx::record_timeout(p.status, s_abort, 0x9800);
       ok = __all_sync(0xffffffffu, ok);
+      if (ok) ptx::tc_fence_after();
     }
     // The last run leaves. Its staging may follow another run's in the same
     // item (no P was written in between, so nothing has waited for that
