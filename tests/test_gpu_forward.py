@@ -181,6 +181,39 @@ def test_merge_kernel_against_oracle(n, rows, H, d):
     assert np.isneginf(f32_to_f64(lo)[2, 5]) and np.all(f32_to_f64(of)[5, 2] == 0)
 
 
+@pytest.mark.parametrize("n,rows,H,d", [
+    (5, 300, 3, 128),    # one warp per (row, head)
+    (40, 30, 3, 128),    # many parts, few pairs: a block of warps per pair
+    (256, 1, 16, 128),   # a decode row's merge: 256 parts, most of them empty
+])
+def test_merge_never_reads_empty_parts(n, rows, H, d):
+    """A part with LSE = -inf has weight 0 and its O rows are never read: they
+    hold NaN here (as a slot that no kernel wrote may), and the result must
+    equal the merge of the other parts alone (the LSE merge of "Ring Attention
+    Algorithms": a part with no visible key contributes nothing)."""
+    rng = np.random.default_rng(11)
+    o = rng.standard_normal((n, rows, H, d)).astype(np.float32)
+    lse = (rng.standard_normal((n, H, rows)) * 3).astype(np.float32)
+    empty = rng.random(n) < 0.6
+    empty[0] = False                 # every (row, head) keeps a part with keys
+    lse[empty] = -np.inf
+    o[empty] = np.nan
+    parts = [(o[i].astype(np.float64), lse[i].astype(np.float64)) for i in range(n)
+             if not empty[i]]
+    O_ref, L_ref = oracle.lse_merge(parts)
+    to = torch.from_numpy(o).cuda()
+    tl = torch.from_numpy(lse).cuda()
+    ob = torch.empty((rows, H, d), dtype=torch.bfloat16, device="cuda")
+    of = torch.empty((rows, H, d), dtype=torch.float32, device="cuda")
+    lo = torch.empty((H, rows), dtype=torch.float32, device="cuda")
+    cpa.merge_lse(n, rows, H, d, to, rows * H * d, tl, H * rows, ob, of, lo)
+    torch.cuda.synchronize()
+    assert np.isfinite(f32_to_f64(of)).all() and np.isfinite(f32_to_f64(lo)).all()
+    assert_close(f32_to_f64(of), O_ref, 1e-4, "merge (empty parts) O fp32")
+    assert_close_bf16(bf16_to_f64(ob), O_ref, 1e-3, "merge (empty parts) O bf16")
+    assert_close(f32_to_f64(lo), L_ref, 1e-4, "merge (empty parts) LSE")
+
+
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 def test_layout_permute_bit_exact(layout):
     w = Workload("lay", 2048, 2, 1, 64, 4, kv_prefix_len=1024)
