@@ -1174,8 +1174,10 @@ cp_attn_status launch_tc(const void* k, const void* v, const DecTcParams& p, int
   if (grid_n > items) grid_n = items;
   {
     const cudaError_t e = cudaMemsetAsync(q.counters, 0, sizeof(int) * p.Hkv, s);
-    if (e != cudaSuccess)
+    if (e != cudaSuccess) {
+      cudaGetLastError();
       return fail(CP_ATTN_ERR_CUDA, std::string("decode_tc counters: ") + cudaGetErrorString(e));
+    }
   }
   const unsigned grid = static_cast<unsigned>(grid_n);
   kernel<<<grid, threads, smem, s>>>(tk, tv, q);

@@ -416,7 +416,10 @@ cp_attn_status merge_lse_typed(int n_parts, int64_t rows, int heads, int d, cons
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, n_parts, rows, heads, d, o_parts,
                                                part_stride, lse_parts, lse_part_stride, o_out,
                                                o_out_f32, lse_out);
-    if (err != cudaSuccess) return fail(CP_ATTN_ERR_CUDA, std::string("merge_lse: ") + cudaGetErrorString(err));
+    if (err != cudaSuccess) {
+      cudaGetLastError();
+      return fail(CP_ATTN_ERR_CUDA, std::string("merge_lse: ") + cudaGetErrorString(err));
+    }
     return check_launch("merge_lse");
   }
   const int64_t blocks = (warps * 32 + 255) / 256;
