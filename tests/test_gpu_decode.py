@@ -51,6 +51,7 @@ def _check(B, T, Hq, Hkv, d, R, seed, qk_scale=1.0):
     (3, 1536, 12, 1, 128, 2),     # 12 heads per group, 128-key runs of a 768-key shard
     (2, 1536, 48, 3, 128, 2),     # 16 heads per group, 3 KV heads (the grid is a multiple of 3)
     (4, 16384, 32, 2, 128, 2),    # 16 heads per group, a CTA's runs cross sequences
+    (2, 4096, 32, 32, 128, 2),    # one head per group, 32 KV heads (9 CTAs per KV head)
 ])
 def test_decode_small(B, T, Hq, Hkv, d, R):
     _check(B, T, Hq, Hkv, d, R, seed=B * 100 + R)

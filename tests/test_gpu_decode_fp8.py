@@ -117,6 +117,7 @@ def _run(q, k, v, R, device_quantize=False):
     (2, 8192, 64, 4, 4),      # 16 heads per group (six-slot ring), 128-key runs, 2 sequences
     (2, 1536, 48, 3, 2),      # 16 heads per group, 3 KV heads
     (4, 16384, 32, 2, 2),     # 16 heads per group, a CTA's runs cross sequences
+    (2, 4096, 32, 32, 2),     # one head per group, 32 KV heads
 ])
 def test_decode_fp8_small(B, T, Hq, Hkv, R):
     q, k, v = make_decode_inputs(B, T, Hq, Hkv, D, seed=B * 31 + R)
