@@ -321,15 +321,15 @@ enum : int {
   TB_FULL = 0,                      // [kDecMaxSlots] tile of the slot landed
   TB_EMPTY = kDecMaxSlots,          // [kDecMaxSlots] slot read by its MMAs
   TB_S = 2 * kDecMaxSlots,          // all scores of the run in TMEM
-  TB_P = 2 * kDecMaxSlots + 1,      // softmax-warp arrivals: P in shared memory
-  TB_O = 2 * kDecMaxSlots + 2,      // O^T complete
-  TB_RED = 2 * kDecMaxSlots + 3,    // softmax-warp arrivals per phase: partial maxima, then sums
-  TB_Q = 2 * kDecMaxSlots + 4,      // softmax-warp arrivals: the next group's query rows written
-  TB_DONE = 2 * kDecMaxSlots + 5,   // every MMA of the CTA complete
-  TB_OST = 2 * kDecMaxSlots + 6,    // softmax-warp arrivals: a run's O staged for its store
-  TB_SFREE = 2 * kDecMaxSlots + 7,  // the staging buffer's last store has read it (once)
-  TB_ITEM = 2 * kDecMaxSlots + 8,   // [kDecItemRing] the producer published an item
-  TB_COUNT = 2 * kDecMaxSlots + 8 + 8
+  TB_P = 2 * kDecMaxSlots + 1,      // [4] softmax-warp arrivals: P of tile t in shared memory
+  TB_O = 2 * kDecMaxSlots + 5,      // O^T complete
+  TB_RED = 2 * kDecMaxSlots + 6,    // softmax-warp arrivals per phase: partial maxima, then sums
+  TB_Q = 2 * kDecMaxSlots + 7,      // softmax-warp arrivals: the next group's query rows written
+  TB_DONE = 2 * kDecMaxSlots + 8,   // every MMA of the CTA complete
+  TB_OST = 2 * kDecMaxSlots + 9,    // softmax-warp arrivals: a run's O staged for its store
+  TB_SFREE = 2 * kDecMaxSlots + 10, // the staging buffer's last store has read it (once)
+  TB_ITEM = 2 * kDecMaxSlots + 11,  // [kDecItemRing] the producer published an item
+  TB_COUNT = 2 * kDecMaxSlots + 11 + 8
 };
 constexpr int kDecItemRing = 8;  // items published ahead of their consumers, at most
 
@@ -537,7 +537,10 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
     // rows and the TMEM allocation; nobody else touches a barrier before the
     // block barrier
     for (int i = 0; i < TB_COUNT; ++i)
-      ptx::mbar_init(bar(i), (i == TB_P || i == TB_RED || i == TB_Q || i == TB_OST) ? 32u * SW : 1u);
+      ptx::mbar_init(bar(i), ((i >= TB_P && i < TB_P + kTcMaxTiles) || i == TB_RED || i == TB_Q ||
+                              i == TB_OST)
+                                 ? 32u * SW
+                                 : 1u);
     *s_abort = 0;
     ptx::fence_barrier_init();
     s_item[0] = item0;
@@ -719,11 +722,12 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
       }
       if (!ok) break;
       ptx::mma_commit_w(bar(TB_S), leader);
-      if (!wait_w(bar(TB_P), j & 1, 0x9300)) { ok = false; break; }
-      ptx::tc_fence_after();
+      // O^T += V^T P^T tile by tile, each as soon as its P and its V are in
+      // (an early tile's product frees its V slot for the next item's K)
       for (int t = 0; ok && t < nt; ++t) {
         const int g = j * 2 * nt + nt + t;
         const int slot = g % NSL;
+        if (!wait_w(bar(TB_P + t), j & 1, 0x9300 + t)) { ok = false; break; }
         if (!wait_w(bar(TB_FULL + slot), (g / NSL) & 1, 0x9400 + t)) { ok = false; break; }
         ptx::tc_fence_after();
         if constexpr (F8) {
@@ -938,16 +942,22 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
           ptx::tmem_st_n<HPW>(tmem + lane_base + 64 + h0, o);
         }
       }
-      // P = 2^(x - m) (bf16 or E4M3 into shared memory) and the per-head sums
+      // P = 2^(x - m) (bf16 or E4M3 into shared memory) tile by tile, each
+      // tile handed to the MMA warp as soon as it is written (the first
+      // hand-over also covers the O^T scaling above), and the per-head sums
+      float mr[HPW];
 #pragma unroll
       for (int h = 0; h < HPW; ++h) {
-        const float mr = __uint_as_float(rm[h]);
-        float sum = 0.f;
+        mr[h] = __uint_as_float(rm[h]);
+        l[h] = 0.f;
+      }
 #pragma unroll
-        for (int i = 0; i < kTcMaxTiles; ++i) {
-          if (i < nt) {
-            const float e = ptx::ex2(x[i][h] - mr);
-            sum += e;
+      for (int i = 0; i < kTcMaxTiles; ++i) {
+        if (i < nt) {
+#pragma unroll
+          for (int h = 0; h < HPW; ++h) {
+            const float e = ptx::ex2(x[i][h] - mr[h]);
+            l[h] += e;
             if constexpr (F8) {
               // 2^8 P <= 256: probabilities down to 2^-14 stay normal
               smem[S::kP + kmaj16_off8(h0 + h, i * 128 + t)] =
@@ -957,18 +967,17 @@ __global__ void __launch_bounds__(32 * (dec_softmax_warps(NH) + 2), dec_min_ctas
                   __float2bfloat16_rn(e);
             }
           }
+          ptx::fence_proxy_async_smem();
+          // this warp's reads of S^T and its scaling of O^T are done
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(TB_P + i));
         }
-        l[h] = sum;
       }
       {
         const float sm = warp_reduce_heads<HPW, false>(l, lane);
         if ((lane & ((1 << kHeadShift) - 1)) == 0)
           red[4 * kTcN + qw * kTcN + h0 + (lane >> kHeadShift)] = sm;
       }
-      ptx::fence_proxy_async_smem();
-      // this warp's reads of S^T and its scaling of O^T are done
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(TB_P));
       ptx::mbar_arrive(bar(TB_RED));
       ok = ptx::mbar_wait(bar(TB_RED), 1, s_abort, p.wait_limit_ns);
       if (!ok) ptx::record_timeout(p.status, s_abort, 0x9700);
